@@ -1,0 +1,137 @@
+"""FP64 CPU oracle for paged-KV GQA attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or runs it; the two share no code.
+
+The arithmetic lives in ``pa_oracle.c`` (plain C, double precision); this
+module only marshals numpy arrays of bfloat16 bit patterns (uint16) into it.
+See that file's header for the sources and readings each function follows.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+        u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+        f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+        c_int, c_i64, c_dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_kv_write.restype = c_int
+        lib.oracle_kv_write.argtypes = [u16p, u16p, u16p, u16p, i32p, i32p, ctypes.c_void_p,
+                                        c_int, c_int, c_int, c_int, c_int, c_int]
+        lib.oracle_attention.restype = c_int
+        lib.oracle_attention.argtypes = [u16p, u16p, u16p, i32p, i32p, ctypes.c_void_p,
+                                         c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                         c_dbl, ctypes.c_void_p, c_i64, f64p, c_int]
+        lib.oracle_dense_attention.restype = None
+        lib.oracle_dense_attention.argtypes = [f64p, f64p, f64p, c_i64, c_int, c_dbl, f64p,
+                                               ctypes.POINTER(c_dbl), f64p]
+        lib.oracle_combine.restype = None
+        lib.oracle_combine.argtypes = [f64p, f64p, c_i64, c_int, c_int, f64p]
+        lib.oracle_max_threads.restype = c_int
+        lib.oracle_max_threads.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def _u16(a):
+    """bf16 data as a C-contiguous uint16 numpy view (accepts torch or numpy)."""
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().cpu().contiguous()
+        if a.dtype == torch.bfloat16:
+            a = a.view(torch.int16)
+        return np.ascontiguousarray(a.numpy().view(np.uint16))
+    a = np.ascontiguousarray(a)
+    assert a.dtype.itemsize == 2, a.dtype
+    return a.view(np.uint16)
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk_lens,
+             num_pages, max_pages_per_seq, page_size=128):
+    """Returns (k_cache', v_cache', skipped) with the new tokens' rows copied into
+    their slots (uint16 arrays); the inputs are not modified."""
+    kc = _u16(k_cache).copy()
+    vc = _u16(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    ctx = _i32(context_lens)
+    B = ctx.shape[0]
+    hkv, d = kc.shape[-2], kc.shape[-1]
+    cl = None if chunk_lens is None else _i32(chunk_lens)
+    skipped = _load().oracle_kv_write(
+        kn, vn, kc, vc, _i32(block_table).reshape(-1), ctx,
+        None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
+        B, hkv, d, page_size, num_pages, max_pages_per_seq)
+    return kc, vc, skipped
+
+
+def attention(q, k_cache, v_cache, block_table, context_lens, chunk_lens, scale,
+              num_q_heads, num_kv_heads, num_pages, max_pages_per_seq, rows=None,
+              num_threads=None, page_size=128, head_dim=128):
+    """Paged attention in float64.  q is [T, Hq, D] (decode: T = B, chunk_lens=None).
+    Returns [T, Hq, D] float64, or [len(rows), D] for the (token*Hq + head) ids in rows."""
+    qq = _u16(q).reshape(-1)
+    kc, vc = _u16(k_cache).reshape(-1), _u16(v_cache).reshape(-1)
+    ctx = _i32(context_lens)
+    B = ctx.shape[0]
+    cl = None if chunk_lens is None else _i32(chunk_lens)
+    T = B if cl is None else int(np.maximum(cl, 0).sum())
+    if rows is None:
+        nrows, rp, out_shape = T * num_q_heads, None, (T, num_q_heads, head_dim)
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows, rp, out_shape = rows.shape[0], rows.ctypes.data_as(ctypes.c_void_p), (rows.shape[0], head_dim)
+    out = np.zeros((max(nrows, 1), head_dim), dtype=np.float64)
+    nt = num_threads if num_threads is not None else max_threads()
+    rc = _load().oracle_attention(
+        qq, kc, vc, _i32(block_table).reshape(-1), ctx,
+        None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
+        B, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
+        float(scale), rp, nrows, out, int(nt))
+    if rc != 0:
+        raise ValueError("oracle_attention: bad row index")
+    return out[:nrows].reshape(out_shape)
+
+
+def dense_attention(q, K, V, scale):
+    """One query q [D] over dense keys K, V [n, D] (float64). Returns (out [D], lse)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    K = np.ascontiguousarray(K, dtype=np.float64).reshape(-1, q.shape[0])
+    V = np.ascontiguousarray(V, dtype=np.float64).reshape(-1, q.shape[0])
+    out = np.zeros(q.shape[0], dtype=np.float64)
+    lse = ctypes.c_double(0.0)
+    x = np.zeros(max(K.shape[0], 1), dtype=np.float64)
+    _load().oracle_dense_attention(q, K, V, K.shape[0], q.shape[0], float(scale), out,
+                                   ctypes.byref(lse), x)
+    return out, lse.value
+
+
+def combine(part_o, part_lse):
+    """part_o [R, S, D], part_lse [R, S] (float64) -> [R, D] LSE-weighted merge."""
+    po = np.ascontiguousarray(part_o, dtype=np.float64)
+    pl = np.ascontiguousarray(part_lse, dtype=np.float64)
+    R, S, D = po.shape
+    out = np.zeros((max(R, 1), D), dtype=np.float64)
+    _load().oracle_combine(po, pl, R, S, D, out)
+    return out[:R]

@@ -1,0 +1,270 @@
+/*
+ * Paged-KV GQA attention oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct CPU implementation of what the paged
+ * attention path computes, in double precision.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load this file's
+ * library; the product path never does.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * Sources (page title, section):
+ *  - "Qwen3-14B" (pypto-lib model doc), "Model structure, top down":
+ *    decode_fwd writes the new token into the KV cache and then runs paged
+ *    attention; prefill_fwd does "KV cache update -> causal attention" over
+ *    token-major packed inputs (T = sum(chunk_lens)).  "Deployment
+ *    configuration": 128-token pages.  The attention ABI: Q/O are token-major
+ *    (TND), the flat paged K/V buffers are ordered [page, token, kv_head, dim].
+ *  - "Qwen 3" (TensorSharp model doc), section 11 "Batched / paged forward":
+ *    K/V are scattered to slot blockId*blockSize + offset and gathered per
+ *    sequence from the block tables and sequence lengths; section 3 "Forward
+ *    graph" and 4.1 "Attention": full causal GQA, no window, no sinks, the
+ *    softmax scale 1/sqrt(headDim) folded into the scores.
+ *  - "Qwen4-Exp QSA trafia na Ascend..." (orcarouter blog), first section's
+ *    size-limit bullet: -1 padding is not a valid slot, fully masked rows
+ *    produce zero output.
+ *
+ * Readings where the pages are silent (each also listed in the design doc):
+ *  - query head g reads KV head g / (Hq/Hkv) (contiguous groups);
+ *  - context_lens[s] counts tokens AFTER the write; chunk_lens[s] new tokens;
+ *    new token j of sequence s sits at position context_lens[s]-chunk_lens[s]+j
+ *    and sees keys 0..position (decode: chunk_lens == NULL means 1 each);
+ *  - scores are multiplied by the caller's `scale`;
+ *  - an empty context, or any referenced block-table entry outside
+ *    [0, num_pages), or lengths that do not fit the block table, give an
+ *    all-zero output for every row of that sequence.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bfloat16 bits -> double, exactly (a bf16 is the top half of an IEEE float). */
+static double bf16_to_f64(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Validity of sequence s: lengths consistent and every page it references in
+ * range.  Returns 1 when the sequence may be attended/written. */
+static int seq_valid(const int32_t* block_table, const int32_t* context_lens,
+                     const int32_t* chunk_lens, int s, int page_size,
+                     int num_pages, int max_pages_per_seq) {
+  int64_t ctx = context_lens[s];
+  int64_t n = chunk_lens ? chunk_lens[s] : 1;
+  if (ctx < 0 || n < 0 || n > ctx) return 0;
+  if (ctx > (int64_t)max_pages_per_seq * page_size) return 0;
+  int64_t used = (ctx + page_size - 1) / page_size;
+  for (int64_t i = 0; i < used; ++i) {
+    int32_t p = block_table[(int64_t)s * max_pages_per_seq + i];
+    if (p < 0 || p >= num_pages) return 0;
+  }
+  return 1;
+}
+
+/*
+ * KV write ("KV cache write" / "KV cache update" in the Qwen3-14B doc;
+ * ScatterKv in the TensorSharp doc, section 11): for new token j of sequence
+ * s, position pos = ctx - n + j, slot = block_table[s][pos / P] * P + pos % P;
+ * copy the token's [Hkv, D] K and V rows into the cache at that slot.  A byte
+ * copy: no arithmetic on the values.  Tokens of an invalid sequence are not
+ * written.  Returns the number of sequences skipped as invalid.
+ */
+int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new,
+                    uint16_t* k_cache, uint16_t* v_cache,
+                    const int32_t* block_table, const int32_t* context_lens,
+                    const int32_t* chunk_lens, int num_seqs, int num_kv_heads,
+                    int head_dim, int page_size, int num_pages,
+                    int max_pages_per_seq) {
+  const int64_t row = (int64_t)num_kv_heads * head_dim; /* elements per token */
+  int64_t token = 0;
+  int skipped = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    int64_t n = chunk_lens ? chunk_lens[s] : 1;
+    if (!seq_valid(block_table, context_lens, chunk_lens, s, page_size,
+                   num_pages, max_pages_per_seq)) {
+      ++skipped;
+      token += n > 0 ? n : 0;
+      continue;
+    }
+    int64_t ctx = context_lens[s];
+    for (int64_t j = 0; j < n; ++j, ++token) {
+      int64_t pos = ctx - n + j;
+      int64_t page = block_table[(int64_t)s * max_pages_per_seq + pos / page_size];
+      int64_t slot = page * page_size + pos % page_size;
+      memcpy(k_cache + slot * row, k_new + token * row, (size_t)row * 2);
+      memcpy(v_cache + slot * row, v_new + token * row, (size_t)row * 2);
+    }
+  }
+  return skipped;
+}
+
+/*
+ * Dense softmax attention of one query over n keys (steps 2-3 of the
+ * definition): x_t = scale * <q, K_t>, m = max_t x_t, w_t = exp(x_t - m),
+ * out = sum_t w_t V_t / sum_t w_t.  Also returns lse = m + log(sum_t w_t), the
+ * natural-log normaliser of this key set (used to pin the split combine).
+ * n == 0 gives out = 0 and lse = -inf.
+ */
+void oracle_dense_attention(const double* q, const double* K, const double* V,
+                            int64_t n, int head_dim, double scale, double* out,
+                            double* lse, double* x /* scratch, n */) {
+  for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+  if (n <= 0) { if (lse) *lse = -INFINITY; return; }
+  double m = -INFINITY;
+  for (int64_t t = 0; t < n; ++t) {
+    double dot = 0.0;
+    for (int d = 0; d < head_dim; ++d) dot += q[d] * K[t * head_dim + d];
+    x[t] = scale * dot;
+    if (x[t] > m) m = x[t];
+  }
+  double denom = 0.0;
+  for (int64_t t = 0; t < n; ++t) {
+    double w = exp(x[t] - m);
+    denom += w;
+    for (int d = 0; d < head_dim; ++d) out[d] += w * V[t * head_dim + d];
+  }
+  for (int d = 0; d < head_dim; ++d) out[d] /= denom;
+  if (lse) *lse = m + log(denom);
+}
+
+/*
+ * One (token, query head) row: step 1 of the definition gathers K_t, V_t for
+ * t = 0..pos through the block table (slot = page * P + t % P) into dense
+ * double buffers, then the dense attention above.
+ */
+static void attend_row(const uint16_t* qrow, const uint16_t* k_cache,
+                       const uint16_t* v_cache, const int32_t* bt_row,
+                       int64_t pos, int kv_head, int num_kv_heads,
+                       int head_dim, int page_size, double scale, double* out,
+                       double* qd, double* K, double* V, double* x) {
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  int64_t nkeys = pos + 1;
+  for (int d = 0; d < head_dim; ++d) qd[d] = bf16_to_f64(qrow[d]);
+  for (int64_t t = 0; t < nkeys; ++t) {
+    int64_t slot = (int64_t)bt_row[t / page_size] * page_size + t % page_size;
+    const uint16_t* k = k_cache + slot * row + (int64_t)kv_head * head_dim;
+    const uint16_t* v = v_cache + slot * row + (int64_t)kv_head * head_dim;
+    for (int d = 0; d < head_dim; ++d) {
+      K[t * head_dim + d] = bf16_to_f64(k[d]);
+      V[t * head_dim + d] = bf16_to_f64(v[d]);
+    }
+  }
+  oracle_dense_attention(qd, K, V, nkeys, head_dim, scale, out, NULL, x);
+}
+
+/*
+ * Attention over the paged cache for packed token-major queries.
+ *   q:   [T, Hq, D] bf16 bits, T = sum(chunk_lens) (decode: chunk_lens == NULL,
+ *        T = num_seqs, one token per sequence)
+ *   out: [nrows, D] doubles; row r is (token, head) = rows[r] / Hq, rows[r] % Hq,
+ *        or every row in order when rows == NULL (nrows must then be T*Hq).
+ * Returns 0, or -1 if a requested row index is out of range.
+ */
+int oracle_attention(const uint16_t* q, const uint16_t* k_cache,
+                     const uint16_t* v_cache, const int32_t* block_table,
+                     const int32_t* context_lens, const int32_t* chunk_lens,
+                     int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int page_size, int num_pages,
+                     int max_pages_per_seq, double scale, const int64_t* rows,
+                     int64_t nrows, double* out, int num_threads) {
+  /* token -> (sequence, index within its chunk) */
+  int64_t T = 0;
+  for (int s = 0; s < num_seqs; ++s) T += chunk_lens ? (chunk_lens[s] > 0 ? chunk_lens[s] : 0) : 1;
+  int32_t* tok_seq = (int32_t*)malloc(sizeof(int32_t) * (T > 0 ? T : 1));
+  int64_t* tok_j = (int64_t*)malloc(sizeof(int64_t) * (T > 0 ? T : 1));
+  int64_t maxctx = 1;
+  {
+    int64_t t = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+      int64_t n = chunk_lens ? chunk_lens[s] : 1;
+      for (int64_t j = 0; j < n; ++j, ++t) { tok_seq[t] = s; tok_j[t] = j; }
+      if (context_lens[s] > maxctx) maxctx = context_lens[s];
+    }
+  }
+  const int group = num_q_heads / num_kv_heads;
+  int64_t total = rows ? nrows : T * num_q_heads;
+  int bad = 0;
+  if (!rows && nrows != T * num_q_heads) bad = 1;
+  if (rows)
+    for (int64_t r = 0; r < nrows; ++r)
+      if (rows[r] < 0 || rows[r] >= T * num_q_heads) bad = 1;
+  if (bad) { free(tok_seq); free(tok_j); return -1; }
+
+#ifdef _OPENMP
+  if (num_threads < 1) num_threads = 1;
+#pragma omp parallel num_threads(num_threads)
+#endif
+  {
+    double* x = (double*)malloc(sizeof(double) * (size_t)maxctx);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    double* K = (double*)malloc(sizeof(double) * (size_t)maxctx * head_dim);
+    double* V = (double*)malloc(sizeof(double) * (size_t)maxctx * head_dim);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < total; ++r) {
+      int64_t id = rows ? rows[r] : r;
+      int64_t token = id / num_q_heads;
+      int g = (int)(id % num_q_heads);
+      int s = tok_seq[token];
+      double* o = out + r * head_dim;
+      int64_t n = chunk_lens ? chunk_lens[s] : 1;
+      int64_t pos = (int64_t)context_lens[s] - n + tok_j[token];
+      if (!seq_valid(block_table, context_lens, chunk_lens, s, page_size,
+                     num_pages, max_pages_per_seq) || pos < 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      attend_row(q + (token * num_q_heads + g) * (int64_t)head_dim, k_cache,
+                 v_cache, block_table + (int64_t)s * max_pages_per_seq, pos,
+                 g / group, num_kv_heads, head_dim, page_size, scale, o, qd, K, V, x);
+    }
+    free(x);
+    free(qd);
+    free(K);
+    free(V);
+  }
+  free(tok_seq);
+  free(tok_j);
+  return 0;
+}
+
+/*
+ * Log-sum-exp merge of S partial attention states for each of R rows:
+ * part_o [R, S, D] (each state normalised by its own softmax sum),
+ * part_lse [R, S] natural-log sum of exp(scores) of that state's keys.
+ * out = sum_i exp(lse_i - LSE) o_i with LSE = log sum_i exp(lse_i).  States
+ * with lse = -inf hold no keys and are skipped; a row with none is zero.
+ */
+void oracle_combine(const double* part_o, const double* part_lse, int64_t R,
+                    int S, int head_dim, double* out) {
+  for (int64_t r = 0; r < R; ++r) {
+    const double* lse = part_lse + r * S;
+    double M = -INFINITY;
+    for (int i = 0; i < S; ++i) if (lse[i] > M) M = lse[i];
+    double* o = out + r * head_dim;
+    for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+    if (M == -INFINITY) continue;
+    double L = 0.0;
+    for (int i = 0; i < S; ++i) if (lse[i] != -INFINITY) L += exp(lse[i] - M);
+    for (int i = 0; i < S; ++i) {
+      if (lse[i] == -INFINITY) continue;
+      double w = exp(lse[i] - M) / L;
+      for (int d = 0; d < head_dim; ++d) o[d] += w * part_o[(r * S + i) * head_dim + d];
+    }
+  }
+}
+
+/* OpenMP threads the library would use for num_threads <= 0 requests. */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
