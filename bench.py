@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV GQA attention hot path on one GB300.
+
+Default workload: Qwen3-14B bandwidth-bound decode -- batch 128, every context
+4096 tokens (32 pages of 128), 40 query heads over 8 KV heads, head_dim 128,
+BF16 K/V ~ N(0,1) in a 4096-page pool under a seeded random block table.  One
+step = pa_kv_write of each sequence's new token, then pa_decode (the
+flash-decoding kernel plus its split combine).  The K+V read per step
+(2.147 GB) is far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (see the keys below).  `--impl reference` times the FP64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attn: KV GB/s (% of GB300 HBM peak), seqs/s; prefill TFLOP/s"
+UNIT = "GB/s"
+WORKLOAD = "qwen3-14b-decode-b128-ctx4096"
+B, HQ, HKV, D, PAGE, CTX = 128, 40, 8, 128, 128, 4096
+KV_BYTES = B * CTX * HKV * D * 2 * 2          # K and V, bf16: 2.147 GB
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_WORKLOAD = "chunked-prefill-b8-c512"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def decode_traffic_from_profile():
+    """dram bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_gqa_write_gb300", "csrc", "pa_decode.cu")
+    prof = os.path.join(ROOT, "profiles", "decode_kernel_qwen3-14b-b128.md")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in open(prof):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+        if vals.get("source_sha256_16") != h:
+            return None
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def cpu_oracle_rate(case, seconds, rank0=True):
+    """Time the FP64 oracle on whole decode steps of `case` (host copies) until
+    `seconds` have passed; returns (GB/s of K+V processed, threads, sample text)."""
+    import oracle
+    nt = oracle.max_threads()
+    kb = case.k_cache.cpu()
+    vb = case.v_cache.cpu()
+    q = case.q.cpu()
+    bt = case.block_table.cpu()
+    ctx = case.context_lens.cpu()
+    rows_total = case.B * case.Hq
+    # one chunk = 1/8 of a step (640 rows), so short budgets still finish
+    import numpy as np
+    chunk = max(1, rows_total // 8)
+    done_rows, t0 = 0, time.perf_counter()
+    i = 0
+    while True:
+        lo = (i * chunk) % rows_total
+        rows = np.arange(lo, min(rows_total, lo + chunk), dtype=np.int64)
+        oracle.attention(q, kb, vb, bt, ctx, None, case.scale, case.Hq, case.Hkv, case.num_pages,
+                         case.max_pages_per_seq, rows=rows, num_threads=nt)
+        done_rows += rows.shape[0]
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    kv = KV_BYTES * done_rows / rows_total
+    sample = (f"{done_rows} of the {rows_total} (sequence, query head) rows of one step "
+              f"({done_rows / rows_total:.2f} steps), FP64, {nt} OpenMP threads, {el:.1f} s")
+    return kv / el / 1e9, nt, sample
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import workloads as W
+    from oracle import build as ob
+    ob.build()
+    case = W.qwen3_14b_decode_b128(device="cpu", with_new=False, poison=True)
+    # each step: a bounded sample so that warmup + steps end within minutes
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(case, per_step / 4)
+    vals, threads, sample = [], 0, ""
+    for _ in range(args.steps):
+        v, threads, sample = cpu_oracle_rate(case, per_step)
+        vals.append(v)
+    value = statistics.mean(vals)
+    ms = KV_BYTES / (value * 1e9) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": B, "context_len": CTX, "q_heads": HQ,
+                       "kv_heads": HKV, "head_dim": D, "page_size": PAGE},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill(pa, W, torch, steps=20, warmup=3):
+    """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
+    case = W.chunked_prefill(device="cuda", pool_device="cuda")
+    flops = 0.0
+    for s in range(case.B):
+        n = int(case.chunk_lens[s])
+        prior = int(case.context_lens[s]) - n
+        flops += case.Hq * 4 * D * sum(prior + j + 1 for j in range(n))
+    out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache, case.block_table,
+                       case.context_lens, case.chunk_lens, status=st)
+        pa.pa_prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table,
+                            case.context_lens, case.chunk_lens, case.scale, out=out, status=st)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush.zero_()                      # L2 flush between steps (working set < L2)
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    return {"workload": PREFILL_WORKLOAD, "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms,
+            "gflop_causal": flops / 1e9, "status": int(st.item()),
+            "step": "pa_kv_write (4096 tokens) + pa_prefill_chunk", "l2": "flushed between steps"}
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_setup(args)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_write_gb300 as pa
+    import workloads as W
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = W.qwen3_14b_decode_b128(device=dev, with_new=True, pool_device=dev)
+    dims = pa.make_dims(B, HQ, HKV, case.num_pages, case.max_pages_per_seq)
+    splits = args.num_splits if args.num_splits > 0 else pa.pa_decode_auto_splits(dims)
+    ws_bytes = pa.pa_decode_workspace_size(dims, splits)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache, case.block_table,
+                       case.context_lens, None, status=status, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_decode(case.q, case.k_cache, case.v_cache, case.block_table, case.context_lens,
+                     case.scale, out=out, workspace=workspace, num_splits=splits, status=status,
+                     stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(dec_ev[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), ws)
+    ms_per_step = elapsed_ms / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    launches_per_step = 2 + (1 if splits > 1 else 0)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    hq = case.q.cpu().pin_memory()
+    hk = case.k_new.cpu().pin_memory()
+    hv = case.v_new.cpu().pin_memory()
+    hbt = case.block_table.cpu().pin_memory()
+    hctx = case.context_lens.cpu().pin_memory()
+    hout = torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new)
+    dbt, dctx = torch.empty_like(case.block_table), torch.empty_like(case.context_lens)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hctx))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dctx.copy_(hctx, non_blocking=True)
+        pa.pa_kv_write(dk, dv, case.k_cache, case.v_cache, dbt, dctx, None, status=status,
+                       stream=stream)
+        pa.pa_decode(dq, case.k_cache, case.v_cache, dbt, dctx, case.scale, out=out,
+                     workspace=workspace, num_splits=splits, status=status, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, args.steps // 4)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), ws) / e2e_steps
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    hbm, bf16, bf16_sus, src = peaks()
+    value = KV_BYTES * ws / (ms_per_step * 1e-3) / 1e9
+    achieved = KV_BYTES / (dec_ms * 1e-3) / 1e9
+    prefill = None
+    if not args.no_prefill:
+        try:
+            prefill = run_prefill(pa, W, torch)
+            prefill["peak_tflops"] = bf16
+            prefill["frac"] = prefill["tflops"] / bf16
+        except Exception as e:  # report, do not hide
+            prefill = {"error": str(e).splitlines()[0][:200]}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, nt, sample = cpu_oracle_rate(case, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accum_dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "context_len": CTX, "q_heads": HQ,
+                   "kv_heads": HKV, "head_dim": D, "page_size": PAGE,
+                   "kv_bytes_per_step": KV_BYTES, "num_splits": splits,
+                   "step": "pa_kv_write (1 token/seq) + pa_decode (decode kernel + combine)",
+                   "l2": "inputs larger than L2 (2.147 GB K+V per step), no flush",
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu"},
+        "seqs_per_s": B * ws / (ms_per_step * 1e-3),
+        "pct_hbm_peak": 100.0 * value / ws / hbm,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": decode_traffic_from_profile(),
+                     "kernel": "pa_decode (decode_kernel + combine_kernel)",
+                     "peak_source": f"{src} hbm_gbs (burst)",
+                     "ms_per_launch": dec_ms},
+        "e2e": {"value": KV_BYTES * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

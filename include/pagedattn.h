@@ -1,0 +1,192 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: paged-KV grouped-query attention
+ * for Qwen3-style dense decoding on NVIDIA GB300 (sm_103a).
+ *
+ * Operations and the passages that define them:
+ *  - pa_kv_write: "KV cache write" (decode) / "KV cache update" (prefill) in
+ *    the "Qwen3-14B" pypto-lib doc, "Model structure, top down"; the slot
+ *    formula blockId * blockSize + offset of ScatterKv in the "Qwen 3"
+ *    TensorSharp doc, section 11 "Batched / paged forward".
+ *  - pa_decode: the paged attention stage of decode_fwd ("Qwen3-14B",
+ *    "decode_fwd"): vLLM ABI, token-major Q/O, flat K/V ordered
+ *    [page, token, kv_head, dim]; K/V gathered per sequence from the block
+ *    table and the sequence lengths ("Qwen 3", section 11).  Split across
+ *    KV ranges (flash-decoding) and merged by pa_combine.
+ *  - pa_prefill_chunk: "KV cache update -> causal attention" of prefill_fwd
+ *    ("Qwen3-14B", "prefill_fwd"), inputs packed token-major with
+ *    T = sum(chunk_lens); full causal attention without window or sinks
+ *    ("Qwen 3", 4.1 "Attention").
+ *  - pa_combine: log-sum-exp merge of partial softmax states over disjoint
+ *    key ranges (the split-K step of flash-decoding; not on the pages).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *    library allocates no device memory.  Calls are asynchronous on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream).
+ *  - bf16 = IEEE bfloat16.  Layouts are dense row-major:
+ *      q, out (decode)   [B, Hq, D]          (one query token per sequence)
+ *      q, out (prefill)  [T, Hq, D]          (token-major, sequences in order)
+ *      k_new, v_new      [T, Hkv, D]
+ *      k_cache, v_cache  [num_pages, P, Hkv, D]
+ *      block_table       int32 [B, max_pages_per_seq]
+ *      context_lens      int32 [B]  tokens in the cache AFTER this step's write
+ *      chunk_lens        int32 [B]  new tokens of each sequence this step
+ *    with D = 128 (head_dim) and P = 128 (page_size).  New token j of
+ *    sequence s sits at position context_lens[s] - chunk_lens[s] + j, in slot
+ *    block_table[s][pos / P] * P + pos % P, and attends to keys 0..pos.
+ *    Query head g uses KV head g / (Hq / Hkv).
+ *  - Block-table entries past ceil(context_lens[s] / P) are never read (any
+ *    value, e.g. -1, is fine there).  A referenced entry outside
+ *    [0, num_pages), a negative length, chunk_lens[s] > context_lens[s] or
+ *    context_lens[s] > max_pages_per_seq * P makes that sequence invalid: the
+ *    kernels set a bit in *status (when status != NULL), write nothing to the
+ *    cache for it and give it all-zero attention output.  They never trap.
+ *  - context_lens[s] == 0 gives all-zero output rows (padding rows of a
+ *    padded batch are expressed this way).
+ *  - Return value: PA_OK, a negative PA_ERR_* found on the host before any
+ *    launch (nothing was enqueued), or a positive cudaError_t from a launch.
+ *  - Pointers passed to the tensor-memory-access (TMA) path -- k_cache and
+ *    v_cache -- must be 16-byte aligned; q, out, k_new, v_new and workspace
+ *    must be 16-byte aligned as well.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+typedef struct pa_dims {
+  int32_t num_seqs;          /* B, >= 0 (0 = nothing to do)                  */
+  int32_t num_q_heads;       /* Hq, multiple of Hkv, Hq / Hkv <= 16          */
+  int32_t num_kv_heads;      /* Hkv >= 1                                     */
+  int32_t head_dim;          /* D, must be 128                               */
+  int32_t page_size;         /* P, must be 128                               */
+  int32_t num_pages;         /* pages in the pool, >= 1, num_pages*P < 2^31  */
+  int32_t max_pages_per_seq; /* row length of block_table, >= 1              */
+} pa_dims;
+
+/* output element types */
+#define PA_BF16 0
+#define PA_F32 1
+
+/* host-side argument errors (returned; nothing launched) */
+#define PA_OK 0
+#define PA_ERR_NULL_POINTER (-1)
+#define PA_ERR_HEAD_DIM (-2)
+#define PA_ERR_PAGE_SIZE (-3)
+#define PA_ERR_HEADS (-4)
+#define PA_ERR_DIMS (-5)
+#define PA_ERR_ALIGNMENT (-6)
+#define PA_ERR_OUT_DTYPE (-7)
+#define PA_ERR_WORKSPACE (-8)
+#define PA_ERR_SPLITS (-9)
+#define PA_ERR_TOO_MANY_SEQS (-10)
+#define PA_ERR_TENSOR_MAP (-11)
+#define PA_ERR_NO_DEVICE (-12)
+
+/* device-side status bits OR-ed into *status */
+#define PA_STATUS_BAD_PAGE 1    /* referenced block-table entry out of range */
+#define PA_STATUS_BAD_LENGTH 2  /* inconsistent context/chunk lengths        */
+#define PA_STATUS_BAD_TOKENS 4  /* sum(chunk_lens) != num_tokens             */
+#define PA_STATUS_TIMEOUT 8     /* a bounded wait inside a kernel gave up    */
+
+/* Largest batch accepted by the calls that take chunk_lens (the per-sequence
+ * token offsets are built in shared memory). */
+#define PA_MAX_CHUNKED_SEQS 16384
+
+/*
+ * pa_kv_write -- copy the new tokens' K and V rows into their cache slots.
+ *   k_new, v_new   bf16 [num_tokens, Hkv, D], token-major in sequence order
+ *   k_cache,v_cache bf16 [num_pages, P, Hkv, D], written in place
+ *   block_table, context_lens: as above (context_lens counts the new tokens)
+ *   chunk_lens     int32 [B] new tokens per sequence, or NULL for decode
+ *                  (one token per sequence, num_tokens must equal B)
+ *   status         device int32, may be NULL; bits PA_STATUS_* are OR-ed in
+ * A bit copy: every written byte equals the source byte; no other cache byte
+ * changes.  Two sequences must not write the same slot in one call.
+ */
+int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                const int32_t* block_table, const int32_t* context_lens,
+                const int32_t* chunk_lens, int32_t num_tokens, pa_dims dims,
+                int32_t* status, pa_stream_t stream);
+
+/*
+ * pa_decode -- single-token paged GQA attention, one query token per sequence.
+ *   q              bf16 [B, Hq, D]
+ *   scale          multiplies every score q.k (1/sqrt(D) for Qwen3)
+ *   out            [B, Hq, D], element type out_dtype (PA_BF16 or PA_F32)
+ *   workspace      device scratch for split partials, at least
+ *                  pa_decode_workspace_size(dims, num_splits) bytes; may be
+ *                  NULL when that size is 0.  Caller-owned; contents need no
+ *                  initialisation and are overwritten.
+ *   num_splits     how many KV ranges each sequence's pages are divided into
+ *                  (1..max_pages_per_seq), or 0 to let the library choose
+ *                  from the shape and the device's SM count.  With one split
+ *                  the kernel writes `out` directly; otherwise it writes
+ *                  partials to the workspace and runs the pa_combine kernel.
+ * The result depends only on logical positions, never on which physical
+ * pages hold them: the same inputs under a permuted pool and rewritten block
+ * table give bit-identical output.
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_table, const int32_t* context_lens, float scale,
+              void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
+              int32_t num_splits, pa_dims dims, int32_t* status, pa_stream_t stream);
+
+/* Workspace bytes pa_decode needs for num_splits (0 = the automatic choice on
+ * the current device).  Returns 0 when no workspace is needed, and
+ * (size_t)-1 for invalid dims. */
+size_t pa_decode_workspace_size(pa_dims dims, int32_t num_splits);
+
+/* The split count pa_decode uses for num_splits == 0 on the current device
+ * (>= 1), or a negative PA_ERR_* for invalid dims. */
+int32_t pa_decode_auto_splits(pa_dims dims);
+
+/*
+ * pa_prefill_chunk -- causal attention of a packed chunk of new tokens over
+ * the paged cache (prior context plus the chunk itself, which pa_kv_write
+ * must already have written).
+ *   q              bf16 [num_tokens, Hq, D], token-major in sequence order
+ *   chunk_lens     int32 [B], sum must equal num_tokens (B <= PA_MAX_CHUNKED_SEQS)
+ *   out            [num_tokens, Hq, D], element type out_dtype
+ * Token j of sequence s attends to keys 0..context_lens[s]-chunk_lens[s]+j.
+ */
+int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* context_lens,
+                     const int32_t* chunk_lens, int32_t num_tokens, float scale,
+                     void* out, int32_t out_dtype, pa_dims dims, int32_t* status,
+                     pa_stream_t stream);
+
+/*
+ * pa_combine -- merge num_splits partial attention states per (sequence, head).
+ *   part_o         float32 [B, Hq, num_splits, D]; state i normalised by its own
+ *                  softmax sum
+ *   part_lse       float32 [B, Hq, num_splits]; natural-log sum of exp(score)
+ *                  over state i's keys, -inf for a state with no keys
+ *   out            [B, Hq, D], out_dtype
+ * out = sum_i exp(lse_i - LSE) * o_i with LSE = log(sum_i exp(lse_i)); a row
+ * whose states are all -inf is zero; a row with any +inf lse (the marker
+ * pa_decode writes for an invalid sequence) is zero.  Uses num_seqs,
+ * num_q_heads and head_dim of dims.
+ */
+int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
+               int32_t out_dtype, pa_dims dims, pa_stream_t stream);
+
+/* Human-readable text for a return code (negative PA_ERR_* or positive CUDA
+ * error).  Never NULL; the string is static. */
+const char* pa_status_string(int32_t code);
+
+/* ABI version of this header (major * 100 + minor). */
+int32_t pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

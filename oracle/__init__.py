@@ -29,7 +29,7 @@ def _load():
         c_int, c_i64, c_dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_kv_write.restype = c_int
         lib.oracle_kv_write.argtypes = [u16p, u16p, u16p, u16p, i32p, i32p, ctypes.c_void_p,
-                                        c_int, c_int, c_int, c_int, c_int, c_int]
+                                        c_i64, c_int, c_int, c_int, c_int, c_int, c_int]
         lib.oracle_attention.restype = c_int
         lib.oracle_attention.argtypes = [u16p, u16p, u16p, i32p, i32p, ctypes.c_void_p,
                                          c_int, c_int, c_int, c_int, c_int, c_int, c_int,
@@ -75,6 +75,8 @@ def kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk_le
     kc = _u16(k_cache).copy()
     vc = _u16(v_cache).copy()
     kn, vn = _u16(k_new), _u16(v_new)
+    row = kc.shape[-2] * kc.shape[-1]
+    T = kn.size // row
     ctx = _i32(context_lens)
     B = ctx.shape[0]
     hkv, d = kc.shape[-2], kc.shape[-1]
@@ -82,7 +84,7 @@ def kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk_le
     skipped = _load().oracle_kv_write(
         kn, vn, kc, vc, _i32(block_table).reshape(-1), ctx,
         None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
-        B, hkv, d, page_size, num_pages, max_pages_per_seq)
+        T, B, hkv, d, page_size, num_pages, max_pages_per_seq)
     return kc, vc, skipped
 
 

@@ -72,13 +72,14 @@ static int seq_valid(const int32_t* block_table, const int32_t* context_lens,
  * s, position pos = ctx - n + j, slot = block_table[s][pos / P] * P + pos % P;
  * copy the token's [Hkv, D] K and V rows into the cache at that slot.  A byte
  * copy: no arithmetic on the values.  Tokens of an invalid sequence are not
- * written.  Returns the number of sequences skipped as invalid.
+ * written, and neither are tokens past the num_tokens rows the caller passed.
+ * Returns the number of sequences skipped as invalid.
  */
 int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new,
                     uint16_t* k_cache, uint16_t* v_cache,
                     const int32_t* block_table, const int32_t* context_lens,
-                    const int32_t* chunk_lens, int num_seqs, int num_kv_heads,
-                    int head_dim, int page_size, int num_pages,
+                    const int32_t* chunk_lens, int64_t num_tokens, int num_seqs,
+                    int num_kv_heads, int head_dim, int page_size, int num_pages,
                     int max_pages_per_seq) {
   const int64_t row = (int64_t)num_kv_heads * head_dim; /* elements per token */
   int64_t token = 0;
@@ -92,7 +93,7 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new,
       continue;
     }
     int64_t ctx = context_lens[s];
-    for (int64_t j = 0; j < n; ++j, ++token) {
+    for (int64_t j = 0; j < n && token < num_tokens; ++j, ++token) {
       int64_t pos = ctx - n + j;
       int64_t page = block_table[(int64_t)s * max_pages_per_seq + pos / page_size];
       int64_t slot = page * page_size + pos % page_size;

@@ -1,0 +1,227 @@
+"""Python binding of libpagedattn.so -- paged-KV GQA attention for GB300.
+
+Thin ctypes marshalling over the C ABI declared in ``include/pagedattn.h``:
+the functions here have the C entry points' names, derive ``pa_dims`` from
+tensor shapes, check dtypes/devices, pass raw device pointers and the current
+CUDA stream, and raise on a non-zero return code.  Every step of the path runs
+in the library's CUDA kernels; there is no fallback.  PyTorch supplies device
+memory and streams only.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedattn.so")
+
+HEAD_DIM = 128
+PAGE_SIZE = 128
+PA_BF16, PA_F32 = 0, 1
+PA_STATUS_BAD_PAGE, PA_STATUS_BAD_LENGTH, PA_STATUS_BAD_TOKENS, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+PA_MAX_CHUNKED_SEQS = 16384
+
+EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
+            "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version")
+
+
+class pa_dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({pa_status_string(code)})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                           f"g.build()\"` (there is no non-CUDA path)")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.pa_kv_write.restype = ctypes.c_int
+    lib.pa_kv_write.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, pa_dims, vp, vp]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, vp, sz, i32, pa_dims, vp, vp]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode_workspace_size.argtypes = [pa_dims, i32]
+    lib.pa_decode_auto_splits.restype = i32
+    lib.pa_decode_auto_splits.argtypes = [pa_dims]
+    lib.pa_prefill_chunk.restype = ctypes.c_int
+    lib.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, f32, vp, i32, pa_dims, vp, vp]
+    lib.pa_combine.restype = ctypes.c_int
+    lib.pa_combine.argtypes = [vp, vp, i32, vp, i32, pa_dims, vp]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_abi_version.restype = i32
+    lib.pa_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def pa_status_string(code: int) -> str:
+    return load().pa_status_string(int(code)).decode()
+
+
+def pa_abi_version() -> int:
+    return int(load().pa_abi_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise PagedAttnError(fn, rc)
+
+
+def _need(t, name, dtype, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_dims(num_seqs, num_q_heads, num_kv_heads, num_pages, max_pages_per_seq):
+    return pa_dims(int(num_seqs), int(num_q_heads), int(num_kv_heads), HEAD_DIM, PAGE_SIZE,
+                   int(num_pages), int(max_pages_per_seq))
+
+
+def _cache_dims(q_heads, k_cache, block_table):
+    num_pages, page, hkv, d = k_cache.shape
+    if page != PAGE_SIZE or d != HEAD_DIM:
+        raise ValueError(f"cache must be [pages, {PAGE_SIZE}, Hkv, {HEAD_DIM}], got {tuple(k_cache.shape)}")
+    return make_dims(block_table.shape[0], q_heads, hkv, num_pages, block_table.shape[1])
+
+
+def pa_kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk_lens=None,
+                status=None, stream=None):
+    """Write new tokens' K/V ([T, Hkv, 128] bf16) into the paged caches in place."""
+    dev = k_cache.device
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if chunk_lens is not None:
+        _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    d = _cache_dims(k_cache.shape[2], k_cache, block_table)
+    rc = load().pa_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(block_table), _ptr(context_lens), _ptr(chunk_lens),
+                            int(k_new.shape[0]), d, _ptr(status), _stream(stream))
+    _check("pa_kv_write", rc)
+
+
+def pa_decode_workspace_size(dims, num_splits=0) -> int:
+    n = int(load().pa_decode_workspace_size(dims, int(num_splits)))
+    if n == (1 << 64) - 1:
+        raise ValueError("invalid dims for pa_decode_workspace_size")
+    return n
+
+
+def pa_decode_auto_splits(dims) -> int:
+    r = int(load().pa_decode_auto_splits(dims))
+    if r < 0:
+        raise PagedAttnError("pa_decode_auto_splits", r)
+    return r
+
+
+def pa_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, out=None,
+              out_dtype=torch.bfloat16, workspace=None, num_splits=0, status=None, stream=None):
+    """Single-token paged GQA decode.  q: [B, Hq, 128] bf16.  Returns out [B, Hq, 128]."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    B, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
+    need = pa_decode_workspace_size(d, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    rc = load().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                          _ptr(context_lens), scale, _ptr(out), code, _ptr(workspace),
+                          0 if workspace is None else workspace.numel() * workspace.element_size(),
+                          int(num_splits), d, _ptr(status), _stream(stream))
+    _check("pa_decode", rc)
+    return out
+
+
+def pa_prefill_chunk(q, k_cache, v_cache, block_table, context_lens, chunk_lens, scale=None,
+                     out=None, out_dtype=torch.bfloat16, status=None, stream=None):
+    """Causal chunked prefill over the paged cache.  q: [T, Hq, 128] bf16 token-major."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    T, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    if out is None:
+        out = torch.empty(T, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    rc = load().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                 _ptr(context_lens), _ptr(chunk_lens), int(T), scale, _ptr(out),
+                                 code, d, _ptr(status), _stream(stream))
+    _check("pa_prefill_chunk", rc)
+    return out
+
+
+def pa_combine(part_o, part_lse, out=None, out_dtype=torch.float32, stream=None):
+    """Merge partial states part_o [B, Hq, S, 128] f32 / part_lse [B, Hq, S] f32."""
+    dev = part_o.device
+    _need(part_o, "part_o", torch.float32, dev)
+    _need(part_lse, "part_lse", torch.float32, dev)
+    B, Hq, S, D = part_o.shape
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    d = make_dims(B, Hq, 1, 1, 1)
+    rc = load().pa_combine(_ptr(part_o), _ptr(part_lse), int(S), _ptr(out), code, d,
+                           _stream(stream))
+    _check("pa_combine", rc)
+    return out

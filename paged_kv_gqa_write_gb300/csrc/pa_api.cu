@@ -1,0 +1,356 @@
+// pa_api.cu -- the extern "C" boundary of libpagedattn.so (declared in
+// include/pagedattn.h): host-side argument checks, TMA tensor-map encoding,
+// the split-count choice and stream-ordered kernel launches.  Everything the
+// path computes runs in the kernels; nothing here touches tensor data.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pa_launch.cuh"
+
+namespace {
+
+using pa::kHeadDim;
+using pa::kPage;
+
+constexpr int kMaxGroup = 16;    // query heads per KV head
+constexpr int kMaxGcPerCta = 8;  // query heads one decode CTA serves
+
+int check_dims(const pa_dims& d) {
+  if (d.head_dim != kHeadDim) return PA_ERR_HEAD_DIM;
+  if (d.page_size != kPage) return PA_ERR_PAGE_SIZE;
+  if (d.num_kv_heads < 1 || d.num_q_heads < d.num_kv_heads ||
+      d.num_q_heads % d.num_kv_heads != 0 || d.num_q_heads / d.num_kv_heads > kMaxGroup)
+    return PA_ERR_HEADS;
+  if (d.num_seqs < 0 || d.num_pages < 1 || d.max_pages_per_seq < 1) return PA_ERR_DIMS;
+  if ((int64_t)d.num_pages * kPage > INT32_MAX) return PA_ERR_DIMS;
+  if ((int64_t)d.max_pages_per_seq * kPage > INT32_MAX) return PA_ERR_DIMS;
+  if ((int64_t)d.num_kv_heads * kHeadDim > 65536) return PA_ERR_HEADS;
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Head groups per KV head so that each decode CTA serves at most 8 query heads:
+// the smallest divisor NG of G with G / NG <= 8.
+int head_groups(int G) {
+  for (int ng = 1; ng <= G; ++ng)
+    if (G % ng == 0 && G / ng <= kMaxGcPerCta) return ng;
+  return G;
+}
+
+int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
+
+// Split count for num_splits == 0.  Cost model in units of "page loads on the
+// busiest SM", assuming every sequence is full length: rounds of the
+// round-robin item deal times pages per item, plus a small per-item merge cost
+// and a fixed cost for the combine launch when there is more than one split.
+int auto_splits(const pa_dims& d, int num_sms) {
+  const int64_t units = (int64_t)d.num_seqs * d.num_kv_heads *
+                        head_groups(d.num_q_heads / d.num_kv_heads);
+  if (units <= 0 || num_sms <= 0) return 1;
+  const int mp = d.max_pages_per_seq;
+  int best = 1, prev_pps = -1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= mp; ++s) {
+    const int pps = (mp + s - 1) / s;
+    if (pps == prev_pps) continue;
+    prev_pps = pps;
+    const int se = (mp + pps - 1) / pps;
+    const int64_t items = units * se;
+    const int64_t rounds = (items + num_sms - 1) / num_sms;
+    const double cost = rounds * (pps + 0.25) + (se > 1 ? 1.5 : 0.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = se;
+    }
+  }
+  return best;
+}
+
+// Effective split count and pages per split for a requested count.
+void split_shape(const pa_dims& d, int requested, int* splits, int* pps) {
+  const int mp = d.max_pages_per_seq;
+  int s = requested < 1 ? 1 : (requested > mp ? mp : requested);
+  *pps = (mp + s - 1) / s;
+  *splits = (mp + *pps - 1) / *pps;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes_for(const pa_dims& d, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  return align256(rows * splits * kHeadDim * sizeof(float)) + align256(rows * splits * sizeof(float));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix with the given row pitch
+// (bytes), a (box_cols x box_rows) box and the given swizzle.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+               uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The caches viewed as [num_pages * 128 rows, Hkv * 128 columns], row pitch
+// Hkv * 128 * 2 bytes; 64-column (128-byte) boxes of 128 rows, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* cache, const pa_dims& d) {
+  return encode_2d(map, cache, (uint64_t)d.num_kv_heads * kHeadDim,
+                   (uint64_t)d.num_pages * kPage, (uint64_t)d.num_kv_heads * kHeadDim * 2, 64,
+                   kPage, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return 100; }
+
+const char* pa_status_string(int32_t code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PA_ERR_HEAD_DIM: return "head_dim must be 128";
+    case PA_ERR_PAGE_SIZE: return "page_size must be 128";
+    case PA_ERR_HEADS: return "num_q_heads must be a multiple of num_kv_heads with ratio <= 16";
+    case PA_ERR_DIMS: return "invalid num_seqs / num_pages / max_pages_per_seq / num_tokens";
+    case PA_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
+    case PA_ERR_OUT_DTYPE: return "out_dtype must be PA_BF16 or PA_F32";
+    case PA_ERR_WORKSPACE: return "workspace is NULL or smaller than pa_decode_workspace_size()";
+    case PA_ERR_SPLITS: return "num_splits must be >= 0";
+    case PA_ERR_TOO_MANY_SEQS: return "num_seqs exceeds PA_MAX_CHUNKED_SEQS for a chunked call";
+    case PA_ERR_TENSOR_MAP: return "TMA tensor map encoding failed";
+    case PA_ERR_NO_DEVICE: return "no CUDA device is current";
+    default: break;
+  }
+  if (code > 0) return cudaGetErrorString(static_cast<cudaError_t>(code));
+  return "unknown status";
+}
+
+int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                const int32_t* block_table, const int32_t* context_lens,
+                const int32_t* chunk_lens, int32_t num_tokens, pa_dims d, int32_t* status,
+                pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_tokens < 0) return PA_ERR_DIMS;
+  if (!chunk_lens && num_tokens != d.num_seqs) return PA_ERR_DIMS;
+  if (chunk_lens && d.num_seqs > PA_MAX_CHUNKED_SEQS) return PA_ERR_TOO_MANY_SEQS;
+  if (num_tokens == 0 || d.num_seqs == 0) return PA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !context_lens)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  pa::KvWriteParams p;
+  p.k_new = static_cast<const uint4*>(k_new);
+  p.v_new = static_cast<const uint4*>(v_new);
+  p.k_cache = static_cast<uint4*>(k_cache);
+  p.v_cache = static_cast<uint4*>(v_cache);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.chunk_lens = chunk_lens;
+  p.status = status;
+  p.B = d.num_seqs;
+  p.T = num_tokens;
+  p.Hkv = d.num_kv_heads;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  return launch_result(pa::launch_kv_write(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t pa_decode_auto_splits(pa_dims d) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  return auto_splits(d, sms);
+}
+
+size_t pa_decode_workspace_size(pa_dims d, int32_t num_splits) {
+  if (check_dims(d) || num_splits < 0) return (size_t)-1;
+  int req = num_splits;
+  if (req == 0) {
+    const int sms = device_sms();
+    if (sms <= 0) return (size_t)-1;
+    req = auto_splits(d, sms);
+  }
+  int splits, pps;
+  split_shape(d, req, &splits, &pps);
+  return workspace_bytes_for(d, splits);
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
+              int32_t out_dtype, void* workspace, size_t ws_bytes, int32_t num_splits,
+              pa_dims d, int32_t* status, pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  if (num_splits < 0) return PA_ERR_SPLITS;
+  if (d.num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  int splits, pps;
+  split_shape(d, num_splits == 0 ? auto_splits(d, sms) : num_splits, &splits, &pps);
+  const size_t need = workspace_bytes_for(d, splits);
+  if (need > 0) {
+    if (!workspace || ws_bytes < need) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+  }
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int NG = head_groups(G);
+  const int64_t items = (int64_t)splits * d.num_seqs * d.num_kv_heads * NG;
+  if (items > INT32_MAX) return PA_ERR_DIMS;
+
+  CUtensorMap tm_k, tm_v;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+    return PA_ERR_TENSOR_MAP;
+
+  pa::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.out = out;
+  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.part_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                     align256(rows * splits * kHeadDim * 4))
+                          : nullptr;
+  p.status = status;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = d.num_seqs;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = G;
+  p.NG = NG;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  p.pps = pps;
+  p.S = splits;
+  p.num_items = (int32_t)items;
+  p.out_f32 = out_dtype == PA_F32;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, p, G / NG, sms, st);
+  if (e != cudaSuccess || splits == 1) return launch_result(e);
+  pa::CombineParams c;
+  c.part_o = p.part_o;
+  c.part_lse = p.part_lse;
+  c.out = out;
+  c.rows = (int32_t)rows;
+  c.S = splits;
+  c.out_f32 = p.out_f32;
+  return launch_result(pa::launch_combine(c, st));
+}
+
+int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
+               int32_t out_dtype, pa_dims d, pa_stream_t stream) {
+  if (d.head_dim != kHeadDim) return PA_ERR_HEAD_DIM;
+  if (d.num_seqs < 0 || d.num_q_heads < 1) return PA_ERR_DIMS;
+  if (num_splits < 1) return PA_ERR_SPLITS;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  const int64_t rows = (int64_t)d.num_seqs * d.num_q_heads;
+  if (rows == 0) return PA_OK;
+  if (rows > INT32_MAX) return PA_ERR_DIMS;
+  if (!part_o || !part_lse || !out) return PA_ERR_NULL_POINTER;
+  if (!aligned16(part_o) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_lse) & 3u))
+    return PA_ERR_ALIGNMENT;
+  pa::CombineParams c;
+  c.part_o = part_o;
+  c.part_lse = part_lse;
+  c.out = out;
+  c.rows = (int32_t)rows;
+  c.S = num_splits;
+  c.out_f32 = out_dtype == PA_F32;
+  return launch_result(pa::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* context_lens,
+                     const int32_t* chunk_lens, int32_t num_tokens, float scale, void* out,
+                     int32_t out_dtype, pa_dims d, int32_t* status, pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  if (num_tokens < 0) return PA_ERR_DIMS;
+  if (d.num_seqs > PA_MAX_CHUNKED_SEQS) return PA_ERR_TOO_MANY_SEQS;
+  if (num_tokens == 0 || d.num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !chunk_lens || !out)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGNMENT;
+  if ((int64_t)num_tokens * d.num_q_heads * kHeadDim > ((int64_t)1 << 40)) return PA_ERR_DIMS;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  CUtensorMap tm_k, tm_v, tm_q;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+    return PA_ERR_TENSOR_MAP;
+  // q viewed as [num_tokens * Hq rows, 128 columns]; 64-column boxes of 128 rows.
+  if (!encode_2d(&tm_q, q, kHeadDim, (uint64_t)num_tokens * d.num_q_heads, kHeadDim * 2, 64,
+                 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return PA_ERR_TENSOR_MAP;
+  pa::PrefillParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.chunk_lens = chunk_lens;
+  p.out = out;
+  p.status = status;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = d.num_seqs;
+  p.T = num_tokens;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = d.num_q_heads / d.num_kv_heads;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  p.out_f32 = out_dtype == PA_F32;
+  return launch_result(
+      pa::launch_prefill(tm_k, tm_v, tm_q, p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,22 @@
+// pa_launch.cuh -- kernel launchers, one per translation unit, called by the C ABI layer.
+#pragma once
+#include "pa_common.cuh"
+
+namespace pa {
+
+cudaError_t launch_kv_write(const KvWriteParams& p, int num_sms, cudaStream_t stream);
+
+// Decode: persistent flash-decoding kernel over (split, sequence, kv head,
+// head group) items.  tm_k / tm_v are 2-D tensor maps over the caches viewed
+// as [num_pages * 128 rows, Hkv * 128 columns] bf16 with 128-byte swizzle and
+// a 64 x 128 box.
+cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                          const DecodeParams& p, int gc, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
+                           cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,113 @@
+"""The C-ABI library loads and exports every entry point include/pagedattn.h
+declares; host-side argument checks return the documented codes before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_gqa_write_gb300 import _build
+    _build.build()
+    import paged_kv_gqa_write_gb300 as pa
+    pa.load()
+    return pa
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pa_\w+)\s*\(", src, flags=re.M)))
+
+
+def _header_defines():
+    vals = {}
+    for m in re.finditer(r"#define\s+(PA_\w+)\s+\(?(-?\d+)\)?", open(HEADER).read()):
+        vals[m.group(1)] = int(m.group(2))
+    return vals
+
+
+def test_every_declared_symbol_is_exported(pa):
+    names = _declared()
+    assert set(names) >= {"pa_kv_write", "pa_decode", "pa_prefill_chunk", "pa_combine"}
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pa.EXPORTED) == set(names)
+
+
+def test_python_constants_match_header(pa):
+    h = _header_defines()
+    assert h["PA_BF16"] == pa.PA_BF16 and h["PA_F32"] == pa.PA_F32
+    assert h["PA_STATUS_BAD_PAGE"] == pa.PA_STATUS_BAD_PAGE
+    assert h["PA_STATUS_BAD_LENGTH"] == pa.PA_STATUS_BAD_LENGTH
+    assert h["PA_STATUS_BAD_TOKENS"] == pa.PA_STATUS_BAD_TOKENS
+    assert h["PA_STATUS_TIMEOUT"] == pa.PA_STATUS_TIMEOUT
+    assert h["PA_MAX_CHUNKED_SEQS"] == pa.PA_MAX_CHUNKED_SEQS
+    assert pa.pa_abi_version() == 100
+
+
+def test_status_strings(pa):
+    h = _header_defines()
+    for k, v in h.items():
+        if k.startswith("PA_ERR_"):
+            s = pa.pa_status_string(v)
+            assert s and s != "unknown status", k
+    assert pa.pa_status_string(0) == "ok"
+
+
+def _dims(pa, **kw):
+    base = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, num_pages=4, max_pages_per_seq=2)
+    base.update(kw)
+    d = pa.make_dims(base["num_seqs"], base["num_q_heads"], base["num_kv_heads"],
+                     base["num_pages"], base["max_pages_per_seq"])
+    for k in ("head_dim", "page_size"):
+        if k in kw:
+            setattr(d, k, kw[k])
+    return d
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: rejected before launch
+MIS = ctypes.c_void_p(0x10008)       # 8-byte aligned only
+
+
+def test_host_checks_decode(pa):
+    lib, h = pa.load(), _header_defines()
+    call = lambda d, q=FAKE, out=FAKE, dt=0, ns=0: lib.pa_decode(
+        q, FAKE, FAKE, FAKE, FAKE, 1.0, out, dt, None, 0, ns, d, None, None)
+    assert call(_dims(pa, head_dim=64)) == h["PA_ERR_HEAD_DIM"]
+    assert call(_dims(pa, page_size=16)) == h["PA_ERR_PAGE_SIZE"]
+    assert call(_dims(pa, num_q_heads=6, num_kv_heads=4)) == h["PA_ERR_HEADS"]
+    assert call(_dims(pa, num_q_heads=34, num_kv_heads=2)) == h["PA_ERR_HEADS"]   # group 17
+    assert call(_dims(pa, num_pages=0)) == h["PA_ERR_DIMS"]
+    assert call(_dims(pa, num_pages=1 << 24)) == h["PA_ERR_DIMS"]
+    assert call(_dims(pa), dt=7) == h["PA_ERR_OUT_DTYPE"]
+    assert call(_dims(pa), ns=-1) == h["PA_ERR_SPLITS"]
+    assert call(_dims(pa), q=None) == h["PA_ERR_NULL_POINTER"]
+    assert call(_dims(pa), out=MIS) == h["PA_ERR_ALIGNMENT"]
+    assert call(_dims(pa, num_seqs=0)) == 0                                      # nothing to do
+
+
+def test_host_checks_kv_write_and_prefill(pa):
+    lib, h = pa.load(), _header_defines()
+    d = _dims(pa)
+    assert lib.pa_kv_write(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 3, d, None, None) == h["PA_ERR_DIMS"]
+    assert lib.pa_kv_write(FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 2, d, None, None) == h["PA_ERR_NULL_POINTER"]
+    assert lib.pa_kv_write(MIS, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, d, None, None) == h["PA_ERR_ALIGNMENT"]
+    big = _dims(pa, num_seqs=h["PA_MAX_CHUNKED_SEQS"] + 1)
+    assert lib.pa_kv_write(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 9, big, None, None) == h["PA_ERR_TOO_MANY_SEQS"]
+    assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 1.0, FAKE, 0, d, None, None) == h["PA_ERR_NULL_POINTER"]
+    assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 3, d, None, None) == h["PA_ERR_OUT_DTYPE"]
+    assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1.0, FAKE, 0, d, None, None) == 0
+    assert lib.pa_combine(FAKE, FAKE, 0, FAKE, 0, d, None) == h["PA_ERR_SPLITS"]
+    assert lib.pa_combine(FAKE, FAKE, 2, MIS, 0, d, None) == h["PA_ERR_ALIGNMENT"]
+
+
+def test_workspace_size_invalid_dims(pa):
+    assert pa.load().pa_decode_workspace_size(_dims(pa, head_dim=64), 2) == ctypes.c_size_t(-1).value
