@@ -192,13 +192,15 @@ def qwen3_14b_decode_b16(device="cpu", with_new=False, pool_device=None) -> Page
                       device=device, with_new=with_new, pool_device=pool_device)
 
 
-def qwen3_14b_decode_b128(device="cpu", with_new=False, pool_device=None, poison=True) -> PagedCase:
+def qwen3_14b_decode_b128(device="cpu", with_new=False, pool_device=None, poison=True,
+                          batch=128) -> PagedCase:
     """Qwen3-14B bandwidth-bound decode: batch 128, every context 4096 (32 pages),
-    block table a seeded permutation of the 4096-page pool (2.147 GB of K+V read)."""
+    block table a seeded permutation of the 4096-page pool (2.147 GB of K+V read).
+    `batch` scales the batch and the pool together (32 pages per sequence)."""
     sb = 3 * 1000
-    ctx = [4096] * 128
-    perm = _perm(4096, sb + _T_PERM)
-    return build_case("qwen3-14b-decode-b128-ctx4096", sb, ctx, 40, 8, 4096,
+    ctx = [4096] * batch
+    perm = _perm(32 * batch, sb + _T_PERM)
+    return build_case(f"qwen3-14b-decode-b{batch}-ctx4096", sb, ctx, 40, 8, 32 * batch,
                       consecutive_runs(ctx, perm), 32, device=device, with_new=with_new,
                       pool_device=pool_device, poison=poison)
 
