@@ -20,8 +20,9 @@
  *    key ranges (the split-K step of flash-decoding; not on the pages).
  *
  * Conventions shared by every entry point
- *  - Every tensor pointer is a DEVICE pointer owned by the caller; the
- *    library allocates no device memory.  Calls are asynchronous on `stream`
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; no call
+ *    allocates device memory (pa_decode_noalloc's fixed scratch array is part
+ *    of the loaded library).  Calls are asynchronous on `stream`
  *    (a cudaStream_t; NULL = the legacy default stream).
  *  - bf16 = IEEE bfloat16.  Layouts are dense row-major:
  *      q, out (decode)   [B, Hq, D]          (one query token per sequence)
@@ -89,6 +90,7 @@ typedef struct pa_dims {
 #define PA_ERR_TOO_MANY_SEQS (-10)
 #define PA_ERR_TENSOR_MAP (-11)
 #define PA_ERR_NO_DEVICE (-12)
+#define PA_ERR_NOALLOC_TOO_LARGE (-13)
 
 /* device-side status bits OR-ed into *status */
 #define PA_STATUS_BAD_PAGE 1    /* referenced block-table entry out of range */
@@ -177,6 +179,43 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
  */
 int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
                int32_t out_dtype, pa_dims dims, pa_stream_t stream);
+
+/* Size of the device array pa_decode_noalloc keeps its split partials in. */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory.  (This entry point has no counterpart on the source pages; it
+ * exists for integration.)  Some callers are handed their input and output
+ * buffers by a host framework that owns every device allocation -- an engine
+ * plugin, or a C host with no device allocator of its own -- and others must
+ * not call cudaMalloc on a latency-critical path, where it can synchronise
+ * the device.  Such callers cannot provide pa_decode's workspace.
+ *
+ * Same arguments, layouts, results and status handling as pa_decode, without
+ * workspace / workspace_bytes.  The split partials go to one device array of
+ * PA_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library; every GPU that loads
+ * the library holds that array until the process exits.  A call whose split
+ * count (num_splits, or the automatic choice for 0) needs more scratch than
+ * that -- (B * Hq * splits * 516 bytes, rounded up) -- returns
+ * PA_ERR_NOALLOC_TOO_LARGE without launching; num_splits = 1 needs none.
+ *
+ * Setup: the first call made with a given device current looks up the
+ * array's device address on that device (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture.  Nothing is allocated, by
+ * this function or by anything it calls.
+ *
+ * Sharing: all calls on a device use the same array, which keeps whatever the
+ * last call left in it.  Nothing in it needs to start at zero -- every partial
+ * the combine step reads is written earlier in the same call -- but calls
+ * that can overlap on the GPU (different streams, or different host threads
+ * without ordering) race on the array and corrupt each other's results:
+ * order them on one stream, or use pa_decode with separate workspaces.
+ */
+int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* context_lens, float scale,
+                      void* out, int32_t out_dtype, int32_t num_splits, pa_dims dims,
+                      int32_t* status, pa_stream_t stream);
 
 /* Human-readable text for a return code (negative PA_ERR_* or positive CUDA
  * error).  Never NULL; the string is static. */

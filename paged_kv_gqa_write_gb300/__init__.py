@@ -23,7 +23,9 @@ PA_STATUS_BAD_PAGE, PA_STATUS_BAD_LENGTH, PA_STATUS_BAD_TOKENS, PA_STATUS_TIMEOU
 PA_MAX_CHUNKED_SEQS = 16384
 
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
-            "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version")
+            "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
+            "pa_decode_noalloc")
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class pa_dims(ctypes.Structure):
@@ -64,6 +66,8 @@ def load(path: str = LIB_PATH):
     lib.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, f32, vp, i32, pa_dims, vp, vp]
     lib.pa_combine.restype = ctypes.c_int
     lib.pa_combine.argtypes = [vp, vp, i32, vp, i32, pa_dims, vp]
+    lib.pa_decode_noalloc.restype = ctypes.c_int
+    lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, i32, pa_dims, vp, vp]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [i32]
     lib.pa_abi_version.restype = i32
@@ -224,4 +228,33 @@ def pa_combine(part_o, part_lse, out=None, out_dtype=torch.float32, stream=None)
     rc = load().pa_combine(_ptr(part_o), _ptr(part_lse), int(S), _ptr(out), code, d,
                            _stream(stream))
     _check("pa_combine", rc)
+    return out
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None, out=None,
+                      out_dtype=torch.bfloat16, num_splits=0, status=None, stream=None):
+    """pa_decode without a workspace, for callers that cannot allocate device
+    memory: the split partials go to the library's fixed device array
+    (PA_NOALLOC_SCRATCH_BYTES).  Calls on one device share that array, so calls
+    that may overlap on the GPU must be ordered on one stream.  `out` should be
+    passed in by such callers (allocating it here is a convenience)."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    B, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    rc = load().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                  _ptr(context_lens), scale, _ptr(out), code, int(num_splits), d,
+                                  _ptr(status), _stream(stream))
+    _check("pa_decode_noalloc", rc)
     return out

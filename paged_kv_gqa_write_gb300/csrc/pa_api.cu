@@ -160,6 +160,8 @@ const char* pa_status_string(int32_t code) {
     case PA_ERR_TOO_MANY_SEQS: return "num_seqs exceeds PA_MAX_CHUNKED_SEQS for a chunked call";
     case PA_ERR_TENSOR_MAP: return "TMA tensor map encoding failed";
     case PA_ERR_NO_DEVICE: return "no CUDA device is current";
+    case PA_ERR_NOALLOC_TOO_LARGE:
+      return "split partials exceed PA_NOALLOC_SCRATCH_BYTES: use fewer splits or pa_decode";
     default: break;
   }
   if (code > 0) return cudaGetErrorString(static_cast<cudaError_t>(code));
@@ -354,3 +356,110 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pa_decode_noalloc: pa_decode for callers that cannot allocate device memory.
+//
+// The split partials live in one file-scope device array instead of a
+// caller-provided workspace.  Its device address is looked up once per device
+// (on the first call made with that device current) and cached; host code
+// must never hand the symbol itself to a kernel, because on the host the name
+// refers to a host-side stand-in, not to device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device, or null with
+// *err set when the lookup fails.
+void* noalloc_scratch(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* context_lens,
+                                 float scale, void* out, int32_t out_dtype, int32_t num_splits,
+                                 pa_dims d, int32_t* status, pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  if (num_splits < 0) return PA_ERR_SPLITS;
+  if (d.num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  int splits, pps;
+  split_shape(d, num_splits == 0 ? auto_splits(d, sms) : num_splits, &splits, &pps);
+  const size_t need = workspace_bytes_for(d, splits);
+  if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_NOALLOC_TOO_LARGE;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int NG = head_groups(G);
+  const int64_t items = (int64_t)splits * d.num_seqs * d.num_kv_heads * NG;
+  if (items > INT32_MAX) return PA_ERR_DIMS;
+  uint8_t* scratch = nullptr;
+  if (need > 0) {
+    cudaError_t e = cudaSuccess;
+    scratch = static_cast<uint8_t*>(noalloc_scratch(&e));
+    if (!scratch) return launch_result(e == cudaSuccess ? cudaErrorUnknown : e);
+  }
+
+  CUtensorMap tm_k, tm_v;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+    return PA_ERR_TENSOR_MAP;
+
+  pa::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.out = out;
+  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  p.part_o = splits > 1 ? reinterpret_cast<float*>(scratch) : nullptr;
+  p.part_lse = splits > 1 ? reinterpret_cast<float*>(scratch + align256(rows * splits * kHeadDim * 4))
+                          : nullptr;
+  p.status = status;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = d.num_seqs;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = G;
+  p.NG = NG;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  p.pps = pps;
+  p.S = splits;
+  p.num_items = (int32_t)items;
+  p.out_f32 = out_dtype == PA_F32;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, p, G / NG, sms, st);
+  if (e != cudaSuccess || splits == 1) return launch_result(e);
+  pa::CombineParams c;
+  c.part_o = p.part_o;
+  c.part_lse = p.part_lse;
+  c.out = out;
+  c.rows = (int32_t)rows;
+  c.S = splits;
+  c.out_f32 = p.out_f32;
+  return launch_result(pa::launch_combine(c, st));
+}
