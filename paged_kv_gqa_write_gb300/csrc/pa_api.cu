@@ -129,6 +129,22 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over a row-major [d2, d1, d0] array (d0 contiguous) with a
+// (box0 x 1 x box2) box: one index of the middle dimension, box2 outer rows.
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t box0, uint32_t box2, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {box0, 1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // The caches viewed as [num_pages * 128 rows, Hkv * 128 columns], row pitch
 // Hkv * 128 * 2 bytes; 64-column (128-byte) boxes of 128 rows, 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* map, const void* cache, const pa_dims& d) {
@@ -331,9 +347,9 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   CUtensorMap tm_k, tm_v, tm_q;
   if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
     return PA_ERR_TENSOR_MAP;
-  // q viewed as [num_tokens * Hq rows, 128 columns]; 64-column boxes of 128 rows.
-  if (!encode_2d(&tm_q, q, kHeadDim, (uint64_t)num_tokens * d.num_q_heads, kHeadDim * 2, 64,
-                 128, CU_TENSOR_MAP_SWIZZLE_128B))
+  // q as [num_tokens, Hq, 128]: a box is 128 tokens of one head, 64 dims wide.
+  if (!encode_3d(&tm_q, q, kHeadDim, d.num_q_heads, (uint64_t)num_tokens, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return PA_ERR_TENSOR_MAP;
   pa::PrefillParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int pg = it.pg0; pg < it.pg1; ++pg) {
       const int page = __ldg(bt + pg);
       bad |= (page < 0 || page >= p.num_pages);
-      if (!mbar_wait(&full[stage], phase, p.status)) { aborted = true; break; }
+      if (!mbar_wait_warp(&full[stage], phase, p.status)) { aborted = true; break; }
       const uint32_t kb = smem_u32(smem + stage * kStageBytes);
       const uint32_t vb = kb + 2 * kBoxBytes;
       const int nvalid = min(max(it.ctx - pg * kPage - 32 * warp, 0), 32);
