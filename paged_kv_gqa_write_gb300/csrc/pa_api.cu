@@ -57,8 +57,11 @@ int device_sms() {
 
 // Split count for num_splits == 0.  Cost model in units of "page loads on the
 // busiest SM", assuming every sequence is full length: rounds of the
-// round-robin item deal times pages per item, plus a small per-item merge cost
-// and a fixed cost for the combine launch when there is more than one split.
+// round-robin item deal times (pages per item + a per-item cost of about 2.5
+// page loads for the cross-warp merge and pipeline restart), plus about 3.5
+// page loads for the combine launch when there is more than one split
+// (constants fitted to GB300 sweeps of 16-256 sequences x 4096 tokens).  With
+// fewer units than SMs, at least enough splits to give every SM two items.
 int auto_splits(const pa_dims& d, int num_sms) {
   const int64_t units = (int64_t)d.num_seqs * d.num_kv_heads *
                         head_groups(d.num_q_heads / d.num_kv_heads);
@@ -73,11 +76,15 @@ int auto_splits(const pa_dims& d, int num_sms) {
     const int se = (mp + pps - 1) / pps;
     const int64_t items = units * se;
     const int64_t rounds = (items + num_sms - 1) / num_sms;
-    const double cost = rounds * (pps + 0.25) + (se > 1 ? 1.5 : 0.0);
+    const double cost = rounds * (pps + 2.5) + (se > 1 ? 3.5 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = se;
     }
+  }
+  if (units < num_sms) {
+    const int64_t want = (2 * (int64_t)num_sms + units - 1) / units;
+    if (want > best) best = (int)(want < mp ? want : mp);
   }
   return best;
 }
