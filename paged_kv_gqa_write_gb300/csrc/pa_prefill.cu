@@ -9,108 +9,212 @@
 // own sequence, read from the paged cache (prior context plus the chunk,
 // which pa_kv_write has already stored).
 //
-// Work item: (sequence, 128-token query tile, query head).  S = Q K^T and
-// O += P V are dense 128x128x128 BF16 products per 128-token key page.
-//  * warp 0, one lane: TMA producer -- the Q tile (3-D map over [T, Hq, 128])
-//    and a 2-deep ring each of K and V page tiles (128-byte swizzle), in the
-//    layout the tensor core reads directly.
-//  * warp 1, one lane: issues tcgen05.mma (M=128, N=128, K=16 steps) for
-//    S_j = Q K_j^T into one of two TMEM score buffers, then O += P_{j-1} V_{j-1}
-//    with V as an MN-major operand, committing completions to mbarriers.  The
-//    warp also owns the TMEM allocation (512 columns: S0, S1, O).
-//  * warps 2-5: one thread per query row.  tcgen05.ld of the score row,
-//    causal mask (only on tiles that cross the row's position), online
-//    softmax in the log2 domain; P (BF16) goes to a swizzled shared-memory
-//    tile the next MMA reads.  O is rescaled in TMEM only when the running
-//    max grows by more than 2^8 (the final O / l is unchanged by the choice of
-//    reference max).  The epilogue divides by l and writes the row.
-// Key pages entirely above the tile's last query position are never loaded
-// (causal tile skipping); V rows past the sequence's context in its last page
-// are zeroed in shared memory before use (P is 0 there, but 0 * NaN is NaN).
+// Work item: (sequence, pair of consecutive 128-token query tiles A and B,
+// query head).  Both tiles share every K/V page tile the CTA loads, so each
+// 64 KB of K/V feeds four 128x128x128 BF16 products (S_A, S_B, P_A.V, P_B.V):
+// with one query tile per load the kernel would be bound by L2 bandwidth
+// (~72 GB/s per SM), with two it needs half that.
+//  * warp 0 (one lane) loads the two Q tiles (3-D TMA map over [T, Hq, 128])
+//    and the K page tiles into a 3-deep ring; warp 10 (one lane) the V page
+//    tiles into a 2-deep ring (128-byte swizzle, the layout the tensor core
+//    reads).
+//  * warp 1 (one lane) issues tcgen05.mma (M=128, N=128, K=16 steps) in the
+//    order P_A(j).V(j), S_A(j+1), P_B(j).V(j), S_B(j+1), so that each softmax
+//    group overlaps the other's MMAs.  P_t(j) is read from tensor memory (it
+//    overwrites the first 64 columns of S_t(j) as packed BF16 pairs); V is an
+//    MN-major shared-memory operand.  The MMAs of one thread execute in issue
+//    order, so P_t(j) is consumed before S_t(j+1) is written.  The warp owns
+//    the TMEM allocation (S_A, S_B, O_A, O_B: 512 columns).
+//  * warps 2-5 (tile A) and 6-9 (tile B): one thread per query row.  Per key
+//    tile: tcgen05.ld of the score row, causal mask (only on tiles that cross
+//    the row's position), online softmax in the log2 domain (max of the raw
+//    scores, one FMA + exp2 per element), P into TMEM.  O_t is rescaled in
+//    TMEM only when the max grows by more than 2^8 (the final O / l is
+//    unchanged by the choice of reference max).  Epilogue: O_t / l per row.
+// Key pages entirely above a tile's last query position are never loaded for
+// it (causal tile skipping); V rows past the sequence's context in its last
+// page are zeroed in shared memory before use (P is 0 there, but 0 * NaN is
+// NaN).  Items are dealt to the persistent CTAs in decreasing order of
+// key-tile count, snaking across CTAs (a greedy longest-first balance every
+// CTA computes from the lengths); very large launches fall back to
+// round-robin.
+#include <type_traits>
+
 #include "pa_launch.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kVWarp = 10;                    // V producer
+constexpr int kThreads = (kVWarp + 1) * 32;
 constexpr int kTileBytes = 128 * 128 * 2;     // 32 KB: one 128x128 bf16 tile
 constexpr int kBox = 16384;                   // 64-column half of a tile
-constexpr int kRing = 2;
+constexpr int kRingK = 3, kRingV = 2;
+constexpr int kMaxList = 64;                  // scheduled items per CTA
 // shared memory layout (offsets from a 1024-aligned base)
-constexpr int kQ = 0;
-constexpr int kK = kQ + kTileBytes;
-constexpr int kV = kK + kRing * kTileBytes;
-constexpr int kP = kV + kRing * kTileBytes;
-constexpr int kBars = kP + kRing * kTileBytes;
-constexpr int kNumBars = 2 + 4 * kRing + 4 * 2 + 2;
+constexpr int kQ = 0;                         // Q_A, Q_B
+constexpr int kK = kQ + 2 * kTileBytes;
+constexpr int kV = kK + kRingK * kTileBytes;
+constexpr int kList = kV + kRingV * kTileBytes;  // schedule [kMaxList][3] int
+constexpr int kBars = kList + kMaxList * 3 * 4;
+constexpr int kNumBars = 2 + 2 * kRingK + 2 * kRingV + 4 * 2;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
+constexpr int kMaxCost = 4096;                // schedule histogram buckets (ring scratch)
 // TMEM columns
-constexpr uint32_t kColS = 0;     // two 128-column score buffers
-constexpr uint32_t kColO = 256;   // 128-column output accumulator
+constexpr uint32_t kColS = 0;     // S_A, S_B: 128 columns each (P in their first 64)
+constexpr uint32_t kColO = 256;   // O_A, O_B: 128 columns each
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Bars {
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* k_full;   // [kRing]
+  uint64_t* k_full;   // [kRingK]
   uint64_t* k_empty;
-  uint64_t* v_full;
+  uint64_t* v_full;   // [kRingV]
   uint64_t* v_empty;
-  uint64_t* s_full;   // [2]
-  uint64_t* s_free;
+  uint64_t* s_full;   // [2] per query tile
   uint64_t* p_full;
-  uint64_t* p_free;
   uint64_t* o_done;
   uint64_t* o_free;
 };
 
-// Walks (sequence, query tile, head) items in increasing order.
-struct Cursor {
-  int s = 0, tiles_before = 0, tok_before = 0;
-  __device__ __forceinline__ int tiles_of(const PrefillParams& p, int seq) const {
-    const int n = __ldg(p.chunk_lens + seq);
-    return n > 0 ? (n + 127) / 128 : 0;
-  }
-  // Advance to the sequence holding query tile `tile`; false when past the end.
-  __device__ __forceinline__ bool seek(const PrefillParams& p, int tile) {
-    while (s < p.B) {
-      const int nt = tiles_of(p, s);
-      if (tile < tiles_before + nt) return true;
-      tiles_before += nt;
-      const int n = __ldg(p.chunk_lens + s);
-      tok_before += n > 0 ? n : 0;
-      ++s;
-    }
-    return false;
-  }
-};
-
 struct Item {
-  int s, g, h, qt;
-  int tok0;      // packed index of the tile's first query token
-  int nrows;     // query rows of this tile that exist (<= 128)
-  int prior;     // context before the chunk
-  int ctx;
-  int nkt;       // key tiles to visit (0: lengths invalid)
+  int s, g, h, pair;
+  int tok0;          // packed index of tile A's first query token
+  int nrows[2];      // query rows of tiles A, B (<= 128; B may be 0)
+  int nkt[2];        // key tiles each query tile visits (0: none / lengths invalid)
+  int nmax;          // key tiles the pair loads
+  int prior, ctx;
   bool len_ok;
 };
 
-__device__ __forceinline__ Item make_item(const PrefillParams& p, const Cursor& c, int tile,
-                                          int g) {
+__device__ __forceinline__ bool lengths_ok(const PrefillParams& p, int n, int ctx) {
+  return ctx >= 0 && n >= 0 && n <= ctx && ctx <= p.max_pages * kPage;
+}
+
+__device__ __forceinline__ Item make_item(const PrefillParams& p, int s, int pair, int g,
+                                          int tok0) {
   Item it;
-  it.s = c.s;
+  it.s = s;
   it.g = g;
   it.h = g / p.G;
-  it.qt = tile - c.tiles_before;
-  const int n = __ldg(p.chunk_lens + c.s);
-  it.ctx = __ldg(p.context_lens + c.s);
-  it.tok0 = c.tok_before + it.qt * 128;
-  it.nrows = min(128, n - it.qt * 128);
-  it.len_ok = it.ctx >= 0 && n >= 0 && n <= it.ctx && it.ctx <= p.max_pages * kPage;
+  it.pair = pair;
+  const int n = __ldg(p.chunk_lens + s);
+  it.ctx = __ldg(p.context_lens + s);
+  it.tok0 = tok0;
+  it.len_ok = lengths_ok(p, n, it.ctx);
   it.prior = it.ctx - n;
-  it.nkt = it.len_ok ? (it.prior + it.qt * 128 + it.nrows - 1) / kPage + 1 : 0;
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = pair * 256 + t * 128;
+    it.nrows[t] = max(0, min(128, n - q0));
+    it.nkt[t] = (it.len_ok && it.nrows[t] > 0) ? (it.prior + q0 + it.nrows[t] - 1) / kPage + 1 : 0;
+  }
+  it.nmax = max(it.nkt[0], it.nkt[1]);
   return it;
+}
+
+__device__ __forceinline__ int pair_cost(const PrefillParams& p, int n, int ctx, int pair) {
+  if (!lengths_ok(p, n, ctx)) return 0;
+  int c = 0;
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = pair * 256 + t * 128;
+    const int nr = min(128, n - q0);
+    if (nr > 0) c += (ctx - n + q0 + nr - 1) / kPage + 1;
+  }
+  return c;
+}
+
+// Greedy longest-first schedule: all items sorted by key-tile count
+// (descending; ties in (sequence, pair, head) order), dealt to CTAs in a snake
+// (0..N-1, N-1..0, ...).  Writes this CTA's items in order and returns their
+// count, or -1 when the launch is too large for the table (round-robin then).
+__device__ int build_schedule(const PrefillParams& p, int* hist, int* list, int N, int c) {
+  const int maxc = 2 * p.max_pages + 1;
+  if (maxc > kMaxCost || p.Hq > 256) return -1;
+  int* start = hist + kMaxCost;
+  for (int b = 0; b < maxc; ++b) hist[b] = 0;
+  int64_t pairs = 0;
+  for (int s = 0; s < p.B; ++s) {
+    const int n = __ldg(p.chunk_lens + s), ctx = __ldg(p.context_lens + s);
+    for (int pr = 0; pr * 256 < n; ++pr) {
+      ++hist[pair_cost(p, n, ctx, pr)];
+      ++pairs;
+    }
+  }
+  const int64_t items = pairs * p.Hq;
+  int rows = 0;  // snake rows that hold an item for this CTA
+  for (int64_t r = 0;; ++r) {
+    const int64_t pos = r * N + ((r & 1) ? N - 1 - c : c);
+    if (pos >= items) break;
+    if (++rows > kMaxList) return -1;
+  }
+  int64_t acc = 0;
+  for (int b = maxc - 1; b >= 0; --b) {
+    start[b] = (int)acc;
+    acc += (int64_t)hist[b] * p.Hq;
+    hist[b] = 0;
+  }
+  const int64_t N2 = 2 * (int64_t)N;
+  int tok = 0;
+  for (int s = 0; s < p.B; ++s) {
+    const int n = __ldg(p.chunk_lens + s), ctx = __ldg(p.context_lens + s);
+    for (int pr = 0; pr * 256 < n; ++pr) {
+      const int cost = pair_cost(p, n, ctx, pr);
+      const int64_t pos0 = start[cost] + (int64_t)(hist[cost]++) * p.Hq;
+      for (int k = 0; k < 2; ++k) {
+        const int64_t res = k ? N2 - 1 - c : c;
+        for (int64_t pos = pos0 + ((res - pos0 % N2) % N2 + N2) % N2; pos < pos0 + p.Hq; pos += N2) {
+          const int r = (int)(pos / N);
+          list[3 * r] = s;
+          list[3 * r + 1] = (pr << 8) | (int)(pos - pos0);
+          list[3 * r + 2] = tok + pr * 256;
+        }
+      }
+    }
+    tok += n > 0 ? n : 0;
+  }
+  return rows;
+}
+
+// Item source shared by all roles: the schedule table, or round-robin over
+// (sequence, pair, head) when the table is unavailable.
+struct ItemSource {
+  const int* list;
+  int count;  // -1: round-robin
+  int s = 0, pairs_before = 0, tok_before = 0;
+  __device__ bool get(const PrefillParams& p, int r, Item& it) {
+    if (count >= 0) {
+      if (r >= count) return false;
+      const int s_ = list[3 * r], qg = list[3 * r + 1];
+      it = make_item(p, s_, qg >> 8, qg & 255, list[3 * r + 2]);
+      return true;
+    }
+    const int i = (int)blockIdx.x + r * (int)gridDim.x;
+    const int pair = i / p.Hq, g = i - pair * p.Hq;
+    while (s < p.B) {
+      const int n = __ldg(p.chunk_lens + s);
+      const int np = n > 0 ? (n + 255) / 256 : 0;
+      if (pair < pairs_before + np) break;
+      pairs_before += np;
+      tok_before += n > 0 ? n : 0;
+      ++s;
+    }
+    if (s >= p.B) return false;
+    const int pr = pair - pairs_before;
+    it = make_item(p, s, pr, g, tok_before + pr * 256);
+    return true;
+  }
+};
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 BF16 (lane = row, pairs per column).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -124,36 +228,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.q_full = bar;
   B.q_empty = bar + 1;
   B.k_full = bar + 2;
-  B.k_empty = B.k_full + kRing;
-  B.v_full = B.k_empty + kRing;
-  B.v_empty = B.v_full + kRing;
-  B.s_full = B.v_empty + kRing;
-  B.s_free = B.s_full + 2;
-  B.p_full = B.s_free + 2;
-  B.p_free = B.p_full + 2;
-  B.o_done = B.p_free + 2;
-  B.o_free = B.o_done + 1;
+  B.k_empty = B.k_full + kRingK;
+  B.v_full = B.k_empty + kRingK;
+  B.v_empty = B.v_full + kRingV;
+  B.s_full = B.v_empty + kRingV;
+  B.p_full = B.s_full + 2;
+  B.o_done = B.p_full + 2;
+  B.o_free = B.o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
+  int* list_count = reinterpret_cast<int*>(tmem_slot + 1);
+  int* list = reinterpret_cast<int*>(smem + kList);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kRingK; ++i) {
       mbar_init(&B.k_full[i], 1);
       mbar_init(&B.k_empty[i], 1);
+    }
+    for (int i = 0; i < kRingV; ++i) {
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_free[i], 128);
       mbar_init(&B.p_full[i], 128);
-      mbar_init(&B.p_free[i], 1);
+      mbar_init(&B.o_done[i], 1);
+      mbar_init(&B.o_free[i], 128);
     }
-    mbar_init(B.o_done, 1);
-    mbar_init(B.o_free, 128);
     fence_mbar_init();
+    // the rings are idle until the first load: scratch for the schedule
+    *list_count = build_schedule(p, reinterpret_cast<int*>(smem + kK), list, gridDim.x, blockIdx.x);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -163,46 +269,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  ItemSource src{list, *list_count};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ producers
+    // warp 0: Q and K tiles; warp 10: V tiles.  Each runs ahead as far as its ring allows.
     if (lane == 0) {
-      prefetch_tensor_map(&tm_q);
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      const int ring_n = is_k ? kRingK : kRingV;
+      uint64_t* full = is_k ? B.k_full : B.v_full;
+      uint64_t* empty = is_k ? B.k_empty : B.v_empty;
+      uint8_t* ring = smem + (is_k ? kK : kV);
+      if (is_k) prefetch_tensor_map(&tm_q);
+      prefetch_tensor_map(map);
       const uint64_t pol_kv = l2_policy_evict_last();  // reused by other tiles/heads
       const uint64_t pol_q = l2_policy_evict_first();
-      Cursor cur;
       uint32_t items = 0, tiles = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok; i += gridDim.x) {
-        const int tile = i / p.Hq, g = i - tile * p.Hq;
-        if (!cur.seek(p, tile)) break;
-        const Item it = make_item(p, cur, tile, g);
-        if (it.nkt == 0) continue;
-        ok = mbar_wait(B.q_empty, (items & 1) ^ 1, p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(B.q_full, kTileBytes);
-        tma_load_3d(smem + kQ, &tm_q, 0, it.g, it.tok0, B.q_full, pol_q);
-        tma_load_3d(smem + kQ + kBox, &tm_q, 64, it.g, it.tok0, B.q_full, pol_q);
+      Item it;
+      for (int r = 0; ok && src.get(p, r, it); ++r) {
+        if (it.nmax == 0) continue;
+        if (is_k) {
+          if (!(ok = mbar_wait(B.q_empty, (items & 1) ^ 1, p.status))) break;
+          mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
+          for (int t = 0; t < 2; ++t) {
+            tma_load_3d(smem + kQ + t * kTileBytes, &tm_q, 0, it.g, it.tok0 + t * 128, B.q_full, pol_q);
+            tma_load_3d(smem + kQ + t * kTileBytes + kBox, &tm_q, 64, it.g, it.tok0 + t * 128,
+                        B.q_full, pol_q);
+          }
+        }
         ++items;
         const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
-        for (int kt = 0; kt < it.nkt; ++kt, ++tiles) {
+        for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
           int page = __ldg(bt + kt);
           if (page < 0 || page >= p.num_pages) page = 0;  // sequence reported invalid
-          const int slot = tiles % kRing;
-          const uint32_t ph = ((tiles / kRing) & 1) ^ 1;
+          const int slot = tiles % ring_n;
           const int x = it.h * kHeadDim, y = page * kPage;
-          if (!(ok = mbar_wait(&B.k_empty[slot], ph, p.status))) break;
-          mbar_arrive_expect_tx(&B.k_full[slot], kTileBytes);
-          tma_load_2d(smem + kK + slot * kTileBytes, &tm_k, x, y, &B.k_full[slot], pol_kv);
-          tma_load_2d(smem + kK + slot * kTileBytes + kBox, &tm_k, x + 64, y, &B.k_full[slot],
-                      pol_kv);
-          if (!(ok = mbar_wait(&B.v_empty[slot], ph, p.status))) break;
-          mbar_arrive_expect_tx(&B.v_full[slot], kTileBytes);
-          tma_load_2d(smem + kV + slot * kTileBytes, &tm_v, x, y, &B.v_full[slot], pol_kv);
-          tma_load_2d(smem + kV + slot * kTileBytes + kBox, &tm_v, x + 64, y, &B.v_full[slot],
-                      pol_kv);
+          if (!(ok = mbar_wait(&empty[slot], ((tiles / ring_n) & 1) ^ 1, p.status))) break;
+          mbar_arrive_expect_tx(&full[slot], kTileBytes);
+          tma_load_2d(ring + slot * kTileBytes, map, x, y, &full[slot], pol_kv);
+          tma_load_2d(ring + slot * kTileBytes + kBox, map, x + 64, y, &full[slot], pol_kv);
         }
       }
     }
@@ -212,67 +319,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, 128, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, 128, false, true);
-      const uint32_t q_addr = smem_u32(smem + kQ);
-      Cursor cur;
       uint32_t items = 0, tiles = 0;
+      uint32_t gt[2] = {0, 0};     // key tiles each query tile has been through (all items)
+      uint32_t gitems[2] = {0, 0};  // items in which each query tile had key tiles
       bool ok = true;
-      // P.V for global tile index j (its P buffer j%2, its V ring slot j%kRing)
-      auto issue_pv = [&](uint32_t j, bool first_of_item) -> bool {
-        const int pb = j & 1, vs = j % kRing;
-        if (!mbar_wait(&B.p_full[pb], (j >> 1) & 1, p.status)) return false;
-        if (!mbar_wait(&B.v_full[vs], (j / kRing) & 1, p.status)) return false;
-        if (first_of_item && items > 1 && !mbar_wait(B.o_free, (items & 1), p.status))
-          return false;
-        tc_fence_after();
-        const uint32_t p_addr = smem_u32(smem + kP + pb * kTileBytes);
-        const uint32_t v_addr = smem_u32(smem + kV + vs * kTileBytes);
+      auto qk = [&](int t, uint32_t kidx) {
+        const uint32_t q_addr = smem_u32(smem + kQ + t * kTileBytes);
+        const uint32_t k_addr = smem_u32(smem + kK + (kidx % kRingK) * kTileBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = umma_sdesc_sw128(p_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_sdesc_sw128(v_addr + k * 2048, kBox, 1024);
-          umma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first_of_item && k == 0) ? 0u : 1u);
+          const uint64_t ad = umma_sdesc_sw128(q_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_sdesc_sw128(k_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + kColS + t * 128, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
-        umma_commit(&B.v_empty[vs]);
-        umma_commit(&B.p_free[pb]);
-        umma_commit(B.o_done);
+        umma_commit(&B.s_full[t]);
+      };
+      auto pv = [&](int t, uint32_t kidx, bool first) -> bool {
+        if (!mbar_wait(&B.p_full[t], gt[t] & 1, p.status)) return false;
+        if (!mbar_wait(&B.v_full[kidx % kRingV], (kidx / kRingV) & 1, p.status)) return false;
+        if (first && gitems[t] > 1 && !mbar_wait(&B.o_free[t], gitems[t] & 1, p.status))
+          return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + kV + (kidx % kRingV) * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t bd = umma_sdesc_sw128(v_addr + k * 2048, kBox, 1024);
+          umma_bf16_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + k * 8, bd, idesc_pv,
+                       (first && k == 0) ? 0u : 1u);
+        }
+        umma_commit(&B.o_done[t]);
+        ++gt[t];
         return true;
       };
-      for (int i = blockIdx.x; ok; i += gridDim.x) {
-        const int tile = i / p.Hq, g = i - tile * p.Hq;
-        if (!cur.seek(p, tile)) break;
-        const Item it = make_item(p, cur, tile, g);
-        if (it.nkt == 0) continue;
+      auto wait_k = [&](uint32_t kidx) -> bool {
+        const bool r = mbar_wait(&B.k_full[kidx % kRingK], (kidx / kRingK) & 1, p.status);
+        tc_fence_after();
+        return r;
+      };
+      Item it;
+      for (int r = 0; ok && src.get(p, r, it); ++r) {
+        if (it.nmax == 0) continue;
         if (!(ok = mbar_wait(B.q_full, items & 1, p.status))) break;
         ++items;
-        const uint32_t first = tiles;
-        for (int kt = 0; kt < it.nkt; ++kt, ++tiles) {
-          const int ks = tiles % kRing, sb = tiles & 1;
-          if (!(ok = mbar_wait(&B.k_full[ks], (tiles / kRing) & 1, p.status))) break;
-          if (!(ok = mbar_wait(&B.s_free[sb], ((tiles >> 1) & 1) ^ 1, p.status))) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + kK + ks * kTileBytes);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = umma_sdesc_sw128(q_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_sdesc_sw128(k_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
-            umma_bf16_ss(tmem + kColS + sb * 128, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+        for (int t = 0; t < 2; ++t) gitems[t] += it.nkt[t] > 0 ? 1u : 0u;
+        const uint32_t k0 = tiles;
+        if (!(ok = wait_k(k0))) break;
+        for (int t = 0; t < 2; ++t)
+          if (it.nkt[t] > 0) qk(t, k0);
+        umma_commit(&B.k_empty[k0 % kRingK]);
+        if (it.nmax == 1) umma_commit(B.q_empty);
+        for (int j = 0; j < it.nmax && ok; ++j) {
+          const uint32_t kidx = k0 + j;
+          const bool next = j + 1 < it.nmax;
+          bool k_ready = false;
+          if (j < it.nkt[0]) {
+            if (!(ok = pv(0, kidx, j == 0))) break;
+            if (j + 1 < it.nkt[0]) {
+              if (!(ok = wait_k(kidx + 1))) break;
+              k_ready = true;
+              qk(0, kidx + 1);
+            }
           }
-          umma_commit(&B.s_full[sb]);
-          umma_commit(&B.k_empty[ks]);
-          if (kt == it.nkt - 1) umma_commit(B.q_empty);
-          if (kt > 0 && !(ok = issue_pv(tiles - 1, tiles - 1 == first))) break;
+          if (j < it.nkt[1]) {
+            if (!(ok = pv(1, kidx, j == 0))) break;
+          }
+          umma_commit(&B.v_empty[kidx % kRingV]);
+          if (j + 1 < it.nkt[1]) {
+            if (!k_ready && !(ok = wait_k(kidx + 1))) break;
+            qk(1, kidx + 1);
+          }
+          if (next) {
+            umma_commit(&B.k_empty[(kidx + 1) % kRingK]);
+            if (j + 2 == it.nmax) umma_commit(B.q_empty);
+          }
         }
-        if (!ok) break;
-        if (!(ok = issue_pv(tiles - 1, tiles - 1 == first))) break;
+        tiles += it.nmax;
       }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax / epilogue
+    // ------------------------------------------------------------ softmax (query tile A or B)
+    const int qtile = (warp - 2) >> 2;       // 0: warps 2-5 (tile A), 1: warps 6-9 (tile B)
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int t = threadIdx.x - 64;          // 0..127 among softmax threads
+    const int t = (warp - 2 - 4 * qtile) * 32 + lane;  // 0..127 within the group
+    const uint32_t s_cols = tmem + lane_base + kColS + qtile * 128;
+    const uint32_t o_cols = tmem + lane_base + kColO + qtile * 128;
+    const float c = p.scale_log2;
     if (blockIdx.x == 0 && warp == 2 && p.status) {
       int sum = 0;
       for (int e = lane; e < p.B; e += 32) sum += max(__ldg(p.chunk_lens + e), 0);
@@ -280,13 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       if (lane == 0 && sum != p.T) atomicOr(p.status, PA_STATUS_BAD_TOKENS);
     }
-    Cursor cur;
-    uint32_t items = 0, tiles = 0;
+    uint32_t tiles = 0, gt = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok; i += gridDim.x) {
-      const int tile = i / p.Hq, g = i - tile * p.Hq;
-      if (!cur.seek(p, tile)) break;
-      const Item it = make_item(p, cur, tile, g);
+    Item it;
+    for (int r = 0; ok && src.get(p, r, it); ++r) {
+      const int nkt = it.nkt[qtile];
+      const uint32_t k0 = tiles;
+      if (it.nmax > 0) tiles += it.nmax;
       // sequence validity: lengths and every referenced block-table entry
       bool bad = !it.len_ok;
       if (!bad) {
@@ -299,48 +433,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bad = __any_sync(0xffffffffu, b);
       }
-      if (bad && t == 0 && it.qt == 0 && g == 0 && p.status)
+      if (bad && qtile == 0 && t == 0 && it.pair == 0 && it.g == 0 && p.status)
         atomicOr(p.status, it.len_ok ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
-      const int64_t tok = (int64_t)it.tok0 + row;
-      const bool row_out = row < it.nrows && tok < p.T;
-      if (it.nkt == 0) {
-        if (row_out) {
-          uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
-                         ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
-          for (int c = 0; c < (p.out_f32 ? 32 : 16); ++c)
-            reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
-        }
+      const int nrows = it.nrows[qtile];
+      const int64_t tok = (int64_t)it.tok0 + qtile * 128 + row;
+      const bool row_out = row < nrows && tok < p.T;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
+                     ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
+      if (nkt == 0) {
+        if (row_out)  // lengths invalid: zero rows
+          for (int cc = 0; cc < (p.out_f32 ? 32 : 16); ++cc)
+            reinterpret_cast<uint4*>(dst)[cc] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      ++items;
-      const int pos = it.prior + it.qt * 128 + min(row, it.nrows - 1);  // query position
+      const int pos = it.prior + it.pair * 256 + qtile * 128 + min(row, nrows - 1);  // query position
       const int last_page = (it.ctx - 1) / kPage;
       const int vtail = it.ctx % kPage;  // rows >= vtail of the last page are past the context
+      // the first P.V to read the last page zeroes its tail: tile A's if it reaches it
+      const bool zero_mine = vtail != 0 && nkt - 1 == last_page &&
+                             (qtile == 0 || it.nkt[0] - 1 != last_page);
       float m = -INFINITY, l = 0.f;
-      uint32_t first = tiles;
-      for (int kt = 0; kt < it.nkt; ++kt, ++tiles) {
-        const int sb = tiles & 1;
-        if (!(ok = mbar_wait_warp(&B.s_full[sb], (tiles >> 1) & 1, p.status))) break;
+      for (int kt = 0; kt < nkt; ++kt, ++gt) {
+        if (!(ok = mbar_wait_warp(&B.s_full[qtile], gt & 1, p.status))) break;
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + kColS + sb * 128 + c * 32, sr[c]);
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_cols + cc * 32, sr[cc]);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&B.s_free[sb]);
-        // scores in log2 units, causal mask only where the tile crosses pos
+        // causal mask only where the tile crosses pos: masked scores take no part
         const int key0 = kt * kPage;
-        const bool full = key0 + kPage - 1 <= pos;
-        float mx = -INFINITY;
+        const int nvis = min(max(pos - key0 + 1, 0), kPage);  // visible keys of this row
+        // row max of the visible raw scores (sign-flipped when the scale is negative)
+        const float sgn = c >= 0.f ? 1.f : -1.f;
+        auto row_max = [&](auto masked) -> float {
+          float mx8[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(sr[c][e]) * p.scale_log2;
-            if (!full && key0 + c * 32 + e > pos) x = -INFINITY;
-            sr[c][e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float sv = __uint_as_float(sr[cc][e]) * sgn;
+              if (decltype(masked)::value) sv = (cc * 32 + e < nvis) ? sv : -INFINITY;
+              mx8[e & 7] = fmaxf(mx8[e & 7], sv);
+            }
+          return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        };
+        // warp-uniform choice: the P store below is a .sync.aligned TMEM op
+        const bool diag = __any_sync(0xffffffffu, nvis < kPage);
+        const float mraw = diag ? row_max(std::true_type{}) : row_max(std::false_type{});
+        // max of c * s over the visible keys (-inf when none is visible)
+        const float mx = mraw == -INFINITY ? -INFINITY : mraw * (c * sgn);
         const float m_new = fmaxf(m, mx);
         bool rescale = false;
         float alpha = 1.f;
@@ -351,85 +495,94 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
           m = m_new;
         }
-        // P buffer sb is free once the P.V two tiles back has completed
-        if (!(ok = mbar_wait_warp(&B.p_free[sb], ((tiles >> 1) & 1) ^ 1, p.status))) break;
-        const uint32_t pbase = smem_u32(smem + kP + sb * kTileBytes) + row * 128;
-        float sum = 0.f;
+        const float m_use = m == -INFINITY ? 0.f : m;  // nothing visible yet: p = 0
+        float sum8[8];
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {  // 8 keys per 16-byte chunk
-          uint32_t w[4];
+        for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+        // P (BF16 pairs) over the first 64 columns of this tile's S buffer
+        auto write_p = [&](auto masked) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k0 = ch * 8 + 2 * e;
-            const float p0 = fast_exp2(__uint_as_float(sr[k0 >> 5][k0 & 31]) - m);
-            const float p1 = fast_exp2(__uint_as_float(sr[(k0 + 1) >> 5][(k0 + 1) & 31]) - m);
-            sum += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int k0e = cc * 32 + 2 * e;
+              float p0 = fast_exp2(fmaf(__uint_as_float(sr[cc][2 * e]), c, -m_use));
+              float p1 = fast_exp2(fmaf(__uint_as_float(sr[cc][2 * e + 1]), c, -m_use));
+              if (decltype(masked)::value) {
+                p0 = k0e < nvis ? p0 : 0.f;
+                p1 = k0e + 1 < nvis ? p1 : 0.f;
+              }
+              sum8[e & 7] += p0 + p1;
+              w[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(s_cols + cc * 16, w);
           }
-          sts128(pbase + (ch >> 3) * kBox + (((ch & 7) ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
-        }
+        };
+        if (diag) write_p(std::true_type{}); else write_p(std::false_type{});
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l = l * alpha + sum;
-        if (kt == it.nkt - 1 && kt == last_page && vtail != 0) {
+        if (zero_mine && kt == nkt - 1) {
           // zero V rows past the context in the last page before P.V reads them
-          const int vs = tiles % kRing;
-          if (!(ok = mbar_wait_warp(&B.v_full[vs], (tiles / kRing) & 1, p.status))) break;
-          const int r = vtail + t;
-          if (r < kPage) {
-            const uint32_t vb = smem_u32(smem + kV + vs * kTileBytes) + r * 128;
+          const uint32_t kidx = k0 + kt;
+          const int vs = kidx % kRingV;
+          if (!(ok = mbar_wait_warp(&B.v_full[vs], (kidx / kRingV) & 1, p.status))) break;
+          const int rr = vtail + t;
+          if (rr < kPage) {
+            const uint32_t vb = smem_u32(smem + kV + vs * kTileBytes) + rr * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
               sts128(vb + ch * 16, 0u, 0u, 0u, 0u);
               sts128(vb + kBox + ch * 16, 0u, 0u, 0u, 0u);
             }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-        if (rescale && tiles > first) {
-          // O holds P.V up to the previous tile: wait for it, then scale in place
-          if (!(ok = mbar_wait_warp(B.o_done, (tiles - 1) & 1, p.status))) break;
+        // warp-uniform: lanes that need no rescale take alpha = 1 (exact)
+        if (__any_sync(0xffffffffu, rescale) && kt > 0) {
+          // O holds P.V up to the previous key tile: wait for it, then scale
+          if (!(ok = mbar_wait_warp(&B.o_done[qtile], (gt - 1) & 1, p.status))) break;
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t orow[32];
-            tmem_ld32(tmem + lane_base + kColO + c * 32, orow);
+            tmem_ld32(o_cols + cc * 32, orow);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
-            tmem_st32(tmem + lane_base + kColO + c * 32, orow);
+            tmem_st32(o_cols + cc * 32, orow);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&B.p_full[sb]);
+        mbar_arrive(&B.p_full[qtile]);
       }
       if (!ok) break;
       // ---- epilogue: O / l for this row
-      if (!(ok = mbar_wait_warp(B.o_done, (tiles - 1) & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp(&B.o_done[qtile], (gt - 1) & 1, p.status))) break;
       tc_fence_after();
-      const float inv = l == 0.f ? 0.f : 1.f / l;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       // an invalid sequence may have read a substitute page: select zeros
       const uint32_t keep = bad ? 0u : 0xffffffffu;
-      uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
-                     ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t orow[32];
-        tmem_ld32(tmem + lane_base + kColO + c * 32, orow);
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o0[32];
+        tmem_ld32(o_cols + cc * 32, o0);
         tmem_wait_ld();
         if (row_out) {
           if (p.out_f32) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst) + c * 8;
+            uint4* d4 = reinterpret_cast<uint4*>(dst) + cc * 8;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              d4[e] = make_uint4(__float_as_uint(__uint_as_float(orow[4 * e]) * inv) & keep,
-                                 __float_as_uint(__uint_as_float(orow[4 * e + 1]) * inv) & keep,
-                                 __float_as_uint(__uint_as_float(orow[4 * e + 2]) * inv) & keep,
-                                 __float_as_uint(__uint_as_float(orow[4 * e + 3]) * inv) & keep);
+              d4[e] = make_uint4(__float_as_uint(__uint_as_float(o0[4 * e]) * inv) & keep,
+                                 __float_as_uint(__uint_as_float(o0[4 * e + 1]) * inv) & keep,
+                                 __float_as_uint(__uint_as_float(o0[4 * e + 2]) * inv) & keep,
+                                 __float_as_uint(__uint_as_float(o0[4 * e + 3]) * inv) & keep);
           } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst) + c * 4;
+            uint4* d4 = reinterpret_cast<uint4*>(dst) + cc * 4;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float* f = reinterpret_cast<const float*>(orow) + 8 * e;
+              const float* f = reinterpret_cast<const float*>(o0) + 8 * e;
               d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv) & keep,
                                  pack_bf16x2(f[2] * inv, f[3] * inv) & keep,
                                  pack_bf16x2(f[4] * inv, f[5] * inv) & keep,
@@ -439,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(B.o_free);
+      mbar_arrive(&B.o_free[qtile]);
     }
   }
   tc_fence_before();
@@ -456,11 +609,12 @@ cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream) {
   static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
+  static_assert(2 * kMaxCost * 4 <= kRingK * kTileBytes, "schedule scratch must fit the K ring");
   cudaError_t e =
       cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (tensor memory and shared memory are sized for one)
-  const int64_t max_items = ((int64_t)p.T / 128 + p.B) * p.Hq;
+  const int64_t max_items = ((int64_t)p.T / 256 + p.B) * p.Hq;
   const int grid = (int)(max_items < num_sms ? max_items : num_sms);
   if (grid < 1) return cudaSuccess;
   prefill_kernel<<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
