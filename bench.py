@@ -70,6 +70,8 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        import threading
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
@@ -77,16 +79,34 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        # nvidia-smi takes a moment to start: wait (bounded) for its first line
+        # so that short timed regions still get samples
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.skip = len(self.lines)
         return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
 
     def __exit__(self, *a):
         self.out = ""
         if self.proc:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.reader.join(timeout=5)
+            # the samples taken before the timed region started are dropped
+            # unless they are all there is
+            got = self.lines[self.skip:] or self.lines
+            self.out = "".join(got)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -188,8 +208,8 @@ def cpu_oracle_rate(case, seconds, rank0=True):
         if el >= seconds:
             break
     kv = KV_BYTES * done_rows / rows_total
-    sample = (f"{done_rows} of the {rows_total} (sequence, query head) rows of one step "
-              f"({done_rows / rows_total:.2f} steps), FP64, {nt} OpenMP threads, {el:.1f} s")
+    sample = (f"{done_rows} (sequence, query head) rows = {done_rows / rows_total:.2f} steps "
+              f"of the {rows_total}-row workload, FP64, {nt} OpenMP threads, {el:.1f} s")
     return kv / el / 1e9, nt, sample
 
 
@@ -379,7 +399,7 @@ def run_ours(args):
                    "kv_heads": HKV, "head_dim": D, "page_size": PAGE,
                    "kv_bytes_per_step": KV_BYTES, "num_splits": splits,
                    "step": "pa_kv_write (1 token/seq) + pa_decode (decode kernel + combine)",
-                   "l2": "inputs larger than L2 (2.147 GB K+V per step), no flush",
+                   "l2": f"inputs larger than L2 ({KV_BYTES / 1e9:.3f} GB K+V per step), no flush",
                    "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu"},
         "seqs_per_s": B * ws / (ms_per_step * 1e-3),
         "pct_hbm_peak": 100.0 * value / ws / hbm,
