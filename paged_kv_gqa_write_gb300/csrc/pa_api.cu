@@ -16,7 +16,7 @@ using pa::kHeadDim;
 using pa::kPage;
 
 constexpr int kMaxGroup = 16;    // query heads per KV head
-constexpr int kMaxGcPerCta = 8;  // query heads one decode CTA serves
+constexpr int kMaxGcPerCta = 16; // query heads one decode work item serves
 
 int check_dims(const pa_dims& d) {
   if (d.head_dim != kHeadDim) return PA_ERR_HEAD_DIM;
@@ -33,8 +33,8 @@ int check_dims(const pa_dims& d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Head groups per KV head so that each decode CTA serves at most 8 query heads:
-// the smallest divisor NG of G with G / NG <= 8.
+// Head groups per KV head so that each decode work item serves at most 16
+// query heads: the smallest divisor NG of G with G / NG <= 16.
 int head_groups(int G) {
   for (int ng = 1; ng <= G; ++ng)
     if (G % ng == 0 && G / ng <= kMaxGcPerCta) return ng;
@@ -160,6 +160,13 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, const pa_dims& d) {
                    kPage, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// q viewed as [B * Hq rows, 128 columns]: one item's gc query heads are gc
+// consecutive rows, loaded as two 64-column boxes with 128-byte swizzle.
+bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int gc) {
+  return encode_2d(map, q, kHeadDim, (uint64_t)d.num_seqs * d.num_q_heads, kHeadDim * 2, 64,
+                   (uint32_t)gc, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
 
 }  // namespace
@@ -272,8 +279,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   const int64_t items = (int64_t)splits * d.num_seqs * d.num_kv_heads * NG;
   if (items > INT32_MAX) return PA_ERR_DIMS;
 
-  CUtensorMap tm_k, tm_v;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+  CUtensorMap tm_k, tm_v, tm_q;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
+      !encode_q_decode_map(&tm_q, q, d, G / NG))
     return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p;
@@ -300,7 +308,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   p.num_items = (int32_t)items;
   p.out_f32 = out_dtype == PA_F32;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, p, G / NG, sms, st);
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
   if (e != cudaSuccess || splits == 1) return launch_result(e);
   pa::CombineParams c;
   c.part_o = p.part_o;
@@ -448,8 +456,9 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
     if (!scratch) return launch_result(e == cudaSuccess ? cudaErrorUnknown : e);
   }
 
-  CUtensorMap tm_k, tm_v;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+  CUtensorMap tm_k, tm_v, tm_q;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
+      !encode_q_decode_map(&tm_q, q, d, G / NG))
     return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p;
@@ -475,7 +484,7 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
   p.num_items = (int32_t)items;
   p.out_f32 = out_dtype == PA_F32;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, p, G / NG, sms, st);
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
   if (e != cudaSuccess || splits == 1) return launch_result(e);
   pa::CombineParams c;
   c.part_o = p.part_o;

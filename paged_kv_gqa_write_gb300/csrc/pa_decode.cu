@@ -1,4 +1,5 @@
-// pa_decode.cu -- paged GQA decode attention, flash-decoding split-K.
+// pa_decode.cu -- paged GQA decode attention, flash-decoding split-K, with the
+// two contractions on the 5th-generation tensor cores.
 //
 // Computes, for every sequence s and query head g (KV head h = g / G):
 //   out[s][g] = softmax(scale * q[s][g] . K_t) V_t over t < context_lens[s],
@@ -7,75 +8,87 @@
 // [page, token, kv_head, dim] K/V; "Qwen 3" TensorSharp doc, section 11: K/V
 // gathered per sequence from the block tables and sequence lengths).
 //
-// Design (GB300, HBM bound: every K/V byte is read once; about 5 flop/byte):
+// Design (GB300; HBM bound: every K/V byte is read once):
 //  * Persistent grid, one CTA per SM.  A work item is (split j, sequence s,
-//    KV head h, head group): a contiguous range of at most `pps` pages.  Items
-//    are dealt round-robin (item i -> CTA i mod grid); split boundaries depend
-//    only on logical positions, so results never depend on physical pages.
-//  * Page tiles stream through a 3-stage ring of 64 KB stages (K and V of one
-//    page); a TMA load takes about 3 us under full load, so two stages in
-//    flight per SM cover it (a load-only run of this ring reaches the device's
-//    copy bandwidth).  Large head groups use two stages, leaving room for
-//    their merge buffer.
-//  * Stager warp: runs up to two items ahead, converting each item's query
-//    heads to FP32 pre-multiplied by scale * log2 e, reading its context
-//    length and block-table entries (validity flag + sanitised page ids) into
-//    a 2-slot item ring.  TMA warp: one lane issues 2-D TMA loads (two 64-column
-//    boxes per tile, 128-byte swizzle, L2 evict-first) of K and V page tiles
-//    from those page ids.  Neither the TMA lane nor the consumers wait on
-//    global memory.
-//  * Eight consumer warps (two per SM sub-partition) share each page; warp w
-//    owns tokens 16w..16w+15.  Scores: lane (token, dim half) reads its 64
-//    dims of the K row once from shared memory and uses them for all GC query
-//    heads (the GQA saving), accumulating with packed FP32 FMAs
-//    (fma.rn.f32x2); one shuffle joins the halves.  Softmax: per-warp running
-//    max by shuffles, exp2, per-lane partial sums.  P.V: a half-warp per
-//    token, each lane owning 8 output dims; tokens past the context are
-//    skipped (a select keeps poisoned tail rows out: 0 * NaN would be NaN).
-//  * Item end: each warp publishes its (m, l, o) to shared memory and moves on
-//    to the next item; one warp (rotating with the item) merges the eight
-//    states in a fixed order and writes `out` (one split) or normalised
-//    partials (o, lse) for the combine kernel.
+//    KV head h, head group): a contiguous range of at most `pps` pages and the
+//    GC <= 16 query heads that share the KV head.  Items are dealt
+//    round-robin; split boundaries depend only on logical positions.
+//  * Per page the two products are transposed so that the 128 keys (or the
+//    128 head dims) fill the 128 rows of one tcgen05.mma and the query heads,
+//    padded to 16, are its N:
+//      S^T[key][g] = K[key][:] . Q[g][:]        (A = K tile, K-major)
+//      O^T[d][g]  += V[:][d] . P[g][:]          (A = V tile, MN-major)
+//    so the K/V tiles are read by the tensor core straight from the TMA ring
+//    (128-byte swizzle), and the FP32 pipes only run the softmax.
+//  * warp 0: validates each item's block-table range, TMA-loads the item's
+//    query heads (rows >= GC stay zero) and its K/V page tiles into a 3-stage
+//    ring of 64 KB (K and V complete on separate mbarriers, so QK^T starts
+//    while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
+//    in page order: QK^T(j), then P.V(j) once P(j) is in shared memory.
+//  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
+//    softmax in the log2 domain with a per-head reference max shared by the
+//    CTA.  The reference only moves when some score exceeds it by more than
+//    2^8 (one bar.red.or per page decides), which rescales O in TMEM; the
+//    first page of an item takes the exact max.  The warps agree through a
+//    small shared-memory exchange on mbarriers (bounded waits, no bar.sync).  P is rounded to BF16 and
+//    written transposed into a K-major operand; the row sums accumulate the
+//    rounded values, so the normalisation matches the weights the MMA used.
+//    V rows past the context in the last page are zeroed before P.V reads
+//    them (P is 0 there, but 0 * NaN is NaN).
+//  * warps 6-9, one thread per head dim: the epilogue of the previous item
+//    (O / l from TMEM, double-buffered) overlaps the next item's pages; it
+//    writes `out` (one split) or normalised partials (o, lse) for the combine.
 #include "pa_launch.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kTmaWarp = kConsumerWarps;
-constexpr int kStagerWarp = kConsumerWarps + 1;
-constexpr int kThreads = kConsumers + 64;
-constexpr int kTokPerWarp = kPage / kConsumerWarps;  // 16
-constexpr int kBoxBytes = 64 * 2 * kPage;     // 64 dims x 128 tokens of bf16 = 16 KB
-constexpr int kStageBytes = 4 * kBoxBytes;    // K lo, K hi, V lo, V hi of a page
-constexpr int kListMax = 64;                  // page ids staged per item
-constexpr int kSmemLimit = 232448;
+constexpr int kTmaWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
+constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
+constexpr int kThreads = 10 * 32;
+constexpr int kStages = 3;
+constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
+constexpr int kStageBytes = 4 * kBox;      // K lo, K hi, V lo, V hi of a page
+constexpr int kN = 16;                     // MMA N: query heads of an item, padded
+constexpr int kAtom = kN * 128;            // 16 rows x 128 bytes
+constexpr int kOpBytes = 2 * kAtom;        // Q or P operand: two 64-element atoms
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
-// q row: each 64-dim half padded to 68 floats so the two halves a warp reads
-// together fall in different shared-memory banks
-constexpr int kQHalf = 68;
-constexpr int kQRow = 2 * kQHalf;
 
-// Ring stages (64 KB each): three, or two when a large head group's merge
-// buffer needs the room.
-template <int GC>
-constexpr int stages_for() { return GC <= 5 ? 3 : 2; }
+// shared memory (offsets from a 1024-aligned base)
+constexpr int kRing = 0;
+constexpr int kQ = kRing + kStages * kStageBytes;  // [2] query operands (item slots)
+constexpr int kP = kQ + 2 * kOpBytes;              // [2] P operands
+constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][16]: softmax-warp exchange
+constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O buffer
+constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [2][4]: ctx, pg0, pg1, flag
+constexpr int kBars = kInfo + 2 * 4 * 4;
+constexpr int kNumBars = 3 * kStages + 2 * 2 + 1 + 6 * 2 + 1;
+constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
+constexpr int kSmemLimit = 232448;
+static_assert(kSmem <= kSmemLimit, "decode shared memory exceeds the per-CTA limit");
 
-template <int GC>
-struct Layout {
-  static constexpr int kStages = stages_for<GC>();
-  static constexpr int PS = 2 * ((GC + 1) & ~1);                 // p row: (p, p) pairs
-  static constexpr int q = kStages * kStageBytes;                // q [2][GC][kQRow] f32
-  static constexpr int info = q + 2 * GC * kQRow * 4;            // [2][2] int: flag, ctx
-  static constexpr int list = info + 16;                         // [2][kListMax] int
-  static constexpr int p = list + 2 * kListMax * 4;              // p_s [8][16][PS] f32
-  static constexpr int mml = p + kConsumerWarps * kTokPerWarp * PS * 4;  // m,l [8][GC][2]
-  static constexpr int mo = (mml + kConsumerWarps * GC * 2 * 4 + 15) & ~15;  // o [8][GC][128]
-  static constexpr int bars = mo + kConsumerWarps * GC * kHeadDim * 4;
-  static constexpr int kNumBars = 2 * kStages + 4 + 2;
-  static constexpr int total = bars + 8 * kNumBars;
-  static constexpr int alloc = total + 1024;                     // room to align to 1024 B
+// TMEM columns
+constexpr uint32_t kColS = 0;   // S^T: 16 columns
+constexpr uint32_t kColO = 16;  // O^T[2]: 16 columns each
+constexpr uint32_t kTmemCols = 64;
+
+struct Bars {
+  uint64_t* k_full;    // [kStages]
+  uint64_t* v_full;    // [kStages]
+  uint64_t* kv_empty;  // [kStages]
+  uint64_t* q_full;    // [2] item slot staged (info + query operand)
+  uint64_t* q_empty;   // [2] item slot read by every role, query operand used
+  uint64_t* s_full;    // S^T of the current page
+  uint64_t* p_full;    // [2]
+  uint64_t* p_free;    // [2]
+  uint64_t* o_full;    // [2] last P.V of the item done
+  uint64_t* o_free;    // [2] epilogue read O and (m, l)
+  uint64_t* ml_full;   // [2] (m, l) of the item published
+  uint64_t* x_full;    // [2] softmax-warp exchange slots (one arrival per warp)
+  uint64_t* mma_done;  // drain at exit
 };
 
 struct Item {
@@ -107,364 +120,467 @@ __device__ __forceinline__ Item decode_item(int i, const DecodeParams& p, int ct
   return it;
 }
 
-template <int GC>
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// NH: query-head columns the softmax and epilogue handle (8 or 16, >= GC).
+template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  using L = Layout<GC>;
-  constexpr int kStages = L::kStages;
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* empty = full + kStages;
-  uint64_t* ifull = empty + kStages;        // item slot staged
-  uint64_t* iempty = ifull + 2;             // item slot consumed
-  uint64_t* merge_ready = iempty + 2;       // all warps published their state
-  uint64_t* merge_free = merge_ready + 1;   // the merging warp has read it
-  float* q_ring = reinterpret_cast<float*>(smem + L::q);
-  int* info = reinterpret_cast<int*>(smem + L::info);
-  int* plist = reinterpret_cast<int*>(smem + L::list);
-  float* p_s = reinterpret_cast<float*>(smem + L::p);
-  float* m_ml = reinterpret_cast<float*>(smem + L::mml);
-  float* m_o = reinterpret_cast<float*>(smem + L::mo);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBars);
+  Bars B;
+  B.k_full = bar;
+  B.v_full = B.k_full + kStages;
+  B.kv_empty = B.v_full + kStages;
+  B.q_full = B.kv_empty + kStages;
+  B.q_empty = B.q_full + 2;
+  B.s_full = B.q_empty + 2;
+  B.p_full = B.s_full + 1;
+  B.p_free = B.p_full + 2;
+  B.o_full = B.p_free + 2;
+  B.o_free = B.o_full + 2;
+  B.ml_full = B.o_free + 2;
+  B.x_full = B.ml_full + 2;
+  B.mma_done = B.x_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
+  int* info = reinterpret_cast<int*>(smem + kInfo);
+  const int GC = p.G / p.NG;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init(&B.k_full[i], 1);
+      mbar_init(&B.v_full[i], 1);
+      mbar_init(&B.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ifull[i], 32);
-      mbar_init(&iempty[i], kConsumerWarps + 1);
+      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_empty[i], 1 + 4 + 4);  // MMA, 4 softmax warps, 4 epilogue warps
+      mbar_init(&B.p_full[i], 128);
+      mbar_init(&B.p_free[i], 1);
+      mbar_init(&B.o_full[i], 1);
+      mbar_init(&B.o_free[i], 128);
+      mbar_init(&B.ml_full[i], 1);
+      mbar_init(&B.x_full[i], 4);
     }
-    mbar_init(merge_ready, kConsumerWarps);
-    mbar_init(merge_free, 1);
+    mbar_init(B.s_full, 1);
+    mbar_init(B.mma_done, 1);
     fence_mbar_init();
   }
+  // query rows >= GC and unused P rows must read as zero: clear both operands
+  for (int o = threadIdx.x * 16; o < 4 * kOpBytes; o += kThreads * 16)
+    sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  if (warp == kStagerWarp) {
-    // ------------------------------------------------------------ stager warp
-    uint32_t n = 0;
-    for (int i = blockIdx.x; i < p.num_items; i += gridDim.x, ++n) {
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+      prefetch_tensor_map(&tm_q);
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t gp = 0, n = 0;
+    // per item slot: parity of its last use if that use loaded a query operand, else -1
+    int q_pending[2] = {-1, -1};
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
       const int slot = n & 1;
-      if (!mbar_wait_warp(&iempty[slot], ((n >> 1) & 1) ^ 1, p.status)) return;
+      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n >> 1) & 1) ^ 1, p.status))) break;
       const Item it = decode_item(i, p, __ldg(p.context_lens + item_seq(i, p)));
-      // query heads of the item -> FP32 * scale * log2(e); lane owns 4 dims
-      const int head0 = it.h * p.G + it.hg * GC;
-      const uint2* qg =
-          reinterpret_cast<const uint2*>(p.q + ((int64_t)it.s * p.Hq + head0) * kHeadDim);
-      float* qd = q_ring + slot * GC * kQRow + (lane >> 4) * kQHalf + (lane & 15) * 4;
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        const uint2 w = __ldg(qg + g * (kHeadDim / 4) + lane);
-        const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
-        *reinterpret_cast<float4*>(qd + g * kQRow) =
-            make_float4(a.x * p.scale_log2, a.y * p.scale_log2, b.x * p.scale_log2,
-                        b.y * p.scale_log2);
-      }
-      // validity of every page the item reads, and the sanitised page ids
       const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
       bool bad = false;
       for (int pg = it.pg0 + lane; pg < it.pg1; pg += 32) {
         const int pid = __ldg(bt + pg);
-        const bool inval = pid < 0 || pid >= p.num_pages;
-        bad |= inval;
-        if (pg - it.pg0 < kListMax) plist[slot * kListMax + pg - it.pg0] = inval ? 0 : pid;
+        bad |= pid < 0 || pid >= p.num_pages;
       }
-      bad = __any_sync(0xffffffffu, bad) || !it.ok;
+      bad = __any_sync(0xffffffffu, bad);
+      const int flag = !it.ok ? 2 : (bad ? 1 : 0);
+      const int npg = flag ? 0 : it.pg1 - it.pg0;
       if (lane == 0) {
-        info[2 * slot] = bad ? (it.ok ? 1 : 2) : 0;
-        info[2 * slot + 1] = it.ctx;
-      }
-      mbar_arrive(&ifull[slot]);
-    }
-    return;
-  }
-
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ TMA warp
-    if (lane == 0) {
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
-      const uint64_t pol = l2_policy_evict_first();
-      int rs = 0;
-      uint32_t rph = 0, n = 0;
-      for (int i = blockIdx.x; i < p.num_items; i += gridDim.x, ++n) {
-        const int slot = n & 1;
-        if (!mbar_wait(&ifull[slot], (n >> 1) & 1, p.status)) return;
-        const Item it = decode_item(i, p, info[2 * slot + 1]);
-        const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
-        const int x = it.h * kHeadDim;
-        for (int pg = it.pg0; pg < it.pg1; ++pg) {
-          int page;
-          if (pg - it.pg0 < kListMax) {
-            page = plist[slot * kListMax + pg - it.pg0];
-          } else {
-            page = __ldg(bt + pg);
-            if (page < 0 || page >= p.num_pages) page = 0;  // output is zeroed anyway
-          }
-          const int y = page * kPage;
-          if (!mbar_wait(&empty[rs], rph ^ 1, p.status)) return;
-          mbar_arrive_expect_tx(&full[rs], kStageBytes);
-          uint8_t* dst = smem + rs * kStageBytes;
-          tma_load_2d(dst, &tm_k, x, y, &full[rs], pol);
-          tma_load_2d(dst + kBoxBytes, &tm_k, x + 64, y, &full[rs], pol);
-          tma_load_2d(dst + 2 * kBoxBytes, &tm_v, x, y, &full[rs], pol);
-          tma_load_2d(dst + 3 * kBoxBytes, &tm_v, x + 64, y, &full[rs], pol);
-          if (++rs == kStages) { rs = 0; rph ^= 1; }
-        }
-        mbar_arrive(&iempty[slot]);
-      }
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int tq = lane & 15, dh = lane >> 4;    // scores: token of the warp's slice, dim half
-  const int half = lane >> 4, jd = lane & 15;  // P.V: token parity, 8-dim chunk
-  const uint32_t p_addr = smem_u32(p_s) + warp * kTokPerWarp * L::PS * 4;
-  int rs = 0;
-  uint32_t rph = 0, n = 0;
-
-  for (int i = blockIdx.x; i < p.num_items; i += gridDim.x, ++n) {
-    const int slot = n & 1;
-    if (!mbar_wait_warp(&ifull[slot], (n >> 1) & 1, p.status)) return;
-    const Item it = decode_item(i, p, info[2 * slot + 1]);
-    const int head0 = it.h * p.G + it.hg * GC;
-    const int flag = info[2 * slot];
-    const bool bad = flag != 0;
-    const uint32_t q_addr = smem_u32(q_ring + slot * GC * kQRow + dh * kQHalf);
-
-    float m[GC], l[GC];
-    float2 o[GC][4];
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) o[g][k] = make_float2(0.f, 0.f);
-    }
-
-    for (int pg = it.pg0; pg < it.pg1; ++pg) {
-      const int nvalid = min(max(it.ctx - pg * kPage - kTokPerWarp * warp, 0), kTokPerWarp);
-      // ---- K tile: scores, lane = (token t, dim half dh), 64 dims of row t
-      if (!mbar_wait_warp(&full[rs], rph, p.status)) return;
-      const uint32_t kb = smem_u32(smem + rs * kStageBytes);
-      float2 acc[GC];
-      if (nvalid > 0) {
-        const int t = kTokPerWarp * warp + tq;
-#pragma unroll
-        for (int g = 0; g < GC; ++g) acc[g] = make_float2(0.f, 0.f);
-        const uint32_t krow = kb + dh * kBoxBytes + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 kw = lds128(krow + ((c ^ (t & 7)) << 4));
-          const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-          const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
-#pragma unroll
-          for (int g = 0; g < GC; ++g) {
-            const float4 qa = lds128f(q_addr + (g * kQRow + c * 8) * 4);
-            const float4 qb = lds128f(q_addr + (g * kQRow + c * 8 + 4) * 4);
-            acc[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[g]);
-            acc[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[g]);
-            acc[g] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[g]);
-            acc[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[g]);
-          }
-        }
-      }
-      if (nvalid > 0) {
-        // ---- online softmax over the warp's 16 tokens (log2 domain)
-        const bool tv = tq < nvalid;
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-          float sc = acc[g].x + acc[g].y;
-          sc += __shfl_xor_sync(0xffffffffu, sc, 16);
-          sc = tv ? sc : -INFINITY;
-          float mx = sc;
-#pragma unroll
-          for (int off = 8; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          const float mn = fmaxf(m[g], mx);  // finite: nvalid > 0
-          const float pv = fast_exp2(sc - mn);
-          if (mn != m[g]) {  // warp-uniform
-            const float alpha = fast_exp2(m[g] - mn);
-            l[g] *= alpha;
-            const float2 aa = make_float2(alpha, alpha);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[g][k] = __fmul2_rn(o[g][k], aa);
-            m[g] = mn;
-          }
-          if (dh == 0) {
-            l[g] += pv;
-            *reinterpret_cast<float2*>(p_s + (warp * kTokPerWarp + tq) * L::PS + 2 * g) =
-                make_float2(pv, pv);
-          }
-        }
-        __syncwarp();
-      }
-      // ---- V tile: P.V, half-warp per token, lane owns dims 8*jd .. 8*jd+7
-      if (nvalid > 0) {
-        const uint32_t vrow = kb + 2 * kBoxBytes + (jd >> 3) * kBoxBytes;
-        const int jc = jd & 7;
-        auto pv_token = [&](int tl, bool active) {
-          const int tt = kTokPerWarp * warp + tl;
-          uint4 vw = lds128(vrow + tt * 128 + ((jc ^ (tt & 7)) << 4));
-          if (!active) vw = make_uint4(0u, 0u, 0u, 0u);
-          const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-          const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
-          float2 pr[L::PS / 2];
-#pragma unroll
-          for (int g2 = 0; g2 < L::PS / 2; g2 += 2) {
-            const float4 pq = lds128f(p_addr + (tl * L::PS + 2 * g2) * 4);
-            pr[g2] = make_float2(pq.x, pq.y);
-            pr[g2 + 1] = make_float2(pq.z, pq.w);
-          }
-#pragma unroll
-          for (int g = 0; g < GC; ++g) {
-            const float2 pp = pr[g];
-            o[g][0] = __ffma2_rn(pp, v0, o[g][0]);
-            o[g][1] = __ffma2_rn(pp, v1, o[g][1]);
-            o[g][2] = __ffma2_rn(pp, v2, o[g][2]);
-            o[g][3] = __ffma2_rn(pp, v3, o[g][3]);
-          }
-        };
-        if (nvalid == kTokPerWarp) {
-#pragma unroll
-          for (int tt = 0; tt < kTokPerWarp; tt += 2) pv_token(tt + half, true);
+        info[4 * slot] = it.ctx;
+        info[4 * slot + 1] = it.pg0;
+        info[4 * slot + 2] = it.pg0 + npg;
+        info[4 * slot + 3] = flag;
+        if (npg > 0) {
+          const int qrow = it.s * p.Hq + it.h * p.G + it.hg * GC;
+          uint8_t* qd = smem + kQ + slot * kOpBytes;
+          mbar_arrive_expect_tx(&B.q_full[slot], 2 * GC * 128);
+          tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
+          tma_load_2d(qd + kAtom, &tm_q, 64, qrow, &B.q_full[slot], pol);
+          q_pending[slot] = (int)((n >> 1) & 1);
         } else {
-          for (int tt = 0; tt < nvalid; tt += 2) {
-            const int tl = tt + half;
-            pv_token(min(tl, kTokPerWarp - 1), tl < nvalid);
-          }
+          mbar_arrive(&B.q_full[slot]);
+          q_pending[slot] = -1;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[rs]);  // page consumed
-      if (++rs == kStages) { rs = 0; rph ^= 1; }
-    }
-    if (lane == 0) mbar_arrive(&iempty[slot]);  // done with the item slot
-
-    // ---- publish this warp's state; one warp (rotating) merges while the
-    //      others move on to the next item
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-#pragma unroll
-      for (int off = 16; off; off >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[g][k].x += __shfl_xor_sync(0xffffffffu, o[g][k].x, 16);
-        o[g][k].y += __shfl_xor_sync(0xffffffffu, o[g][k].y, 16);
+      const int x = it.h * kHeadDim;
+      for (int c = 0; ok && c < npg; c += 32) {
+        const int pid_l = c + lane < npg ? __ldg(bt + it.pg0 + c + lane) : 0;
+        const int cnt = min(32, npg - c);
+        for (int k = 0; k < cnt; ++k) {
+          const int page = __shfl_sync(0xffffffffu, pid_l, k);
+          int lok = 1;
+          if (lane == 0) {
+            const int st = gp % kStages;
+            lok = mbar_wait(&B.kv_empty[st], ((gp / kStages) & 1) ^ 1, p.status);
+            if (lok) {
+              uint8_t* dst = smem + kRing + st * kStageBytes;
+              const int y = page * kPage;
+              mbar_arrive_expect_tx(&B.k_full[st], 2 * kBox);
+              tma_load_2d(dst, &tm_k, x, y, &B.k_full[st], pol);
+              tma_load_2d(dst + kBox, &tm_k, x + 64, y, &B.k_full[st], pol);
+              mbar_arrive_expect_tx(&B.v_full[st], 2 * kBox);
+              tma_load_2d(dst + 2 * kBox, &tm_v, x, y, &B.v_full[st], pol);
+              tma_load_2d(dst + 3 * kBox, &tm_v, x + 64, y, &B.v_full[st], pol);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, lok, 0) != 0;
+          if (!ok) break;
+          ++gp;
+        }
       }
     }
-    if (!mbar_wait_warp(merge_free, (n & 1) ^ 1, p.status)) return;  // previous merge read
-    if (half == 0) {
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        float4* dst = reinterpret_cast<float4*>(m_o + (warp * GC + g) * kHeadDim + jd * 8);
-        dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
-        dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
-      }
-    }
+    // drain: copies still in flight (only after a timeout elsewhere) must land
+    // before the CTA exits
     if (lane == 0) {
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        m_ml[(warp * GC + g) * 2] = m[g];
-        m_ml[(warp * GC + g) * 2 + 1] = l[g];
+      for (uint32_t g = gp > kStages ? gp - kStages : 0; g < gp; ++g) {
+        mbar_wait(&B.k_full[g % kStages], (g / kStages) & 1, nullptr);
+        mbar_wait(&B.v_full[g % kStages], (g / kStages) & 1, nullptr);
       }
+      for (int k = 0; k < 2; ++k)
+        if (q_pending[k] >= 0) mbar_wait(&B.q_full[k], (uint32_t)q_pending[k], nullptr);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(merge_ready);
-    if (warp == (int)(n % kConsumerWarps)) {
-      if (!mbar_wait_warp(merge_ready, n & 1, p.status)) return;
-      if (bad && lane == 0 && p.status)
-        atomicOr(p.status, flag == 1 ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
-      // lane owns dims 4*lane .. 4*lane+3 of every head of the group
-      float4 res[GC];
-      float lse[GC];
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        float mw[kConsumerWarps], M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          mw[w] = m_ml[(w * GC + g) * 2];
-          M = fmaxf(M, mw[w]);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = umma_idesc_bf16(128, kN, false, false);
+      const uint32_t idesc_pv = umma_idesc_bf16(128, kN, true, false);
+      uint32_t gp = 0, n = 0, nb = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+        const int slot = n & 1;
+        if (!(ok = mbar_wait(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+        const int npg = info[4 * slot + 2] - info[4 * slot + 1];
+        if (npg <= 0) {
+          mbar_arrive(&B.q_empty[slot]);
+          continue;
         }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float Lsum = 0.f;
-        if (M != -INFINITY) {
+        const int ob = nb & 1;
+        const uint32_t q_addr = smem_u32(smem + kQ + slot * kOpBytes);
+        for (int j = 0; j < npg; ++j, ++gp) {
+          const int st = gp % kStages;
+          const uint32_t ph = (gp / kStages) & 1;
+          if (!(ok = mbar_wait(&B.k_full[st], ph, p.status))) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float sw = fast_exp2(mw[w] - M);
-            Lsum = fmaf(m_ml[(w * GC + g) * 2 + 1], sw, Lsum);
-            const float4 ow =
-                *reinterpret_cast<const float4*>(m_o + (w * GC + g) * kHeadDim + 4 * lane);
-            acc.x = fmaf(ow.x, sw, acc.x);
-            acc.y = fmaf(ow.y, sw, acc.y);
-            acc.z = fmaf(ow.z, sw, acc.z);
-            acc.w = fmaf(ow.w, sw, acc.w);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
+          umma_commit(B.s_full);
+          if (j == npg - 1) umma_commit(&B.q_empty[slot]);
+          const int pb = gp & 1;
+          if (!(ok = mbar_wait(&B.p_full[pb], (gp >> 1) & 1, p.status))) break;
+          if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
+          if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
+          tc_fence_after();
+          const uint32_t v_addr = k_addr + 2 * kBox;
+          const uint32_t p_addr = smem_u32(smem + kP + pb * kOpBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
+            const uint64_t bd = umma_sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&B.kv_empty[st]);
+          umma_commit(&B.p_free[pb]);
         }
-        const bool zero = bad || Lsum == 0.f;
-        const float inv = zero ? 0.f : 1.f / Lsum;
-        res[g] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                      : make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        lse[g] = bad ? INFINITY : (Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY);
+        if (!ok) break;
+        umma_commit(&B.o_full[ob]);
+        ++nb;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(merge_free);  // shared state consumed into registers
-      const int64_t row0 = (int64_t)it.s * p.Hq + head0;
+      // every MMA this thread issued completes before TMEM is released
+      umma_commit(B.mma_done);
+      mbar_wait(B.mma_done, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ softmax, thread = key
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int key = quarter * 32 + lane;
+    const int wi = warp - kSoftWarp0;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float* xbuf = reinterpret_cast<float*>(smem + kX);
+    float* ml = reinterpret_cast<float*>(smem + kML);
+    const float c = p.scale_log2;
+    // P^T operand, K-major over keys: row g (head), 64-key atoms, 128-byte swizzle
+    const int kc = (key & 63) >> 3;
+    const uint32_t p_key = (uint32_t)((key >> 6) * kAtom + (key & 7) * 2);
+    // Exchange among the four softmax warps: lane 0 of each warp publishes up
+    // to 16 floats in slot (ex & 1) and arrives; every warp then waits (bounded)
+    // and reads all four rows.  A slot is rewritten two exchanges later, after
+    // every warp has arrived at the exchange in between (so has read it).
+    uint32_t ex = 0;
+    auto exchange = [&](const float (&v)[NH], int nv) -> const float* {
+      float* slot = xbuf + (ex & 1) * 4 * kN;
+      if (lane == 0) {
 #pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        const int64_t row = row0 + g;
-        if (p.S == 1) {
-          if (p.out_f32) {
-            reinterpret_cast<float4*>(p.out)[row * (kHeadDim / 4) + lane] = res[g];
-          } else {
-            uint2 u;
-            u.x = pack_bf16x2(res[g].x, res[g].y);
-            u.y = pack_bf16x2(res[g].z, res[g].w);
-            reinterpret_cast<uint2*>(p.out)[row * (kHeadDim / 4) + lane] = u;
+        for (int k = 0; k < NH; ++k)
+          if (k < nv) slot[wi * kN + k] = v[k];
+        mbar_arrive(&B.x_full[ex & 1]);
+      }
+      const bool r = mbar_wait_warp(&B.x_full[ex & 1], (ex >> 1) & 1, p.status);
+      ++ex;
+      return r ? slot : nullptr;
+    };
+    uint32_t gp = 0, n = 0, nb = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+      const int slot = n & 1;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+      const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+      const int npg = pg1 - pg0;
+      if (npg <= 0) continue;
+      const int ob = nb & 1;
+      float m[NH], ls[NH];
+#pragma unroll
+      for (int g = 0; g < NH; ++g) {
+        m[g] = -INFINITY;
+        ls[g] = 0.f;
+      }
+      for (int j = 0; j < npg; ++j, ++gp) {
+        const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
+        const bool kv = key < nvalid;
+        if (!(ok = mbar_wait_warp(B.s_full, gp & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t sr[16];
+        tmem_ld16(tmem + lane_base + kColS, sr);
+        tmem_wait_ld();
+        float d[NH];
+        bool need = j == 0;
+        if (!need) {
+          bool v = false;
+#pragma unroll
+          for (int g = 0; g < NH; ++g) {
+            d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
+            if (g < GC) v |= kv && d[g] > kRescaleThreshold;
           }
-        } else {
-          reinterpret_cast<float4*>(p.part_o)[(row * p.S + it.j) * (kHeadDim / 4) + lane] = res[g];
-          if (lane == 0) p.part_lse[row * p.S + it.j] = lse[g];
+          float vote[NH];
+          vote[0] = __any_sync(0xffffffffu, v) ? 1.f : 0.f;
+          const float* x = exchange(vote, 1);
+          if (!(ok = x != nullptr)) break;
+          need = (x[0] + x[kN]) + (x[2 * kN] + x[3 * kN]) > 0.f;  // uniform over the 4 warps
+        }
+        if (need) {
+          // exact per-head max of this page; the reference becomes max(m, it)
+          float wm[NH];
+#pragma unroll
+          for (int g = 0; g < NH; ++g)
+            wm[g] = g < GC ? warp_max(kv ? __uint_as_float(sr[g]) * c : -INFINITY) : 0.f;
+          const float* x = exchange(wm, GC);
+          if (!(ok = x != nullptr)) break;
+          float alpha[NH];
+#pragma unroll
+          for (int g = 0; g < NH; ++g) {
+            alpha[g] = 1.f;
+            if (g < GC) {
+              const float M = fmaxf(fmaxf(x[g], x[kN + g]), fmaxf(x[2 * kN + g], x[3 * kN + g]));
+              const float mn = fmaxf(m[g], M);  // finite: the page has a visible key
+              if (j > 0) alpha[g] = fast_exp2(m[g] - mn);
+              m[g] = mn;
+              ls[g] *= alpha[g];
+            }
+            d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
+          }
+          if (j > 0) {
+            // O^T holds P.V of the item's earlier pages: the commit that
+            // published S of this page came after the previous P.V finished
+            uint32_t orow[16];
+            const uint32_t o_cols = tmem + lane_base + kColO + ob * kN;
+            tmem_ld16(o_cols, orow);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < NH; ++g)
+              orow[g] = __float_as_uint(__uint_as_float(orow[g]) * alpha[g]);
+            tmem_st16(o_cols, orow);
+          }
+        }
+        // P(j) into the operand buffer P.V(j - 2) has finished reading
+        const int pb = gp & 1;
+        if (!(ok = mbar_wait_warp(&B.p_free[pb], ((gp >> 1) & 1) ^ 1, p.status))) break;
+        const uint32_t pbase = smem_u32(smem + kP + pb * kOpBytes) + p_key;
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          if (g < GC) {
+            const float pv = kv ? fast_exp2(d[g]) : 0.f;
+            const uint16_t pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+            ls[g] += __uint_as_float((uint32_t)pbf << 16);
+            sts16(pbase + (g >> 3) * 1024 + (g & 7) * 128 + ((kc ^ (g & 7)) << 4), pbf);
+          }
+        }
+        if (nvalid < kPage) {
+          // the sequence's last page: zero the V rows past the context
+          const int st = gp % kStages;
+          if (!(ok = mbar_wait_warp(&B.v_full[st], (gp / kStages) & 1, p.status))) break;
+          if (!kv) {
+            const uint32_t vr = smem_u32(smem + kRing + st * kStageBytes + 2 * kBox) + key * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              sts128(vr + ch * 16, 0u, 0u, 0u, 0u);
+              sts128(vr + kBox + ch * 16, 0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        if (need && j > 0) tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&B.p_full[pb]);
+      }
+      if (!ok) break;
+      // item end: row sums over the 128 keys, published with the max
+      float wl[NH];
+#pragma unroll
+      for (int g = 0; g < NH; ++g) wl[g] = g < GC ? warp_sum(ls[g]) : 0.f;
+      const float* x = exchange(wl, GC);
+      if (!(ok = x != nullptr)) break;
+      if (wi == 0) {
+        if (!(ok = mbar_wait_warp(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
+        if (lane < GC) {
+          float mm = 0.f;
+#pragma unroll
+          for (int g = 0; g < NH; ++g)
+            if (lane == g) mm = m[g];
+          ml[(ob * kN + lane) * 2] = mm;
+          ml[(ob * kN + lane) * 2 + 1] =
+              (x[lane] + x[kN + lane]) + (x[2 * kN + lane] + x[3 * kN + lane]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.ml_full[ob]);
+      }
+      ++nb;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue, thread = head dim
+    const int quarter = warp & 3;
+    const int dim = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float* ml = reinterpret_cast<const float*>(smem + kML);
+    uint32_t n = 0, nb = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+      const int slot = n & 1;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+      const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
+      const int flag = info[4 * slot + 3];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+      const Item it = decode_item(i, p, ctx);
+      const int64_t row0 = (int64_t)it.s * p.Hq + it.h * p.G + it.hg * GC;
+      float res[NH], lse[NH];
+      if (pg1 - pg0 <= 0) {
+        // nothing visible (lse -inf), or an invalid sequence (lse +inf: the
+        // combine zeroes the row)
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          res[g] = 0.f;
+          lse[g] = flag ? INFINITY : -INFINITY;
+        }
+        if (flag && warp == kEpiWarp0 && lane == 0 && p.status)
+          atomicOr(p.status, flag == 1 ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
+      } else {
+        const int ob = nb & 1;
+        if (!(ok = mbar_wait_warp(&B.ml_full[ob], (nb >> 1) & 1, p.status))) break;
+        if (!(ok = mbar_wait_warp(&B.o_full[ob], (nb >> 1) & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t orow[16];
+        tmem_ld16(tmem + lane_base + kColO + ob * kN, orow);
+        tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          const float mm = ml[(ob * kN + g) * 2], L = ml[(ob * kN + g) * 2 + 1];
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          res[g] = __uint_as_float(orow[g]) * inv;
+          lse[g] = L > 0.f ? (mm + __log2f(L)) * kLn2 : -INFINITY;
+        }
+        tc_fence_before();
+        mbar_arrive(&B.o_free[ob]);
+        ++nb;
+      }
+#pragma unroll
+      for (int g = 0; g < NH; ++g) {
+        if (g < GC) {
+          const int64_t row = row0 + g;
+          if (p.S == 1) {
+            if (p.out_f32)
+              reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[g];
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.out)[row * kHeadDim + dim] =
+                  __float2bfloat16_rn(res[g]);
+          } else {
+            p.part_o[(row * p.S + it.j) * kHeadDim + dim] = res[g];
+            if (dim == 0) p.part_lse[row * p.S + it.j] = lse[g];
+          }
         }
       }
     }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int GC>
-cudaError_t launch_gc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeParams& p,
-                      int num_sms, cudaStream_t stream) {
-  using L = Layout<GC>;
-  static_assert(L::alloc <= kSmemLimit, "decode shared memory exceeds the per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<GC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+template <int NH>
+cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
+                      const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  int grid = p.num_items < num_sms ? p.num_items : num_sms;
+  const int grid = p.num_items < num_sms ? p.num_items : num_sms;
   if (grid < 1) return cudaSuccess;
-  decode_kernel<GC><<<grid, kThreads, L::alloc, stream>>>(tm_k, tm_v, p);
+  decode_kernel<NH><<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                          const DecodeParams& p, int gc, int num_sms, cudaStream_t stream) {
-  switch (gc) {
-    case 1: return launch_gc<1>(tm_k, tm_v, p, num_sms, stream);
-    case 2: return launch_gc<2>(tm_k, tm_v, p, num_sms, stream);
-    case 3: return launch_gc<3>(tm_k, tm_v, p, num_sms, stream);
-    case 4: return launch_gc<4>(tm_k, tm_v, p, num_sms, stream);
-    case 5: return launch_gc<5>(tm_k, tm_v, p, num_sms, stream);
-    case 6: return launch_gc<6>(tm_k, tm_v, p, num_sms, stream);
-    case 7: return launch_gc<7>(tm_k, tm_v, p, num_sms, stream);
-    case 8: return launch_gc<8>(tm_k, tm_v, p, num_sms, stream);
-    default: return cudaErrorInvalidValue;
-  }
+                          const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
+                          cudaStream_t stream) {
+  if (gc < 1 || gc > kN) return cudaErrorInvalidValue;
+  return gc <= 8 ? launch_nh<8>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_nh<16>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace pa

@@ -85,7 +85,7 @@ def test_qwen3_32b_ragged_with_write(cuda_lib):
 EDGE = [1, 63, 64, 65, 127, 128, 129, 2051, 4096]
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (40, 8), (16, 16), (64, 8), (96, 8), (12, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (40, 8), (16, 16), (64, 8), (96, 8), (12, 2), (32, 2), (16, 1)])
 def test_edge_lengths_and_groups(cuda_lib, Hq, Hkv):
     case = W.custom_case(400 + Hq, EDGE, Hq=Hq, Hkv=Hkv, max_pages_per_seq=32)
     for splits in (0, 1, 5):
