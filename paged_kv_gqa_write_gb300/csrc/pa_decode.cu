@@ -20,10 +20,11 @@
 //      O^T[d][g]  += V[:][d] . P[g][:]          (A = V tile, MN-major)
 //    so the K/V tiles are read by the tensor core straight from the TMA ring
 //    (128-byte swizzle), and the FP32 pipes only run the softmax.
-//  * warp 0: validates each item's block-table range, TMA-loads the item's
-//    query heads (rows >= GC stay zero) and its K/V page tiles into a 3-stage
-//    ring of 64 KB (K and V complete on separate mbarriers, so QK^T starts
-//    while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
+//  * warp 0: validates each item's block-table range (the next item's
+//    metadata is loaded while the current item's pages are issued), stages
+//    up to four items ahead, TMA-loads each item's query heads (rows >= GC
+//    stay zero) and its K/V page tiles into a 3-stage ring of 64 KB (K and V
+//    complete on separate mbarriers, so QK^T starts while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
 //    in page order: QK^T(j), then P.V(j) once P(j) is in shared memory.
 //  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
 //    softmax in the log2 domain with a per-head reference max shared by the
@@ -49,6 +50,7 @@ constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
 constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
 constexpr int kThreads = 10 * 32;
 constexpr int kStages = 3;
+constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
 constexpr int kStageBytes = 4 * kBox;      // K lo, K hi, V lo, V hi of a page
 constexpr int kN = 16;                     // MMA N: query heads of an item, padded
@@ -59,13 +61,13 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 // shared memory (offsets from a 1024-aligned base)
 constexpr int kRing = 0;
-constexpr int kQ = kRing + kStages * kStageBytes;  // [2] query operands (item slots)
-constexpr int kP = kQ + 2 * kOpBytes;              // [2] P operands
-constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][16]: softmax-warp exchange
+constexpr int kQ = kRing + kStages * kStageBytes;  // [kSlots] query operands
+constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
+constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax-warp exchange
 constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O buffer
-constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [2][4]: ctx, pg0, pg1, flag
-constexpr int kBars = kInfo + 2 * 4 * 4;
-constexpr int kNumBars = 3 * kStages + 2 * 2 + 1 + 6 * 2 + 1;
+constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][4]: ctx, pg0, pg1, flag
+constexpr int kBars = kInfo + kSlots * 4 * 4;
+constexpr int kNumBars = 3 * kStages + 2 * kSlots + 2 + 4 * 2 + 1;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 constexpr int kSmemLimit = 232448;
 static_assert(kSmem <= kSmemLimit, "decode shared memory exceeds the per-CTA limit");
@@ -79,11 +81,10 @@ struct Bars {
   uint64_t* k_full;    // [kStages]
   uint64_t* v_full;    // [kStages]
   uint64_t* kv_empty;  // [kStages]
-  uint64_t* q_full;    // [2] item slot staged (info + query operand)
-  uint64_t* q_empty;   // [2] item slot read by every role, query operand used
+  uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
+  uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
   uint64_t* s_full;    // S^T of the current page
-  uint64_t* p_full;    // [2]
-  uint64_t* p_free;    // [2]
+  uint64_t* p_full;    // P of the current page
   uint64_t* o_full;    // [2] last P.V of the item done
   uint64_t* o_free;    // [2] epilogue read O and (m, l)
   uint64_t* ml_full;   // [2] (m, l) of the item published
@@ -147,11 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.v_full = B.k_full + kStages;
   B.kv_empty = B.v_full + kStages;
   B.q_full = B.kv_empty + kStages;
-  B.q_empty = B.q_full + 2;
-  B.s_full = B.q_empty + 2;
+  B.q_empty = B.q_full + kSlots;
+  B.s_full = B.q_empty + kSlots;
   B.p_full = B.s_full + 1;
-  B.p_free = B.p_full + 2;
-  B.o_full = B.p_free + 2;
+  B.o_full = B.p_full + 1;
   B.o_free = B.o_full + 2;
   B.ml_full = B.o_free + 2;
   B.x_full = B.ml_full + 2;
@@ -167,22 +167,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       mbar_init(&B.q_full[i], 1);
       mbar_init(&B.q_empty[i], 1 + 4 + 4);  // MMA, 4 softmax warps, 4 epilogue warps
-      mbar_init(&B.p_full[i], 128);
-      mbar_init(&B.p_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&B.o_full[i], 1);
       mbar_init(&B.o_free[i], 128);
       mbar_init(&B.ml_full[i], 1);
       mbar_init(&B.x_full[i], 4);
     }
     mbar_init(B.s_full, 1);
+    mbar_init(B.p_full, 128);
     mbar_init(B.mma_done, 1);
     fence_mbar_init();
   }
-  // query rows >= GC and unused P rows must read as zero: clear both operands
-  for (int o = threadIdx.x * 16; o < 4 * kOpBytes; o += kThreads * 16)
+  // query rows >= GC and unused P rows must read as zero: clear the operands
+  for (int o = threadIdx.x * 16; o < (kSlots + 1) * kOpBytes; o += kThreads * 16)
     sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
@@ -202,23 +203,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensor_map(&tm_q);
     }
     const uint64_t pol = l2_policy_evict_first();
+    const int U = p.B * p.Hkv * p.NG;
+    // Metadata of the next item, loaded while the current item's pages are
+    // issued: its context length and this lane's block-table entry among the
+    // first 32 pages of its range.
+    int nx_ctx = 0, nx_pid = 0;
+    auto prefetch = [&](int ii) {
+      if (ii < p.num_items) {
+        const int s = item_seq(ii, p);
+        nx_ctx = __ldg(p.context_lens + s);
+        const int pg = (ii / U) * p.pps + lane;
+        nx_pid = pg < p.max_pages ? __ldg(p.block_table + (int64_t)s * p.max_pages + pg) : 0;
+      }
+    };
+    prefetch(blockIdx.x);
     uint32_t gp = 0, n = 0;
     // per item slot: parity of its last use if that use loaded a query operand, else -1
-    int q_pending[2] = {-1, -1};
+    int q_pending[kSlots];
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) q_pending[k] = -1;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
-      const int slot = n & 1;
-      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n >> 1) & 1) ^ 1, p.status))) break;
-      const Item it = decode_item(i, p, __ldg(p.context_lens + item_seq(i, p)));
+      const int pid0 = nx_pid;
+      const Item it = decode_item(i, p, nx_ctx);
       const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
-      bool bad = false;
-      for (int pg = it.pg0 + lane; pg < it.pg1; pg += 32) {
+      bool bad = it.pg0 + lane < it.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
+      for (int pg = it.pg0 + 32 + lane; pg < it.pg1; pg += 32) {
         const int pid = __ldg(bt + pg);
         bad |= pid < 0 || pid >= p.num_pages;
       }
       bad = __any_sync(0xffffffffu, bad);
       const int flag = !it.ok ? 2 : (bad ? 1 : 0);
       const int npg = flag ? 0 : it.pg1 - it.pg0;
+      prefetch(i + gridDim.x);
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
       if (lane == 0) {
         info[4 * slot] = it.ctx;
         info[4 * slot + 1] = it.pg0;
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&B.q_full[slot], 2 * GC * 128);
           tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
           tma_load_2d(qd + kAtom, &tm_q, 64, qrow, &B.q_full[slot], pol);
-          q_pending[slot] = (int)((n >> 1) & 1);
+          q_pending[slot] = (int)((n / kSlots) & 1);
         } else {
           mbar_arrive(&B.q_full[slot]);
           q_pending[slot] = -1;
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int x = it.h * kHeadDim;
       for (int c = 0; ok && c < npg; c += 32) {
-        const int pid_l = c + lane < npg ? __ldg(bt + it.pg0 + c + lane) : 0;
+        const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + it.pg0 + c + lane) : 0);
         const int cnt = min(32, npg - c);
         for (int k = 0; k < cnt; ++k) {
           const int page = __shfl_sync(0xffffffffu, pid_l, k);
@@ -270,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&B.k_full[g % kStages], (g / kStages) & 1, nullptr);
         mbar_wait(&B.v_full[g % kStages], (g / kStages) & 1, nullptr);
       }
-      for (int k = 0; k < 2; ++k)
+      for (int k = 0; k < kSlots; ++k)
         if (q_pending[k] >= 0) mbar_wait(&B.q_full[k], (uint32_t)q_pending[k], nullptr);
     }
     __syncwarp();
@@ -282,8 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gp = 0, n = 0, nb = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
-        const int slot = n & 1;
-        if (!(ok = mbar_wait(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+        const int slot = n % kSlots;
+        if (!(ok = mbar_wait(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
         const int npg = info[4 * slot + 2] - info[4 * slot + 1];
         if (npg <= 0) {
           mbar_arrive(&B.q_empty[slot]);
@@ -305,13 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(B.s_full);
           if (j == npg - 1) umma_commit(&B.q_empty[slot]);
-          const int pb = gp & 1;
-          if (!(ok = mbar_wait(&B.p_full[pb], (gp >> 1) & 1, p.status))) break;
+          if (!(ok = mbar_wait(B.p_full, gp & 1, p.status))) break;
           if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
           if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
           tc_fence_after();
           const uint32_t v_addr = k_addr + 2 * kBox;
-          const uint32_t p_addr = smem_u32(smem + kP + pb * kOpBytes);
+          const uint32_t p_addr = smem_u32(smem + kP);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
@@ -319,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&B.kv_empty[st]);
-          umma_commit(&B.p_free[pb]);
         }
         if (!ok) break;
         umma_commit(&B.o_full[ob]);
@@ -362,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gp = 0, n = 0, nb = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
-      const int slot = n & 1;
-      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
       const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
@@ -433,10 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(o_cols, orow);
           }
         }
-        // P(j) into the operand buffer P.V(j - 2) has finished reading
-        const int pb = gp & 1;
-        if (!(ok = mbar_wait_warp(&B.p_free[pb], ((gp >> 1) & 1) ^ 1, p.status))) break;
-        const uint32_t pbase = smem_u32(smem + kP + pb * kOpBytes) + p_key;
+        // P(j) into the operand: P.V(j - 1) has finished reading it (it completed
+        // before the commit that published S of this page)
+        const uint32_t pbase = smem_u32(smem + kP) + p_key;
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
           if (g < GC) {
@@ -462,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         if (need && j > 0) tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&B.p_full[pb]);
+        mbar_arrive(B.p_full);
       }
       if (!ok) break;
       // item end: row sums over the 128 keys, published with the max
@@ -496,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0, nb = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
-      const int slot = n & 1;
-      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n >> 1) & 1, p.status))) break;
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
       const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
       const int flag = info[4 * slot + 3];
       __syncwarp();
