@@ -39,7 +39,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="0: automatic, -1: page-balanced, >= 1: fixed splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -294,7 +295,11 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = W.qwen3_14b_decode_b128(device=dev, with_new=True, pool_device=dev, batch=B)
     dims = pa.make_dims(B, HQ, HKV, case.num_pages, case.max_pages_per_seq)
-    splits = args.num_splits if args.num_splits > 0 else pa.pa_decode_auto_splits(dims)
+    # schedule: fixed split count >= 1, or 0 / PA_SPLITS_BALANCED for page-balanced
+    splits = args.num_splits if args.num_splits != 0 else pa.pa_decode_auto_splits(dims)
+    balanced = splits in (0, pa.PA_SPLITS_BALANCED)
+    if balanced:
+        splits = pa.PA_SPLITS_BALANCED
     ws_bytes = pa.pa_decode_workspace_size(dims, splits)
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
@@ -332,7 +337,8 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(start.elapsed_time(end), ws)
     ms_per_step = elapsed_ms / args.steps
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
-    launches_per_step = 2 + (1 if splits > 1 else 0)
+    # kv_write + decode, + a combine for the balanced schedule or fixed splits > 1
+    launches_per_step = 2 + (1 if (balanced or splits > 1) else 0)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     hq = case.q.cpu().pin_memory()
@@ -397,7 +403,8 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "context_len": CTX, "q_heads": HQ,
                    "kv_heads": HKV, "head_dim": D, "page_size": PAGE,
-                   "kv_bytes_per_step": KV_BYTES, "num_splits": splits,
+                   "kv_bytes_per_step": KV_BYTES,
+                   "schedule": "page-balanced" if balanced else f"{splits} fixed splits",
                    "step": "pa_kv_write (1 token/seq) + pa_decode (decode kernel + combine)",
                    "l2": f"inputs larger than L2 ({KV_BYTES / 1e9:.3f} GB K+V per step), no flush",
                    "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu"},

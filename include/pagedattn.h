@@ -102,6 +102,11 @@ typedef struct pa_dims {
  * token offsets are built in shared memory). */
 #define PA_MAX_CHUNKED_SEQS 16384
 
+/* num_splits value for pa_decode's page-balanced schedule (see pa_decode). */
+#define PA_SPLITS_BALANCED (-1)
+/* Largest batch the page-balanced schedule takes. */
+#define PA_BALANCED_MAX_SEQS 512
+
 /*
  * pa_kv_write -- copy the new tokens' K and V rows into their cache slots.
  *   k_new, v_new   bf16 [num_tokens, Hkv, D], token-major in sequence order
@@ -127,11 +132,22 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
  *                  pa_decode_workspace_size(dims, num_splits) bytes; may be
  *                  NULL when that size is 0.  Caller-owned; contents need no
  *                  initialisation and are overwritten.
- *   num_splits     how many KV ranges each sequence's pages are divided into
- *                  (1..max_pages_per_seq), or 0 to let the library choose
- *                  from the shape and the device's SM count.  With one split
- *                  the kernel writes `out` directly; otherwise it writes
- *                  partials to the workspace and runs the pa_combine kernel.
+ *   num_splits     the work schedule:
+ *                  1..max_pages_per_seq: fixed splits -- each sequence's pages
+ *                    are divided into that many equal KV ranges, dealt to the
+ *                    SMs round-robin.  With one split the kernel writes `out`
+ *                    directly; otherwise it writes partials to the workspace
+ *                    and runs the pa_combine kernel.
+ *                  PA_SPLITS_BALANCED: page-balanced -- the SMs form groups
+ *                    of one SM per KV head; the sequences' pages, laid end to
+ *                    end, are divided evenly among the groups, so every SM
+ *                    reads the same number of pages and the SMs of a group
+ *                    read the same pages together.  The few sequences cut
+ *                    between two groups are merged by a combine kernel.  This
+ *                    balances ragged batches.  B <= PA_BALANCED_MAX_SEQS and
+ *                    at least two groups must fit on the device.
+ *                  0: the library chooses from the shape and the device's SM
+ *                    count (pa_decode_auto_splits).
  * The result depends only on logical positions, never on which physical
  * pages hold them: the same inputs under a permuted pool and rewritten block
  * table give bit-identical output.
@@ -146,8 +162,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * (size_t)-1 for invalid dims. */
 size_t pa_decode_workspace_size(pa_dims dims, int32_t num_splits);
 
-/* The split count pa_decode uses for num_splits == 0 on the current device
- * (>= 1), or a negative PA_ERR_* for invalid dims. */
+/* The schedule pa_decode uses for num_splits == 0 on the current device: a
+ * split count >= 1, or 0 for the page-balanced schedule; a negative PA_ERR_*
+ * for invalid dims. */
 int32_t pa_decode_auto_splits(pa_dims dims);
 
 /*
@@ -197,8 +214,9 @@ int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, v
  * PA_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library; every GPU that loads
  * the library holds that array until the process exits.  A call whose split
  * count (num_splits, or the automatic choice for 0) needs more scratch than
- * that -- (B * Hq * splits * 516 bytes, rounded up) -- returns
- * PA_ERR_NOALLOC_TOO_LARGE without launching; num_splits = 1 needs none.
+ * that -- (B * Hq * splits * 516 bytes, rounded up; the page-balanced
+ * schedule needs about 2.6 MB) -- returns PA_ERR_NOALLOC_TOO_LARGE without
+ * launching; num_splits = 1 needs none.
  *
  * Setup: the first call made with a given device current looks up the
  * array's device address on that device (cudaGetSymbolAddress) and caches it;

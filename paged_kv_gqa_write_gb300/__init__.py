@@ -21,6 +21,11 @@ PAGE_SIZE = 128
 PA_BF16, PA_F32 = 0, 1
 PA_STATUS_BAD_PAGE, PA_STATUS_BAD_LENGTH, PA_STATUS_BAD_TOKENS, PA_STATUS_TIMEOUT = 1, 2, 4, 8
 PA_MAX_CHUNKED_SEQS = 16384
+PA_SPLITS_BALANCED = -1
+PA_BALANCED_MAX_SEQS = 512
+(PA_ERR_NULL_POINTER, PA_ERR_HEAD_DIM, PA_ERR_PAGE_SIZE, PA_ERR_HEADS, PA_ERR_DIMS,
+ PA_ERR_ALIGNMENT, PA_ERR_OUT_DTYPE, PA_ERR_WORKSPACE, PA_ERR_SPLITS, PA_ERR_TOO_MANY_SEQS,
+ PA_ERR_TENSOR_MAP, PA_ERR_NO_DEVICE, PA_ERR_NOALLOC_TOO_LARGE) = range(-1, -14, -1)
 
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
@@ -146,7 +151,7 @@ def pa_kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk
 def pa_decode_workspace_size(dims, num_splits=0) -> int:
     n = int(load().pa_decode_workspace_size(dims, int(num_splits)))
     if n == (1 << 64) - 1:
-        raise ValueError("invalid dims for pa_decode_workspace_size")
+        raise ValueError("invalid dims or schedule for pa_decode_workspace_size")
     return n
 
 

@@ -105,6 +105,61 @@ size_t workspace_bytes_for(const pa_dims& d, int splits) {
   return align256(rows * splits * kHeadDim * sizeof(float)) + align256(rows * splits * sizeof(float));
 }
 
+// Partial records of the page-balanced schedule: two per decode CTA, 16 head
+// slots of 128 floats plus the lse.
+size_t balanced_ws_bytes(int grid) {
+  return align256((size_t)2 * grid * 16 * kHeadDim * sizeof(float)) +
+         align256((size_t)2 * grid * 16 * sizeof(float));
+}
+
+// Units (KV head x head group) per sequence; the page-balanced schedule runs
+// groups of that many CTAs.
+int units_per_seq(const pa_dims& d) {
+  return d.num_kv_heads * head_groups(d.num_q_heads / d.num_kv_heads);
+}
+
+bool balanced_ok(const pa_dims& d, int num_sms) {
+  return d.num_seqs <= PA_BALANCED_MAX_SEQS && num_sms / units_per_seq(d) >= 2;
+}
+
+// The schedule num_splits == 0 selects: 0 for the page-balanced schedule
+// (every batch it accepts), else the fixed split count of auto_splits.
+int auto_schedule(const pa_dims& d, int num_sms) {
+  return balanced_ok(d, num_sms) ? 0 : auto_splits(d, num_sms);
+}
+
+struct DecodePlan {
+  bool balanced;
+  int splits, pps;  // fixed splits
+  int grid;         // page-balanced: CTAs
+  size_t ws_bytes;
+};
+
+// Resolves num_splits (>= PA_SPLITS_BALANCED) for valid dims with num_seqs > 0;
+// false when the request cannot be served.
+bool make_plan(const pa_dims& d, int num_splits, int num_sms, DecodePlan* pl) {
+  const int req = num_splits == 0 ? auto_schedule(d, num_sms) : num_splits;
+  if (req == 0 || req == PA_SPLITS_BALANCED) {
+    if (!balanced_ok(d, num_sms)) return false;
+    const int ups = units_per_seq(d);
+    const int64_t most = (int64_t)d.num_seqs * d.max_pages_per_seq;  // pages at most
+    int64_t groups = num_sms / ups;
+    if (groups > most) groups = most < 1 ? 1 : most;
+    pl->balanced = true;
+    pl->splits = 1;
+    pl->pps = d.max_pages_per_seq;
+    pl->grid = (int)groups * ups;
+    pl->ws_bytes = balanced_ws_bytes(pl->grid);
+    return true;
+  }
+  if (req < 1) return false;
+  pl->balanced = false;
+  split_shape(d, req, &pl->splits, &pl->pps);
+  pl->grid = 0;
+  pl->ws_bytes = workspace_bytes_for(d, pl->splits);
+  return true;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -169,11 +224,84 @@ bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int 
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
 
+// Shared tail of pa_decode and pa_decode_noalloc: arguments are checked and
+// `ws` holds at least pl.ws_bytes (or is unused when that is 0).
+int run_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
+               int32_t out_dtype, uint8_t* ws, const DecodePlan& pl, const pa_dims& d,
+               int32_t* status, int sms, cudaStream_t st) {
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int NG = head_groups(G);
+  const int64_t items = (int64_t)pl.splits * d.num_seqs * d.num_kv_heads * NG;
+  if (items > INT32_MAX) return PA_ERR_DIMS;
+  CUtensorMap tm_k, tm_v, tm_q;
+  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
+      !encode_q_decode_map(&tm_q, q, d, G / NG))
+    return PA_ERR_TENSOR_MAP;
+
+  pa::DecodeParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.out = out;
+  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  const bool fixed_parts = !pl.balanced && pl.splits > 1;
+  p.part_o = fixed_parts ? reinterpret_cast<float*>(ws) : nullptr;
+  p.part_lse = fixed_parts ? reinterpret_cast<float*>(ws + align256(rows * pl.splits * kHeadDim * 4))
+                           : nullptr;
+  p.status = status;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = d.num_seqs;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = G;
+  p.NG = NG;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  p.pps = pl.pps;
+  p.S = pl.splits;
+  p.num_items = (int32_t)items;
+  p.out_f32 = out_dtype == PA_F32;
+  p.balanced = pl.balanced ? 1 : 0;
+  p.grid = pl.grid;
+  p.bal_o = pl.balanced ? reinterpret_cast<float*>(ws) : nullptr;
+  p.bal_lse = pl.balanced ? reinterpret_cast<float*>(
+                                ws + align256((size_t)2 * pl.grid * 16 * kHeadDim * sizeof(float)))
+                          : nullptr;
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
+  if (e != cudaSuccess) return launch_result(e);
+  if (pl.balanced) {
+    pa::BalCombineParams c;
+    c.context_lens = context_lens;
+    c.bal_o = p.bal_o;
+    c.bal_lse = p.bal_lse;
+    c.out = out;
+    c.B = d.num_seqs;
+    c.Hq = d.num_q_heads;
+    c.G = G;
+    c.NG = NG;
+    c.GC = G / NG;
+    c.max_pages = d.max_pages_per_seq;
+    c.grid = pl.grid;
+    c.out_f32 = p.out_f32;
+    return launch_result(pa::launch_bal_combine(c, st));
+  }
+  if (pl.splits == 1) return PA_OK;
+  pa::CombineParams c;
+  c.part_o = p.part_o;
+  c.part_lse = p.part_lse;
+  c.out = out;
+  c.rows = (int32_t)rows;
+  c.S = pl.splits;
+  c.out_f32 = p.out_f32;
+  return launch_result(pa::launch_combine(c, st));
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 100; }
+int32_t pa_abi_version(void) { return 101; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -186,7 +314,8 @@ const char* pa_status_string(int32_t code) {
     case PA_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
     case PA_ERR_OUT_DTYPE: return "out_dtype must be PA_BF16 or PA_F32";
     case PA_ERR_WORKSPACE: return "workspace is NULL or smaller than pa_decode_workspace_size()";
-    case PA_ERR_SPLITS: return "num_splits must be >= 0";
+    case PA_ERR_SPLITS:
+      return "num_splits must be >= 0, or PA_SPLITS_BALANCED with num_seqs <= PA_BALANCED_MAX_SEQS";
     case PA_ERR_TOO_MANY_SEQS: return "num_seqs exceeds PA_MAX_CHUNKED_SEQS for a chunked call";
     case PA_ERR_TENSOR_MAP: return "TMA tensor map encoding failed";
     case PA_ERR_NO_DEVICE: return "no CUDA device is current";
@@ -236,20 +365,17 @@ int32_t pa_decode_auto_splits(pa_dims d) {
   if (rc) return rc;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
-  return auto_splits(d, sms);
+  return auto_schedule(d, sms);
 }
 
 size_t pa_decode_workspace_size(pa_dims d, int32_t num_splits) {
-  if (check_dims(d) || num_splits < 0) return (size_t)-1;
-  int req = num_splits;
-  if (req == 0) {
-    const int sms = device_sms();
-    if (sms <= 0) return (size_t)-1;
-    req = auto_splits(d, sms);
-  }
-  int splits, pps;
-  split_shape(d, req, &splits, &pps);
-  return workspace_bytes_for(d, splits);
+  if (check_dims(d) || num_splits < PA_SPLITS_BALANCED) return (size_t)-1;
+  if (d.num_seqs == 0) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return (size_t)-1;
+  DecodePlan pl;
+  if (!make_plan(d, num_splits, sms, &pl)) return (size_t)-1;
+  return pl.ws_bytes;
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -259,7 +385,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   int rc = check_dims(d);
   if (rc) return rc;
   if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
-  if (num_splits < 0) return PA_ERR_SPLITS;
+  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
   if (d.num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
     return PA_ERR_NULL_POINTER;
@@ -267,57 +393,15 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
     return PA_ERR_ALIGNMENT;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
-  int splits, pps;
-  split_shape(d, num_splits == 0 ? auto_splits(d, sms) : num_splits, &splits, &pps);
-  const size_t need = workspace_bytes_for(d, splits);
-  if (need > 0) {
-    if (!workspace || ws_bytes < need) return PA_ERR_WORKSPACE;
+  DecodePlan pl;
+  if (!make_plan(d, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (pl.ws_bytes > 0) {
+    if (!workspace || ws_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
   }
-  const int G = d.num_q_heads / d.num_kv_heads;
-  const int NG = head_groups(G);
-  const int64_t items = (int64_t)splits * d.num_seqs * d.num_kv_heads * NG;
-  if (items > INT32_MAX) return PA_ERR_DIMS;
-
-  CUtensorMap tm_k, tm_v, tm_q;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
-      !encode_q_decode_map(&tm_q, q, d, G / NG))
-    return PA_ERR_TENSOR_MAP;
-
-  pa::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.block_table = block_table;
-  p.context_lens = context_lens;
-  p.out = out;
-  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
-  p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
-  p.part_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                     align256(rows * splits * kHeadDim * 4))
-                          : nullptr;
-  p.status = status;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.B = d.num_seqs;
-  p.Hq = d.num_q_heads;
-  p.Hkv = d.num_kv_heads;
-  p.G = G;
-  p.NG = NG;
-  p.num_pages = d.num_pages;
-  p.max_pages = d.max_pages_per_seq;
-  p.pps = pps;
-  p.S = splits;
-  p.num_items = (int32_t)items;
-  p.out_f32 = out_dtype == PA_F32;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
-  if (e != cudaSuccess || splits == 1) return launch_result(e);
-  pa::CombineParams c;
-  c.part_o = p.part_o;
-  c.part_lse = p.part_lse;
-  c.out = out;
-  c.rows = (int32_t)rows;
-  c.S = splits;
-  c.out_f32 = p.out_f32;
-  return launch_result(pa::launch_combine(c, st));
+  return run_decode(q, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
+                    static_cast<uint8_t*>(workspace), pl, d, status, sms,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
@@ -433,7 +517,7 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
   int rc = check_dims(d);
   if (rc) return rc;
   if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
-  if (num_splits < 0) return PA_ERR_SPLITS;
+  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
   if (d.num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
     return PA_ERR_NULL_POINTER;
@@ -441,57 +525,15 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
     return PA_ERR_ALIGNMENT;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
-  int splits, pps;
-  split_shape(d, num_splits == 0 ? auto_splits(d, sms) : num_splits, &splits, &pps);
-  const size_t need = workspace_bytes_for(d, splits);
-  if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_NOALLOC_TOO_LARGE;
-  const int G = d.num_q_heads / d.num_kv_heads;
-  const int NG = head_groups(G);
-  const int64_t items = (int64_t)splits * d.num_seqs * d.num_kv_heads * NG;
-  if (items > INT32_MAX) return PA_ERR_DIMS;
+  DecodePlan pl;
+  if (!make_plan(d, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (pl.ws_bytes > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_NOALLOC_TOO_LARGE;
   uint8_t* scratch = nullptr;
-  if (need > 0) {
+  if (pl.ws_bytes > 0) {
     cudaError_t e = cudaSuccess;
     scratch = static_cast<uint8_t*>(noalloc_scratch(&e));
     if (!scratch) return launch_result(e == cudaSuccess ? cudaErrorUnknown : e);
   }
-
-  CUtensorMap tm_k, tm_v, tm_q;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
-      !encode_q_decode_map(&tm_q, q, d, G / NG))
-    return PA_ERR_TENSOR_MAP;
-
-  pa::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.block_table = block_table;
-  p.context_lens = context_lens;
-  p.out = out;
-  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
-  p.part_o = splits > 1 ? reinterpret_cast<float*>(scratch) : nullptr;
-  p.part_lse = splits > 1 ? reinterpret_cast<float*>(scratch + align256(rows * splits * kHeadDim * 4))
-                          : nullptr;
-  p.status = status;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.B = d.num_seqs;
-  p.Hq = d.num_q_heads;
-  p.Hkv = d.num_kv_heads;
-  p.G = G;
-  p.NG = NG;
-  p.num_pages = d.num_pages;
-  p.max_pages = d.max_pages_per_seq;
-  p.pps = pps;
-  p.S = splits;
-  p.num_items = (int32_t)items;
-  p.out_f32 = out_dtype == PA_F32;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
-  if (e != cudaSuccess || splits == 1) return launch_result(e);
-  pa::CombineParams c;
-  c.part_o = p.part_o;
-  c.part_lse = p.part_lse;
-  c.out = out;
-  c.rows = (int32_t)rows;
-  c.S = splits;
-  c.out_f32 = p.out_f32;
-  return launch_result(pa::launch_combine(c, st));
+  return run_decode(q, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
+                    scratch, pl, d, status, sms, reinterpret_cast<cudaStream_t>(stream));
 }

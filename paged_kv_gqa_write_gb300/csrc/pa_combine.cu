@@ -6,15 +6,24 @@
 // over the union of the key ranges.  States with lse = -inf hold no keys and
 // are skipped (their o is never read, so it may be garbage); any +inf lse
 // marks an invalid sequence and zeroes the row.  Memory bound and small: one
-// warp per row, each lane owning 4 of the 128 dims (16-byte loads).
+// warp per row, each lane owning 4 of the 128 dims (16-byte loads).  Two
+// record layouts: fixed splits ([row][split]) and the page-balanced
+// schedule's cut units (two records per decode CTA).
 #include "pa_launch.cuh"
 
 namespace pa {
 namespace {
 
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  // launched as a programmatic dependent of the decode kernel: its partials
+  // are complete and visible after this wait
+  grid_dependency_wait();
   if (row >= p.rows) return;
   const float* lse = p.part_lse + (int64_t)row * p.S;
   float M = -INFINITY;
@@ -61,12 +70,184 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   }
 }
 
+__device__ __forceinline__ int bal_pages(int ctx, int max_pages) {
+  return (ctx >= 0 && ctx <= max_pages * kPage) ? (ctx + kPage - 1) / kPage : 0;
+}
+
+// Page-balanced decode: the decode CTAs form groups of UPS = Hkv * NG (CTA
+// g * UPS + j serves unit j, a KV head and head group); the sequences' pages
+// laid end to end (n_s pages for sequence s, W in total) are divided among the
+// groups, group g taking positions [floor(W g / ng), floor(W (g+1) / ng)).  A
+// sequence cut by a group boundary left one partial record per unit in every
+// group that touched it: record 2c (CTA c) if the sequence held the group's
+// first position, else 2c + 1.  Block b (boundary b = 1 .. ng-1) merges the
+// sequence that boundary b cuts, if it starts in group b-1 (so every cut
+// sequence is merged exactly once): one warp per (unit, query head) row.
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParams p) {
+  __shared__ int64_t sh_P, sh_W;
+  __shared__ int sh_s, sh_n, sh_go;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int UPS = (p.Hq / p.G) * p.NG;
+  const int ng = p.grid / UPS;
+  const int b = blockIdx.x + 1;
+  if (warp == 0) {
+    // prologue, overlapping the decode kernel: locate the sequence at
+    // boundary b (all context lengths at once: B <= PA_BALANCED_MAX_SEQS)
+    constexpr int R = PA_BALANCED_MAX_SEQS / 32;
+    // (unconditional loads of a clamped index, so that they issue together)
+    int np[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(r * 32 + lane, p.B - 1));
+#pragma unroll
+    for (int r = 0; r < R; ++r) np[r] = r * 32 + lane < p.B ? bal_pages(np[r], p.max_pages) : 0;
+    int64_t tot = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) tot += np[r];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const int64_t W = tot;
+    const int64_t X = W * b / ng, lo_prev = W * (b - 1) / ng;
+    int go = 0, s_hit = 0, n = 0;
+    bool found = false;
+    int64_t P = 0, base = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t span = np[r];
+      int64_t incl = span;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int64_t start = base + incl - span;
+      const unsigned m = __ballot_sync(0xffffffffu, span > 0 && start < X && X < start + span);
+      if (m && !found) {
+        found = true;
+        const int f = __ffs(m) - 1;
+        s_hit = r * 32 + f;
+        n = __shfl_sync(0xffffffffu, np[r], f);
+        P = __shfl_sync(0xffffffffu, start, f);
+        go = P >= lo_prev ? 1 : 0;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      sh_go = go;
+      sh_s = s_hit;
+      sh_n = n;
+      sh_P = P;
+      sh_W = W;
+    }
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  if (!sh_go) return;
+  const int64_t W = sh_W, P = sh_P;
+  const int n = sh_n;
+  // the groups b-1 .. that touched pages [P, P + n), 32 at a time: lane k
+  // holds group b-1+k of the current chunk (its record load runs in parallel)
+  for (int r = warp; r < p.Hq; r += blockDim.x >> 5) {
+    const int j = r / p.GC, g = r - j * p.GC;
+    float M = -INFINITY;
+    bool inval = false;
+    for (int g0 = b - 1; g0 < ng; g0 += 32) {
+      const int gg = g0 + lane;
+      const int64_t lo = W * gg / ng, hi = W * (gg + 1) / ng;
+      const bool has = gg < ng && lo < P + n && lo != hi;
+      const float v = has ? p.bal_lse[(2 * (gg * UPS + j) + (P <= lo ? 0 : 1)) * 16 + g] : -INFINITY;
+      inval |= v == INFINITY;
+      M = fmaxf(M, v);
+      if (!__any_sync(0xffffffffu, gg < ng && lo < P + n)) break;
+    }
+    M = warp_max(M);
+    inval = __any_sync(0xffffffffu, inval);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!inval && M != -INFINITY) {
+      float Lsum = 0.f;
+      for (int g0 = b - 1; g0 < ng; g0 += 32) {
+        const int gg = g0 + lane;
+        const int64_t lo = W * gg / ng, hi = W * (gg + 1) / ng;
+        const bool has = gg < ng && lo < P + n && lo != hi;
+        const int rec = 2 * (gg * UPS + j) + (P <= lo ? 0 : 1);
+        const float v = has ? p.bal_lse[rec * 16 + g] : -INFINITY;
+        const float w = v == -INFINITY ? 0.f : expf(v - M);
+        Lsum += w;
+        unsigned m = __ballot_sync(0xffffffffu, w != 0.f);
+        while (m) {
+          const int k = __ffs(m) - 1;
+          m &= m - 1;
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+          const int rk = __shfl_sync(0xffffffffu, rec, k);
+          const float4 x =
+              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)rk * 16 + g) * kHeadDim)[lane];
+          acc.x = fmaf(wk, x.x, acc.x);
+          acc.y = fmaf(wk, x.y, acc.y);
+          acc.z = fmaf(wk, x.z, acc.z);
+          acc.w = fmaf(wk, x.w, acc.w);
+        }
+        if (!__any_sync(0xffffffffu, gg < ng && lo < P + n)) break;
+      }
+      const float inv = 1.f / warp_sum(Lsum);
+      acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    const int64_t row = (int64_t)sh_s * p.Hq + r;
+    if (p.out_f32) {
+      reinterpret_cast<float4*>(p.out)[row * (kHeadDim / 4) + lane] = acc;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 c2 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&c2);
+      reinterpret_cast<uint2*>(p.out)[row * (kHeadDim / 4) + lane] = u;
+    }
+  }
+}
+
+// Launch as a programmatic dependent of the kernel before it on the stream
+// (its prologue may overlap that kernel; griddepcontrol.wait orders the reads).
+template <typename P>
+cudaError_t launch_dependent(void (*kernel)(P), const P& p, int grid, int block,
+                             cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  combine_kernel<<<(p.rows + 3) / 4, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_dependent(combine_kernel, p, (p.rows + 3) / 4, 128, stream);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream) {
+  const int ng = p.grid / ((p.Hq / p.G) * p.NG);
+  if (ng <= 1) return cudaSuccess;
+  const int warps = p.Hq < 32 ? p.Hq : 32;
+  cudaError_t e = launch_dependent(bal_combine_kernel, p, ng - 1, 32 * warps, stream);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace pa

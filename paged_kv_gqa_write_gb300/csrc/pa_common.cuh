@@ -324,7 +324,23 @@ struct DecodeParams {
   int32_t num_pages, max_pages;
   int32_t pps;                  // pages per split
   int32_t S;                    // splits
-  int32_t num_items;            // S * B * Hkv * NG
+  int32_t num_items;            // S * B * Hkv * NG (fixed splits)
+  int32_t out_f32;
+  int32_t balanced;             // page-balanced schedule instead of fixed splits
+  int32_t grid;                 // CTAs of the page-balanced schedule (groups x Hkv*NG)
+  float* bal_o;                 // [2 * grid][16][D] partial records of cut sequences
+  float* bal_lse;               // [2 * grid][16]
+};
+
+// Merge of the sequences that the page-balanced decode schedule cut between
+// CTA groups.
+struct BalCombineParams {
+  const int32_t* context_lens;
+  const float* bal_o;
+  const float* bal_lse;
+  void* out;
+  int32_t B, Hq, G, NG, GC, max_pages;
+  int32_t grid;                 // CTAs of the decode launch
   int32_t out_f32;
 };
 

@@ -51,6 +51,7 @@ constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
 constexpr int kThreads = 10 * 32;
 constexpr int kStages = 3;
 constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
+constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
 constexpr int kStageBytes = 4 * kBox;      // K lo, K hi, V lo, V hi of a page
 constexpr int kN = 16;                     // MMA N: query heads of an item, padded
@@ -65,8 +66,8 @@ constexpr int kQ = kRing + kStages * kStageBytes;  // [kSlots] query operands
 constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
 constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax-warp exchange
 constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O buffer
-constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][4]: ctx, pg0, pg1, flag
-constexpr int kBars = kInfo + kSlots * 4 * 4;
+constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][kInfoInts]: item records
+constexpr int kBars = kInfo + kSlots * 8 * 4;
 constexpr int kNumBars = 3 * kStages + 2 * kSlots + 2 + 4 * 2 + 1;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 constexpr int kSmemLimit = 232448;
@@ -92,33 +93,30 @@ struct Bars {
   uint64_t* mma_done;  // drain at exit
 };
 
-struct Item {
-  int s, h, hg, j, pg0, pg1, ctx;
-  bool ok;
+// Item record in shared memory, written by the TMA warp, read by every role.
+enum : int {
+  kICtx = 0,   // context length of the sequence
+  kIPg0 = 1,   // first page of the item
+  kIPg1 = 2,   // end page (== kIPg0 when the item has no pages to read)
+  kIFlag = 3,  // 0 ok, 1 invalid block-table entry, 2 invalid context length
+  kISeq = 4,   // sequence
+  kIUnit = 5,  // KV head * NG + head group
+  kIDest = 6,  // -1: out; else the partial record (split index, or 2 * CTA + cut side)
+  kIDone = 7,  // no more items
+  kInfoInts = 8
 };
 
-__device__ __forceinline__ int item_seq(int i, const DecodeParams& p) {
-  const int per_seq = p.Hkv * p.NG;
-  return (i % (p.B * per_seq)) / per_seq;
+// A work item: pages [pg0, pg1) of unit (s, unit) whose result goes to `dest`.
+struct Work {
+  int s, unit, ctx, pg0, pg1, dest;
+};
+
+__device__ __forceinline__ bool ctx_ok(int ctx, const DecodeParams& p) {
+  return ctx >= 0 && ctx <= p.max_pages * kPage;
 }
 
-__device__ __forceinline__ Item decode_item(int i, const DecodeParams& p, int ctx) {
-  Item it;
-  const int per_seq = p.Hkv * p.NG;
-  const int U = p.B * per_seq;
-  it.j = i / U;
-  const int u = i - it.j * U;
-  it.s = u / per_seq;
-  const int r = u - it.s * per_seq;
-  it.h = r / p.NG;
-  it.hg = r - it.h * p.NG;
-  it.ctx = ctx;
-  it.ok = it.ctx >= 0 && it.ctx <= p.max_pages * kPage;
-  const int npg = it.ok ? (it.ctx + kPage - 1) / kPage : 0;
-  it.pg0 = it.j * p.pps;
-  it.pg1 = min(npg, it.pg0 + p.pps);
-  if (it.pg1 < it.pg0) it.pg1 = it.pg0;
-  return it;
+__device__ __forceinline__ int pages_of(int ctx, const DecodeParams& p) {
+  return ctx_ok(ctx, p) ? (ctx + kPage - 1) / kPage : 0;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -194,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // a combine launched as a programmatic dependent may start its prologue now;
+  // it reads partials only after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -203,48 +204,168 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensor_map(&tm_q);
     }
     const uint64_t pol = l2_policy_evict_first();
-    const int U = p.B * p.Hkv * p.NG;
-    // Metadata of the next item, loaded while the current item's pages are
-    // issued: its context length and this lane's block-table entry among the
-    // first 32 pages of its range.
-    int nx_ctx = 0, nx_pid = 0;
-    auto prefetch = [&](int ii) {
-      if (ii < p.num_items) {
-        const int s = item_seq(ii, p);
-        nx_ctx = __ldg(p.context_lens + s);
-        const int pg = (ii / U) * p.pps + lane;
-        nx_pid = pg < p.max_pages ? __ldg(p.block_table + (int64_t)s * p.max_pages + pg) : 0;
+    // ---- work generator (warp-uniform state).  Fixed splits: items
+    // i = blockIdx.x + k * gridDim.x of (split, sequence, unit).  Page-balanced:
+    // the CTAs form groups of UPS (one CTA per unit = KV head x head group);
+    // the sequences' pages laid end to end (n_s pages for sequence s, W in
+    // total) are divided evenly among the groups, and the CTA with unit j of a
+    // group takes unit j of every sequence in the group's range [lo, hi) --
+    // so the CTAs of a group read the same pages at about the same time.  A
+    // sequence cut by lo or hi leaves partial records for the balanced
+    // combine; an empty sequence (or one with an invalid length) belongs to
+    // the group whose range holds its position (the last group for W).
+    const int UPS = p.Hkv * p.NG;  // units per sequence
+    int gi = blockIdx.x;           // fixed: next item index
+    int bs = p.B, bn = 0, bctx = 0;  // balanced: sequence, its pages, its context length
+    int64_t bP = 0, lo = 0, hi = 0, W = 0;
+    const int ngroups = gridDim.x / UPS, grp = blockIdx.x / UPS, unit_j = blockIdx.x % UPS;
+    int cbase = -64, cval = 0;     // 32 context lengths starting at cbase (lane's in cval)
+    const bool last_grp = grp == ngroups - 1;
+    auto ctx_at = [&](int sq) -> int {
+      if (sq < cbase || sq >= cbase + 32) {
+        cbase = sq;
+        cval = cbase + lane < p.B ? __ldg(p.context_lens + cbase + lane) : 0;
       }
+      return __shfl_sync(0xffffffffu, cval, sq - cbase);
     };
-    prefetch(blockIdx.x);
+    if (p.balanced && grp < ngroups) {
+      // all context lengths at once (B <= kBalMaxSeqs), then the page prefix
+      // (unconditional loads of a clamped index, so that they issue together)
+      int np[kBalMaxSeqs / 32];
+#pragma unroll
+      for (int r = 0; r < kBalMaxSeqs / 32; ++r)
+        np[r] = __ldg(p.context_lens + min(r * 32 + lane, p.B - 1));
+#pragma unroll
+      for (int r = 0; r < kBalMaxSeqs / 32; ++r)
+        np[r] = r * 32 + lane < p.B ? pages_of(np[r], p) : 0;
+      int64_t tot = 0;
+#pragma unroll
+      for (int r = 0; r < kBalMaxSeqs / 32; ++r) tot += np[r];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      W = tot;
+      lo = W * grp / ngroups;
+      hi = W * (grp + 1) / ngroups;
+      // first sequence the group touches: it reaches past lo, or it is empty
+      // and sits at or after lo
+      int64_t base = 0;
+#pragma unroll
+      for (int r = 0; r < kBalMaxSeqs / 32; ++r) {
+        const int sq = r * 32 + lane;
+        const int64_t span = np[r];
+        int64_t incl = span;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const int64_t start = base + incl - span;
+        const bool hit = sq < p.B && (start + span > lo || (span == 0 && start >= lo));
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m && bs == p.B) {
+          const int f = __ffs(m) - 1;
+          bs = r * 32 + f;
+          bP = __shfl_sync(0xffffffffu, start, f);
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (bs < p.B) {
+        bctx = ctx_at(bs);
+        bn = pages_of(bctx, p);
+      }
+    }
+    auto gen_next = [&](Work& w) -> bool {
+      if (!p.balanced) {
+        if (gi >= p.num_items) return false;
+        const int U = p.B * UPS;
+        const int jsp = gi / U, u = gi - jsp * U;
+        w.s = u / UPS;
+        w.unit = u - w.s * UPS;
+        w.ctx = __ldg(p.context_lens + w.s);
+        w.pg0 = jsp * p.pps;
+        w.pg1 = max(w.pg0, min(pages_of(w.ctx, p), w.pg0 + p.pps));
+        w.dest = p.S == 1 ? -1 : jsp;
+        gi += gridDim.x;
+        return true;
+      }
+      if (grp >= ngroups || bs >= p.B) return false;
+      if (bn == 0) {
+        if (bP >= hi && !(last_grp && bP == W)) {
+          bs = p.B;
+          return false;
+        }
+        w.pg0 = 0;
+        w.pg1 = 0;
+        w.dest = -1;
+      } else {
+        if (bP >= hi || lo >= hi) {  // past the range, or an empty range
+          bs = p.B;
+          return false;
+        }
+        const int64_t a = max(bP, lo), b = min(bP + bn, hi);
+        w.pg0 = (int)(a - bP);
+        w.pg1 = (int)(b - bP);
+        w.dest = (a == bP && b == bP + bn) ? -1 : 2 * (int)blockIdx.x + (bP <= lo ? 0 : 1);
+      }
+      w.s = bs;
+      w.unit = unit_j;
+      w.ctx = bctx;
+      bP += bn;
+      ++bs;
+      if (bs < p.B) {
+        bctx = ctx_at(bs);
+        bn = pages_of(bctx, p);
+      }
+      return true;
+    };
+    // this lane's block-table entry among the first 32 pages of an item
+    auto first_pid = [&](const Work& w) -> int {
+      const int pg = w.pg0 + lane;
+      return pg < w.pg1 ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
+    };
+    Work nx;
+    bool have = gen_next(nx);
+    int nx_pid = have ? first_pid(nx) : 0;
     uint32_t gp = 0, n = 0;
     // per item slot: parity of its last use if that use loaded a query operand, else -1
     int q_pending[kSlots];
 #pragma unroll
     for (int k = 0; k < kSlots; ++k) q_pending[k] = -1;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+    for (; ok; ++n) {
+      const Work w = nx;
       const int pid0 = nx_pid;
-      const Item it = decode_item(i, p, nx_ctx);
-      const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
-      bool bad = it.pg0 + lane < it.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
-      for (int pg = it.pg0 + 32 + lane; pg < it.pg1; pg += 32) {
-        const int pid = __ldg(bt + pg);
-        bad |= pid < 0 || pid >= p.num_pages;
+      const bool item = have;
+      int flag = 0, npg = 0;
+      if (item) {
+        // validate every page of the item; the next item's metadata loads
+        // while this one's pages are issued
+        const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
+        bool bad = w.pg0 + lane < w.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
+        for (int pg = w.pg0 + 32 + lane; pg < w.pg1; pg += 32) {
+          const int pid = __ldg(bt + pg);
+          bad |= pid < 0 || pid >= p.num_pages;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        flag = !ctx_ok(w.ctx, p) ? 2 : (bad ? 1 : 0);
+        npg = flag ? 0 : w.pg1 - w.pg0;
+        have = gen_next(nx);
+        if (have) nx_pid = first_pid(nx);
       }
-      bad = __any_sync(0xffffffffu, bad);
-      const int flag = !it.ok ? 2 : (bad ? 1 : 0);
-      const int npg = flag ? 0 : it.pg1 - it.pg0;
-      prefetch(i + gridDim.x);
       const int slot = n % kSlots;
       if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
       if (lane == 0) {
-        info[4 * slot] = it.ctx;
-        info[4 * slot + 1] = it.pg0;
-        info[4 * slot + 2] = it.pg0 + npg;
-        info[4 * slot + 3] = flag;
+        int* rec = info + kInfoInts * slot;
+        rec[kICtx] = w.ctx;
+        rec[kIPg0] = w.pg0;
+        rec[kIPg1] = w.pg0 + npg;
+        rec[kIFlag] = flag;
+        rec[kISeq] = w.s;
+        rec[kIUnit] = w.unit;
+        rec[kIDest] = w.dest;
+        rec[kIDone] = item ? 0 : 1;
         if (npg > 0) {
-          const int qrow = it.s * p.Hq + it.h * p.G + it.hg * GC;
+          const int qrow = w.s * p.Hq + (w.unit / p.NG) * p.G + (w.unit % p.NG) * GC;
           uint8_t* qd = smem + kQ + slot * kOpBytes;
           mbar_arrive_expect_tx(&B.q_full[slot], 2 * GC * 128);
           tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
@@ -255,9 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_pending[slot] = -1;
         }
       }
-      const int x = it.h * kHeadDim;
+      if (!item) break;
+      const int x = (w.unit / p.NG) * kHeadDim;
+      const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
       for (int c = 0; ok && c < npg; c += 32) {
-        const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + it.pg0 + c + lane) : 0);
+        const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + w.pg0 + c + lane) : 0);
         const int cnt = min(32, npg - c);
         for (int k = 0; k < cnt; ++k) {
           const int page = __shfl_sync(0xffffffffu, pid_l, k);
@@ -298,12 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, kN, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, kN, true, false);
-      uint32_t gp = 0, n = 0, nb = 0;
+      uint32_t gp = 0, nb = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+      for (uint32_t n = 0; ok; ++n) {
         const int slot = n % kSlots;
         if (!(ok = mbar_wait(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
-        const int npg = info[4 * slot + 2] - info[4 * slot + 1];
+        const int* rec = info + kInfoInts * slot;
+        if (rec[kIDone]) break;
+        const int npg = rec[kIPg1] - rec[kIPg0];
         if (npg <= 0) {
           mbar_arrive(&B.q_empty[slot]);
           continue;
@@ -376,12 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ex;
       return r ? slot : nullptr;
     };
-    uint32_t gp = 0, n = 0, nb = 0;
+    uint32_t gp = 0, nb = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+    for (uint32_t n = 0; ok; ++n) {
       const int slot = n % kSlots;
       if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
-      const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
+      const int* rec = info + kInfoInts * slot;
+      if (rec[kIDone]) break;
+      const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
@@ -509,17 +636,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dim = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float* ml = reinterpret_cast<const float*>(smem + kML);
-    uint32_t n = 0, nb = 0;
+    uint32_t nb = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x, ++n) {
+    for (uint32_t n = 0; ok; ++n) {
       const int slot = n % kSlots;
       if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
-      const int ctx = info[4 * slot], pg0 = info[4 * slot + 1], pg1 = info[4 * slot + 2];
-      const int flag = info[4 * slot + 3];
+      const int* rec = info + kInfoInts * slot;
+      if (rec[kIDone]) break;
+      const int pg0 = rec[kIPg0], pg1 = rec[kIPg1], flag = rec[kIFlag];
+      const int sq = rec[kISeq], unit = rec[kIUnit], dest = rec[kIDest];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
-      const Item it = decode_item(i, p, ctx);
-      const int64_t row0 = (int64_t)it.s * p.Hq + it.h * p.G + it.hg * GC;
+      const int64_t row0 = (int64_t)sq * p.Hq + (unit / p.NG) * p.G + (unit % p.NG) * GC;
       float res[NH], lse[NH];
       if (pg1 - pg0 <= 0) {
         // nothing visible (lse -inf), or an invalid sequence (lse +inf: the
@@ -554,15 +682,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = 0; g < NH; ++g) {
         if (g < GC) {
           const int64_t row = row0 + g;
-          if (p.S == 1) {
+          if (dest < 0) {
             if (p.out_f32)
               reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[g];
             else
               reinterpret_cast<__nv_bfloat16*>(p.out)[row * kHeadDim + dim] =
                   __float2bfloat16_rn(res[g]);
+          } else if (p.balanced) {
+            p.bal_o[((int64_t)dest * kN + g) * kHeadDim + dim] = res[g];
+            if (dim == 0) p.bal_lse[dest * kN + g] = lse[g];
           } else {
-            p.part_o[(row * p.S + it.j) * kHeadDim + dim] = res[g];
-            if (dim == 0) p.part_lse[row * p.S + it.j] = lse[g];
+            p.part_o[(row * p.S + dest) * kHeadDim + dim] = res[g];
+            if (dim == 0) p.part_lse[row * p.S + dest] = lse[g];
           }
         }
       }
@@ -583,7 +714,7 @@ cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CU
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  const int grid = p.num_items < num_sms ? p.num_items : num_sms;
+  const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
   if (grid < 1) return cudaSuccess;
   decode_kernel<NH><<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
   return cudaGetLastError();

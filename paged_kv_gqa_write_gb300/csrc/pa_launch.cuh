@@ -17,6 +17,9 @@ cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
+// Merge of the units a page-balanced decode launch of p.grid CTAs cut.
+cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream);
+
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream);

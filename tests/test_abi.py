@@ -50,7 +50,12 @@ def test_python_constants_match_header(pa):
     assert h["PA_STATUS_BAD_TOKENS"] == pa.PA_STATUS_BAD_TOKENS
     assert h["PA_STATUS_TIMEOUT"] == pa.PA_STATUS_TIMEOUT
     assert h["PA_MAX_CHUNKED_SEQS"] == pa.PA_MAX_CHUNKED_SEQS
-    assert pa.pa_abi_version() == 100
+    assert h["PA_SPLITS_BALANCED"] == pa.PA_SPLITS_BALANCED
+    assert h["PA_BALANCED_MAX_SEQS"] == pa.PA_BALANCED_MAX_SEQS
+    for k, v in h.items():
+        if k.startswith("PA_ERR_"):
+            assert getattr(pa, k) == v, k
+    assert pa.pa_abi_version() == 101
 
 
 def test_status_strings(pa):
@@ -88,7 +93,7 @@ def test_host_checks_decode(pa):
     assert call(_dims(pa, num_pages=0)) == h["PA_ERR_DIMS"]
     assert call(_dims(pa, num_pages=1 << 24)) == h["PA_ERR_DIMS"]
     assert call(_dims(pa), dt=7) == h["PA_ERR_OUT_DTYPE"]
-    assert call(_dims(pa), ns=-1) == h["PA_ERR_SPLITS"]
+    assert call(_dims(pa), ns=-2) == h["PA_ERR_SPLITS"]
     assert call(_dims(pa), q=None) == h["PA_ERR_NULL_POINTER"]
     assert call(_dims(pa), out=MIS) == h["PA_ERR_ALIGNMENT"]
     assert call(_dims(pa, num_seqs=0)) == 0                                      # nothing to do

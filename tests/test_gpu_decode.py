@@ -19,7 +19,10 @@ def _decode(pa, c, num_splits=0, out_dtype=torch.float32):
     return out, int(st.item())
 
 
-@pytest.mark.parametrize("splits", [0, 1, 2])
+BAL = -1  # PA_SPLITS_BALANCED: the page-balanced schedule
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, BAL])
 def test_tiny(cuda_lib, splits):
     case = W.tiny_decode()
     out, st = _decode(cuda_lib, case.to("cuda"), splits)
@@ -36,7 +39,7 @@ def test_tiny_single_token_is_v_exactly(cuda_lib):
         assert torch.equal(out[0, g].cpu(), v)
 
 
-@pytest.mark.parametrize("splits", [0, 1, 3, 32])
+@pytest.mark.parametrize("splits", [0, 1, 3, 32, BAL])
 def test_qwen3_14b_b16(cuda_lib, splits):
     case = W.qwen3_14b_decode_b16()
     out, st = _decode(cuda_lib, case.to("cuda"), splits)
@@ -96,23 +99,24 @@ def test_edge_lengths_and_groups(cuda_lib, Hq, Hkv):
 
 def test_zero_context_rows_are_exactly_zero(cuda_lib):
     case = W.custom_case(410, [0, 300, 0, 1], Hq=8, Hkv=2)
-    for splits in (1, 2):
+    for splits in (1, 2, BAL):
         out, st = _decode(cuda_lib, case.to("cuda"), splits)
         assert st == 0
         assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
         assert_close(out, oracle_decode(case), what="zero ctx")
 
 
-def test_page_permutation_gives_bitwise_identical_output(cuda_lib):
+@pytest.mark.parametrize("splits", [3, BAL])
+def test_page_permutation_gives_bitwise_identical_output(cuda_lib, splits):
     case = W.custom_case(411, [300, 129, 4000, 17], Hq=40, Hkv=8, extra_pages=9,
                          max_pages_per_seq=32)
-    base, _ = _decode(cuda_lib, case.to("cuda"), 3)
+    base, _ = _decode(cuda_lib, case.to("cuda"), splits)
     perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(5))
     inv = torch.empty_like(perm); inv[perm] = torch.arange(case.num_pages)
     case.k_cache, case.v_cache = case.k_cache[perm], case.v_cache[perm]
     m = case.block_table >= 0
     case.block_table[m] = inv[case.block_table[m].long()].to(torch.int32)
-    again, _ = _decode(cuda_lib, case.to("cuda"), 3)
+    again, _ = _decode(cuda_lib, case.to("cuda"), splits)
     assert torch.equal(base, again)
 
 
@@ -124,7 +128,7 @@ def test_shared_prefix_pages(cuda_lib):
     assert st == 0 and torch.equal(out[0], out[1])
 
 
-@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("splits", [1, 2, BAL])
 def test_invalid_page_zeroes_sequence_and_flags(cuda_lib, splits):
     case = W.custom_case(413, [300, 300], Hq=8, Hkv=2)
     ref = oracle_decode(case)
@@ -135,12 +139,15 @@ def test_invalid_page_zeroes_sequence_and_flags(cuda_lib, splits):
     assert_close(out[1], ref[1], what="valid neighbour")
 
 
-def test_context_too_long_flags_length(cuda_lib):
+@pytest.mark.parametrize("splits", [1, BAL])
+def test_context_too_long_flags_length(cuda_lib, splits):
     case = W.custom_case(414, [10, 200], Hq=4, Hkv=1)
+    ref = oracle_decode(case)
     case.context_lens[0] = case.max_pages_per_seq * 128 + 1
-    out, st = _decode(cuda_lib, case.to("cuda"), 1)
+    out, st = _decode(cuda_lib, case.to("cuda"), splits)
     assert st & cuda_lib.PA_STATUS_BAD_LENGTH
     assert torch.count_nonzero(out[0]) == 0
+    assert_close(out[1], ref[1], what="valid neighbour")
 
 
 def test_repeated_calls_are_deterministic(cuda_lib):
@@ -148,3 +155,62 @@ def test_repeated_calls_are_deterministic(cuda_lib):
     a, _ = _decode(cuda_lib, case, 0)
     b, _ = _decode(cuda_lib, case, 0)
     assert torch.equal(a, b)
+
+
+# ---- page-balanced schedule: cut units, empty ranges, empty sequences
+
+def test_balanced_one_unit_cut_into_one_page_pieces(cuda_lib):
+    """One (sequence, KV head) of 32 pages: the launch has 32 CTAs of one page
+    each, so the combine merges 32 partial records."""
+    case = W.custom_case(420, [4096], Hq=8, Hkv=1, max_pages_per_seq=32)
+    out, st = _decode(cuda_lib, case.to("cuda"), BAL)
+    assert st == 0
+    assert_close(out, oracle_decode(case), what="one unit, 32 pieces")
+
+
+def test_balanced_more_ctas_than_pages(cuda_lib):
+    """Fewer pages than CTAs: many CTAs have an empty range."""
+    case = W.custom_case(421, [8000, 3, 0], Hq=4, Hkv=1, max_pages_per_seq=63)
+    out, st = _decode(cuda_lib, case.to("cuda"), BAL)
+    assert st == 0
+    assert torch.count_nonzero(out[2]) == 0
+    assert_close(out, oracle_decode(case), what="empty CTA ranges")
+
+
+def test_balanced_empty_sequences_everywhere(cuda_lib):
+    """Empty contexts first, between and last (the last CTA owns position W)."""
+    ctx = [0, 5, 0, 0, 1300, 129, 0, 2051, 0]
+    case = W.custom_case(422, ctx, Hq=16, Hkv=2, max_pages_per_seq=17)
+    out, st = _decode(cuda_lib, case.to("cuda"), BAL)
+    assert st == 0
+    for s, c in enumerate(ctx):
+        if c == 0:
+            assert torch.count_nonzero(out[s]) == 0
+    assert_close(out, oracle_decode(case), what="empty sequences")
+
+
+def test_balanced_largest_batch(cuda_lib):
+    lens = torch.randint(1, 400, (cuda_lib.PA_BALANCED_MAX_SEQS,),
+                         generator=torch.Generator().manual_seed(423)).tolist()
+    lens[7] = 0
+    case = W.custom_case(423, lens, Hq=4, Hkv=2, max_pages_per_seq=4)
+    out, st = _decode(cuda_lib, case.to("cuda"), BAL)
+    assert st == 0
+    assert_close(out, oracle_decode(case), what="largest balanced batch")
+
+
+def test_balanced_rejects_too_many_sequences(cuda_lib):
+    case = W.custom_case(424, [3] * (cuda_lib.PA_BALANCED_MAX_SEQS + 1), Hq=2, Hkv=1,
+                         max_pages_per_seq=1).to("cuda")
+    d = cuda_lib.make_dims(case.B, case.Hq, case.Hkv, case.num_pages, case.max_pages_per_seq)
+    assert cuda_lib.load().pa_decode_workspace_size(d, BAL) == 2**64 - 1
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty(case.B, case.Hq, 128, dtype=torch.float32, device="cuda")
+    rc = cuda_lib.load().pa_decode(
+        cuda_lib._ptr(case.q), cuda_lib._ptr(case.k_cache), cuda_lib._ptr(case.v_cache),
+        cuda_lib._ptr(case.block_table), cuda_lib._ptr(case.context_lens), case.scale,
+        cuda_lib._ptr(out), cuda_lib.PA_F32, cuda_lib._ptr(ws), ws.numel(), BAL, d, None, None)
+    assert rc == cuda_lib.PA_ERR_SPLITS
+    # the automatic choice falls back to fixed splits for that batch
+    out, st = _decode(cuda_lib, case, 0)
+    assert st == 0
