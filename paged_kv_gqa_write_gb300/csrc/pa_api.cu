@@ -118,8 +118,12 @@ int units_per_seq(const pa_dims& d) {
   return d.num_kv_heads * head_groups(d.num_q_heads / d.num_kv_heads);
 }
 
+// The page-balanced schedule takes B <= PA_BALANCED_MAX_SEQS, page positions
+// that fit in 31 bits, and at least two CTA groups.
 bool balanced_ok(const pa_dims& d, int num_sms) {
-  return d.num_seqs <= PA_BALANCED_MAX_SEQS && num_sms / units_per_seq(d) >= 2;
+  return d.num_seqs <= PA_BALANCED_MAX_SEQS &&
+         (int64_t)d.num_seqs * d.max_pages_per_seq < ((int64_t)1 << 31) &&
+         num_sms / units_per_seq(d) >= 2 && num_sms / units_per_seq(d) <= 1024;
 }
 
 // The schedule num_splits == 0 selects: 0 for the page-balanced schedule

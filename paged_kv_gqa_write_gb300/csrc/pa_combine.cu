@@ -96,52 +96,57 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParams p) {
-  __shared__ int64_t sh_P, sh_W;
-  __shared__ int sh_s, sh_n, sh_go;
+  constexpr int kMaxGroups = 1024;
+  __shared__ int sh_lo[kMaxGroups + 1];  // group boundaries
+  __shared__ int sh_P, sh_s, sh_n, sh_go, sh_W;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int UPS = (p.Hq / p.G) * p.NG;
   const int ng = p.grid / UPS;
   const int b = blockIdx.x + 1;
   if (warp == 0) {
     // prologue, overlapping the decode kernel: locate the sequence at
-    // boundary b (all context lengths at once: B <= PA_BALANCED_MAX_SEQS)
+    // boundary b.  Lane l holds the page counts of sequences 16l .. 16l+15
+    // (B <= PA_BALANCED_MAX_SEQS; W < 2^31).
     constexpr int R = PA_BALANCED_MAX_SEQS / 32;
-    // (unconditional loads of a clamped index, so that they issue together)
     int np[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(r * 32 + lane, p.B - 1));
-#pragma unroll
-    for (int r = 0; r < R; ++r) np[r] = r * 32 + lane < p.B ? bal_pages(np[r], p.max_pages) : 0;
-    int64_t tot = 0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) tot += np[r];
-#pragma unroll
-    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const int64_t W = tot;
-    const int64_t X = W * b / ng, lo_prev = W * (b - 1) / ng;
-    int go = 0, s_hit = 0, n = 0;
-    bool found = false;
-    int64_t P = 0, base = 0;
+    for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(lane * R + r, p.B - 1));
+    int lsum = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int64_t span = np[r];
-      int64_t incl = span;
+      np[r] = lane * R + r < p.B ? bal_pages(np[r], p.max_pages) : 0;
+      lsum += np[r];
+    }
+    int incl = lsum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int W = __shfl_sync(0xffffffffu, incl, 31);
+    const int X = (int)((int64_t)W * b / ng), lo_prev = (int)((int64_t)W * (b - 1) / ng);
+    int start = incl - lsum, hit_r = -1, hit_start = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (hit_r < 0 && np[r] > 0 && start < X && X < start + np[r]) {
+        hit_r = r;
+        hit_start = start;
       }
-      const int64_t start = base + incl - span;
-      const unsigned m = __ballot_sync(0xffffffffu, span > 0 && start < X && X < start + span);
-      if (m && !found) {
-        found = true;
-        const int f = __ffs(m) - 1;
-        s_hit = r * 32 + f;
-        n = __shfl_sync(0xffffffffu, np[r], f);
-        P = __shfl_sync(0xffffffffu, start, f);
-        go = P >= lo_prev ? 1 : 0;
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      start += np[r];
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit_r >= 0);
+    int go = 0, s_hit = 0, n = 0, P = 0;
+    if (m) {
+      const int f = __ffs(m) - 1;
+      const int rr = __shfl_sync(0xffffffffu, hit_r, f);
+      s_hit = f * R + rr;
+      P = __shfl_sync(0xffffffffu, hit_start, f);
+      int nv = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r == rr) nv = np[r];
+      n = __shfl_sync(0xffffffffu, nv, f);
+      go = P >= lo_prev ? 1 : 0;
     }
     if (lane == 0) {
       sh_go = go;
@@ -152,19 +157,21 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
     }
   }
   __syncthreads();
-  grid_dependency_wait();
   if (!sh_go) return;
-  const int64_t W = sh_W, P = sh_P;
-  const int n = sh_n;
+  for (int gg = threadIdx.x; gg <= ng && gg <= kMaxGroups; gg += blockDim.x)
+    sh_lo[gg] = (int)((int64_t)sh_W * gg / ng);
+  __syncthreads();
+  grid_dependency_wait();
+  const int P = sh_P, n = sh_n;
   // the groups b-1 .. that touched pages [P, P + n), 32 at a time: lane k
-  // holds group b-1+k of the current chunk (its record load runs in parallel)
+  // holds group b-1+k of the current chunk (its record loads run in parallel)
   for (int r = warp; r < p.Hq; r += blockDim.x >> 5) {
     const int j = r / p.GC, g = r - j * p.GC;
     float M = -INFINITY;
     bool inval = false;
     for (int g0 = b - 1; g0 < ng; g0 += 32) {
       const int gg = g0 + lane;
-      const int64_t lo = W * gg / ng, hi = W * (gg + 1) / ng;
+      const int lo = gg < ng ? sh_lo[gg] : INT32_MAX, hi = gg < ng ? sh_lo[gg + 1] : INT32_MAX;
       const bool has = gg < ng && lo < P + n && lo != hi;
       const float v = has ? p.bal_lse[(2 * (gg * UPS + j) + (P <= lo ? 0 : 1)) * 16 + g] : -INFINITY;
       inval |= v == INFINITY;
@@ -178,16 +185,16 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
       float Lsum = 0.f;
       for (int g0 = b - 1; g0 < ng; g0 += 32) {
         const int gg = g0 + lane;
-        const int64_t lo = W * gg / ng, hi = W * (gg + 1) / ng;
+        const int lo = gg < ng ? sh_lo[gg] : INT32_MAX, hi = gg < ng ? sh_lo[gg + 1] : INT32_MAX;
         const bool has = gg < ng && lo < P + n && lo != hi;
         const int rec = 2 * (gg * UPS + j) + (P <= lo ? 0 : 1);
         const float v = has ? p.bal_lse[rec * 16 + g] : -INFINITY;
         const float w = v == -INFINITY ? 0.f : expf(v - M);
         Lsum += w;
-        unsigned m = __ballot_sync(0xffffffffu, w != 0.f);
-        while (m) {
-          const int k = __ffs(m) - 1;
-          m &= m - 1;
+        unsigned mk = __ballot_sync(0xffffffffu, w != 0.f);
+        while (mk) {
+          const int k = __ffs(mk) - 1;
+          mk &= mk - 1;
           const float wk = __shfl_sync(0xffffffffu, w, k);
           const int rk = __shfl_sync(0xffffffffu, rec, k);
           const float4 x =

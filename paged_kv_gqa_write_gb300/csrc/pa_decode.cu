@@ -229,47 +229,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, cval, sq - cbase);
     };
     if (p.balanced && grp < ngroups) {
-      // all context lengths at once (B <= kBalMaxSeqs), then the page prefix
-      // (unconditional loads of a clamped index, so that they issue together)
-      int np[kBalMaxSeqs / 32];
+      // lane l holds the page counts of sequences 16l .. 16l+15 (B <= 512;
+      // the host guarantees W < 2^31).  Loads of a clamped index are
+      // unconditional, so they issue together.
+      constexpr int R = kBalMaxSeqs / 32;
+      int np[R];
 #pragma unroll
-      for (int r = 0; r < kBalMaxSeqs / 32; ++r)
-        np[r] = __ldg(p.context_lens + min(r * 32 + lane, p.B - 1));
+      for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(lane * R + r, p.B - 1));
+      int lsum = 0;
 #pragma unroll
-      for (int r = 0; r < kBalMaxSeqs / 32; ++r)
-        np[r] = r * 32 + lane < p.B ? pages_of(np[r], p) : 0;
-      int64_t tot = 0;
+      for (int r = 0; r < R; ++r) {
+        np[r] = lane * R + r < p.B ? pages_of(np[r], p) : 0;
+        lsum += np[r];
+      }
+      int incl = lsum;
 #pragma unroll
-      for (int r = 0; r < kBalMaxSeqs / 32; ++r) tot += np[r];
-#pragma unroll
-      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      W = tot;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      W = __shfl_sync(0xffffffffu, incl, 31);
       lo = W * grp / ngroups;
       hi = W * (grp + 1) / ngroups;
       // first sequence the group touches: it reaches past lo, or it is empty
       // and sits at or after lo
-      int64_t base = 0;
+      int start = incl - lsum, hit_r = -1, hit_start = 0;
 #pragma unroll
-      for (int r = 0; r < kBalMaxSeqs / 32; ++r) {
-        const int sq = r * 32 + lane;
-        const int64_t span = np[r];
-        int64_t incl = span;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
+      for (int r = 0; r < R; ++r) {
+        const bool hit = lane * R + r < p.B &&
+                         (start + np[r] > lo || (np[r] == 0 && start >= lo));
+        if (hit && hit_r < 0) {
+          hit_r = r;
+          hit_start = start;
         }
-        const int64_t start = base + incl - span;
-        const bool hit = sq < p.B && (start + span > lo || (span == 0 && start >= lo));
-        const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (m && bs == p.B) {
-          const int f = __ffs(m) - 1;
-          bs = r * 32 + f;
-          bP = __shfl_sync(0xffffffffu, start, f);
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+        start += np[r];
       }
-      if (bs < p.B) {
+      const unsigned m = __ballot_sync(0xffffffffu, hit_r >= 0);
+      if (m) {
+        const int f = __ffs(m) - 1;
+        bs = f * R + __shfl_sync(0xffffffffu, hit_r, f);
+        bP = __shfl_sync(0xffffffffu, hit_start, f);
         bctx = ctx_at(bs);
         bn = pages_of(bctx, p);
       }
@@ -319,9 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // this lane's block-table entry among the first 32 pages of an item
+    // (it does not wait for the context length: entries past the sequence's
+    // pages are in the row and are never used)
     auto first_pid = [&](const Work& w) -> int {
       const int pg = w.pg0 + lane;
-      return pg < w.pg1 ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
+      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
     };
     Work nx;
     bool have = gen_next(nx);
