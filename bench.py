@@ -244,6 +244,64 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer larger than L2, then
+    reads another, so the timed kernel starts with clean (not dirty) lines."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
+    """One of the smaller decode configurations, timed per step with an L2
+    flush in between (their K+V is about the size of L2)."""
+    if name == "qwen3-14b-decode-b16":
+        case = W.qwen3_14b_decode_b16(device="cuda", pool_device="cuda")
+        with_write = False
+    else:
+        case = W.qwen3_32b_ragged(device="cuda", pool_device="cuda")
+        with_write = True
+    kv_bytes = int(case.context_lens.sum()) * case.Hkv * D * 2 * 2
+    out = torch.empty(case.B, case.Hq, D, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dims = pa.make_dims(case.B, case.Hq, case.Hkv, case.num_pages, case.max_pages_per_seq)
+    sched = pa.pa_decode_auto_splits(dims)
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(dims, 0)), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        if with_write:
+            pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                           case.block_table, case.context_lens, None, status=st)
+        pa.pa_decode(case.q, case.k_cache, case.v_cache, case.block_table, case.context_lens,
+                     case.scale, out=out, workspace=ws, num_splits=0, status=st)
+
+    flush = L2Flush(torch)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    return {"workload": name, "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv,
+            "kv_bytes": kv_bytes, "ms": ms, "gbs": kv_bytes / (ms * 1e-3) / 1e9,
+            "seqs_per_s": case.B / (ms * 1e-3), "status": int(st.item()),
+            "schedule": "page-balanced" if sched == 0 else f"{sched} fixed splits",
+            "step": ("pa_kv_write (1 token/seq) + " if with_write else "") + "pa_decode",
+            "l2": "flushed between steps"}
+
+
 def run_prefill(pa, W, torch, steps=20, warmup=3):
     """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
     case = W.chunked_prefill(device="cuda", pool_device="cuda")
@@ -261,14 +319,14 @@ def run_prefill(pa, W, torch, steps=20, warmup=3):
         pa.pa_prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table,
                             case.context_lens, case.chunk_lens, case.scale, out=out, status=st)
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for a, b in ev:
-        flush.zero_()                      # L2 flush between steps (working set < L2)
+        flush()                            # L2 flush between steps (working set < L2)
         a.record()
         step()
         b.record()
@@ -391,6 +449,16 @@ def run_ours(args):
             prefill["frac"] = prefill["tflops"] / bf16
         except Exception as e:  # report, do not hide
             prefill = {"error": str(e).splitlines()[0][:200]}
+    other = None
+    if not args.no_prefill:
+        other = []
+        for name in ("qwen3-14b-decode-b16", "qwen3-32b-ragged-b64"):
+            try:
+                r = run_decode_config(pa, W, torch, name)
+                r["frac"] = r["gbs"] / hbm
+                other.append(r)
+            except Exception as e:  # report, do not hide
+                other.append({"workload": name, "error": str(e).splitlines()[0][:200]})
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, nt, sample = cpu_oracle_rate(case, args.cpu_seconds)
@@ -421,6 +489,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "decode_configs": other,
         "cpu_baseline": cpu,
     }
     if rank == 0:

@@ -463,66 +463,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         // causal mask only where the tile crosses pos: masked scores take no part
         const int key0 = kt * kPage;
         const int nvis = min(max(pos - key0 + 1, 0), kPage);  // visible keys of this row
-        // row max of the visible raw scores (sign-flipped when the scale is negative)
-        const float sgn = c >= 0.f ? 1.f : -1.f;
-        auto row_max = [&](auto masked) -> float {
-          float mx8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float sv = __uint_as_float(sr[cc][e]) * sgn;
-              if (decltype(masked)::value) sv = (cc * 32 + e < nvis) ? sv : -INFINITY;
-              mx8[e & 7] = fmaxf(mx8[e & 7], sv);
-            }
-          return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        };
-        // warp-uniform choice: the P store below is a .sync.aligned TMEM op
+        // warp-uniform choices: the TMEM loads and stores below are .sync.aligned
         const bool diag = __any_sync(0xffffffffu, nvis < kPage);
-        const float mraw = diag ? row_max(std::true_type{}) : row_max(std::false_type{});
-        // max of c * s over the visible keys (-inf when none is visible)
-        const float mx = mraw == -INFINITY ? -INFINITY : mraw * (c * sgn);
-        const float m_new = fmaxf(m, mx);
-        bool rescale = false;
-        float alpha = 1.f;
-        if (m == -INFINITY) {
-          m = m_new;
-        } else if (m_new > m + kRescaleThreshold) {
-          alpha = fast_exp2(m - m_new);
-          rescale = true;
-          m = m_new;
-        }
-        const float m_use = m == -INFINITY ? 0.f : m;  // nothing visible yet: p = 0
-        float sum8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-        // P (BF16 pairs) over the first 64 columns of this tile's S buffer
-        auto write_p = [&](auto masked) {
+        const float2 c2 = make_float2(c, c);
+        if (__any_sync(0xffffffffu, m == -INFINITY)) {
+          // the row's first key tile: the exact max of c * s over the visible keys
+          float mx = -INFINITY;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
-            uint32_t w[16];
+            uint32_t sr[32];
+            tmem_ld32(s_cols + cc * 32, sr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float t = __uint_as_float(sr[e]) * c;
+              mx = fmaxf(mx, cc * 32 + e < nvis ? t : -INFINITY);
+            }
+          }
+          if (m == -INFINITY) m = mx;
+        }
+        // One pass, speculatively against the running reference m: p = 2^(c s - m),
+        // tracking the largest exponent.  The reference moves (and the tile is
+        // redone) only when some visible score exceeds it by more than 2^8.
+        float alpha = 1.f;
+        bool rescale = false;
+        uint32_t pw[64];  // P as BF16 pairs
+        float2 sum2;
+        auto pass = [&](float m_ref, auto masked) -> float {
+          const float2 nm2 = make_float2(-m_ref, -m_ref);
+          float dmax = -INFINITY;
+          sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t sr[32];
+            tmem_ld32(s_cols + cc * 32, sr);
+            tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int k0e = cc * 32 + 2 * e;
-              float p0 = fast_exp2(fmaf(__uint_as_float(sr[cc][2 * e]), c, -m_use));
-              float p1 = fast_exp2(fmaf(__uint_as_float(sr[cc][2 * e + 1]), c, -m_use));
+              float2 d2 = __ffma2_rn(make_float2(__uint_as_float(sr[2 * e]),
+                                                 __uint_as_float(sr[2 * e + 1])), c2, nm2);
               if (decltype(masked)::value) {
-                p0 = k0e < nvis ? p0 : 0.f;
-                p1 = k0e + 1 < nvis ? p1 : 0.f;
+                const int k0e = cc * 32 + 2 * e;
+                d2.x = k0e < nvis ? d2.x : -INFINITY;
+                d2.y = k0e + 1 < nvis ? d2.y : -INFINITY;
               }
-              sum8[e & 7] += p0 + p1;
-              w[e] = pack_bf16x2(p0, p1);
+              dmax = fmaxf(dmax, fmaxf(d2.x, d2.y));
+              const float2 p2 = make_float2(fast_exp2(d2.x), fast_exp2(d2.y));
+              sum2 = __fadd2_rn(sum2, p2);
+              pw[cc * 16 + e] = pack_bf16x2(p2.x, p2.y);
             }
-            tmem_st16(s_cols + cc * 16, w);
           }
+          return dmax;
         };
-        if (diag) write_p(std::true_type{}); else write_p(std::false_type{});
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        l = l * alpha + sum;
+        const float m_use = m == -INFINITY ? 0.f : m;  // nothing visible yet: every p = 0
+        const float dmax = diag ? pass(m_use, std::true_type{}) : pass(m_use, std::false_type{});
+        const bool over = dmax > kRescaleThreshold;
+        if (__any_sync(0xffffffffu, over)) {
+          // rare: move this row's reference up to its tile max and redo the tile
+          const float m_new = over ? m_use + dmax : m_use;
+          if (over) {
+            alpha = fast_exp2(-dmax);
+            rescale = true;
+            m = m_new;
+          }
+          if (diag) pass(m_new, std::true_type{}); else pass(m_new, std::false_type{});
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pw[cc * 16 + e];
+          tmem_st16(s_cols + cc * 16, w);
+        }
+        l = l * alpha + (sum2.x + sum2.y);
         if (zero_mine && kt == nkt - 1) {
           // zero V rows past the context in the last page before P.V reads them
           const uint32_t kidx = k0 + kt;
