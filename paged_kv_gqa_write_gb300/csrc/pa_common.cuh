@@ -19,6 +19,8 @@ constexpr int kPage = 128;
 // last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kMaxPolls = 1u << 30;
+// Longest a waiting thread sleeps per poll (it wakes earlier when the phase completes).
+constexpr uint32_t kSleepHintNs = 20000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,6 +63,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As above, but the thread may sleep up to `hint_ns` waiting for the phase
+// instead of returning at once, so a waiting warp does not take issue slots
+// from the other warps of its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -73,8 +91,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if ((i & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
   }
   if (status) atomicOr(status, PA_STATUS_TIMEOUT);
   return false;

@@ -49,7 +49,7 @@ constexpr int kVWarp = 10;                    // V producer
 constexpr int kThreads = (kVWarp + 1) * 32;
 constexpr int kTileBytes = 128 * 128 * 2;     // 32 KB: one 128x128 bf16 tile
 constexpr int kBox = 16384;                   // 64-column half of a tile
-constexpr int kRingK = 3, kRingV = 2;
+constexpr int kRingK = 2, kRingV = 3;
 constexpr int kMaxList = 64;                  // scheduled items per CTA
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kQ = 0;                         // Q_A, Q_B
