@@ -165,10 +165,13 @@ def decode_traffic_from_profile():
     """dram bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
     import hashlib
-    src = os.path.join(ROOT, "paged_kv_gqa_write_gb300", "csrc", "pa_decode.cu")
+    csrc = os.path.join(ROOT, "paged_kv_gqa_write_gb300", "csrc")
     prof = os.path.join(ROOT, "profiles", "decode_kernel_qwen3-14b-b16.md")
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        # the decode path: its kernel, the combines and the shared device helpers
+        blob = b"".join(open(os.path.join(csrc, f), "rb").read()
+                        for f in ("pa_decode.cu", "pa_combine.cu", "pa_common.cuh"))
+        h = hashlib.sha256(blob).hexdigest()[:16]
         vals = {}
         for line in open(prof):
             if ":" in line and line.strip().startswith("- "):
