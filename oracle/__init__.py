@@ -39,6 +39,14 @@ def _load():
                                                ctypes.POINTER(c_dbl), f64p]
         lib.oracle_combine.restype = None
         lib.oracle_combine.argtypes = [f64p, f64p, c_i64, c_int, c_int, f64p]
+        f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+        lib.oracle_qk_norm_rope_write.restype = c_int
+        lib.oracle_qk_norm_rope_write.argtypes = [u16p, f32p, f32p, c_dbl, c_dbl, c_dbl, c_dbl,
+                                                  f64p, u16p, u16p, i32p, i32p, ctypes.c_void_p,
+                                                  c_i64, c_int, c_int, c_int, c_int, c_int,
+                                                  c_int, c_int]
+        lib.oracle_rope_neox.restype = None
+        lib.oracle_rope_neox.argtypes = [f64p, c_int, c_dbl, c_dbl, c_dbl]
         lib.oracle_max_threads.restype = c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -137,3 +145,36 @@ def combine(part_o, part_lse):
     out = np.zeros((max(R, 1), D), dtype=np.float64)
     _load().oracle_combine(po, pl, R, S, D, out)
     return out[:R]
+
+
+def rope_neox(x, pos, base, scale=1.0):
+    """NeoX rotary embedding of one head vector x [D] (float64) at position pos."""
+    y = np.array(x, dtype=np.float64, copy=True)
+    _load().oracle_rope_neox(y, y.shape[0], float(pos), float(base), float(scale))
+    return y
+
+
+def qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table,
+                       context_lens, chunk_lens, num_q_heads, num_kv_heads, num_pages,
+                       max_pages_per_seq, eps=1e-6, rope_base=1e6, rope_scale=1.0,
+                       q_scale=1.0, page_size=128, head_dim=128):
+    """The prologue: per-head RMSNorm of Q and K, NeoX RoPE at each token's
+    position, Q times q_scale; K (bf16-rounded) and V written to their slots.
+    qkv is [T, (Hq + 2 Hkv) * D] bf16.  Returns (q_out [T, Hq, D] float64,
+    k_cache', v_cache', skipped); the caches passed in are not modified."""
+    x = _u16(qkv).reshape(-1)
+    T = x.size // ((num_q_heads + 2 * num_kv_heads) * head_dim)
+    kc = _u16(k_cache).copy()
+    vc = _u16(v_cache).copy()
+    ctx = _i32(context_lens)
+    cl = None if chunk_lens is None else _i32(chunk_lens)
+    q_out = np.zeros((max(T, 1), num_q_heads, head_dim), dtype=np.float64)
+    wq = np.ascontiguousarray(q_norm_w, dtype=np.float32)
+    wk = np.ascontiguousarray(k_norm_w, dtype=np.float32)
+    skipped = _load().oracle_qk_norm_rope_write(
+        x, wq, wk, float(eps), float(rope_base), float(rope_scale), float(q_scale), q_out,
+        kc.reshape(-1), vc.reshape(-1), _i32(block_table).reshape(-1), ctx,
+        None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
+        T, ctx.shape[0], num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+        max_pages_per_seq)
+    return q_out[:T], kc, vc, skipped

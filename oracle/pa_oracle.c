@@ -269,3 +269,121 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * Decode / prefill prologue: Q/K norm -> RoPE -> KV cache write.
+ *
+ * "Qwen 3" (TensorSharp model doc), section 3 "Forward graph": after the
+ * fused QKV projection, per-head RMSNorm(Q) with attn_q_norm.weight and
+ * per-head RMSNorm(K) with attn_k_norm.weight, then RoPE_NeoX(Q, K) at the
+ * tokens' positions, then Q <- Q * (1/sqrt(headDim)), then (K, V) appended to
+ * the KV cache.  Section 4.1: QK-norm is an RMSNorm over each head's headDim
+ * values with a weight vector of size headDim; RoPE is NeoX-style with
+ * frequencies from rope.freq_base and rope.scale (section 5: "frequency scale
+ * divisor").  Section 4.3: epsilon from the config (typically 1e-6).
+ * "Qwen3-14B" (pypto-lib), "Model structure, top down": decode_fwd runs
+ * "Q/K norm -> RoPE" before the KV cache write; "Deployment configuration":
+ * FP32 RMSNorm weights.
+ *
+ * Readings (each also in the design doc):
+ *  - RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w, over the head's D values;
+ *  - NeoX RoPE rotates the pair (x[i], x[i + D/2]), i < D/2, by the angle
+ *    pos * f_i with f_i = base^(-2i/D) / scale:
+ *      x'[i]       = x[i] cos - x[i + D/2] sin,
+ *      x'[i + D/2] = x[i + D/2] cos + x[i] sin;
+ *  - the input is the fused projection output, one row per token laid out as
+ *    [Hq heads | Hkv heads (K) | Hkv heads (V)] of D values each;
+ *  - the position of new token j of sequence s is ctx[s] - n[s] + j, as in
+ *    the KV write; Q is multiplied by q_scale (1/sqrt(D) for the pages'
+ *    folding, or 1 when the attention call applies the scale itself);
+ *  - K is rounded to bf16 (round to nearest even, through float) before it
+ *    is stored; V is stored bit for bit.
+ * ------------------------------------------------------------------------ */
+
+/* float -> bf16 bits, round to nearest even (finite inputs). */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t rounding = 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)((u + rounding) >> 16);
+}
+
+/* RMSNorm of one head (section 4.1 QK-norm, section 4.3 epsilon). */
+static void rms_norm_head(const double* x, const float* w, int d, double eps, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+  double r = 1.0 / sqrt(ss / d + eps);
+  for (int i = 0; i < d; ++i) y[i] = x[i] * r * (double)w[i];
+}
+
+/* NeoX rotary embedding of one head at position pos (section 4.1 RoPE). */
+void oracle_rope_neox(double* y, int d, double pos, double base, double scale) {
+  int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    double f = pow(base, -2.0 * i / d) / scale;
+    double a = pos * f;
+    double c = cos(a), s = sin(a);
+    double x0 = y[i], x1 = y[i + half];
+    y[i] = x0 * c - x1 * s;
+    y[i + half] = x1 * c + x0 * s;
+  }
+}
+
+/*
+ * qkv      bf16 [num_tokens, (Hq + 2 Hkv) * D]
+ * q_out    double [num_tokens, Hq, D] (normed, rotated, times q_scale); rows of
+ *          invalid sequences are zero
+ * k_cache, v_cache  bf16 pools, written like oracle_kv_write (K normed+rotated,
+ *          rounded to bf16; V copied)
+ * Returns the number of sequences skipped as invalid.
+ */
+int oracle_qk_norm_rope_write(const uint16_t* qkv, const float* wq, const float* wk,
+                              double eps, double rope_base, double rope_scale,
+                              double q_scale, double* q_out, uint16_t* k_cache,
+                              uint16_t* v_cache, const int32_t* block_table,
+                              const int32_t* context_lens, const int32_t* chunk_lens,
+                              int64_t num_tokens, int num_seqs, int hq, int hkv, int d,
+                              int page_size, int num_pages, int max_pages_per_seq) {
+  const int64_t row_in = (int64_t)(hq + 2 * hkv) * d;
+  const int64_t row_kv = (int64_t)hkv * d;
+  double* x = (double*)malloc(sizeof(double) * d);
+  double* y = (double*)malloc(sizeof(double) * d);
+  int64_t token = 0;
+  int skipped = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    int64_t n = chunk_lens ? chunk_lens[s] : 1;
+    int ok = seq_valid(block_table, context_lens, chunk_lens, s, page_size, num_pages,
+                       max_pages_per_seq);
+    if (!ok) ++skipped;
+    int64_t ctx = context_lens[s];
+    for (int64_t j = 0; j < n && token < num_tokens; ++j, ++token) {
+      const uint16_t* r = qkv + token * row_in;
+      int64_t pos = ctx - n + j;
+      for (int h = 0; h < hq; ++h) {
+        double* dst = q_out + (token * hq + h) * d;
+        if (!ok) {
+          for (int i = 0; i < d; ++i) dst[i] = 0.0;
+          continue;
+        }
+        for (int i = 0; i < d; ++i) x[i] = bf16_to_f64(r[h * d + i]);
+        rms_norm_head(x, wq, d, eps, y);
+        oracle_rope_neox(y, d, (double)pos, rope_base, rope_scale);
+        for (int i = 0; i < d; ++i) dst[i] = y[i] * q_scale;
+      }
+      if (!ok) continue;
+      int64_t page = block_table[(int64_t)s * max_pages_per_seq + pos / page_size];
+      int64_t slot = page * page_size + pos % page_size;
+      for (int h = 0; h < hkv; ++h) {
+        for (int i = 0; i < d; ++i) x[i] = bf16_to_f64(r[(hq + h) * d + i]);
+        rms_norm_head(x, wk, d, eps, y);
+        oracle_rope_neox(y, d, (double)pos, rope_base, rope_scale);
+        for (int i = 0; i < d; ++i)
+          k_cache[slot * row_kv + h * d + i] = f32_to_bf16_rne((float)y[i]);
+      }
+      memcpy(v_cache + slot * row_kv, r + (int64_t)(hq + hkv) * d, (size_t)row_kv * 2);
+    }
+  }
+  free(x);
+  free(y);
+  return skipped;
+}
