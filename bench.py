@@ -305,6 +305,46 @@ def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
             "l2": "flushed between steps"}
 
 
+def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
+    """pa_qk_norm_rope_write (Q/K RMSNorm -> NeoX RoPE -> KV write) on the decode
+    batch (128 tokens) and on the 8 x 512 prefill chunk, with a clean L2 flush
+    between steps.  Bytes: the fused QKV rows read, Q and the K/V rows written."""
+    out = {}
+    flush = L2Flush(torch)
+    for name, case in (("decode-b128", W.qwen3_14b_decode_b128(device="cuda", pool_device="cuda",
+                                                                with_new=False)),
+                       ("prefill-b8-c512", W.chunked_prefill(device="cuda", pool_device="cuda"))):
+        qkv, wq, wk = W.prologue_inputs(case, 600, device="cuda")
+        chunked = case.chunk_lens is not None
+        q_out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def step():
+            pa.pa_qk_norm_rope_write(qkv, wq, wk, case.k_cache, case.v_cache, case.block_table,
+                                     case.context_lens, case.chunk_lens if chunked else None,
+                                     q_scale=1.0 / math.sqrt(D), q_out=q_out, status=st)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush()
+            a.record()
+            step()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        nbytes = case.T * (case.Hq + 2 * case.Hkv) * D * 2 * 2
+        out[name] = {"tokens": case.T, "us": ms * 1e3, "bytes": nbytes,
+                     "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                     "status": int(st.item())}
+    out["step"] = "pa_qk_norm_rope_write"
+    out["l2"] = "flushed between steps"
+    return out
+
+
 def run_prefill(pa, W, torch, steps=20, warmup=3):
     """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
     case = W.chunked_prefill(device="cuda", pool_device="cuda")
@@ -452,6 +492,12 @@ def run_ours(args):
             prefill["frac"] = prefill["tflops"] / bf16
         except Exception as e:  # report, do not hide
             prefill = {"error": str(e).splitlines()[0][:200]}
+    prologue = None
+    if not args.no_prefill:
+        try:
+            prologue = run_prologue(pa, W, torch, hbm)
+        except Exception as e:  # report, do not hide
+            prologue = {"error": str(e).splitlines()[0][:200]}
     other = None
     if not args.no_prefill:
         other = []
@@ -493,6 +539,7 @@ def run_ours(args):
         "clocks": clocks,
         "prefill": prefill,
         "decode_configs": other,
+        "prologue": prologue,
         "cpu_baseline": cpu,
     }
     if rank == 0:

@@ -124,6 +124,38 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
                 int32_t* status, pa_stream_t stream);
 
 /*
+ * pa_qk_norm_rope_write -- the prologue of decode and prefill: per-head
+ * RMSNorm of Q and K, NeoX rotary embedding at each new token's position, and
+ * the KV cache write, fused in one pass.  "Qwen 3" (TensorSharp model doc),
+ * section 3 "Forward graph" (per-head RMSNorm(Q) / RMSNorm(K) with
+ * attn_q_norm / attn_k_norm, RoPE_NeoX at the tokens' positions, Q times
+ * 1/sqrt(headDim), (K, V) appended to the cache), section 4.1 (QK-norm over
+ * each head's headDim values; NeoX RoPE from rope.freq_base and rope.scale),
+ * section 4.3 (epsilon); "Qwen3-14B" (pypto-lib), "Model structure, top down"
+ * (decode_fwd: Q/K norm -> RoPE -> KV cache write; FP32 RMSNorm weights).
+ *   qkv            bf16 [num_tokens, (Hq + 2 Hkv) * D]: the fused projection's
+ *                  rows, [Hq query heads | Hkv key heads | Hkv value heads]
+ *   q_norm_w, k_norm_w  float32 [D], the per-head RMSNorm weights
+ *   eps            RMSNorm epsilon: y = x / sqrt(mean(x^2) + eps) * w
+ *   rope_base, rope_scale  pair (i, i + D/2) turns by pos * base^(-2i/D) / scale
+ *   q_scale        multiplies Q after RoPE (1/sqrt(D) to fold the softmax scale
+ *                  into Q, then call pa_decode with scale 1; or 1)
+ *   q_out          bf16 [num_tokens, Hq, D], the input of pa_decode /
+ *                  pa_prefill_chunk; rows of an invalid sequence are zero
+ *   k_cache, v_cache, block_table, context_lens, chunk_lens, num_tokens,
+ *   status: exactly as pa_kv_write (K is written normed and rotated, rounded
+ *   to bf16; V bit for bit).  Positions are context_lens[s] - chunk_lens[s] + j.
+ * Returns PA_ERR_DIMS for eps < 0, rope_base <= 0, rope_scale <= 0 or a
+ * non-finite value; every pointer must be 16-byte aligned.
+ */
+int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                          float eps, float rope_base, float rope_scale, float q_scale,
+                          void* q_out, void* k_cache, void* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          const int32_t* chunk_lens, int32_t num_tokens, pa_dims dims,
+                          int32_t* status, pa_stream_t stream);
+
+/*
  * pa_decode -- single-token paged GQA attention, one query token per sequence.
  *   q              bf16 [B, Hq, D]
  *   scale          multiplies every score q.k (1/sqrt(D) for Qwen3)

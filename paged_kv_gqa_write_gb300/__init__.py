@@ -29,7 +29,7 @@ PA_BALANCED_MAX_SEQS = 512
 
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
-            "pa_decode_noalloc")
+            "pa_decode_noalloc", "pa_qk_norm_rope_write")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -61,6 +61,9 @@ def load(path: str = LIB_PATH):
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     lib.pa_kv_write.restype = ctypes.c_int
     lib.pa_kv_write.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, pa_dims, vp, vp]
+    lib.pa_qk_norm_rope_write.restype = ctypes.c_int
+    lib.pa_qk_norm_rope_write.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, vp,
+                                          vp, i32, pa_dims, vp, vp]
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, vp, sz, i32, pa_dims, vp, vp]
     lib.pa_decode_workspace_size.restype = sz
@@ -146,6 +149,39 @@ def pa_kv_write(k_new, v_new, k_cache, v_cache, block_table, context_lens, chunk
                             _ptr(block_table), _ptr(context_lens), _ptr(chunk_lens),
                             int(k_new.shape[0]), d, _ptr(status), _stream(stream))
     _check("pa_kv_write", rc)
+
+
+def pa_qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table,
+                          context_lens, chunk_lens=None, eps=1e-6, rope_base=1e6,
+                          rope_scale=1.0, q_scale=1.0, q_out=None, status=None, stream=None):
+    """Q/K RMSNorm -> NeoX RoPE -> KV cache write for the new tokens.  qkv is the
+    fused projection output [T, (Hq + 2 Hkv) * 128] bf16; returns q_out [T, Hq, 128]."""
+    dev = k_cache.device
+    _need(qkv, "qkv", torch.bfloat16, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(q_norm_w, "q_norm_w", torch.float32, dev)
+    _need(k_norm_w, "k_norm_w", torch.float32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if chunk_lens is not None:
+        _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    Hkv = k_cache.shape[2]
+    T = qkv.shape[0]
+    Hq = qkv.reshape(T, -1).shape[1] // HEAD_DIM - 2 * Hkv
+    d = _cache_dims(Hq, k_cache, block_table)
+    if q_out is None:
+        q_out = torch.empty(T, Hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", torch.bfloat16, dev)
+    rc = load().pa_qk_norm_rope_write(
+        _ptr(qkv), _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base),
+        float(rope_scale), float(q_scale), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), _ptr(context_lens), _ptr(chunk_lens), int(T), d, _ptr(status),
+        _stream(stream))
+    _check("pa_qk_norm_rope_write", rc)
+    return q_out
 
 
 def pa_decode_workspace_size(dims, num_splits=0) -> int:

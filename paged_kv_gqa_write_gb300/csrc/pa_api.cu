@@ -305,7 +305,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 101; }
+int32_t pa_abi_version(void) { return 102; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -362,6 +362,53 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   return launch_result(pa::launch_kv_write(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                          float eps, float rope_base, float rope_scale, float q_scale,
+                          void* q_out, void* k_cache, void* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          const int32_t* chunk_lens, int32_t num_tokens, pa_dims d,
+                          int32_t* status, pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_tokens < 0) return PA_ERR_DIMS;
+  if (!chunk_lens && num_tokens != d.num_seqs) return PA_ERR_DIMS;
+  if (chunk_lens && d.num_seqs > PA_MAX_CHUNKED_SEQS) return PA_ERR_TOO_MANY_SEQS;
+  if (!(eps >= 0.f) || !(rope_base > 0.f) || !(rope_scale > 0.f) || !std::isfinite(eps) ||
+      !std::isfinite(rope_base) || !std::isfinite(rope_scale) || !std::isfinite(q_scale))
+    return PA_ERR_DIMS;
+  if (num_tokens == 0 || d.num_seqs == 0) return PA_OK;
+  if (!qkv || !q_norm_w || !k_norm_w || !q_out || !k_cache || !v_cache || !block_table ||
+      !context_lens)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(qkv) || !aligned16(q_norm_w) || !aligned16(k_norm_w) || !aligned16(q_out) ||
+      !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  pa::PrologueParams p;
+  p.qkv = static_cast<const uint2*>(qkv);
+  p.wq = q_norm_w;
+  p.wk = k_norm_w;
+  p.q_out = static_cast<uint2*>(q_out);
+  p.k_cache = static_cast<uint2*>(k_cache);
+  p.v_cache = static_cast<uint2*>(v_cache);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.chunk_lens = chunk_lens;
+  p.status = status;
+  p.eps = eps;
+  p.q_scale = q_scale;
+  p.log2_base = std::log2((double)rope_base);
+  p.rope_scale = rope_scale;
+  p.B = d.num_seqs;
+  p.T = num_tokens;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.num_pages = d.num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  return launch_result(pa::launch_prologue(p, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t pa_decode_auto_splits(pa_dims d) {

@@ -328,6 +328,64 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr) {
   return v;
 }
 
+// ---------------------------------------------------------------- token -> slot
+// (used by the kernels that write new tokens into the cache)
+// Inclusive prefix sums of max(chunk_lens, 0) into off[0..B), built by the
+// whole block.  Returns (in every thread) whether any chunk length was negative.
+__device__ __forceinline__ bool block_chunk_offsets(const int32_t* chunk_lens, int B, int32_t* off,
+                                    int32_t* scratch /* blockDim.x ints */) {
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const int per = (B + nt - 1) / nt;
+  const int lo = min(B, tid * per), hi = min(B, lo + per);
+  int sum = 0, neg = 0;
+  for (int i = lo; i < hi; ++i) {
+    int c = chunk_lens[i];
+    neg |= c < 0;
+    sum += c > 0 ? c : 0;
+    off[i] = sum;
+  }
+  scratch[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < nt; ++i) {
+      int v = scratch[i];
+      scratch[i] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  for (int i = lo; i < hi; ++i) off[i] += scratch[tid];
+  return __syncthreads_or(neg) != 0;
+}
+
+// Sequence holding packed token `token`: the first s with off[s] > token, or B.
+__device__ __forceinline__ int seq_of_token(const int32_t* off, int B, int token) {
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (off[mid] > token) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// Warp-wide check that sequence s has consistent lengths and that every
+// block-table entry it references lies in [0, num_pages).  Returns 0 when
+// valid, else a PA_STATUS_* bit.
+__device__ __forceinline__ int warp_check_sequence(const int32_t* block_table, int s, int ctx, int n,
+                                   int num_pages, int max_pages) {
+  if (ctx < 0 || n < 0 || n > ctx || ctx > max_pages * kPage) return PA_STATUS_BAD_LENGTH;
+  const int used = (ctx + kPage - 1) / kPage;
+  const int lane = threadIdx.x & 31;
+  const int32_t* row = block_table + (int64_t)s * max_pages;
+  bool bad = false;
+  for (int i = lane; i < used; i += 32) {
+    int p = row[i];
+    bad |= (p < 0 || p >= num_pages);
+  }
+  return __any_sync(0xffffffffu, bad) ? PA_STATUS_BAD_PAGE : 0;
+}
+
 // ---------------------------------------------------------------- params
 struct DecodeParams {
   const __nv_bfloat16* q;       // [B, Hq, D]
@@ -348,6 +406,23 @@ struct DecodeParams {
   int32_t grid;                 // CTAs of the page-balanced schedule (groups x Hkv*NG)
   float* bal_o;                 // [2 * grid][16][D] partial records of cut sequences
   float* bal_lse;               // [2 * grid][16]
+};
+
+// Q/K RMSNorm -> NeoX RoPE -> KV cache write for the new tokens.
+struct PrologueParams {
+  const uint2* qkv;             // [T, (Hq + 2 Hkv) * D] bf16, 4 values per uint2
+  const float* wq;              // [D] Q norm weight
+  const float* wk;              // [D] K norm weight
+  uint2* q_out;                 // [T, Hq, D] bf16
+  uint2* k_cache;               // [num_pages, 128, Hkv, D] bf16
+  uint2* v_cache;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  const int32_t* chunk_lens;    // may be null (one token per sequence)
+  int32_t* status;
+  float eps, q_scale;
+  double log2_base, rope_scale;  // RoPE: log2 of the frequency base, scale divisor
+  int32_t B, T, Hq, Hkv, num_pages, max_pages;
 };
 
 // Merge of the sequences that the page-balanced decode schedule cut between

@@ -10,62 +10,6 @@
 
 namespace pa {
 
-// Inclusive prefix sums of max(chunk_lens, 0) into off[0..B), built by the
-// whole block.  Returns (in every thread) whether any chunk length was negative.
-__device__ bool block_chunk_offsets(const int32_t* chunk_lens, int B, int32_t* off,
-                                    int32_t* scratch /* blockDim.x ints */) {
-  const int nt = blockDim.x, tid = threadIdx.x;
-  const int per = (B + nt - 1) / nt;
-  const int lo = min(B, tid * per), hi = min(B, lo + per);
-  int sum = 0, neg = 0;
-  for (int i = lo; i < hi; ++i) {
-    int c = chunk_lens[i];
-    neg |= c < 0;
-    sum += c > 0 ? c : 0;
-    off[i] = sum;
-  }
-  scratch[tid] = sum;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < nt; ++i) {
-      int v = scratch[i];
-      scratch[i] = run;
-      run += v;
-    }
-  }
-  __syncthreads();
-  for (int i = lo; i < hi; ++i) off[i] += scratch[tid];
-  return __syncthreads_or(neg) != 0;
-}
-
-// Sequence holding packed token `token`: the first s with off[s] > token, or B.
-__device__ __forceinline__ int seq_of_token(const int32_t* off, int B, int token) {
-  int lo = 0, hi = B;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (off[mid] > token) hi = mid; else lo = mid + 1;
-  }
-  return lo;
-}
-
-// Warp-wide check that sequence s has consistent lengths and that every
-// block-table entry it references lies in [0, num_pages).  Returns 0 when
-// valid, else a PA_STATUS_* bit.
-__device__ int warp_check_sequence(const int32_t* block_table, int s, int ctx, int n,
-                                   int num_pages, int max_pages) {
-  if (ctx < 0 || n < 0 || n > ctx || ctx > max_pages * kPage) return PA_STATUS_BAD_LENGTH;
-  const int used = (ctx + kPage - 1) / kPage;
-  const int lane = threadIdx.x & 31;
-  const int32_t* row = block_table + (int64_t)s * max_pages;
-  bool bad = false;
-  for (int i = lane; i < used; i += 32) {
-    int p = row[i];
-    bad |= (p < 0 || p >= num_pages);
-  }
-  return __any_sync(0xffffffffu, bad) ? PA_STATUS_BAD_PAGE : 0;
-}
-
 __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
   extern __shared__ int32_t kvw_smem[];
   int32_t* off = kvw_smem;              // [B] when chunk_lens != null

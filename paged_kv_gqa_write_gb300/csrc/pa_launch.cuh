@@ -6,6 +6,9 @@ namespace pa {
 
 cudaError_t launch_kv_write(const KvWriteParams& p, int num_sms, cudaStream_t stream);
 
+// Q/K RMSNorm, NeoX RoPE and the KV write of the new tokens, fused.
+cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t stream);
+
 // Decode: persistent flash-decoding kernel over (split, sequence, kv head,
 // head group) items.  tm_k / tm_v are 2-D tensor maps over the caches viewed
 // as [num_pages * 128 rows, Hkv * 128 columns] bf16 with 128-byte swizzle and

@@ -55,7 +55,7 @@ def test_python_constants_match_header(pa):
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
-    assert pa.pa_abi_version() == 101
+    assert pa.pa_abi_version() == 102
 
 
 def test_status_strings(pa):
@@ -111,6 +111,15 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 3, d, None, None) == h["PA_ERR_OUT_DTYPE"]
     assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1.0, FAKE, 0, d, None, None) == 0
     assert lib.pa_combine(FAKE, FAKE, 0, FAKE, 0, d, None) == h["PA_ERR_SPLITS"]
+    pro = lambda eps=1e-6, base=1e6, scale=1.0, qkv=FAKE, n=2, cl=None: lib.pa_qk_norm_rope_write(
+        qkv, FAKE, FAKE, eps, base, scale, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, cl, n, d, None, None)
+    assert pro(eps=-1.0) == h["PA_ERR_DIMS"]
+    assert pro(base=0.0) == h["PA_ERR_DIMS"]
+    assert pro(scale=float("nan")) == h["PA_ERR_DIMS"]
+    assert pro(n=3) == h["PA_ERR_DIMS"]                    # decode: one token per sequence
+    assert pro(qkv=None) == h["PA_ERR_NULL_POINTER"]
+    assert pro(qkv=MIS) == h["PA_ERR_ALIGNMENT"]
+    assert pro(n=0, cl=FAKE) == 0
     assert lib.pa_combine(FAKE, FAKE, 2, MIS, 0, d, None) == h["PA_ERR_ALIGNMENT"]
 
 

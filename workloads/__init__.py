@@ -28,6 +28,7 @@ NAN_BF16 = 0x7FC0
 
 # tensor ids inside a config's seed space
 _T_K, _T_V, _T_Q, _T_KNEW, _T_VNEW, _T_LEN, _T_PERM, _T_PRIOR = 1, 2, 3, 4, 5, 6, 7, 8
+_T_QKV, _T_WQ, _T_WK = 9, 10, 11
 
 
 @dataclass
@@ -273,3 +274,15 @@ CONFIGS = {
     "qwen3-32b-ragged": qwen3_32b_ragged,
     "chunked-prefill": chunked_prefill,
 }
+
+
+def prologue_inputs(case: PagedCase, seed: int, device="cpu"):
+    """Inputs of the QK-norm / RoPE / KV-write prologue for `case`'s new tokens:
+    the fused projection rows qkv [T, (Hq + 2 Hkv) * 128] bf16 ~ N(0, 1) and the
+    FP32 per-head norm weights q_norm_w, k_norm_w [128] ~ U[0.5, 1.5]."""
+    T = case.T
+    row = (case.Hq + 2 * case.Hkv) * PAGE
+    qkv = randn_bf16((T, row), seed + _T_QKV, device=device)
+    wq = (torch.rand(PAGE, generator=_gen(seed + _T_WQ)) + 0.5).to(device)
+    wk = (torch.rand(PAGE, generator=_gen(seed + _T_WK)) + 0.5).to(device)
+    return qkv, wq, wk
