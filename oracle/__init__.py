@@ -47,6 +47,8 @@ def _load():
                                                   c_int, c_int]
         lib.oracle_rope_neox.restype = None
         lib.oracle_rope_neox.argtypes = [f64p, c_int, c_dbl, c_dbl, c_dbl]
+        lib.oracle_topk.restype = None
+        lib.oracle_topk.argtypes = [f32p, c_i64, c_int, c_int, c_int, f32p, i32p]
         lib.oracle_max_threads.restype = c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -178,3 +180,14 @@ def qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table,
         T, ctx.shape[0], num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
         max_pages_per_seq)
     return q_out[:T], kc, vc, skipped
+
+
+def topk(logits, k):
+    """Exact top-k of each row of logits [rows, vocab] (float32): values and int32
+    indices [rows, k], larger first, NaN above +inf, ties by smaller index."""
+    x = np.ascontiguousarray(logits, dtype=np.float32)
+    rows, vocab = x.shape
+    vals = np.zeros((max(rows, 1), k), dtype=np.float32)
+    idx = np.zeros((max(rows, 1), k), dtype=np.int32)
+    _load().oracle_topk(x, vocab, rows, vocab, int(k), vals, idx)
+    return vals[:rows], idx[:rows]

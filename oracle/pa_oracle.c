@@ -387,3 +387,53 @@ int oracle_qk_norm_rope_write(const uint16_t* qkv, const float* wq, const float*
   free(y);
   return skipped;
 }
+
+/* ------------------------------------------------------------------------
+ * Exact top-k over rows of logits.
+ *
+ * pypto-serving PR #77 (page 3), "Exactness Design": an exact Top-32 of a
+ * row's full-vocabulary logits (151936 real entries for Qwen3-14B), checked
+ * against torch.topk(logits[:, :REAL_VOCAB], 32); the selector returns the
+ * candidate values and token IDs.  The oracle is the plain definition: sort the
+ * row's (value, index) pairs and take the first k.
+ *
+ * Readings (each also in the design doc):
+ *  - order: larger value first; NaN ranks above +inf (as torch.topk does);
+ *    among equal values the smaller index comes first (the page fixes no tie
+ *    order; this one is total, so the result is unique);
+ *  - output: k values (as given) and their int32 indices, in that order.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  float v;
+  int32_t i;
+} vi_pair;
+
+static int nan_or(float x) { return x != x; }
+
+/* qsort comparator: descending value (NaN largest), then ascending index. */
+static int cmp_desc(const void* a, const void* b) {
+  const vi_pair* x = (const vi_pair*)a;
+  const vi_pair* y = (const vi_pair*)b;
+  int xn = nan_or(x->v), yn = nan_or(y->v);
+  if (xn != yn) return xn ? -1 : 1;
+  if (!xn && x->v != y->v) return x->v > y->v ? -1 : 1;
+  return (x->i < y->i) ? -1 : (x->i > y->i);
+}
+
+void oracle_topk(const float* logits, int64_t row_stride, int rows, int vocab, int k,
+                 float* out_values, int32_t* out_indices) {
+  vi_pair* buf = (vi_pair*)malloc(sizeof(vi_pair) * (size_t)(vocab > 0 ? vocab : 1));
+  for (int r = 0; r < rows; ++r) {
+    const float* row = logits + (int64_t)r * row_stride;
+    for (int i = 0; i < vocab; ++i) {
+      buf[i].v = row[i];
+      buf[i].i = i;
+    }
+    qsort(buf, (size_t)vocab, sizeof(vi_pair), cmp_desc);
+    for (int j = 0; j < k; ++j) {
+      out_values[(int64_t)r * k + j] = buf[j].v;
+      out_indices[(int64_t)r * k + j] = buf[j].i;
+    }
+  }
+  free(buf);
+}
