@@ -345,6 +345,43 @@ def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
     return out
 
 
+def run_topk(pa, torch, hbm, steps=50, warmup=5):
+    """Exact top-32 of 16 rows of 151936 logits (the Qwen3-14B real vocabulary in
+    rows padded to 152064), the selector's batch-16 configuration; L2 flushed
+    between steps.  Bytes: the logits read once."""
+    g = torch.Generator(device="cuda").manual_seed(706)
+    buf = torch.randn(16, 152064, generator=g, device="cuda", dtype=torch.float32)
+    logits = buf[:, :151936]
+    vals = torch.empty(16, 32, dtype=torch.float32, device="cuda")
+    idx = torch.empty(16, 32, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, pa.load().pa_topk_workspace_size(16, 151936, 32)), dtype=torch.uint8,
+                     device="cuda")
+    flush = L2Flush(torch)
+
+    def step():
+        pa.pa_topk(logits, 32, out_values=vals, out_indices=idx, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    nbytes = 16 * 151936 * 4
+    ref = torch.topk(logits, 32, dim=1)
+    exact = bool(torch.equal(ref.indices.to(torch.int32), idx)) and bool(torch.equal(ref.values, vals))
+    return {"workload": "topk-b16-v151936-k32", "us": ms * 1e3, "bytes": nbytes,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "matches_torch_topk": exact, "step": "pa_topk (slice select + merge)",
+            "l2": "flushed between steps"}
+
+
 def run_prefill(pa, W, torch, steps=20, warmup=3):
     """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
     case = W.chunked_prefill(device="cuda", pool_device="cuda")
@@ -498,6 +535,12 @@ def run_ours(args):
             prologue = run_prologue(pa, W, torch, hbm)
         except Exception as e:  # report, do not hide
             prologue = {"error": str(e).splitlines()[0][:200]}
+    topk = None
+    if not args.no_prefill:
+        try:
+            topk = run_topk(pa, torch, hbm)
+        except Exception as e:  # report, do not hide
+            topk = {"error": str(e).splitlines()[0][:200]}
     other = None
     if not args.no_prefill:
         other = []
@@ -540,6 +583,7 @@ def run_ours(args):
         "prefill": prefill,
         "decode_configs": other,
         "prologue": prologue,
+        "topk": topk,
         "cpu_baseline": cpu,
     }
     if rank == 0:

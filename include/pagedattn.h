@@ -229,6 +229,34 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
 int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
                int32_t out_dtype, pa_dims dims, pa_stream_t stream);
 
+/* Largest k pa_topk takes (the pages' fixed candidate capacity). */
+#define PA_TOPK_MAX_K 32
+
+/*
+ * pa_topk -- exact top-k of each row of logits: the sampling candidates.
+ * pypto-serving PR #77 ("Qwen3-14B device top-k"), "Exactness Design": an
+ * exact Top-32 of the full-vocabulary logits (151936 real entries for
+ * Qwen3-14B), merged hierarchically from exact per-group Top-k sets, returning
+ * candidate values and token IDs; checked against torch.topk.
+ *   logits         float32, row r at logits + r * row_stride, its first vocab
+ *                  entries used (row_stride >= vocab; 4-byte aligned)
+ *   k              1 .. PA_TOPK_MAX_K, <= vocab
+ *   out_values     float32 [rows, k], out_indices int32 [rows, k]: the k
+ *                  largest entries, larger first; NaN ranks above +inf; equal
+ *                  values (including -0 and +0) by smaller index.  A value is the
+ *                  logit as given.
+ *   workspace      device scratch of pa_topk_workspace_size(rows, vocab, k)
+ *                  bytes (16-byte aligned), contents need no initialisation
+ * Returns PA_ERR_DIMS for an unsupported k / vocab / row_stride.
+ */
+int pa_topk(const float* logits, int64_t row_stride, int32_t rows, int32_t vocab, int32_t k,
+            float* out_values, int32_t* out_indices, void* workspace, size_t workspace_bytes,
+            pa_stream_t stream);
+
+/* Workspace bytes pa_topk needs on the current device, (size_t)-1 for invalid
+ * arguments. */
+size_t pa_topk_workspace_size(int32_t rows, int32_t vocab, int32_t k);
+
 /* Size of the device array pa_decode_noalloc keeps its split partials in. */
 #define PA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

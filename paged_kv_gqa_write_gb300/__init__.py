@@ -23,13 +23,14 @@ PA_STATUS_BAD_PAGE, PA_STATUS_BAD_LENGTH, PA_STATUS_BAD_TOKENS, PA_STATUS_TIMEOU
 PA_MAX_CHUNKED_SEQS = 16384
 PA_SPLITS_BALANCED = -1
 PA_BALANCED_MAX_SEQS = 512
+PA_TOPK_MAX_K = 32
 (PA_ERR_NULL_POINTER, PA_ERR_HEAD_DIM, PA_ERR_PAGE_SIZE, PA_ERR_HEADS, PA_ERR_DIMS,
  PA_ERR_ALIGNMENT, PA_ERR_OUT_DTYPE, PA_ERR_WORKSPACE, PA_ERR_SPLITS, PA_ERR_TOO_MANY_SEQS,
  PA_ERR_TENSOR_MAP, PA_ERR_NO_DEVICE, PA_ERR_NOALLOC_TOO_LARGE) = range(-1, -14, -1)
 
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
-            "pa_decode_noalloc", "pa_qk_norm_rope_write")
+            "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -64,6 +65,10 @@ def load(path: str = LIB_PATH):
     lib.pa_qk_norm_rope_write.restype = ctypes.c_int
     lib.pa_qk_norm_rope_write.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, vp,
                                           vp, i32, pa_dims, vp, vp]
+    lib.pa_topk.restype = ctypes.c_int
+    lib.pa_topk.argtypes = [vp, ctypes.c_int64, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.pa_topk_workspace_size.restype = sz
+    lib.pa_topk_workspace_size.argtypes = [i32, i32, i32]
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, vp, sz, i32, pa_dims, vp, vp]
     lib.pa_decode_workspace_size.restype = sz
@@ -182,6 +187,29 @@ def pa_qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table
         _stream(stream))
     _check("pa_qk_norm_rope_write", rc)
     return q_out
+
+
+def pa_topk(logits, k, out_values=None, out_indices=None, workspace=None, stream=None):
+    """Exact top-k of each row of logits [rows, vocab] float32 (row stride may
+    exceed vocab).  Returns (values [rows, k] float32, indices [rows, k] int32)."""
+    dev = logits.device
+    if logits.dtype != torch.float32 or logits.dim() != 2 or logits.stride(1) != 1:
+        raise TypeError("logits must be a float32 [rows, vocab] tensor with unit column stride")
+    rows, vocab = logits.shape
+    if out_values is None:
+        out_values = torch.empty(rows, k, dtype=torch.float32, device=dev)
+    if out_indices is None:
+        out_indices = torch.empty(rows, k, dtype=torch.int32, device=dev)
+    need = int(load().pa_topk_workspace_size(rows, vocab, int(k)))
+    if need == (1 << 64) - 1:
+        raise ValueError("unsupported rows / vocab / k for pa_topk")
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = load().pa_topk(_ptr(logits), int(logits.stride(0)), int(rows), int(vocab), int(k),
+                        _ptr(out_values), _ptr(out_indices), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pa_topk", rc)
+    return out_values, out_indices
 
 
 def pa_decode_workspace_size(dims, num_splits=0) -> int:

@@ -228,6 +228,28 @@ bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int 
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
 
+// Top-k slicing: about two CTAs per SM over all rows, slices of at most 16384
+// entries (64 KB of keys in shared memory), a multiple of 4 long.
+void topk_plan(int rows, int vocab, int num_sms, int* slices, int* slice_len) {
+  const int target = rows > 0 ? (2 * num_sms + rows - 1) / rows : 1;
+  int len = (vocab + target - 1) / target;
+  if (len < 1024) len = 1024;
+  if (len > 16384) len = 16384;
+  len = (len + 3) & ~3;
+  *slice_len = len;
+  *slices = (vocab + len - 1) / len;
+}
+
+bool topk_args_ok(int rows, int vocab, int k) {
+  return rows >= 0 && k >= 1 && k <= PA_TOPK_MAX_K && vocab >= k && vocab <= (1 << 28);
+}
+
+size_t topk_ws_bytes(int rows, int vocab, int k, int num_sms) {
+  int slices, len;
+  topk_plan(rows, vocab, num_sms, &slices, &len);
+  return (size_t)rows * slices * k * sizeof(unsigned long long);
+}
+
 // Shared tail of pa_decode and pa_decode_noalloc: arguments are checked and
 // `ws` holds at least pl.ws_bytes (or is unused when that is 0).
 int run_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -305,7 +327,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 102; }
+int32_t pa_abi_version(void) { return 103; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -409,6 +431,39 @@ int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   return launch_result(pa::launch_prologue(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_topk_workspace_size(int32_t rows, int32_t vocab, int32_t k) {
+  if (!topk_args_ok(rows, vocab, k)) return (size_t)-1;
+  const int sms = device_sms();
+  if (sms <= 0) return (size_t)-1;
+  return topk_ws_bytes(rows, vocab, k, sms);
+}
+
+int pa_topk(const float* logits, int64_t row_stride, int32_t rows, int32_t vocab, int32_t k,
+            float* out_values, int32_t* out_indices, void* workspace, size_t ws_bytes,
+            pa_stream_t stream) {
+  if (!topk_args_ok(rows, vocab, k) || row_stride < vocab) return PA_ERR_DIMS;
+  if (rows == 0) return PA_OK;
+  if (!logits || !out_values || !out_indices || !workspace) return PA_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(out_values) & 3u) || (reinterpret_cast<uintptr_t>(out_indices) & 3u))
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  if (ws_bytes < topk_ws_bytes(rows, vocab, k, sms)) return PA_ERR_WORKSPACE;
+  pa::TopkParams p;
+  p.logits = logits;
+  p.row_stride = row_stride;
+  p.out_values = out_values;
+  p.out_indices = out_indices;
+  p.cand = static_cast<unsigned long long*>(workspace);
+  p.rows = rows;
+  p.vocab = vocab;
+  p.k = k;
+  topk_plan(rows, vocab, sms, &p.slices, &p.slice_len);
+  if ((int64_t)p.slices * k * 8 > 200 * 1024) return PA_ERR_DIMS;
+  return launch_result(pa::launch_topk(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t pa_decode_auto_splits(pa_dims d) {

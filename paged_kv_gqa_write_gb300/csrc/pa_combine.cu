@@ -223,24 +223,6 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
   }
 }
 
-// Launch as a programmatic dependent of the kernel before it on the stream
-// (its prologue may overlap that kernel; griddepcontrol.wait orders the reads).
-template <typename P>
-cudaError_t launch_dependent(void (*kernel)(P), const P& p, int grid, int block,
-                             cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
-}
-
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {

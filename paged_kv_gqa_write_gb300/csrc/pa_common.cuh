@@ -425,6 +425,17 @@ struct PrologueParams {
   int32_t B, T, Hq, Hkv, num_pages, max_pages;
 };
 
+// Exact top-k over rows of logits.
+struct TopkParams {
+  const float* logits;          // [rows] x row_stride floats, the first vocab of each used
+  int64_t row_stride;
+  float* out_values;            // [rows, k]
+  int32_t* out_indices;         // [rows, k]
+  unsigned long long* cand;     // [rows, slices, k] candidate keys (workspace)
+  int32_t rows, vocab, k;
+  int32_t slices, slice_len;    // slices per row of slice_len entries (a multiple of 4)
+};
+
 // Merge of the sequences that the page-balanced decode schedule cut between
 // CTA groups.
 struct BalCombineParams {

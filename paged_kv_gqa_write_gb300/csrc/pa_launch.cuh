@@ -4,6 +4,25 @@
 
 namespace pa {
 
+// Launch as a programmatic dependent of the kernel before it on the stream
+// (its prologue may overlap that kernel; griddepcontrol.wait orders the reads).
+template <typename P>
+inline cudaError_t launch_dependent(void (*kernel)(P), const P& p, int grid, int block,
+                             cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+
 cudaError_t launch_kv_write(const KvWriteParams& p, int num_sms, cudaStream_t stream);
 
 // Q/K RMSNorm, NeoX RoPE and the KV write of the new tokens, fused.
@@ -22,6 +41,9 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Merge of the units a page-balanced decode launch of p.grid CTAs cut.
 cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream);
+
+// Exact top-k of logit rows: per-slice candidates, then a per-row merge.
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,

@@ -55,7 +55,7 @@ def test_python_constants_match_header(pa):
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
-    assert pa.pa_abi_version() == 102
+    assert pa.pa_abi_version() == 103
 
 
 def test_status_strings(pa):
@@ -120,6 +120,14 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert pro(qkv=None) == h["PA_ERR_NULL_POINTER"]
     assert pro(qkv=MIS) == h["PA_ERR_ALIGNMENT"]
     assert pro(n=0, cl=FAKE) == 0
+    tk = lambda rows=2, vocab=100, k=8, stride=100, ptr=FAKE: lib.pa_topk(
+        ptr, stride, rows, vocab, k, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert tk(k=0) == h["PA_ERR_DIMS"] and tk(k=33) == h["PA_ERR_DIMS"]
+    assert tk(vocab=4, k=8) == h["PA_ERR_DIMS"] and tk(stride=50) == h["PA_ERR_DIMS"]
+    assert tk(ptr=None) == h["PA_ERR_NULL_POINTER"]
+    assert tk(ptr=ctypes.c_void_p(0x10002)) == h["PA_ERR_ALIGNMENT"]
+    assert tk(rows=0) == 0
+    assert h["PA_TOPK_MAX_K"] == pa.PA_TOPK_MAX_K
     assert lib.pa_combine(FAKE, FAKE, 2, MIS, 0, d, None) == h["PA_ERR_ALIGNMENT"]
 
 
