@@ -305,6 +305,60 @@ def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
             "l2": "flushed between steps"}
 
 
+def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3):
+    """Multi-token decode (64 sequences x 4096 tokens, 4 new tokens each, 40/8
+    heads): the 256 new tokens' KV write, then pa_decode_multi -- and the same
+    attention through pa_prefill_chunk for comparison.  Bytes: the K+V of every
+    context read once (1.07 GB; the working set is far larger than L2)."""
+    q_len = 4
+    case = W.multi_token_decode(device="cuda", pool_device="cuda", q_len=q_len)
+    kv_bytes = int(case.context_lens.sum()) * case.Hkv * D * 2 * 2
+    out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dims = pa.make_dims(case.B, case.Hq, case.Hkv, case.num_pages, case.max_pages_per_seq)
+    ws = torch.empty(max(1, pa.pa_decode_multi_workspace_size(dims, q_len, 0)),
+                     dtype=torch.uint8, device="cuda")
+    sched = pa.pa_decode_auto_splits(pa.make_dims(case.B * q_len, case.Hq, case.Hkv,
+                                                  case.num_pages, case.max_pages_per_seq))
+
+    def write():
+        pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache, case.block_table,
+                       case.context_lens, case.chunk_lens, status=st)
+
+    def via_decode():
+        write()
+        pa.pa_decode_multi(case.q, case.k_cache, case.v_cache, case.block_table,
+                           case.context_lens, q_len, case.scale, out=out, workspace=ws,
+                           num_splits=0, status=st)
+
+    def via_prefill():
+        write()
+        pa.pa_prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table,
+                            case.context_lens, case.chunk_lens, case.scale, out=out, status=st)
+
+    res = {"workload": f"multi-token-decode-b{case.B}-q{q_len}-ctx4096", "batch": case.B,
+           "q_len": q_len, "q_heads": case.Hq, "kv_heads": case.Hkv, "kv_bytes": kv_bytes,
+           "schedule": "page-balanced" if sched == 0 else f"{sched} fixed splits",
+           "step": f"pa_kv_write ({case.T} tokens) + attention", "l2": "working set > L2"}
+    for name, fn in (("pa_decode_multi", via_decode), ("pa_prefill_chunk", via_prefill)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "gbs": gbs, "frac": gbs / hbm,
+                     "tokens_per_s": case.T / (ms * 1e-3)}
+    res["status"] = int(st.item())
+    return res
+
+
 def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
     """pa_qk_norm_rope_write (Q/K RMSNorm -> NeoX RoPE -> KV write) on the decode
     batch (128 tokens) and on the 8 x 512 prefill chunk, with a clean L2 flush
@@ -535,6 +589,12 @@ def run_ours(args):
             prologue = run_prologue(pa, W, torch, hbm)
         except Exception as e:  # report, do not hide
             prologue = {"error": str(e).splitlines()[0][:200]}
+    multi = None
+    if not args.no_prefill:
+        try:
+            multi = run_multi_token(pa, W, torch, hbm)
+        except Exception as e:  # report, do not hide
+            multi = {"error": str(e).splitlines()[0][:200]}
     topk = None
     if not args.no_prefill:
         try:
@@ -584,6 +644,7 @@ def run_ours(args):
         "decode_configs": other,
         "prologue": prologue,
         "topk": topk,
+        "multi_token_decode": multi,
         "cpu_baseline": cpu,
     }
     if rank == 0:

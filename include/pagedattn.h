@@ -12,6 +12,8 @@
  *    [page, token, kv_head, dim]; K/V gathered per sequence from the block
  *    table and the sequence lengths ("Qwen 3", section 11).  Split across
  *    KV ranges (flash-decoding) and merged by pa_combine.
+ *  - pa_decode_multi: the same causal attention for q_len new tokens per
+ *    sequence (every chunk q_len long), run as B * q_len decode queries.
  *  - pa_prefill_chunk: "KV cache update -> causal attention" of prefill_fwd
  *    ("Qwen3-14B", "prefill_fwd"), inputs packed token-major with
  *    T = sum(chunk_lens); full causal attention without window or sinks
@@ -198,6 +200,39 @@ size_t pa_decode_workspace_size(pa_dims dims, int32_t num_splits);
  * split count >= 1, or 0 for the page-balanced schedule; a negative PA_ERR_*
  * for invalid dims. */
 int32_t pa_decode_auto_splits(pa_dims dims);
+
+/* Largest q_len pa_decode_multi takes. */
+#define PA_MAX_Q_LEN 16
+
+/*
+ * pa_decode_multi -- multi-token decode (speculative-decoding verification,
+ * multi-token prediction): q_len new tokens per sequence, each attending
+ * causally over the paged cache.  This is the causal attention step of
+ * "prefill_fwd" ("Qwen3-14B", pypto-lib doc) with every chunk q_len long,
+ * run on the decode kernel: token j of sequence s is one decode query at
+ * position context_lens[s] - q_len + j whose keys are 0 .. that position.
+ *   q              bf16 [B * q_len, Hq, D], token-major in sequence order
+ *                  (the packing of pa_prefill_chunk with chunk_lens = q_len)
+ *   q_len          1 .. PA_MAX_Q_LEN; the new tokens must already be in the
+ *                  cache (pa_kv_write with chunk_lens = q_len)
+ *   out            [B * q_len, Hq, D], element type out_dtype
+ *   workspace      at least pa_decode_multi_workspace_size(dims, q_len,
+ *                  num_splits) bytes (caller-owned, no initialisation)
+ *   num_splits     as pa_decode, over the B * q_len queries (the balanced
+ *                  schedule needs B * q_len <= PA_BALANCED_MAX_SEQS)
+ *   dims.num_seqs  B (sequences; the block table has B rows)
+ * A sequence with 0 < context_lens[s] < q_len is invalid (status bit
+ * PA_STATUS_BAD_LENGTH, zero output); context_lens[s] == 0 gives zero rows.
+ * q_len == 1 is exactly pa_decode.  Returns PA_ERR_DIMS for q_len out of range.
+ */
+int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_table, const int32_t* context_lens, int32_t q_len,
+                    float scale, void* out, int32_t out_dtype, void* workspace,
+                    size_t workspace_bytes, int32_t num_splits, pa_dims dims,
+                    int32_t* status, pa_stream_t stream);
+
+/* Workspace bytes pa_decode_multi needs; (size_t)-1 for invalid arguments. */
+size_t pa_decode_multi_workspace_size(pa_dims dims, int32_t q_len, int32_t num_splits);
 
 /*
  * pa_prefill_chunk -- causal attention of a packed chunk of new tokens over

@@ -24,13 +24,15 @@ PA_MAX_CHUNKED_SEQS = 16384
 PA_SPLITS_BALANCED = -1
 PA_BALANCED_MAX_SEQS = 512
 PA_TOPK_MAX_K = 32
+PA_MAX_Q_LEN = 16
 (PA_ERR_NULL_POINTER, PA_ERR_HEAD_DIM, PA_ERR_PAGE_SIZE, PA_ERR_HEADS, PA_ERR_DIMS,
  PA_ERR_ALIGNMENT, PA_ERR_OUT_DTYPE, PA_ERR_WORKSPACE, PA_ERR_SPLITS, PA_ERR_TOO_MANY_SEQS,
  PA_ERR_TENSOR_MAP, PA_ERR_NO_DEVICE, PA_ERR_NOALLOC_TOO_LARGE) = range(-1, -14, -1)
 
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
-            "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size")
+            "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
+            "pa_decode_multi", "pa_decode_multi_workspace_size")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -71,6 +73,11 @@ def load(path: str = LIB_PATH):
     lib.pa_topk_workspace_size.argtypes = [i32, i32, i32]
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, vp, sz, i32, pa_dims, vp, vp]
+    lib.pa_decode_multi.restype = ctypes.c_int
+    lib.pa_decode_multi.argtypes = [vp, vp, vp, vp, vp, i32, f32, vp, i32, vp, sz, i32, pa_dims,
+                                    vp, vp]
+    lib.pa_decode_multi_workspace_size.restype = sz
+    lib.pa_decode_multi_workspace_size.argtypes = [pa_dims, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode_workspace_size.argtypes = [pa_dims, i32]
     lib.pa_decode_auto_splits.restype = i32
@@ -254,6 +261,51 @@ def pa_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, out=No
                           0 if workspace is None else workspace.numel() * workspace.element_size(),
                           int(num_splits), d, _ptr(status), _stream(stream))
     _check("pa_decode", rc)
+    return out
+
+
+def pa_decode_multi_workspace_size(dims, q_len, num_splits=0) -> int:
+    n = int(load().pa_decode_multi_workspace_size(dims, int(q_len), int(num_splits)))
+    if n == (1 << 64) - 1:
+        raise ValueError("invalid dims, q_len or schedule for pa_decode_multi_workspace_size")
+    return n
+
+
+def pa_decode_multi(q, k_cache, v_cache, block_table, context_lens, q_len, scale=None, out=None,
+                    out_dtype=torch.bfloat16, workspace=None, num_splits=0, status=None,
+                    stream=None):
+    """Multi-token decode: q_len new tokens per sequence, q [B * q_len, Hq, 128] bf16
+    token-major; token j of sequence s attends to keys 0 .. context_lens[s] - q_len + j.
+    Returns out [B * q_len, Hq, 128]."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    T, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    q_len = int(q_len)
+    if q_len < 1 or T != d.num_seqs * q_len:
+        raise ValueError(f"q has {T} rows; expected num_seqs ({d.num_seqs}) x q_len ({q_len})")
+    if out is None:
+        out = torch.empty(T, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    need = pa_decode_multi_workspace_size(d, q_len, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().pa_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                _ptr(context_lens), q_len, scale, _ptr(out), code,
+                                _ptr(workspace), ws_bytes, int(num_splits), d, _ptr(status),
+                                _stream(stream))
+    _check("pa_decode_multi", rc)
     return out
 
 

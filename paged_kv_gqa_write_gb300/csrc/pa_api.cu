@@ -250,12 +250,13 @@ size_t topk_ws_bytes(int rows, int vocab, int k, int num_sms) {
   return (size_t)rows * slices * k * sizeof(unsigned long long);
 }
 
-// Shared tail of pa_decode and pa_decode_noalloc: arguments are checked and
-// `ws` holds at least pl.ws_bytes (or is unused when that is 0).
+// Shared tail of pa_decode, pa_decode_multi and pa_decode_noalloc: arguments
+// are checked and `ws` holds at least pl.ws_bytes (or is unused when that is
+// 0).  `d` counts queries (num_seqs = sequences x q_len), `q_len` tokens each.
 int run_decode(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
                int32_t out_dtype, uint8_t* ws, const DecodePlan& pl, const pa_dims& d,
-               int32_t* status, int sms, cudaStream_t st) {
+               int32_t q_len, int32_t* status, int sms, cudaStream_t st) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int NG = head_groups(G);
   const int64_t items = (int64_t)pl.splits * d.num_seqs * d.num_kv_heads * NG;
@@ -294,6 +295,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.bal_lse = pl.balanced ? reinterpret_cast<float*>(
                                 ws + align256((size_t)2 * pl.grid * 16 * kHeadDim * sizeof(float)))
                           : nullptr;
+  p.L = q_len;
   cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
   if (e != cudaSuccess) return launch_result(e);
   if (pl.balanced) {
@@ -308,6 +310,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
     c.NG = NG;
     c.GC = G / NG;
     c.max_pages = d.max_pages_per_seq;
+    c.L = q_len;
     c.grid = pl.grid;
     c.out_f32 = p.out_f32;
     return launch_result(pa::launch_bal_combine(c, st));
@@ -327,7 +330,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 103; }
+int32_t pa_abi_version(void) { return 104; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -474,9 +477,12 @@ int32_t pa_decode_auto_splits(pa_dims d) {
   return auto_schedule(d, sms);
 }
 
-size_t pa_decode_workspace_size(pa_dims d, int32_t num_splits) {
+size_t pa_decode_multi_workspace_size(pa_dims d, int32_t q_len, int32_t num_splits) {
   if (check_dims(d) || num_splits < PA_SPLITS_BALANCED) return (size_t)-1;
+  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return (size_t)-1;
   if (d.num_seqs == 0) return 0;
+  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return (size_t)-1;
+  d.num_seqs *= q_len;
   const int sms = device_sms();
   if (sms <= 0) return (size_t)-1;
   DecodePlan pl;
@@ -484,15 +490,22 @@ size_t pa_decode_workspace_size(pa_dims d, int32_t num_splits) {
   return pl.ws_bytes;
 }
 
-int pa_decode(const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
-              int32_t out_dtype, void* workspace, size_t ws_bytes, int32_t num_splits,
-              pa_dims d, int32_t* status, pa_stream_t stream) {
+size_t pa_decode_workspace_size(pa_dims d, int32_t num_splits) {
+  return pa_decode_multi_workspace_size(d, 1, num_splits);
+}
+
+int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_table, const int32_t* context_lens, int32_t q_len,
+                    float scale, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                    int32_t num_splits, pa_dims d, int32_t* status, pa_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
+  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return PA_ERR_DIMS;
   if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
   if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
   if (d.num_seqs == 0) return PA_OK;
+  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
+  d.num_seqs *= q_len;  // one decode query per new token
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
     return PA_ERR_NULL_POINTER;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
@@ -506,8 +519,16 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
   }
   return run_decode(q, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
-                    static_cast<uint8_t*>(workspace), pl, d, status, sms,
+                    static_cast<uint8_t*>(workspace), pl, d, q_len, status, sms,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
+              int32_t out_dtype, void* workspace, size_t ws_bytes, int32_t num_splits,
+              pa_dims d, int32_t* status, pa_stream_t stream) {
+  return pa_decode_multi(q, k_cache, v_cache, block_table, context_lens, 1, scale, out,
+                         out_dtype, workspace, ws_bytes, num_splits, d, status, stream);
 }
 
 int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,
@@ -641,5 +662,5 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
     if (!scratch) return launch_result(e == cudaSuccess ? cudaErrorUnknown : e);
   }
   return run_decode(q, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
-                    scratch, pl, d, status, sms, reinterpret_cast<cudaStream_t>(stream));
+                    scratch, pl, d, 1, status, sms, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
     constexpr int R = PA_BALANCED_MAX_SEQS / 32;
     int np[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(lane * R + r, p.B - 1));
+    for (int r = 0; r < R; ++r)
+      np[r] = query_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L, p.max_pages * kPage);
     int lsum = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {

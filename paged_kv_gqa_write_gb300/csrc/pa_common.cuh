@@ -406,7 +406,25 @@ struct DecodeParams {
   int32_t grid;                 // CTAs of the page-balanced schedule (groups x Hkv*NG)
   float* bal_o;                 // [2 * grid][16][D] partial records of cut sequences
   float* bal_lse;               // [2 * grid][16]
+  int32_t L;                    // query tokens per sequence; B counts queries (B = seqs * L)
 };
+
+// Multi-token decode: the L new tokens of each sequence are B * L single-token
+// queries v = s * L + j (q and out rows in that order, as in the token-major
+// packing of the chunk).  Query j of sequence s sits at position
+// context_lens[s] - L + j and sees keys 0 .. that position, so its context
+// length is context_lens[s] - (L - 1 - j); it reads sequence s's block-table
+// row.  A sequence with 0 < context_lens[s] < L or a length past the table
+// makes all of its queries invalid (-1); context 0 leaves them all empty.
+// With L = 1 this is the plain decode (the length is returned unchanged).
+__device__ __forceinline__ int query_ctx(const int32_t* context_lens, int v, int L, int max_ctx) {
+  if (L == 1) return __ldg(context_lens + v);
+  const int s = v / L, j = v - s * L;
+  const int c = __ldg(context_lens + s);
+  if (c == 0) return 0;
+  if (c < L || c > max_ctx) return -1;
+  return c - (L - 1 - j);
+}
 
 // Q/K RMSNorm -> NeoX RoPE -> KV cache write for the new tokens.
 struct PrologueParams {
@@ -444,6 +462,7 @@ struct BalCombineParams {
   const float* bal_lse;
   void* out;
   int32_t B, Hq, G, NG, GC, max_pages;
+  int32_t L;                    // query tokens per sequence (B counts queries)
   int32_t grid;                 // CTAs of the decode launch
   int32_t out_f32;
 };

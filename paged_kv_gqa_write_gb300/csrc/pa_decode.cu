@@ -220,11 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t bP = 0, lo = 0, hi = 0, W = 0;
     const int ngroups = gridDim.x / UPS, grp = blockIdx.x / UPS, unit_j = blockIdx.x % UPS;
     int cbase = -64, cval = 0;     // 32 context lengths starting at cbase (lane's in cval)
+    const int max_ctx = p.max_pages * kPage;
     const bool last_grp = grp == ngroups - 1;
     auto ctx_at = [&](int sq) -> int {
       if (sq < cbase || sq >= cbase + 32) {
         cbase = sq;
-        cval = cbase + lane < p.B ? __ldg(p.context_lens + cbase + lane) : 0;
+        cval = cbase + lane < p.B ? query_ctx(p.context_lens, cbase + lane, p.L, max_ctx) : 0;
       }
       return __shfl_sync(0xffffffffu, cval, sq - cbase);
     };
@@ -235,7 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int R = kBalMaxSeqs / 32;
       int np[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(lane * R + r, p.B - 1));
+      for (int r = 0; r < R; ++r)
+        np[r] = query_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L, max_ctx);
       int lsum = 0;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jsp = gi / U, u = gi - jsp * U;
         w.s = u / UPS;
         w.unit = u - w.s * UPS;
-        w.ctx = __ldg(p.context_lens + w.s);
+        w.ctx = query_ctx(p.context_lens, w.s, p.L, max_ctx);
         w.pg0 = jsp * p.pps;
         w.pg1 = max(w.pg0, min(pages_of(w.ctx, p), w.pg0 + p.pps));
         w.dest = p.S == 1 ? -1 : jsp;
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pages are in the row and are never used)
     auto first_pid = [&](const Work& w) -> int {
       const int pg = w.pg0 + lane;
-      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
+      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)(w.s / p.L) * p.max_pages + pg) : 0;
     };
     Work nx;
     bool have = gen_next(nx);
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item) {
         // validate every page of the item; the next item's metadata loads
         // while this one's pages are issued
-        const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)(w.s / p.L) * p.max_pages;
         bool bad = w.pg0 + lane < w.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
         for (int pg = w.pg0 + 32 + lane; pg < w.pg1; pg += 32) {
           const int pid = __ldg(bt + pg);
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!item) break;
       const int x = (w.unit / p.NG) * kHeadDim;
-      const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
+      const int32_t* bt = p.block_table + (int64_t)(w.s / p.L) * p.max_pages;
       for (int c = 0; ok && c < npg; c += 32) {
         const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + w.pg0 + c + lane) : 0);
         const int cnt = min(32, npg - c);

@@ -52,10 +52,11 @@ def test_python_constants_match_header(pa):
     assert h["PA_MAX_CHUNKED_SEQS"] == pa.PA_MAX_CHUNKED_SEQS
     assert h["PA_SPLITS_BALANCED"] == pa.PA_SPLITS_BALANCED
     assert h["PA_BALANCED_MAX_SEQS"] == pa.PA_BALANCED_MAX_SEQS
+    assert h["PA_MAX_Q_LEN"] == pa.PA_MAX_Q_LEN
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
-    assert pa.pa_abi_version() == 103
+    assert pa.pa_abi_version() == 104
 
 
 def test_status_strings(pa):
@@ -133,3 +134,18 @@ def test_host_checks_kv_write_and_prefill(pa):
 
 def test_workspace_size_invalid_dims(pa):
     assert pa.load().pa_decode_workspace_size(_dims(pa, head_dim=64), 2) == ctypes.c_size_t(-1).value
+
+
+def test_decode_multi_rejects_q_len_on_the_host(pa):
+    """q_len outside 1..PA_MAX_Q_LEN is refused before any device work."""
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    lib.pa_decode_multi.restype = ctypes.c_int
+    lib.pa_decode_multi_workspace_size.restype = ctypes.c_size_t
+    d = pa.make_dims(4, 40, 8, 64, 16)
+    for bad in (0, -1, pa.PA_MAX_Q_LEN + 1):
+        rc = lib.pa_decode_multi(None, None, None, None, None, ctypes.c_int32(bad),
+                                 ctypes.c_float(0.1), None, ctypes.c_int32(pa.PA_BF16), None,
+                                 ctypes.c_size_t(0), ctypes.c_int32(1), d, None, None)
+        assert rc == pa.PA_ERR_DIMS, (bad, rc)
+        n = lib.pa_decode_multi_workspace_size(d, ctypes.c_int32(bad), ctypes.c_int32(1))
+        assert n == ctypes.c_size_t(-1).value

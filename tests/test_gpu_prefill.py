@@ -139,3 +139,26 @@ def test_page_permutation_bitwise(cuda_lib):
     case.block_table[m] = inv[case.block_table[m].long()].to(torch.int32)
     _, again, _ = _write_and_prefill(cuda_lib, case)
     assert torch.equal(base, again)
+
+
+@pytest.mark.parametrize("profile", ["ramp", "jump", "fall"])
+def test_scores_that_move_the_reference(cuda_lib, profile):
+    """Online softmax with a lazily moved reference: scores that rise by about
+    ten octaves per 32-key chunk (every chunk moves the running reference, so
+    P already in tensor memory, the partial sum, O and l are rescaled), one
+    jump of about 130 octaves in the middle of a chunk (the old state scales
+    to zero), and falling scores (the first chunk's maximum stays the
+    reference).  The normalised output does not depend on the reference."""
+    n = 700
+    case = W.custom_case(611, [n], Hq=8, Hkv=2, chunk_lens=[n], with_new=True)
+    j = torch.arange(n, dtype=torch.float32)
+    f = {"ramp": 0.02 * j,
+         "jump": torch.where(j >= 317, torch.full_like(j, 8.0), torch.zeros_like(j)),
+         "fall": -0.02 * j}[profile]
+    # q = 1 and k_j = f(j) in every dimension: c * q.k_j = 128 f(j) / sqrt(128) * log2(e)
+    case.q = torch.ones_like(case.q)
+    case.k_new = (f[:, None, None] * torch.ones(1, case.Hkv, 128)).to(torch.bfloat16)
+    _, out, st = _write_and_prefill(cuda_lib, case)
+    assert st == 0
+    ref, _, _ = _oracle_after_write(case)
+    assert_close(out, ref, what=f"prefill {profile} scores")

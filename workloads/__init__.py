@@ -237,6 +237,22 @@ def qwen3_32b_ragged(device="cpu", with_new=True, pool_device=None) -> PagedCase
     return case
 
 
+def multi_token_decode(device="cpu", pool_device=None, B=64, q_len=4, ctx=4096, Hq=40, Hkv=8,
+                       seed_index=6) -> PagedCase:
+    """Multi-token decode (speculative-decoding verification): B sequences of
+    context `ctx` after the write, the last q_len tokens new (K/V with the case,
+    slots poisoned), 40/8 heads, a seeded permutation of a pool of exactly the
+    pages used (64 x 4096 tokens: 1.07 GB of K+V)."""
+    sb = seed_index * 1000
+    ctxs = [ctx] * B
+    need = B * ((ctx + PAGE - 1) // PAGE)
+    perm = _perm(need, sb + _T_PERM)
+    return build_case(f"multi-token-decode-b{B}-q{q_len}-ctx{ctx}", sb, ctxs, Hq, Hkv, need,
+                      consecutive_runs(ctxs, perm), (ctx + PAGE - 1) // PAGE,
+                      chunk_lens=[q_len] * B, with_new=True, device=device,
+                      pool_device=pool_device)
+
+
 def chunked_prefill(device="cpu", pool_device=None, B=8, chunk=512, Hq=40, Hkv=8,
                     max_prior=3584, seed_index=5) -> PagedCase:
     """Chunked paged prefill: 8 sequences packed token-major, 512 new tokens each
