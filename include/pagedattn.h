@@ -209,8 +209,11 @@ int32_t pa_decode_auto_splits(pa_dims dims);
  * multi-token prediction): q_len new tokens per sequence, each attending
  * causally over the paged cache.  This is the causal attention step of
  * "prefill_fwd" ("Qwen3-14B", pypto-lib doc) with every chunk q_len long,
- * run on the decode kernel: token j of sequence s is one decode query at
- * position context_lens[s] - q_len + j whose keys are 0 .. that position.
+ * run on the decode kernel: token j of sequence s sits at position
+ * context_lens[s] - q_len + j and attends to keys 0 .. that position.  Each
+ * decode work item stacks (token, query head) pairs of one KV head -- up to 16
+ * of them -- in the columns of its tensor-core products, so a K/V page is read
+ * once for all the tokens it serves.
  *   q              bf16 [B * q_len, Hq, D], token-major in sequence order
  *                  (the packing of pa_prefill_chunk with chunk_lens = q_len)
  *   q_len          1 .. PA_MAX_Q_LEN; the new tokens must already be in the
@@ -218,8 +221,8 @@ int32_t pa_decode_auto_splits(pa_dims dims);
  *   out            [B * q_len, Hq, D], element type out_dtype
  *   workspace      at least pa_decode_multi_workspace_size(dims, q_len,
  *                  num_splits) bytes (caller-owned, no initialisation)
- *   num_splits     as pa_decode, over the B * q_len queries (the balanced
- *                  schedule needs B * q_len <= PA_BALANCED_MAX_SEQS)
+ *   num_splits     as pa_decode (the balanced schedule needs
+ *                  B <= PA_BALANCED_MAX_SEQS)
  *   dims.num_seqs  B (sequences; the block table has B rows)
  * A sequence with 0 < context_lens[s] < q_len is invalid (status bit
  * PA_STATUS_BAD_LENGTH, zero output); context_lens[s] == 0 gives zero rows.

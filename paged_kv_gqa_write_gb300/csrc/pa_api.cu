@@ -16,7 +16,7 @@ using pa::kHeadDim;
 using pa::kPage;
 
 constexpr int kMaxGroup = 16;    // query heads per KV head
-constexpr int kMaxGcPerCta = 16; // query heads one decode work item serves
+constexpr int kMaxColumns = 16;  // (token, query head) columns of one decode work item
 
 int check_dims(const pa_dims& d) {
   if (d.head_dim != kHeadDim) return PA_ERR_HEAD_DIM;
@@ -33,12 +33,19 @@ int check_dims(const pa_dims& d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Head groups per KV head so that each decode work item serves at most 16
-// query heads: the smallest divisor NG of G with G / NG <= 16.
-int head_groups(int G) {
-  for (int ng = 1; ng <= G; ++ng)
-    if (G % ng == 0 && G / ng <= kMaxGcPerCta) return ng;
-  return G;
+// Token groups of a decode step with L new tokens per sequence: a work item
+// takes Lg tokens x G query heads <= 16 MMA columns.  NT = the fewest groups
+// that fit, Lg = the tokens of the largest (groups as even as possible).
+void token_groups(int G, int L, int* NT, int* Lg) {
+  const int per = kMaxColumns / G;  // >= 1 (G <= 16)
+  *NT = (L + per - 1) / per;
+  *Lg = (L + *NT - 1) / *NT;
+}
+
+int token_group_count(const pa_dims& d, int L) {
+  int nt, lg;
+  token_groups(d.num_q_heads / d.num_kv_heads, L, &nt, &lg);
+  return nt;
 }
 
 int device_sms() {
@@ -62,9 +69,8 @@ int device_sms() {
 // page loads for the combine launch when there is more than one split
 // (constants fitted to GB300 sweeps of 16-256 sequences x 4096 tokens).  With
 // fewer units than SMs, at least enough splits to give every SM two items.
-int auto_splits(const pa_dims& d, int num_sms) {
-  const int64_t units = (int64_t)d.num_seqs * d.num_kv_heads *
-                        head_groups(d.num_q_heads / d.num_kv_heads);
+int auto_splits(const pa_dims& d, int L, int num_sms) {
+  const int64_t units = (int64_t)d.num_seqs * d.num_kv_heads * token_group_count(d, L);
   if (units <= 0 || num_sms <= 0) return 1;
   const int mp = d.max_pages_per_seq;
   int best = 1, prev_pps = -1;
@@ -99,9 +105,9 @@ void split_shape(const pa_dims& d, int requested, int* splits, int* pps) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t workspace_bytes_for(const pa_dims& d, int splits) {
+size_t workspace_bytes_for(const pa_dims& d, int L, int splits) {
   if (splits <= 1) return 0;
-  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  const size_t rows = (size_t)d.num_seqs * L * d.num_q_heads;
   return align256(rows * splits * kHeadDim * sizeof(float)) + align256(rows * splits * sizeof(float));
 }
 
@@ -112,24 +118,22 @@ size_t balanced_ws_bytes(int grid) {
          align256((size_t)2 * grid * 16 * sizeof(float));
 }
 
-// Units (KV head x head group) per sequence; the page-balanced schedule runs
+// Units (KV head x token group) per sequence; the page-balanced schedule runs
 // groups of that many CTAs.
-int units_per_seq(const pa_dims& d) {
-  return d.num_kv_heads * head_groups(d.num_q_heads / d.num_kv_heads);
-}
+int units_per_seq(const pa_dims& d, int L) { return d.num_kv_heads * token_group_count(d, L); }
 
 // The page-balanced schedule takes B <= PA_BALANCED_MAX_SEQS, page positions
 // that fit in 31 bits, and at least two CTA groups.
-bool balanced_ok(const pa_dims& d, int num_sms) {
+bool balanced_ok(const pa_dims& d, int L, int num_sms) {
   return d.num_seqs <= PA_BALANCED_MAX_SEQS &&
          (int64_t)d.num_seqs * d.max_pages_per_seq < ((int64_t)1 << 31) &&
-         num_sms / units_per_seq(d) >= 2 && num_sms / units_per_seq(d) <= 1024;
+         num_sms / units_per_seq(d, L) >= 2 && num_sms / units_per_seq(d, L) <= 1024;
 }
 
 // The schedule num_splits == 0 selects: 0 for the page-balanced schedule
 // (every batch it accepts), else the fixed split count of auto_splits.
-int auto_schedule(const pa_dims& d, int num_sms) {
-  return balanced_ok(d, num_sms) ? 0 : auto_splits(d, num_sms);
+int auto_schedule(const pa_dims& d, int L, int num_sms) {
+  return balanced_ok(d, L, num_sms) ? 0 : auto_splits(d, L, num_sms);
 }
 
 struct DecodePlan {
@@ -141,11 +145,11 @@ struct DecodePlan {
 
 // Resolves num_splits (>= PA_SPLITS_BALANCED) for valid dims with num_seqs > 0;
 // false when the request cannot be served.
-bool make_plan(const pa_dims& d, int num_splits, int num_sms, DecodePlan* pl) {
-  const int req = num_splits == 0 ? auto_schedule(d, num_sms) : num_splits;
+bool make_plan(const pa_dims& d, int L, int num_splits, int num_sms, DecodePlan* pl) {
+  const int req = num_splits == 0 ? auto_schedule(d, L, num_sms) : num_splits;
   if (req == 0 || req == PA_SPLITS_BALANCED) {
-    if (!balanced_ok(d, num_sms)) return false;
-    const int ups = units_per_seq(d);
+    if (!balanced_ok(d, L, num_sms)) return false;
+    const int ups = units_per_seq(d, L);
     const int64_t most = (int64_t)d.num_seqs * d.max_pages_per_seq;  // pages at most
     int64_t groups = num_sms / ups;
     if (groups > most) groups = most < 1 ? 1 : most;
@@ -160,7 +164,7 @@ bool make_plan(const pa_dims& d, int num_splits, int num_sms, DecodePlan* pl) {
   pl->balanced = false;
   split_shape(d, req, &pl->splits, &pl->pps);
   pl->grid = 0;
-  pl->ws_bytes = workspace_bytes_for(d, pl->splits);
+  pl->ws_bytes = workspace_bytes_for(d, L, pl->splits);
   return true;
 }
 
@@ -219,11 +223,22 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, const pa_dims& d) {
                    kPage, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// q viewed as [B * Hq rows, 128 columns]: one item's gc query heads are gc
-// consecutive rows, loaded as two 64-column boxes with 128-byte swizzle.
-bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int gc) {
-  return encode_2d(map, q, kHeadDim, (uint64_t)d.num_seqs * d.num_q_heads, kHeadDim * 2, 64,
-                   (uint32_t)gc, CU_TENSOR_MAP_SWIZZLE_128B);
+// q viewed as [B * L tokens][Hq][128]: one item's columns are a box of lg
+// tokens x g heads (g x lg rows of 128 elements in shared memory, token-major),
+// loaded as two 64-column boxes with 128-byte swizzle.
+bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int L, int g,
+                         int lg) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)d.num_q_heads,
+                        (cuuint64_t)d.num_seqs * L};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)d.num_q_heads * kHeadDim * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)lg};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
@@ -252,18 +267,19 @@ size_t topk_ws_bytes(int rows, int vocab, int k, int num_sms) {
 
 // Shared tail of pa_decode, pa_decode_multi and pa_decode_noalloc: arguments
 // are checked and `ws` holds at least pl.ws_bytes (or is unused when that is
-// 0).  `d` counts queries (num_seqs = sequences x q_len), `q_len` tokens each.
+// 0); q_len new tokens per sequence.
 int run_decode(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
                int32_t out_dtype, uint8_t* ws, const DecodePlan& pl, const pa_dims& d,
                int32_t q_len, int32_t* status, int sms, cudaStream_t st) {
   const int G = d.num_q_heads / d.num_kv_heads;
-  const int NG = head_groups(G);
-  const int64_t items = (int64_t)pl.splits * d.num_seqs * d.num_kv_heads * NG;
+  int NT, Lg;
+  token_groups(G, q_len, &NT, &Lg);
+  const int64_t items = (int64_t)pl.splits * d.num_seqs * d.num_kv_heads * NT;
   if (items > INT32_MAX) return PA_ERR_DIMS;
   CUtensorMap tm_k, tm_v, tm_q;
   if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
-      !encode_q_decode_map(&tm_q, q, d, G / NG))
+      !encode_q_decode_map(&tm_q, q, d, q_len, G, Lg))
     return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p = {};
@@ -271,7 +287,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.block_table = block_table;
   p.context_lens = context_lens;
   p.out = out;
-  const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+  const size_t rows = (size_t)d.num_seqs * q_len * d.num_q_heads;
   const bool fixed_parts = !pl.balanced && pl.splits > 1;
   p.part_o = fixed_parts ? reinterpret_cast<float*>(ws) : nullptr;
   p.part_lse = fixed_parts ? reinterpret_cast<float*>(ws + align256(rows * pl.splits * kHeadDim * 4))
@@ -282,7 +298,9 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.Hq = d.num_q_heads;
   p.Hkv = d.num_kv_heads;
   p.G = G;
-  p.NG = NG;
+  p.L = q_len;
+  p.NT = NT;
+  p.Lg = Lg;
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   p.pps = pl.pps;
@@ -295,8 +313,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.bal_lse = pl.balanced ? reinterpret_cast<float*>(
                                 ws + align256((size_t)2 * pl.grid * 16 * kHeadDim * sizeof(float)))
                           : nullptr;
-  p.L = q_len;
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G / NG, sms, st);
+  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G * Lg, sms, st);
   if (e != cudaSuccess) return launch_result(e);
   if (pl.balanced) {
     pa::BalCombineParams c;
@@ -307,10 +324,10 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
     c.B = d.num_seqs;
     c.Hq = d.num_q_heads;
     c.G = G;
-    c.NG = NG;
-    c.GC = G / NG;
     c.max_pages = d.max_pages_per_seq;
     c.L = q_len;
+    c.NT = NT;
+    c.Lg = Lg;
     c.grid = pl.grid;
     c.out_f32 = p.out_f32;
     return launch_result(pa::launch_bal_combine(c, st));
@@ -474,7 +491,7 @@ int32_t pa_decode_auto_splits(pa_dims d) {
   if (rc) return rc;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
-  return auto_schedule(d, sms);
+  return auto_schedule(d, 1, sms);
 }
 
 size_t pa_decode_multi_workspace_size(pa_dims d, int32_t q_len, int32_t num_splits) {
@@ -482,11 +499,10 @@ size_t pa_decode_multi_workspace_size(pa_dims d, int32_t q_len, int32_t num_spli
   if (q_len < 1 || q_len > PA_MAX_Q_LEN) return (size_t)-1;
   if (d.num_seqs == 0) return 0;
   if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return (size_t)-1;
-  d.num_seqs *= q_len;
   const int sms = device_sms();
   if (sms <= 0) return (size_t)-1;
   DecodePlan pl;
-  if (!make_plan(d, num_splits, sms, &pl)) return (size_t)-1;
+  if (!make_plan(d, q_len, num_splits, sms, &pl)) return (size_t)-1;
   return pl.ws_bytes;
 }
 
@@ -505,7 +521,6 @@ int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
   if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
   if (d.num_seqs == 0) return PA_OK;
   if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
-  d.num_seqs *= q_len;  // one decode query per new token
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
     return PA_ERR_NULL_POINTER;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
@@ -513,7 +528,7 @@ int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   DecodePlan pl;
-  if (!make_plan(d, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (!make_plan(d, q_len, num_splits, sms, &pl)) return PA_ERR_SPLITS;
   if (pl.ws_bytes > 0) {
     if (!workspace || ws_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
@@ -653,7 +668,7 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   DecodePlan pl;
-  if (!make_plan(d, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (!make_plan(d, 1, num_splits, sms, &pl)) return PA_ERR_SPLITS;
   if (pl.ws_bytes > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_NOALLOC_TOO_LARGE;
   uint8_t* scratch = nullptr;
   if (pl.ws_bytes > 0) {

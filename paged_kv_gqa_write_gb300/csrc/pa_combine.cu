@@ -74,15 +74,17 @@ __device__ __forceinline__ int bal_pages(int ctx, int max_pages) {
   return (ctx >= 0 && ctx <= max_pages * kPage) ? (ctx + kPage - 1) / kPage : 0;
 }
 
-// Page-balanced decode: the decode CTAs form groups of UPS = Hkv * NG (CTA
-// g * UPS + j serves unit j, a KV head and head group); the sequences' pages
+// Page-balanced decode: the decode CTAs form groups of UPS = Hkv * NT (CTA
+// g * UPS + j serves unit j, a KV head and token group); the sequences' pages
 // laid end to end (n_s pages for sequence s, W in total) are divided among the
 // groups, group g taking positions [floor(W g / ng), floor(W (g+1) / ng)).  A
 // sequence cut by a group boundary left one partial record per unit in every
 // group that touched it: record 2c (CTA c) if the sequence held the group's
 // first position, else 2c + 1.  Block b (boundary b = 1 .. ng-1) merges the
 // sequence that boundary b cuts, if it starts in group b-1 (so every cut
-// sequence is merged exactly once): one warp per (unit, query head) row.
+// sequence is merged exactly once): one warp per output row (new token, query
+// head) of the sequence, read from column (t % Lg) G + h % G of unit
+// (h / G) NT + t / Lg.
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
   __shared__ int sh_lo[kMaxGroups + 1];  // group boundaries
   __shared__ int sh_P, sh_s, sh_n, sh_go, sh_W;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int UPS = (p.Hq / p.G) * p.NG;
+  const int UPS = (p.Hq / p.G) * p.NT;
   const int ng = p.grid / UPS;
   const int b = blockIdx.x + 1;
   if (warp == 0) {
@@ -110,8 +112,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
     constexpr int R = PA_BALANCED_MAX_SEQS / 32;
     int np[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-      np[r] = query_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L, p.max_pages * kPage);
+    for (int r = 0; r < R; ++r) np[r] = seq_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L);
     int lsum = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -166,8 +167,9 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
   const int P = sh_P, n = sh_n;
   // the groups b-1 .. that touched pages [P, P + n), 32 at a time: lane k
   // holds group b-1+k of the current chunk (its record loads run in parallel)
-  for (int r = warp; r < p.Hq; r += blockDim.x >> 5) {
-    const int j = r / p.GC, g = r - j * p.GC;
+  for (int r = warp; r < p.L * p.Hq; r += blockDim.x >> 5) {
+    const int t = r / p.Hq, hd = r - t * p.Hq;
+    const int j = (hd / p.G) * p.NT + t / p.Lg, g = (t % p.Lg) * p.G + hd % p.G;
     float M = -INFINITY;
     bool inval = false;
     for (int g0 = b - 1; g0 < ng; g0 += 32) {
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
       const float inv = 1.f / warp_sum(Lsum);
       acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    const int64_t row = (int64_t)sh_s * p.Hq + r;
+    const int64_t row = (int64_t)sh_s * p.L * p.Hq + r;
     if (p.out_f32) {
       reinterpret_cast<float4*>(p.out)[row * (kHeadDim / 4) + lane] = acc;
     } else {
@@ -233,9 +235,9 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream) {
-  const int ng = p.grid / ((p.Hq / p.G) * p.NG);
+  const int ng = p.grid / ((p.Hq / p.G) * p.NT);
   if (ng <= 1) return cudaSuccess;
-  const int warps = p.Hq < 32 ? p.Hq : 32;
+  const int warps = p.L * p.Hq < 32 ? p.L * p.Hq : 32;
   cudaError_t e = launch_dependent(bal_combine_kernel, p, ng - 1, 32 * warps, stream);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }

@@ -396,7 +396,9 @@ struct DecodeParams {
   float* part_lse;              // [B, Hq, S]
   int32_t* status;
   float scale_log2;             // scale * log2(e)
-  int32_t B, Hq, Hkv, G, NG;    // NG head groups of GC heads per KV head
+  int32_t B, Hq, Hkv, G;
+  int32_t L;                    // new tokens (queries) per sequence
+  int32_t NT, Lg;               // token groups per KV head, tokens per group
   int32_t num_pages, max_pages;
   int32_t pps;                  // pages per split
   int32_t S;                    // splits
@@ -406,24 +408,19 @@ struct DecodeParams {
   int32_t grid;                 // CTAs of the page-balanced schedule (groups x Hkv*NG)
   float* bal_o;                 // [2 * grid][16][D] partial records of cut sequences
   float* bal_lse;               // [2 * grid][16]
-  int32_t L;                    // query tokens per sequence; B counts queries (B = seqs * L)
 };
 
-// Multi-token decode: the L new tokens of each sequence are B * L single-token
-// queries v = s * L + j (q and out rows in that order, as in the token-major
-// packing of the chunk).  Query j of sequence s sits at position
-// context_lens[s] - L + j and sees keys 0 .. that position, so its context
-// length is context_lens[s] - (L - 1 - j); it reads sequence s's block-table
-// row.  A sequence with 0 < context_lens[s] < L or a length past the table
-// makes all of its queries invalid (-1); context 0 leaves them all empty.
-// With L = 1 this is the plain decode (the length is returned unchanged).
-__device__ __forceinline__ int query_ctx(const int32_t* context_lens, int v, int L, int max_ctx) {
-  if (L == 1) return __ldg(context_lens + v);
-  const int s = v / L, j = v - s * L;
+// Decode with L new tokens per sequence (multi-token decode; L = 1 is the
+// plain decode): token t of sequence s sits at position context_lens[s] - L + t
+// and sees keys 0 .. that position.  A work item serves one KV head and a
+// group of Lg consecutive tokens: its MMA columns are (token, query head)
+// pairs, token-major, so every K/V page it loads serves all of them.  The
+// item reads the sequence's pages up to context_lens[s] (its last token's
+// keys); column c masks keys at or past context_lens[s] - (L - 1 - t(c)).
+// A sequence with 0 < context_lens[s] < L is invalid (-1 here).
+__device__ __forceinline__ int seq_ctx(const int32_t* context_lens, int s, int L) {
   const int c = __ldg(context_lens + s);
-  if (c == 0) return 0;
-  if (c < L || c > max_ctx) return -1;
-  return c - (L - 1 - j);
+  return (L > 1 && c > 0 && c < L) ? -1 : c;
 }
 
 // Q/K RMSNorm -> NeoX RoPE -> KV cache write for the new tokens.
@@ -461,8 +458,8 @@ struct BalCombineParams {
   const float* bal_o;
   const float* bal_lse;
   void* out;
-  int32_t B, Hq, G, NG, GC, max_pages;
-  int32_t L;                    // query tokens per sequence (B counts queries)
+  int32_t B, Hq, G, max_pages;
+  int32_t L, NT, Lg;            // new tokens per sequence, token groups, tokens per group
   int32_t grid;                 // CTAs of the decode launch
   int32_t out_f32;
 };

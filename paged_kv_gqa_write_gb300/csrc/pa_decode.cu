@@ -10,9 +10,11 @@
 //
 // Design (GB300; HBM bound: every K/V byte is read once):
 //  * Persistent grid, one CTA per SM.  A work item is (split j, sequence s,
-//    KV head h, head group): a contiguous range of at most `pps` pages and the
-//    GC <= 16 query heads that share the KV head.  Items are dealt
-//    round-robin; split boundaries depend only on logical positions.
+//    KV head h, token group): a contiguous range of at most `pps` pages and
+//    the GC = Lg * G <= 16 (token, query head) columns of the G query heads
+//    that share the KV head, for Lg of the sequence's L new tokens (L = 1:
+//    the plain decode, one column per head).  Items are dealt round-robin;
+//    split boundaries depend only on logical positions.
 //  * Per page the two products are transposed so that the 128 keys (or the
 //    128 head dims) fill the 128 rows of one tcgen05.mma and the query heads,
 //    padded to 16, are its N:
@@ -22,8 +24,8 @@
 //    (128-byte swizzle), and the FP32 pipes only run the softmax.
 //  * warp 0: validates each item's block-table range (the next item's
 //    metadata is loaded while the current item's pages are issued), stages
-//    up to four items ahead, TMA-loads each item's query heads (rows >= GC
-//    stay zero) and its K/V page tiles into a 3-stage ring of 64 KB (K and V
+//    up to four items ahead, TMA-loads each item's query rows (a 3-D box of
+//    Lg tokens x G heads; rows past it stay zero) and its K/V page tiles into a 3-stage ring of 64 KB (K and V
 //    complete on separate mbarriers, so QK^T starts while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
 //    in page order: QK^T(j), then P.V(j) once P(j) is in shared memory.
 //  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
@@ -100,7 +102,7 @@ enum : int {
   kIPg1 = 2,   // end page (== kIPg0 when the item has no pages to read)
   kIFlag = 3,  // 0 ok, 1 invalid block-table entry, 2 invalid context length
   kISeq = 4,   // sequence
-  kIUnit = 5,  // KV head * NG + head group
+  kIUnit = 5,  // KV head * NT + token group
   kIDest = 6,  // -1: out; else the partial record (split index, or 2 * CTA + cut side)
   kIDone = 7,  // no more items
   kInfoInts = 8
@@ -131,7 +133,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// NH: query-head columns the softmax and epilogue handle (8 or 16, >= GC).
+// Columns of work unit `unit` (KV head x token group): the group's tokens
+// (the last group may hold fewer) times the query heads per KV head.
+__device__ __forceinline__ int unit_columns(const DecodeParams& p, int unit) {
+  const int t0 = (unit % p.NT) * p.Lg;
+  return min(p.Lg, p.L - t0) * p.G;
+}
+
+// NH: columns the softmax and epilogue handle (8 or 16, >= any item's GC).
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -156,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.mma_done = B.x_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
   int* info = reinterpret_cast<int*>(smem + kInfo);
-  const int GC = p.G / p.NG;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -180,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(B.mma_done, 1);
     fence_mbar_init();
   }
-  // query rows >= GC and unused P rows must read as zero: clear the operands
+  // query rows past every item's box and unused P rows read as zero: clear the
+  // operands (columns past an item's GC are computed and never used)
   for (int o = threadIdx.x * 16; o < (kSlots + 1) * kOpBytes; o += kThreads * 16)
     sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
@@ -214,18 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sequence cut by lo or hi leaves partial records for the balanced
     // combine; an empty sequence (or one with an invalid length) belongs to
     // the group whose range holds its position (the last group for W).
-    const int UPS = p.Hkv * p.NG;  // units per sequence
+    const int UPS = p.Hkv * p.NT;  // units per sequence
     int gi = blockIdx.x;           // fixed: next item index
     int bs = p.B, bn = 0, bctx = 0;  // balanced: sequence, its pages, its context length
     int64_t bP = 0, lo = 0, hi = 0, W = 0;
     const int ngroups = gridDim.x / UPS, grp = blockIdx.x / UPS, unit_j = blockIdx.x % UPS;
     int cbase = -64, cval = 0;     // 32 context lengths starting at cbase (lane's in cval)
-    const int max_ctx = p.max_pages * kPage;
     const bool last_grp = grp == ngroups - 1;
     auto ctx_at = [&](int sq) -> int {
       if (sq < cbase || sq >= cbase + 32) {
         cbase = sq;
-        cval = cbase + lane < p.B ? query_ctx(p.context_lens, cbase + lane, p.L, max_ctx) : 0;
+        cval = cbase + lane < p.B ? seq_ctx(p.context_lens, cbase + lane, p.L) : 0;
       }
       return __shfl_sync(0xffffffffu, cval, sq - cbase);
     };
@@ -236,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int R = kBalMaxSeqs / 32;
       int np[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-        np[r] = query_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L, max_ctx);
+      for (int r = 0; r < R; ++r) np[r] = seq_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L);
       int lsum = 0;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jsp = gi / U, u = gi - jsp * U;
         w.s = u / UPS;
         w.unit = u - w.s * UPS;
-        w.ctx = query_ctx(p.context_lens, w.s, p.L, max_ctx);
+        w.ctx = seq_ctx(p.context_lens, w.s, p.L);
         w.pg0 = jsp * p.pps;
         w.pg1 = max(w.pg0, min(pages_of(w.ctx, p), w.pg0 + p.pps));
         w.dest = p.S == 1 ? -1 : jsp;
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pages are in the row and are never used)
     auto first_pid = [&](const Work& w) -> int {
       const int pg = w.pg0 + lane;
-      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)(w.s / p.L) * p.max_pages + pg) : 0;
+      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
     };
     Work nx;
     bool have = gen_next(nx);
@@ -343,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item) {
         // validate every page of the item; the next item's metadata loads
         // while this one's pages are issued
-        const int32_t* bt = p.block_table + (int64_t)(w.s / p.L) * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
         bool bad = w.pg0 + lane < w.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
         for (int pg = w.pg0 + 32 + lane; pg < w.pg1; pg += 32) {
           const int pid = __ldg(bt + pg);
@@ -368,11 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         rec[kIDest] = w.dest;
         rec[kIDone] = item ? 0 : 1;
         if (npg > 0) {
-          const int qrow = w.s * p.Hq + (w.unit / p.NG) * p.G + (w.unit % p.NG) * GC;
+          // q as [tokens][Hq][128]: Lg tokens x the G heads of this KV head
+          // (rows of a short last group past the sequence's tokens are loaded
+          // too and never used)
+          const int qh = (w.unit / p.NT) * p.G, qt = w.s * p.L + (w.unit % p.NT) * p.Lg;
           uint8_t* qd = smem + kQ + slot * kOpBytes;
-          mbar_arrive_expect_tx(&B.q_full[slot], 2 * GC * 128);
-          tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
-          tma_load_2d(qd + kAtom, &tm_q, 64, qrow, &B.q_full[slot], pol);
+          mbar_arrive_expect_tx(&B.q_full[slot], 2 * p.Lg * p.G * 128);
+          tma_load_3d(qd, &tm_q, 0, qh, qt, &B.q_full[slot], pol);
+          tma_load_3d(qd + kAtom, &tm_q, 64, qh, qt, &B.q_full[slot], pol);
           q_pending[slot] = (int)((n / kSlots) & 1);
         } else {
           mbar_arrive(&B.q_full[slot]);
@@ -380,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!item) break;
-      const int x = (w.unit / p.NG) * kHeadDim;
-      const int32_t* bt = p.block_table + (int64_t)(w.s / p.L) * p.max_pages;
+      const int x = (w.unit / p.NT) * kHeadDim;
+      const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
       for (int c = 0; ok && c < npg; c += 32) {
         const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + w.pg0 + c + lane) : 0);
         const int cnt = min(32, npg - c);
@@ -511,11 +521,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
       const int* rec = info + kInfoInts * slot;
       if (rec[kIDone]) break;
-      const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1];
+      const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1], unit = rec[kIUnit];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
       if (npg <= 0) continue;
+      const int GC = unit_columns(p, unit);
+      // column g (token t0 + g / G) sees key positions below lim[g]
+      int lim[NH];
+      {
+        const int t0 = (unit % p.NT) * p.Lg;
+#pragma unroll
+        for (int g = 0; g < NH; ++g) lim[g] = g < GC ? ctx - (p.L - 1 - (t0 + g / p.G)) : 0;
+      }
       const int ob = nb & 1;
       float m[NH], ls[NH];
 #pragma unroll
@@ -525,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < npg; ++j, ++gp) {
         const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
-        const bool kv = key < nvalid;
+        const bool kv = key < nvalid;  // within the sequence's context
+        const int kpos = (pg0 + j) * kPage + key;
         if (!(ok = mbar_wait_warp(B.s_full, gp & 1, p.status))) break;
         tc_fence_after();
         uint32_t sr[16];
@@ -538,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int g = 0; g < NH; ++g) {
             d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
-            if (g < GC) v |= kv && d[g] > kRescaleThreshold;
+            if (g < GC) v |= kpos < lim[g] && d[g] > kRescaleThreshold;
           }
           float vote[NH];
           vote[0] = __any_sync(0xffffffffu, v) ? 1.f : 0.f;
@@ -551,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float wm[NH];
 #pragma unroll
           for (int g = 0; g < NH; ++g)
-            wm[g] = g < GC ? warp_max(kv ? __uint_as_float(sr[g]) * c : -INFINITY) : 0.f;
+            wm[g] = g < GC ? warp_max(kpos < lim[g] ? __uint_as_float(sr[g]) * c : -INFINITY)
+                           : 0.f;
           const float* x = exchange(wm, GC);
           if (!(ok = x != nullptr)) break;
           float alpha[NH];
@@ -560,8 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             alpha[g] = 1.f;
             if (g < GC) {
               const float M = fmaxf(fmaxf(x[g], x[kN + g]), fmaxf(x[2 * kN + g], x[3 * kN + g]));
-              const float mn = fmaxf(m[g], M);  // finite: the page has a visible key
-              if (j > 0) alpha[g] = fast_exp2(m[g] - mn);
+              // -inf while the column has seen no visible key (a split that
+              // starts past its token's position): nothing to rescale yet
+              const float mn = fmaxf(m[g], M);
+              if (j > 0 && mn != -INFINITY) alpha[g] = fast_exp2(m[g] - mn);
               m[g] = mn;
               ls[g] *= alpha[g];
             }
@@ -586,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
           if (g < GC) {
-            const float pv = kv ? fast_exp2(d[g]) : 0.f;
+            const float pv = kpos < lim[g] ? fast_exp2(d[g]) : 0.f;
             const uint16_t pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
             ls[g] += __uint_as_float((uint32_t)pbf << 16);
             sts16(pbase + (g >> 3) * 1024 + (g & 7) * 128 + ((kc ^ (g & 7)) << 4), pbf);
@@ -650,7 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sq = rec[kISeq], unit = rec[kIUnit], dest = rec[kIDest];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
-      const int64_t row0 = (int64_t)sq * p.Hq + (unit / p.NG) * p.G + (unit % p.NG) * GC;
+      const int GC = unit_columns(p, unit);
+      // output row of column g: token t0 + g / G, query head h G + g % G
+      const int64_t tok0 = (int64_t)sq * p.L + (unit % p.NT) * p.Lg;
+      const int head0 = (unit / p.NT) * p.G;
       float res[NH], lse[NH];
       if (pg1 - pg0 <= 0) {
         // nothing visible (lse -inf), or an invalid sequence (lse +inf: the
@@ -684,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < NH; ++g) {
         if (g < GC) {
-          const int64_t row = row0 + g;
+          const int64_t row = (tok0 + g / p.G) * p.Hq + head0 + g % p.G;
           if (dest < 0) {
             if (p.out_f32)
               reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[g];
