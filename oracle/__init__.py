@@ -49,6 +49,20 @@ def _load():
         lib.oracle_rope_neox.argtypes = [f64p, c_int, c_dbl, c_dbl, c_dbl]
         lib.oracle_topk.restype = None
         lib.oracle_topk.argtypes = [f32p, c_i64, c_int, c_int, c_int, f32p, i32p]
+        u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [f32p, c_i64, u8p]
+        lib.oracle_e4m3_decode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [u8p, c_i64, f64p]
+        lib.oracle_kv_write_fp8.restype = c_int
+        lib.oracle_kv_write_fp8.argtypes = [u16p, u16p, u8p, u8p, f32p, f32p, i32p, i32p,
+                                            ctypes.c_void_p, c_i64, c_int, c_int, c_int, c_int,
+                                            c_int, c_int]
+        lib.oracle_attention_fp8.restype = c_int
+        lib.oracle_attention_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, i32p,
+                                             ctypes.c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                             c_int, c_int, c_dbl, ctypes.c_void_p, c_i64, f64p,
+                                             c_int]
         lib.oracle_max_threads.restype = c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -123,6 +137,89 @@ def attention(q, k_cache, v_cache, block_table, context_lens, chunk_lens, scale,
         float(scale), rp, nrows, out, int(nt))
     if rc != 0:
         raise ValueError("oracle_attention: bad row index")
+    return out[:nrows].reshape(out_shape)
+
+
+def _u8(a):
+    """FP8 cache data as a C-contiguous uint8 numpy view (torch uint8/float8 or numpy)."""
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().cpu().contiguous()
+        if a.dtype != torch.uint8:
+            a = a.view(torch.uint8)
+        return np.ascontiguousarray(a.numpy())
+    a = np.ascontiguousarray(a)
+    assert a.dtype.itemsize == 1, a.dtype
+    return a.view(np.uint8)
+
+
+def _f32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def e4m3_encode(x):
+    """Nearest e4m3 codes (uint8) of float32 values: ties to even, saturating at
+    +-448, NaN to a NaN code."""
+    x = _f32(x)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(x.reshape(-1), x.size, out.reshape(-1))
+    return out
+
+
+def e4m3_decode(codes):
+    """Exact float64 values of e4m3 codes."""
+    c = _u8(codes)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode_array(c.reshape(-1), c.size, out.reshape(-1))
+    return out
+
+
+def kv_write_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                 chunk_lens, num_pages, max_pages_per_seq, page_size=128):
+    """FP8 KV write: returns (k_cache', v_cache', skipped), uint8 e4m3 caches with
+    the new tokens' rows quantized (bf16 value / per-head FP32 scale) into their
+    slots; the inputs are not modified."""
+    kc = _u8(k_cache).copy()
+    vc = _u8(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    hkv, d = kc.shape[-2], kc.shape[-1]
+    T = kn.size // (hkv * d)
+    ctx = _i32(context_lens)
+    cl = None if chunk_lens is None else _i32(chunk_lens)
+    skipped = _load().oracle_kv_write_fp8(
+        kn, vn, kc, vc, _f32(k_scale), _f32(v_scale), _i32(block_table).reshape(-1), ctx,
+        None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
+        T, ctx.shape[0], hkv, d, page_size, num_pages, max_pages_per_seq)
+    return kc, vc, skipped
+
+
+def attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, chunk_lens,
+                  scale, num_q_heads, num_kv_heads, num_pages, max_pages_per_seq, rows=None,
+                  num_threads=None, page_size=128, head_dim=128):
+    """Paged attention in float64 over an FP8 cache (uint8 e4m3 codes, per-KV-head
+    FP32 scales).  Same shapes and row selection as attention()."""
+    qq = _u16(q).reshape(-1)
+    kc, vc = _u8(k_cache).reshape(-1), _u8(v_cache).reshape(-1)
+    ctx = _i32(context_lens)
+    B = ctx.shape[0]
+    cl = None if chunk_lens is None else _i32(chunk_lens)
+    T = B if cl is None else int(np.maximum(cl, 0).sum())
+    if rows is None:
+        nrows, rp, out_shape = T * num_q_heads, None, (T, num_q_heads, head_dim)
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows, rp, out_shape = rows.shape[0], rows.ctypes.data_as(ctypes.c_void_p), (rows.shape[0], head_dim)
+    out = np.zeros((max(nrows, 1), head_dim), dtype=np.float64)
+    nt = num_threads if num_threads is not None else max_threads()
+    rc = _load().oracle_attention_fp8(
+        qq, kc, vc, _f32(k_scale), _f32(v_scale), _i32(block_table).reshape(-1), ctx,
+        None if cl is None else cl.ctypes.data_as(ctypes.c_void_p),
+        B, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
+        float(scale), rp, nrows, out, int(nt))
+    if rc != 0:
+        raise ValueError("oracle_attention_fp8: bad row index")
     return out[:nrows].reshape(out_shape)
 
 

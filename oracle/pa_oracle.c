@@ -49,6 +49,62 @@ static double bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
+/* ---------------------------------------------------------------------------
+ * FP8 KV cache ("fp8_e4m3" KV cache in the SGLang measurement of the
+ * "Qwen4-Exp QSA trafia na Ascend..." blog; a quantized KV dtype is also the
+ * --kv-cache-dtype option of the "Qwen 3" TensorSharp doc, section 11).
+ * Readings (each also in the design doc): e4m3 is the e4m3fn encoding (sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is
+ * NaN; largest finite 448); every KV head h has one FP32 scale for K and one
+ * for V; a cached value means code_value * scale; writing divides the bf16
+ * value by the scale in FP32 and rounds that quotient to the nearest e4m3
+ * value, ties to the even code, saturating at +-448.
+ * ------------------------------------------------------------------------- */
+
+/* Value of e4m3 code c (NaN for the two NaN codes). */
+double oracle_e4m3_decode(uint8_t c) {
+  int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return sgn ? -v : v;
+}
+
+/* Nearest e4m3 code to x: the finite code of least distance, the even code
+ * on a tie; |x| >= 448 (infinity too) gives +-448, NaN a NaN code; the sign
+ * of x (zero included) is kept. */
+uint8_t oracle_e4m3_encode(float x) {
+  uint8_t sgn = signbit(x) ? 0x80 : 0;
+  if (isnan(x)) return sgn | 0x7F;
+  double a = fabs((double)x);
+  if (a >= 448.0) return sgn | 0x7E;
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return sgn | (uint8_t)best;
+}
+
+/* Array forms for the Python side. */
+void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}
+
+/* Cache element formats: bf16 values, or e4m3 codes times a per-head scale. */
+enum { KV_BF16 = 0, KV_E4M3 = 1 };
+
+static double kv_value(const void* cache, int64_t idx, int fmt, double scale) {
+  if (fmt == KV_BF16) return bf16_to_f64(((const uint16_t*)cache)[idx]);
+  return oracle_e4m3_decode(((const uint8_t*)cache)[idx]) * scale;
+}
+
 /* Validity of sequence s: lengths consistent and every page it references in
  * range.  Returns 1 when the sequence may be attended/written. */
 static int seq_valid(const int32_t* block_table, const int32_t* context_lens,
@@ -105,6 +161,46 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new,
 }
 
 /*
+ * FP8 KV write: the same slots as oracle_kv_write; element d of KV head h of a
+ * token is stored as the e4m3 code of (float)x / scale[h] (an FP32 quotient).
+ * Returns the number of sequences skipped as invalid.
+ */
+int oracle_kv_write_fp8(const uint16_t* k_new, const uint16_t* v_new, uint8_t* k_cache,
+                        uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                        const int32_t* block_table, const int32_t* context_lens,
+                        const int32_t* chunk_lens, int64_t num_tokens, int num_seqs,
+                        int num_kv_heads, int head_dim, int page_size, int num_pages,
+                        int max_pages_per_seq) {
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  int64_t token = 0;
+  int skipped = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    int64_t n = chunk_lens ? chunk_lens[s] : 1;
+    if (!seq_valid(block_table, context_lens, chunk_lens, s, page_size, num_pages,
+                   max_pages_per_seq)) {
+      ++skipped;
+      token += n > 0 ? n : 0;
+      continue;
+    }
+    int64_t ctx = context_lens[s];
+    for (int64_t j = 0; j < n && token < num_tokens; ++j, ++token) {
+      int64_t pos = ctx - n + j;
+      int64_t page = block_table[(int64_t)s * max_pages_per_seq + pos / page_size];
+      int64_t slot = page * page_size + pos % page_size;
+      for (int h = 0; h < num_kv_heads; ++h)
+        for (int d = 0; d < head_dim; ++d) {
+          int64_t i = (int64_t)h * head_dim + d;
+          float kq = (float)bf16_to_f64(k_new[token * row + i]) / k_scale[h];
+          float vq = (float)bf16_to_f64(v_new[token * row + i]) / v_scale[h];
+          k_cache[slot * row + i] = oracle_e4m3_encode(kq);
+          v_cache[slot * row + i] = oracle_e4m3_encode(vq);
+        }
+    }
+  }
+  return skipped;
+}
+
+/*
  * Dense softmax attention of one query over n keys (steps 2-3 of the
  * definition): x_t = scale * <q, K_t>, m = max_t x_t, w_t = exp(x_t - m),
  * out = sum_t w_t V_t / sum_t w_t.  Also returns lse = m + log(sum_t w_t), the
@@ -138,9 +234,9 @@ void oracle_dense_attention(const double* q, const double* K, const double* V,
  * t = 0..pos through the block table (slot = page * P + t % P) into dense
  * double buffers, then the dense attention above.
  */
-static void attend_row(const uint16_t* qrow, const uint16_t* k_cache,
-                       const uint16_t* v_cache, const int32_t* bt_row,
-                       int64_t pos, int kv_head, int num_kv_heads,
+static void attend_row(const uint16_t* qrow, const void* k_cache,
+                       const void* v_cache, int fmt, double ks, double vs,
+                       const int32_t* bt_row, int64_t pos, int kv_head, int num_kv_heads,
                        int head_dim, int page_size, double scale, double* out,
                        double* qd, double* K, double* V, double* x) {
   const int64_t row = (int64_t)num_kv_heads * head_dim;
@@ -148,11 +244,10 @@ static void attend_row(const uint16_t* qrow, const uint16_t* k_cache,
   for (int d = 0; d < head_dim; ++d) qd[d] = bf16_to_f64(qrow[d]);
   for (int64_t t = 0; t < nkeys; ++t) {
     int64_t slot = (int64_t)bt_row[t / page_size] * page_size + t % page_size;
-    const uint16_t* k = k_cache + slot * row + (int64_t)kv_head * head_dim;
-    const uint16_t* v = v_cache + slot * row + (int64_t)kv_head * head_dim;
+    int64_t base = slot * row + (int64_t)kv_head * head_dim;
     for (int d = 0; d < head_dim; ++d) {
-      K[t * head_dim + d] = bf16_to_f64(k[d]);
-      V[t * head_dim + d] = bf16_to_f64(v[d]);
+      K[t * head_dim + d] = kv_value(k_cache, base + d, fmt, ks);
+      V[t * head_dim + d] = kv_value(v_cache, base + d, fmt, vs);
     }
   }
   oracle_dense_attention(qd, K, V, nkeys, head_dim, scale, out, NULL, x);
@@ -166,13 +261,13 @@ static void attend_row(const uint16_t* qrow, const uint16_t* k_cache,
  *        or every row in order when rows == NULL (nrows must then be T*Hq).
  * Returns 0, or -1 if a requested row index is out of range.
  */
-int oracle_attention(const uint16_t* q, const uint16_t* k_cache,
-                     const uint16_t* v_cache, const int32_t* block_table,
-                     const int32_t* context_lens, const int32_t* chunk_lens,
-                     int num_seqs, int num_q_heads, int num_kv_heads,
-                     int head_dim, int page_size, int num_pages,
-                     int max_pages_per_seq, double scale, const int64_t* rows,
-                     int64_t nrows, double* out, int num_threads) {
+static int attention_impl(const uint16_t* q, const void* k_cache, const void* v_cache,
+                          int fmt, const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          const int32_t* chunk_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int page_size, int num_pages,
+                          int max_pages_per_seq, double scale, const int64_t* rows,
+                          int64_t nrows, double* out, int num_threads) {
   /* token -> (sequence, index within its chunk) */
   int64_t T = 0;
   for (int s = 0; s < num_seqs; ++s) T += chunk_lens ? (chunk_lens[s] > 0 ? chunk_lens[s] : 0) : 1;
@@ -221,9 +316,12 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_cache,
         for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
         continue;
       }
-      attend_row(q + (token * num_q_heads + g) * (int64_t)head_dim, k_cache,
-                 v_cache, block_table + (int64_t)s * max_pages_per_seq, pos,
-                 g / group, num_kv_heads, head_dim, page_size, scale, o, qd, K, V, x);
+      const int h = g / group;
+      attend_row(q + (token * num_q_heads + g) * (int64_t)head_dim, k_cache, v_cache, fmt,
+                 fmt == KV_E4M3 ? (double)k_scale[h] : 1.0,
+                 fmt == KV_E4M3 ? (double)v_scale[h] : 1.0,
+                 block_table + (int64_t)s * max_pages_per_seq, pos, h, num_kv_heads,
+                 head_dim, page_size, scale, o, qd, K, V, x);
     }
     free(x);
     free(qd);
@@ -233,6 +331,33 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_cache,
   free(tok_seq);
   free(tok_j);
   return 0;
+}
+
+int oracle_attention(const uint16_t* q, const uint16_t* k_cache,
+                     const uint16_t* v_cache, const int32_t* block_table,
+                     const int32_t* context_lens, const int32_t* chunk_lens,
+                     int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int page_size, int num_pages,
+                     int max_pages_per_seq, double scale, const int64_t* rows,
+                     int64_t nrows, double* out, int num_threads) {
+  return attention_impl(q, k_cache, v_cache, KV_BF16, NULL, NULL, block_table, context_lens,
+                        chunk_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size,
+                        num_pages, max_pages_per_seq, scale, rows, nrows, out, num_threads);
+}
+
+/* The same attention over an FP8 cache: K_t = e4m3(k) * k_scale[h], V_t =
+ * e4m3(v) * v_scale[h], exactly, in double precision. */
+int oracle_attention_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                         const float* k_scale, const float* v_scale,
+                         const int32_t* block_table, const int32_t* context_lens,
+                         const int32_t* chunk_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int page_size, int num_pages,
+                         int max_pages_per_seq, double scale, const int64_t* rows,
+                         int64_t nrows, double* out, int num_threads) {
+  return attention_impl(q, k_cache, v_cache, KV_E4M3, k_scale, v_scale, block_table,
+                        context_lens, chunk_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                        page_size, num_pages, max_pages_per_seq, scale, rows, nrows, out,
+                        num_threads);
 }
 
 /*
