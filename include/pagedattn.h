@@ -14,6 +14,8 @@
  *    KV ranges (flash-decoding) and merged by pa_combine.
  *  - pa_decode_multi: the same causal attention for q_len new tokens per
  *    sequence (every chunk q_len long), run as B * q_len decode queries.
+ *  - pa_kv_write_fp8 / pa_decode_fp8: the same write and decode over an FP8
+ *    (e4m3) cache with per-KV-head scales.
  *  - pa_prefill_chunk: "KV cache update -> causal attention" of prefill_fwd
  *    ("Qwen3-14B", "prefill_fwd"), inputs packed token-major with
  *    T = sum(chunk_lens); full causal attention without window or sinks
@@ -99,6 +101,7 @@ typedef struct pa_dims {
 #define PA_STATUS_BAD_LENGTH 2  /* inconsistent context/chunk lengths        */
 #define PA_STATUS_BAD_TOKENS 4  /* sum(chunk_lens) != num_tokens             */
 #define PA_STATUS_TIMEOUT 8     /* a bounded wait inside a kernel gave up    */
+#define PA_STATUS_Q_RANGE 16    /* FP8-cache decode: |q| too large for F16   */
 
 /* Largest batch accepted by the calls that take chunk_lens (the per-sequence
  * token offsets are built in shared memory). */
@@ -234,8 +237,48 @@ int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
                     size_t workspace_bytes, int32_t num_splits, pa_dims dims,
                     int32_t* status, pa_stream_t stream);
 
-/* Workspace bytes pa_decode_multi needs; (size_t)-1 for invalid arguments. */
+/* Workspace bytes pa_decode_multi (and pa_decode_fp8) need; (size_t)-1 for
+ * invalid arguments. */
 size_t pa_decode_multi_workspace_size(pa_dims dims, int32_t q_len, int32_t num_splits);
+
+/*
+ * FP8 KV cache: the "fp8_e4m3" KV cache dtype (SGLang, as quoted in the
+ * "Qwen4-Exp QSA trafia na Ascend..." blog; a quantized KV dtype is also the
+ * --kv-cache-dtype option of the "Qwen 3" TensorSharp doc, section 11).
+ * k_cache, v_cache  uint8 [num_pages, P, Hkv, D] e4m3fn codes (sign, 4
+ *                   exponent bits with bias 7, 3 mantissa bits; no infinities;
+ *                   largest finite 448) -- half the bytes of the bf16 cache
+ * k_scale, v_scale  float32 [Hkv] device arrays: a cached code c of KV head h
+ *                   means value(c) * scale[h]
+ */
+
+/*
+ * pa_kv_write_fp8 -- pa_kv_write into an FP8 cache: element d of KV head h is
+ * stored as the e4m3 code of x / scale[h] (the FP32 quotient, rounded to
+ * nearest with ties to even, saturating at +-448; NaN stays NaN).  Slots,
+ * validity rules and status bits are those of pa_kv_write.  k_scale and
+ * v_scale must be non-null and 4-byte aligned.
+ */
+int pa_kv_write_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    const int32_t* context_lens, const int32_t* chunk_lens,
+                    int32_t num_tokens, pa_dims dims, int32_t* status, pa_stream_t stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode_multi over an FP8 cache (q_len = 1: single-token
+ * decode).  The K/V pages are read as e4m3 (half the bytes) and converted on
+ * the chip to F16, which holds every e4m3 value exactly; q is converted to F16
+ * too, so |q| must stay below 65520 (larger elements set PA_STATUS_Q_RANGE and
+ * make that item's output undefined); P is rounded to F16 for the P.V
+ * product.  The scores are q . K * k_scale[h] * scale and the output is
+ * multiplied by v_scale[h].  Arguments, schedules, workspace
+ * (pa_decode_multi_workspace_size) and status bits as pa_decode_multi.
+ */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, const int32_t* block_table,
+                  const int32_t* context_lens, int32_t q_len, float scale, void* out,
+                  int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                  int32_t num_splits, pa_dims dims, int32_t* status, pa_stream_t stream);
 
 /*
  * pa_prefill_chunk -- causal attention of a packed chunk of new tokens over

@@ -20,6 +20,7 @@ HEAD_DIM = 128
 PAGE_SIZE = 128
 PA_BF16, PA_F32 = 0, 1
 PA_STATUS_BAD_PAGE, PA_STATUS_BAD_LENGTH, PA_STATUS_BAD_TOKENS, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+PA_STATUS_Q_RANGE = 16
 PA_MAX_CHUNKED_SEQS = 16384
 PA_SPLITS_BALANCED = -1
 PA_BALANCED_MAX_SEQS = 512
@@ -32,7 +33,8 @@ PA_MAX_Q_LEN = 16
 EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_auto_splits",
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
-            "pa_decode_multi", "pa_decode_multi_workspace_size")
+            "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
+            "pa_decode_fp8")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -76,6 +78,11 @@ def load(path: str = LIB_PATH):
     lib.pa_decode_multi.restype = ctypes.c_int
     lib.pa_decode_multi.argtypes = [vp, vp, vp, vp, vp, i32, f32, vp, i32, vp, sz, i32, pa_dims,
                                     vp, vp]
+    lib.pa_kv_write_fp8.restype = ctypes.c_int
+    lib.pa_kv_write_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, pa_dims, vp, vp]
+    lib.pa_decode_fp8.restype = ctypes.c_int
+    lib.pa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, i32, vp, sz, i32,
+                                  pa_dims, vp, vp]
     lib.pa_decode_multi_workspace_size.restype = sz
     lib.pa_decode_multi_workspace_size.argtypes = [pa_dims, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
@@ -306,6 +313,78 @@ def pa_decode_multi(q, k_cache, v_cache, block_table, context_lens, q_len, scale
                                 _ptr(workspace), ws_bytes, int(num_splits), d, _ptr(status),
                                 _stream(stream))
     _check("pa_decode_multi", rc)
+    return out
+
+
+def _need_fp8_cache(t, name, dev):
+    if t.device != dev or t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        raise TypeError(f"{name} must be a uint8 (or float8_e4m3fn) tensor on {dev}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def pa_kv_write_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                    chunk_lens=None, status=None, stream=None):
+    """Quantizing KV write into an FP8 (e4m3) cache [num_pages, 128, Hkv, 128] with
+    per-KV-head float32 scales."""
+    dev = k_cache.device
+    _need(k_new, "k_new", torch.bfloat16, dev)
+    _need(v_new, "v_new", torch.bfloat16, dev)
+    _need_fp8_cache(k_cache, "k_cache", dev)
+    _need_fp8_cache(v_cache, "v_cache", dev)
+    _need(k_scale, "k_scale", torch.float32, dev)
+    _need(v_scale, "v_scale", torch.float32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if chunk_lens is not None:
+        _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    T = k_new.shape[0]
+    d = _cache_dims(k_cache.shape[2], k_cache, block_table)
+    rc = load().pa_kv_write_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                                _ptr(context_lens), _ptr(chunk_lens), T, d, _ptr(status),
+                                _stream(stream))
+    _check("pa_kv_write_fp8", rc)
+
+
+def pa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, q_len=1,
+                  scale=None, out=None, out_dtype=torch.bfloat16, workspace=None, num_splits=0,
+                  status=None, stream=None):
+    """Decode (q_len new tokens per sequence) over an FP8 (e4m3) cache with
+    per-KV-head scales.  q: [B * q_len, Hq, 128] bf16.  Returns out [B * q_len, Hq, 128]."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need_fp8_cache(k_cache, "k_cache", dev)
+    _need_fp8_cache(v_cache, "v_cache", dev)
+    _need(k_scale, "k_scale", torch.float32, dev)
+    _need(v_scale, "v_scale", torch.float32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    T, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    q_len = int(q_len)
+    if q_len < 1 or T != d.num_seqs * q_len:
+        raise ValueError(f"q has {T} rows; expected num_seqs ({d.num_seqs}) x q_len ({q_len})")
+    if out is None:
+        out = torch.empty(T, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    need = pa_decode_multi_workspace_size(d, q_len, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                              _ptr(v_scale), _ptr(block_table), _ptr(context_lens), q_len, scale,
+                              _ptr(out), code, _ptr(workspace), ws_bytes, int(num_splits), d,
+                              _ptr(status), _stream(stream))
+    _check("pa_decode_fp8", rc)
     return out
 
 

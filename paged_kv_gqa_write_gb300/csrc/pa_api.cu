@@ -215,6 +215,21 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
   return r == CUDA_SUCCESS;
 }
 
+// An FP8 (e4m3) cache viewed as [num_pages * 128 rows, Hkv * 128 one-byte
+// columns]: 128-byte boxes (one KV head's row) of 128 rows, 128-byte swizzle.
+bool encode_cache_map_fp8(CUtensorMap* map, const void* cache, const pa_dims& d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d.num_kv_heads * kHeadDim, (cuuint64_t)d.num_pages * kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)d.num_kv_heads * kHeadDim};
+  cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kPage};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // The caches viewed as [num_pages * 128 rows, Hkv * 128 columns], row pitch
 // Hkv * 128 * 2 bytes; 64-column (128-byte) boxes of 128 rows, 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* map, const void* cache, const pa_dims& d) {
@@ -271,16 +286,20 @@ size_t topk_ws_bytes(int rows, int vocab, int k, int num_sms) {
 int run_decode(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
                int32_t out_dtype, uint8_t* ws, const DecodePlan& pl, const pa_dims& d,
-               int32_t q_len, int32_t* status, int sms, cudaStream_t st) {
+               int32_t q_len, int32_t* status, int sms, cudaStream_t st,
+               const float* k_scale = nullptr, const float* v_scale = nullptr) {
+  const bool fp8 = k_scale != nullptr;
   const int G = d.num_q_heads / d.num_kv_heads;
   int NT, Lg;
   token_groups(G, q_len, &NT, &Lg);
   const int64_t items = (int64_t)pl.splits * d.num_seqs * d.num_kv_heads * NT;
   if (items > INT32_MAX) return PA_ERR_DIMS;
   CUtensorMap tm_k, tm_v, tm_q;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d) ||
-      !encode_q_decode_map(&tm_q, q, d, q_len, G, Lg))
-    return PA_ERR_TENSOR_MAP;
+  const bool maps_ok = fp8 ? encode_cache_map_fp8(&tm_k, k_cache, d) &&
+                                 encode_cache_map_fp8(&tm_v, v_cache, d)
+                           : encode_cache_map(&tm_k, k_cache, d) &&
+                                 encode_cache_map(&tm_v, v_cache, d);
+  if (!maps_ok || !encode_q_decode_map(&tm_q, q, d, q_len, G, Lg)) return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -301,6 +320,8 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.L = q_len;
   p.NT = NT;
   p.Lg = Lg;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   p.pps = pl.pps;
@@ -373,10 +394,14 @@ const char* pa_status_string(int32_t code) {
   return "unknown status";
 }
 
-int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                const int32_t* block_table, const int32_t* context_lens,
-                const int32_t* chunk_lens, int32_t num_tokens, pa_dims d, int32_t* status,
-                pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int kv_write_impl(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                  const float* k_scale, const float* v_scale, const int32_t* block_table,
+                  const int32_t* context_lens, const int32_t* chunk_lens, int32_t num_tokens,
+                  pa_dims d, int32_t* status, pa_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_tokens < 0) return PA_ERR_DIMS;
@@ -394,6 +419,8 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
   p.v_new = static_cast<const uint4*>(v_new);
   p.k_cache = static_cast<uint4*>(k_cache);
   p.v_cache = static_cast<uint4*>(v_cache);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_table = block_table;
   p.context_lens = context_lens;
   p.chunk_lens = chunk_lens;
@@ -404,6 +431,29 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   return launch_result(pa::launch_kv_write(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                const int32_t* block_table, const int32_t* context_lens,
+                const int32_t* chunk_lens, int32_t num_tokens, pa_dims d, int32_t* status,
+                pa_stream_t stream) {
+  return kv_write_impl(k_new, v_new, k_cache, v_cache, nullptr, nullptr, block_table,
+                       context_lens, chunk_lens, num_tokens, d, status, stream);
+}
+
+int pa_kv_write_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    const int32_t* context_lens, const int32_t* chunk_lens, int32_t num_tokens,
+                    pa_dims d, int32_t* status, pa_stream_t stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL_POINTER;
+  if (((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
+    return PA_ERR_ALIGNMENT;
+  return kv_write_impl(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table,
+                       context_lens, chunk_lens, num_tokens, d, status, stream);
 }
 
 int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
@@ -544,6 +594,37 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               pa_dims d, int32_t* status, pa_stream_t stream) {
   return pa_decode_multi(q, k_cache, v_cache, block_table, context_lens, 1, scale, out,
                          out_dtype, workspace, ws_bytes, num_splits, d, status, stream);
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, const int32_t* block_table,
+                  const int32_t* context_lens, int32_t q_len, float scale, void* out,
+                  int32_t out_dtype, void* workspace, size_t ws_bytes, int32_t num_splits,
+                  pa_dims d, int32_t* status, pa_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return PA_ERR_DIMS;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
+  if (d.num_seqs == 0) return PA_OK;
+  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !context_lens ||
+      !out)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
+    return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  DecodePlan pl;
+  if (!make_plan(d, q_len, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (pl.ws_bytes > 0) {
+    if (!workspace || ws_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+  }
+  return run_decode(q, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
+                    static_cast<uint8_t*>(workspace), pl, d, q_len, status, sms,
+                    reinterpret_cast<cudaStream_t>(stream), k_scale, v_scale);
 }
 
 int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, void* out,

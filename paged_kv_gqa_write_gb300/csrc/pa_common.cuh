@@ -181,6 +181,15 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, 
          | ((uint32_t)(M >> 4) << 24);        // M / 16
 }
 
+// The same with F16 A and B (the FP8-cache decode: e4m3 values are exact in F16).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                            // D format: F32
+         | ((a_mn ? 1u : 0u) << 15)           // A major (A and B format 0: F16)
+         | ((b_mn ? 1u : 0u) << 16)           // B major
+         | ((uint32_t)(N >> 3) << 17)         // N / 8
+         | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand whose
 // swizzle atoms (8 rows of 128 bytes) start on 1024-byte boundaries.
 // lbo / sbo: leading / stride byte offsets of the canonical layout.
@@ -399,6 +408,8 @@ struct DecodeParams {
   int32_t B, Hq, Hkv, G;
   int32_t L;                    // new tokens (queries) per sequence
   int32_t NT, Lg;               // token groups per KV head, tokens per group
+  const float* k_scale;         // FP8 cache: [Hkv] per-head K and V scales (else null)
+  const float* v_scale;
   int32_t num_pages, max_pages;
   int32_t pps;                  // pages per split
   int32_t S;                    // splits
@@ -476,8 +487,10 @@ struct CombineParams {
 struct KvWriteParams {
   const uint4* k_new;
   const uint4* v_new;
-  uint4* k_cache;
+  uint4* k_cache;               // bf16 rows, or e4m3 rows for the FP8 write
   uint4* v_cache;
+  const float* k_scale;         // FP8 write: [Hkv] per-head scales (else null)
+  const float* v_scale;
   const int32_t* block_table;
   const int32_t* context_lens;
   const int32_t* chunk_lens;  // may be null

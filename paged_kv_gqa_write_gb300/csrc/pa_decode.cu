@@ -41,6 +41,9 @@
 //  * warps 6-9, one thread per head dim: the epilogue of the previous item
 //    (O / l from TMEM, double-buffered) overlaps the next item's pages; it
 //    writes `out` (one split) or normalised partials (o, lse) for the combine.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "pa_launch.cuh"
 
 namespace pa {
@@ -50,8 +53,7 @@ constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
 constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
-constexpr int kThreads = 10 * 32;
-constexpr int kStages = 3;
+constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert, one thread per key row
 constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
 constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
@@ -62,18 +64,34 @@ constexpr int kOpBytes = 2 * kAtom;        // Q or P operand: two 64-element ato
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// shared memory (offsets from a 1024-aligned base)
-constexpr int kRing = 0;
-constexpr int kQ = kRing + kStages * kStageBytes;  // [kSlots] query operands
-constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
-constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax-warp exchange
-constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O buffer
-constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][kInfoInts]: item records
-constexpr int kBars = kInfo + kSlots * 8 * 4;
-constexpr int kNumBars = 3 * kStages + 2 * kSlots + 2 + 4 * 2 + 1;
-constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
+// Shared memory (offsets from a 1024-aligned base).  BF16 cache: a 3-stage
+// ring of K/V operand pages loaded by TMA.  FP8 cache: a 2-stage ring of e4m3
+// pages (32 KB each) loaded by TMA, converted by warps 10-13 into a 2-stage
+// ring of F16 operand pages (the tensor core reads F16; every e4m3 value is
+// exact in it).
+constexpr int kBox8 = 128 * kPage;         // 128 one-byte dims x 128 tokens = 16 KB
+template <bool FP8, int NH = 16>
+struct Layout {
+  static constexpr int kStages = FP8 ? 2 : 3;   // operand pages (K lo, K hi, V lo, V hi)
+  static constexpr int kStages8 = FP8 ? 2 : 0;  // e4m3 pages (K, V)
+  // converter warps: 8 (K and V converted side by side) where the registers
+  // allow it (the 8-column softmax), else 4 (K, then V)
+  static constexpr int kConvWarps = FP8 ? (NH == 8 ? 8 : 4) : 0;
+  static constexpr int kThreads = (10 + kConvWarps) * 32;
+  static constexpr int kRing = 0;
+  static constexpr int kRing8 = kRing + kStages * kStageBytes;
+  static constexpr int kQ = kRing8 + kStages8 * 2 * kBox8;  // [kSlots] query operands
+  static constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
+  static constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax exchange
+  static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O
+  static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][8]: item records
+  static constexpr int kBars = kInfo + kSlots * 8 * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * kSlots + 2 + 4 * 2 + 1;
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
+};
 constexpr int kSmemLimit = 232448;
-static_assert(kSmem <= kSmemLimit, "decode shared memory exceeds the per-CTA limit");
+static_assert(Layout<false>::kSmem <= kSmemLimit, "decode shared memory exceeds the limit");
+static_assert(Layout<true>::kSmem <= kSmemLimit, "FP8 decode shared memory exceeds the limit");
 
 // TMEM columns
 constexpr uint32_t kColS = 0;   // S^T: 16 columns
@@ -81,9 +99,11 @@ constexpr uint32_t kColO = 16;  // O^T[2]: 16 columns each
 constexpr uint32_t kTmemCols = 64;
 
 struct Bars {
-  uint64_t* k_full;    // [kStages]
-  uint64_t* v_full;    // [kStages]
-  uint64_t* kv_empty;  // [kStages]
+  uint64_t* k_full;    // [kStages] operand page: K ready (TMA, or the FP8 converters)
+  uint64_t* v_full;    // [kStages] V ready
+  uint64_t* kv_empty;  // [kStages] P.V of the page done
+  uint64_t* kv8_full;  // [kStages8] FP8: e4m3 page landed
+  uint64_t* kv8_empty; // [kStages8] FP8: e4m3 page converted
   uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
   uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
   uint64_t* s_full;    // S^T of the current page
@@ -140,12 +160,36 @@ __device__ __forceinline__ int unit_columns(const DecodeParams& p, int unit) {
   return min(p.Lg, p.L - t0) * p.G;
 }
 
+// 4 e4m3 codes (bytes 0..3 of w) -> 4 F16 values (exact): two F16 pairs.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 16 e4m3 codes -> 16 F16 values (exact), as two 16-byte chunks.
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4& lo, uint4& hi) {
+  e4m3x4_to_f16x4(c.x, lo.x, lo.y);
+  e4m3x4_to_f16x4(c.y, lo.z, lo.w);
+  e4m3x4_to_f16x4(c.z, hi.x, hi.y);
+  e4m3x4_to_f16x4(c.w, hi.z, hi.w);
+}
+
 // NH: columns the softmax and epilogue handle (8 or 16, >= any item's GC).
-template <int NH>
-__global__ void __launch_bounds__(kThreads, 1)
+// FP8: the cache holds e4m3 codes with per-KV-head scales.
+template <int NH, bool FP8>
+__global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  using Lay = Layout<FP8, NH>;
+  constexpr int kConvWarps = Lay::kConvWarps;
+  constexpr int kStages = Lay::kStages;
+  constexpr int kStages8 = FP8 ? Lay::kStages8 : 1;  // (the bf16 kernel has no e4m3 ring)
+  constexpr int kRing = Lay::kRing, kRing8 = Lay::kRing8, kQ = Lay::kQ, kP = Lay::kP;
+  constexpr int kX = Lay::kX, kML = Lay::kML, kInfo = Lay::kInfo, kBars = Lay::kBars;
+  constexpr int kNumBars = Lay::kNumBars, kThreads = Lay::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.k_full = bar;
   B.v_full = B.k_full + kStages;
   B.kv_empty = B.v_full + kStages;
-  B.q_full = B.kv_empty + kStages;
+  B.kv8_full = B.kv_empty + kStages;
+  B.kv8_empty = B.kv8_full + Lay::kStages8;  // (none in the bf16 kernel)
+  B.q_full = B.kv8_empty + Lay::kStages8;
   B.q_empty = B.q_full + kSlots;
   B.s_full = B.q_empty + kSlots;
   B.p_full = B.s_full + 1;
@@ -169,13 +215,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&B.k_full[i], 1);
-      mbar_init(&B.v_full[i], 1);
+      mbar_init(&B.k_full[i], FP8 ? 4 : 1);  // FP8: one arrival per converter warp
+      mbar_init(&B.v_full[i], FP8 ? 4 : 1);
       mbar_init(&B.kv_empty[i], 1);
+    }
+    for (int i = 0; i < Lay::kStages8; ++i) {
+      mbar_init(&B.kv8_full[i], 1);
+      mbar_init(&B.kv8_empty[i], kConvWarps);
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&B.q_full[i], 1);
-      mbar_init(&B.q_empty[i], 1 + 4 + 4);  // MMA, 4 softmax warps, 4 epilogue warps
+      // MMA, 4 softmax warps, 4 epilogue warps (, the converter warps)
+      mbar_init(&B.q_empty[i], 1 + 4 + 4 + kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.o_full[i], 1);
@@ -364,6 +415,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int slot = n % kSlots;
       if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
+      if constexpr (FP8) {
+        if (npg > 0) {
+          // the tensor core reads F16 here: the warp converts the item's query
+          // rows (bf16 -> F16, exact below 65520 in magnitude) into the operand
+          const uint32_t qd = smem_u32(smem + kQ + slot * kOpBytes);
+          const int qh = (w.unit / p.NT) * p.G;
+          const int64_t qt = (int64_t)w.s * p.L + (w.unit % p.NT) * p.Lg;
+          const int64_t T = (int64_t)p.B * p.L;
+          bool big = false;
+          for (int i = lane; i < p.Lg * p.G * 16; i += 32) {
+            const int r = i >> 4, k = i & 15;
+            const int64_t tok = qt + r / p.G;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (tok < T)
+              v = __ldg(reinterpret_cast<const uint4*>(
+                            p.q + (tok * p.Hq + qh + r % p.G) * kHeadDim) + k);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = __uint_as_float(wv[e] << 16);
+              const float b = __uint_as_float(wv[e] & 0xffff0000u);
+              big |= fabsf(a) >= 65520.f || fabsf(b) >= 65520.f;
+              const __half2 h2 = __floats2half2_rn(a, b);
+              o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            sts128(qd + (k >> 3) * kAtom + r * 128 + (((k & 7) ^ (r & 7)) << 4), o[0], o[1],
+                   o[2], o[3]);
+          }
+          if (__any_sync(0xffffffffu, big) && lane == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_Q_RANGE);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+      }
       if (lane == 0) {
         int* rec = info + kInfoInts * slot;
         rec[kICtx] = w.ctx;
@@ -374,7 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         rec[kIUnit] = w.unit;
         rec[kIDest] = w.dest;
         rec[kIDone] = item ? 0 : 1;
-        if (npg > 0) {
+        if (FP8 || npg <= 0) {
+          mbar_arrive(&B.q_full[slot]);  // FP8: the rows above are in place
+          q_pending[slot] = -1;
+        } else {
           // q as [tokens][Hq][128]: Lg tokens x the G heads of this KV head
           // (rows of a short last group past the sequence's tokens are loaded
           // too and never used)
@@ -384,9 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(qd, &tm_q, 0, qh, qt, &B.q_full[slot], pol);
           tma_load_3d(qd + kAtom, &tm_q, 64, qh, qt, &B.q_full[slot], pol);
           q_pending[slot] = (int)((n / kSlots) & 1);
-        } else {
-          mbar_arrive(&B.q_full[slot]);
-          q_pending[slot] = -1;
         }
       }
       if (!item) break;
@@ -398,7 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < cnt; ++k) {
           const int page = __shfl_sync(0xffffffffu, pid_l, k);
           int lok = 1;
-          if (lane == 0) {
+          if (lane == 0 && FP8) {
+            // e4m3 K and V tiles (128 one-byte dims x 128 tokens each)
+            const int st = gp % kStages8;
+            lok = mbar_wait(&B.kv8_empty[st], ((gp / kStages8) & 1) ^ 1, p.status);
+            if (lok) {
+              uint8_t* dst = smem + kRing8 + st * 2 * kBox8;
+              const int y = page * kPage;
+              mbar_arrive_expect_tx(&B.kv8_full[st], 2 * kBox8);
+              tma_load_2d(dst, &tm_k, x, y, &B.kv8_full[st], pol);
+              tma_load_2d(dst + kBox8, &tm_v, x, y, &B.kv8_full[st], pol);
+            }
+          } else if (lane == 0) {
             const int st = gp % kStages;
             lok = mbar_wait(&B.kv_empty[st], ((gp / kStages) & 1) ^ 1, p.status);
             if (lok) {
@@ -420,7 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // drain: copies still in flight (only after a timeout elsewhere) must land
     // before the CTA exits
-    if (lane == 0) {
+    if (lane == 0 && FP8) {
+      for (uint32_t g = gp > kStages8 ? gp - kStages8 : 0; g < gp; ++g)
+        mbar_wait(&B.kv8_full[g % kStages8], (g / kStages8) & 1, nullptr);
+    } else if (lane == 0) {
       for (uint32_t g = gp > kStages ? gp - kStages : 0; g < gp; ++g) {
         mbar_wait(&B.k_full[g % kStages], (g / kStages) & 1, nullptr);
         mbar_wait(&B.v_full[g % kStages], (g / kStages) & 1, nullptr);
@@ -432,8 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = umma_idesc_bf16(128, kN, false, false);
-      const uint32_t idesc_pv = umma_idesc_bf16(128, kN, true, false);
+      const uint32_t idesc_qk = FP8 ? umma_idesc_f16(128, kN, false, false)
+                                    : umma_idesc_bf16(128, kN, false, false);
+      const uint32_t idesc_pv = FP8 ? umma_idesc_f16(128, kN, true, false)
+                                    : umma_idesc_bf16(128, kN, true, false);
       uint32_t gp = 0, nb = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
@@ -485,6 +587,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(B.mma_done, 0, nullptr);
     }
     __syncwarp();
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ FP8 converters, thread = key
+    // Each page: wait for its e4m3 tiles and for the operand page to be free
+    // (P.V of the previous page done), then rewrite K and V as F16 in the
+    // swizzled layout the bf16 path gets from TMA; K is published first so
+    // that QK^T starts while V converts.
+    if constexpr (FP8) {
+      const int ct = threadIdx.x - kConvWarp0 * 32;
+      const int row = ct & 127;                       // key 0..127
+      const int sw = row & 7;                         // 128-byte swizzle of the row
+      // with 8 converter warps, warps 10-13 convert K and 14-17 V
+      const int t_lo = kConvWarps == 8 ? (ct >> 7) : 0, t_hi = kConvWarps == 8 ? t_lo + 1 : 2;
+      uint32_t gp = 0;
+      bool ok = true;
+      for (uint32_t n = 0; ok; ++n) {
+        const int slot = n % kSlots;
+        if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
+        const int* rec = info + kInfoInts * slot;
+        if (rec[kIDone]) break;
+        const int npg = rec[kIPg1] - rec[kIPg0];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+        for (int j = 0; j < npg; ++j, ++gp) {
+          const int st8 = gp % kStages8, st = gp % kStages;
+          if (!(ok = mbar_wait_warp(&B.kv8_full[st8], (gp / kStages8) & 1, p.status))) break;
+          if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((gp / kStages) & 1) ^ 1, p.status))) break;
+          const uint32_t src = smem_u32(smem + kRing8 + st8 * 2 * kBox8) + row * 128;
+          const uint32_t dst = smem_u32(smem + kRing + st * kStageBytes) + row * 128;
+          for (int t = t_lo; t < t_hi; ++t) {  // K, then V
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // dims 16c .. 16c + 15
+              uint4 lo, hi;
+              e4m3x16_to_f16(lds128(src + t * kBox8 + ((c ^ sw) << 4)), lo, hi);
+              const uint32_t d = dst + t * 2 * kBox + (c >> 2) * kBox;
+              sts128(d + (((2 * (c & 3)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
+              sts128(d + (((2 * (c & 3) + 1) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(t == 0 ? &B.k_full[st] : &B.v_full[st]);
+          }
+          if (lane == 0) mbar_arrive(&B.kv8_empty[st8]);
+        }
+      }
+    }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ softmax, thread = key
     const int quarter = warp & 3;  // TMEM lanes this warp may access
@@ -493,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     float* xbuf = reinterpret_cast<float*>(smem + kX);
     float* ml = reinterpret_cast<float*>(smem + kML);
-    const float c = p.scale_log2;
+    float c = p.scale_log2;  // FP8: times the item's K scale
     // P^T operand, K-major over keys: row g (head), 64-key atoms, 128-byte swizzle
     const int kc = (key & 63) >> 3;
     const uint32_t p_key = (uint32_t)((key >> 6) * kAtom + (key & 7) * 2);
@@ -527,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npg = pg1 - pg0;
       if (npg <= 0) continue;
       const int GC = unit_columns(p, unit);
+      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
       // column g (token t0 + g / G) sees key positions below lim[g]
       int lim[NH];
       {
@@ -609,8 +757,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < NH; ++g) {
           if (g < GC) {
             const float pv = kpos < lim[g] ? fast_exp2(d[g]) : 0.f;
-            const uint16_t pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
-            ls[g] += __uint_as_float((uint32_t)pbf << 16);
+            uint16_t pbf;
+            if constexpr (FP8) {
+              const __half ph = __float2half_rn(pv);  // the F16 operand
+              pbf = __half_as_ushort(ph);
+              ls[g] += __half2float(ph);
+            } else {
+              pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+              ls[g] += __uint_as_float((uint32_t)pbf << 16);
+            }
             sts16(pbase + (g >> 3) * 1024 + (g & 7) * 128 + ((kc ^ (g & 7)) << 4), pbf);
           }
         }
@@ -673,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int GC = unit_columns(p, unit);
+      const float vsc = FP8 ? __ldg(p.v_scale + unit / p.NT) : 1.f;  // FP8: V scale
       // output row of column g: token t0 + g / G, query head h G + g % G
       const int64_t tok0 = (int64_t)sq * p.L + (unit % p.NT) * p.Lg;
       const int head0 = (unit / p.NT) * p.G;
@@ -698,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
           const float mm = ml[(ob * kN + g) * 2], L = ml[(ob * kN + g) * 2 + 1];
-          const float inv = L > 0.f ? 1.f / L : 0.f;
+          const float inv = L > 0.f ? vsc / L : 0.f;
           res[g] = __uint_as_float(orow[g]) * inv;
           lse[g] = L > 0.f ? (mm + __log2f(L)) * kLn2 : -INFINITY;
         }
@@ -736,15 +892,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NH>
+template <int NH, bool FP8>
 cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                       const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr int smem = Layout<FP8, NH>::kSmem, threads = Layout<FP8, NH>::kThreads;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
   if (grid < 1) return cudaSuccess;
-  decode_kernel<NH><<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
+  decode_kernel<NH, FP8><<<grid, threads, smem, stream>>>(tm_k, tm_v, tm_q, p);
   return cudaGetLastError();
 }
 
@@ -754,8 +911,11 @@ cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
                           cudaStream_t stream) {
   if (gc < 1 || gc > kN) return cudaErrorInvalidValue;
-  return gc <= 8 ? launch_nh<8>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                 : launch_nh<16>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  if (p.k_scale)  // FP8 cache
+    return gc <= 8 ? launch_nh<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                   : launch_nh<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  return gc <= 8 ? launch_nh<8, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_nh<16, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace pa

@@ -6,10 +6,40 @@
 // blockId * blockSize + offset.  A pure byte copy, bound by launch latency at
 // decode sizes and by HBM at prefill sizes: one warp per token moves the
 // token's Hkv*256-byte K row and V row with 16-byte accesses.
+//
+// The FP8 variant quantizes instead of copying (an "fp8_e4m3" KV cache, as in
+// the SGLang measurement quoted by the "Qwen4-Exp QSA trafia na Ascend..."
+// blog): element d of KV head h becomes the e4m3 code of x / scale[h] -- the
+// FP32 quotient rounded to nearest, ties to even, saturating at +-448 -- so a
+// token row shrinks to Hkv * 128 bytes.
+#include <cuda_fp8.h>
+
 #include "pa_launch.cuh"
 
 namespace pa {
 
+// 16 bf16 values (two 16-byte chunks) divided by s -> 16 e4m3 codes.
+__device__ __forceinline__ uint4 quantize16(uint4 a, uint4 b, float s) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t x = w[2 * i + k];
+      float2 f;
+      f.x = __fdiv_rn(__uint_as_float(x << 16), s);
+      f.y = __fdiv_rn(__uint_as_float(x & 0xffff0000u), s);
+      const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      r |= (uint32_t)q << (16 * k);
+    }
+    o[i] = r;
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
   extern __shared__ int32_t kvw_smem[];
   int32_t* off = kvw_smem;              // [B] when chunk_lens != null
@@ -48,13 +78,27 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
     const int64_t slot = (int64_t)page * kPage + pos % kPage;
     const uint4* ks = p.k_new + (int64_t)token * row_chunks;
     const uint4* vs = p.v_new + (int64_t)token * row_chunks;
-    uint4* kd = p.k_cache + slot * row_chunks;
-    uint4* vd = p.v_cache + slot * row_chunks;
-    for (int c = lane; c < row_chunks; c += 32) {
-      uint4 a = __ldg(ks + c);
-      uint4 b = __ldg(vs + c);
-      kd[c] = a;
-      vd[c] = b;
+    if constexpr (FP8) {
+      // 16 elements (32 input bytes, 16 output bytes) per step
+      uint4* kd = p.k_cache + slot * (row_chunks / 2);
+      uint4* vd = p.v_cache + slot * (row_chunks / 2);
+      for (int c = lane; c < row_chunks / 2; c += 32) {
+        const int h = c / (kHeadDim / 16);
+        const float sk = __ldg(p.k_scale + h), sv = __ldg(p.v_scale + h);
+        const uint4 k0 = __ldg(ks + 2 * c), k1 = __ldg(ks + 2 * c + 1);
+        const uint4 v0 = __ldg(vs + 2 * c), v1 = __ldg(vs + 2 * c + 1);
+        kd[c] = quantize16(k0, k1, sk);
+        vd[c] = quantize16(v0, v1, sv);
+      }
+    } else {
+      uint4* kd = p.k_cache + slot * row_chunks;
+      uint4* vd = p.v_cache + slot * row_chunks;
+      for (int c = lane; c < row_chunks; c += 32) {
+        uint4 a = __ldg(ks + c);
+        uint4 b = __ldg(vs + c);
+        kd[c] = a;
+        vd[c] = b;
+      }
     }
   }
 }
@@ -67,12 +111,20 @@ cudaError_t launch_kv_write(const KvWriteParams& p, int num_sms, cudaStream_t st
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
   size_t smem = p.chunk_lens ? (size_t)(p.B + threads) * sizeof(int32_t) : 0;
+  const bool fp8 = p.k_scale != nullptr;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kv_write_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = fp8 ? cudaFuncSetAttribute(kv_write_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem)
+                        : cudaFuncSetAttribute(kv_write_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kv_write_kernel<<<blocks, threads, smem, stream>>>(p);
+  if (fp8)
+    kv_write_kernel<true><<<blocks, threads, smem, stream>>>(p);
+  else
+    kv_write_kernel<false><<<blocks, threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,7 @@ def test_python_constants_match_header(pa):
     assert h["PA_SPLITS_BALANCED"] == pa.PA_SPLITS_BALANCED
     assert h["PA_BALANCED_MAX_SEQS"] == pa.PA_BALANCED_MAX_SEQS
     assert h["PA_MAX_Q_LEN"] == pa.PA_MAX_Q_LEN
+    assert h["PA_STATUS_Q_RANGE"] == pa.PA_STATUS_Q_RANGE
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
