@@ -299,7 +299,12 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
                                  encode_cache_map_fp8(&tm_v, v_cache, d)
                            : encode_cache_map(&tm_k, k_cache, d) &&
                                  encode_cache_map(&tm_v, v_cache, d);
-  if (!maps_ok || !encode_q_decode_map(&tm_q, q, d, q_len, G, Lg)) return PA_ERR_TENSOR_MAP;
+  // one token per sequence: q as [B * Hq rows, 128] with G-row boxes; more: a
+  // 3-D map over [tokens][Hq][128] with (G heads x Lg tokens) boxes
+  const bool q_ok = q_len == 1 ? encode_2d(&tm_q, q, kHeadDim, (uint64_t)d.num_seqs * d.num_q_heads,
+                                           kHeadDim * 2, 64, (uint32_t)G, CU_TENSOR_MAP_SWIZZLE_128B)
+                               : encode_q_decode_map(&tm_q, q, d, q_len, G, Lg);
+  if (!maps_ok || !q_ok) return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -1,5 +1,7 @@
 // pa_decode.cu -- paged GQA decode attention, flash-decoding split-K, with the
-// two contractions on the 5th-generation tensor cores.
+// two contractions on the 5th-generation tensor cores: the general kernel
+// (several new tokens per sequence, and the FP8 cache).  A bf16 cache with one
+// new token per sequence runs the same design from pa_decode_plain.cu.
 //
 // Computes, for every sequence s and query head g (KV head h = g / G):
 //   out[s][g] = softmax(scale * q[s][g] . K_t) V_t over t < context_lens[s],
@@ -177,8 +179,10 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4& lo, uint4& hi) {
 }
 
 // NH: columns the softmax and epilogue handle (8 or 16, >= any item's GC).
-// FP8: the cache holds e4m3 codes with per-KV-head scales.
-template <int NH, bool FP8>
+// FP8: the cache holds e4m3 codes with per-KV-head scales.  MULTI: more than
+// one new token per sequence (per-column causal masks, (token, head) columns);
+// without it every column is a query head that sees the whole context.
+template <int NH, bool FP8, bool MULTI>
 __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
@@ -284,7 +288,9 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     auto ctx_at = [&](int sq) -> int {
       if (sq < cbase || sq >= cbase + 32) {
         cbase = sq;
-        cval = cbase + lane < p.B ? seq_ctx(p.context_lens, cbase + lane, p.L) : 0;
+        cval = cbase + lane < p.B ? (MULTI ? seq_ctx(p.context_lens, cbase + lane, p.L)
+                                           : __ldg(p.context_lens + cbase + lane))
+                                  : 0;
       }
       return __shfl_sync(0xffffffffu, cval, sq - cbase);
     };
@@ -295,7 +301,9 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       constexpr int R = kBalMaxSeqs / 32;
       int np[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) np[r] = seq_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L);
+      for (int r = 0; r < R; ++r)
+        np[r] = MULTI ? seq_ctx(p.context_lens, min(lane * R + r, p.B - 1), p.L)
+                      : __ldg(p.context_lens + min(lane * R + r, p.B - 1));
       int lsum = 0;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         const int jsp = gi / U, u = gi - jsp * U;
         w.s = u / UPS;
         w.unit = u - w.s * UPS;
-        w.ctx = seq_ctx(p.context_lens, w.s, p.L);
+        w.ctx = MULTI ? seq_ctx(p.context_lens, w.s, p.L) : __ldg(p.context_lens + w.s);
         w.pg0 = jsp * p.pps;
         w.pg1 = max(w.pg0, min(pages_of(w.ctx, p), w.pg0 + p.pps));
         w.dest = p.S == 1 ? -1 : jsp;
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         if (FP8 || npg <= 0) {
           mbar_arrive(&B.q_full[slot]);  // FP8: the rows above are in place
           q_pending[slot] = -1;
-        } else {
+        } else if (MULTI) {
           // q as [tokens][Hq][128]: Lg tokens x the G heads of this KV head
           // (rows of a short last group past the sequence's tokens are loaded
           // too and never used)
@@ -472,6 +480,14 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           mbar_arrive_expect_tx(&B.q_full[slot], 2 * p.Lg * p.G * 128);
           tma_load_3d(qd, &tm_q, 0, qh, qt, &B.q_full[slot], pol);
           tma_load_3d(qd + kAtom, &tm_q, 64, qh, qt, &B.q_full[slot], pol);
+          q_pending[slot] = (int)((n / kSlots) & 1);
+        } else {
+          // q as [B * Hq rows][128]: the G consecutive rows of this KV head
+          const int qrow = w.s * p.Hq + w.unit * p.G;
+          uint8_t* qd = smem + kQ + slot * kOpBytes;
+          mbar_arrive_expect_tx(&B.q_full[slot], 2 * p.G * 128);
+          tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
+          tma_load_2d(qd + kAtom, &tm_q, 64, qrow, &B.q_full[slot], pol);
           q_pending[slot] = (int)((n / kSlots) & 1);
         }
       }
@@ -673,14 +689,20 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
       if (npg <= 0) continue;
-      const int GC = unit_columns(p, unit);
+      const int GC = MULTI ? unit_columns(p, unit) : p.G;
       if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
-      // column g (token t0 + g / G) sees key positions below lim[g]
+      // MULTI: column g (token t0 + g / G) sees key positions below lim[g]
       int lim[NH];
-      {
-        const int t0 = (unit % p.NT) * p.Lg;
+      if constexpr (MULTI) {
+        int t = (unit % p.NT) * p.Lg, hg = 0;
 #pragma unroll
-        for (int g = 0; g < NH; ++g) lim[g] = g < GC ? ctx - (p.L - 1 - (t0 + g / p.G)) : 0;
+        for (int g = 0; g < NH; ++g) {
+          lim[g] = g < GC ? ctx - (p.L - 1 - t) : 0;
+          if (++hg == p.G) {
+            hg = 0;
+            ++t;
+          }
+        }
       }
       const int ob = nb & 1;
       float m[NH], ls[NH];
@@ -693,6 +715,13 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
         const bool kv = key < nvalid;  // within the sequence's context
         const int kpos = (pg0 + j) * kPage + key;
+        // MULTI: visible columns of this key, bit g
+        uint32_t vis = 0;
+        if constexpr (MULTI) {
+#pragma unroll
+          for (int g = 0; g < NH; ++g) vis |= (kpos < lim[g] ? 1u : 0u) << g;
+        }
+        auto visible = [&](int g) -> bool { return MULTI ? ((vis >> g) & 1u) != 0 : kv; };
         if (!(ok = mbar_wait_warp(B.s_full, gp & 1, p.status))) break;
         tc_fence_after();
         uint32_t sr[16];
@@ -705,7 +734,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
 #pragma unroll
           for (int g = 0; g < NH; ++g) {
             d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
-            if (g < GC) v |= kpos < lim[g] && d[g] > kRescaleThreshold;
+            if (g < GC) v |= visible(g) && d[g] > kRescaleThreshold;
           }
           float vote[NH];
           vote[0] = __any_sync(0xffffffffu, v) ? 1.f : 0.f;
@@ -718,8 +747,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           float wm[NH];
 #pragma unroll
           for (int g = 0; g < NH; ++g)
-            wm[g] = g < GC ? warp_max(kpos < lim[g] ? __uint_as_float(sr[g]) * c : -INFINITY)
-                           : 0.f;
+            wm[g] = g < GC ? warp_max(visible(g) ? __uint_as_float(sr[g]) * c : -INFINITY) : 0.f;
           const float* x = exchange(wm, GC);
           if (!(ok = x != nullptr)) break;
           float alpha[NH];
@@ -731,7 +759,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
               // -inf while the column has seen no visible key (a split that
               // starts past its token's position): nothing to rescale yet
               const float mn = fmaxf(m[g], M);
-              if (j > 0 && mn != -INFINITY) alpha[g] = fast_exp2(m[g] - mn);
+              if (j > 0 && (!MULTI || mn != -INFINITY)) alpha[g] = fast_exp2(m[g] - mn);
               m[g] = mn;
               ls[g] *= alpha[g];
             }
@@ -756,7 +784,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
           if (g < GC) {
-            const float pv = kpos < lim[g] ? fast_exp2(d[g]) : 0.f;
+            const float pv = visible(g) ? fast_exp2(d[g]) : 0.f;
             uint16_t pbf;
             if constexpr (FP8) {
               const __half ph = __float2half_rn(pv);  // the F16 operand
@@ -827,7 +855,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       const int sq = rec[kISeq], unit = rec[kIUnit], dest = rec[kIDest];
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
-      const int GC = unit_columns(p, unit);
+      const int GC = MULTI ? unit_columns(p, unit) : p.G;
       const float vsc = FP8 ? __ldg(p.v_scale + unit / p.NT) : 1.f;  // FP8: V scale
       // output row of column g: token t0 + g / G, query head h G + g % G
       const int64_t tok0 = (int64_t)sq * p.L + (unit % p.NT) * p.Lg;
@@ -862,10 +890,22 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         mbar_arrive(&B.o_free[ob]);
         ++nb;
       }
+      const int64_t row0 = tok0 * p.Hq + head0;
+      int64_t row = row0;  // MULTI: column g's row, advanced below
+      int hg = 0;
 #pragma unroll
       for (int g = 0; g < NH; ++g) {
+        if constexpr (MULTI) {
+          if (g > 0 && ++hg == p.G) {
+            hg = 0;
+            row += p.Hq - (p.G - 1);  // next token, first head of the group
+          } else if (g > 0) {
+            ++row;
+          }
+        } else {
+          row = row0 + g;  // one token: consecutive heads
+        }
         if (g < GC) {
-          const int64_t row = (tok0 + g / p.G) * p.Hq + head0 + g % p.G;
           if (dest < 0) {
             if (p.out_f32)
               reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[g];
@@ -892,17 +932,25 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   }
 }
 
-template <int NH, bool FP8>
+template <int NH, bool FP8, bool MULTI>
 cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                       const DecodeParams& p, int num_sms, cudaStream_t stream) {
   constexpr int smem = Layout<FP8, NH>::kSmem, threads = Layout<FP8, NH>::kThreads;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH, FP8>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH, FP8, MULTI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
   if (grid < 1) return cudaSuccess;
-  decode_kernel<NH, FP8><<<grid, threads, smem, stream>>>(tm_k, tm_v, tm_q, p);
+  decode_kernel<NH, FP8, MULTI><<<grid, threads, smem, stream>>>(tm_k, tm_v, tm_q, p);
   return cudaGetLastError();
+}
+
+template <int NH, bool FP8>
+cudaError_t launch_multi(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         const CUtensorMap& tm_q, const DecodeParams& p, int num_sms,
+                         cudaStream_t stream) {
+  return p.L > 1 ? launch_nh<NH, FP8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_nh<NH, FP8, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace
@@ -912,10 +960,12 @@ cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           cudaStream_t stream) {
   if (gc < 1 || gc > kN) return cudaErrorInvalidValue;
   if (p.k_scale)  // FP8 cache
-    return gc <= 8 ? launch_nh<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                   : launch_nh<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
-  return gc <= 8 ? launch_nh<8, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                 : launch_nh<16, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
+    return gc <= 8 ? launch_multi<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                   : launch_multi<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  // bf16 cache, one new token per sequence: the kernel of pa_decode_plain.cu
+  if (p.L == 1) return launch_decode_plain(tm_k, tm_v, tm_q, p, gc, num_sms, stream);
+  return gc <= 8 ? launch_nh<8, false, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_nh<16, false, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace pa

@@ -1,0 +1,740 @@
+// pa_decode_plain.cu -- paged GQA decode attention, flash-decoding split-K,
+// with the two contractions on the 5th-generation tensor cores: the kernel for
+// a bf16 cache and one new token per sequence (pa_decode), kept apart from the
+// general kernel in pa_decode.cu (multi-token and FP8-cache decode) so that its
+// instruction schedule is exactly the one measured on the single-token
+// workloads.
+//
+// Computes, for every sequence s and query head g (KV head h = g / G):
+//   out[s][g] = softmax(scale * q[s][g] . K_t) V_t over t < context_lens[s],
+// with K_t / V_t gathered through the block table ("Qwen3-14B" pypto-lib doc,
+// "decode_fwd": paged attention after the KV cache write, vLLM ABI with flat
+// [page, token, kv_head, dim] K/V; "Qwen 3" TensorSharp doc, section 11: K/V
+// gathered per sequence from the block tables and sequence lengths).
+//
+// Design (GB300; HBM bound: every K/V byte is read once):
+//  * Persistent grid, one CTA per SM.  A work item is (split j, sequence s,
+//    KV head h, head group): a contiguous range of at most `pps` pages and the
+//    GC <= 16 query heads that share the KV head.  Items are dealt
+//    round-robin; split boundaries depend only on logical positions.
+//  * Per page the two products are transposed so that the 128 keys (or the
+//    128 head dims) fill the 128 rows of one tcgen05.mma and the query heads,
+//    padded to 16, are its N:
+//      S^T[key][g] = K[key][:] . Q[g][:]        (A = K tile, K-major)
+//      O^T[d][g]  += V[:][d] . P[g][:]          (A = V tile, MN-major)
+//    so the K/V tiles are read by the tensor core straight from the TMA ring
+//    (128-byte swizzle), and the FP32 pipes only run the softmax.
+//  * warp 0: validates each item's block-table range (the next item's
+//    metadata is loaded while the current item's pages are issued), stages
+//    up to four items ahead, TMA-loads each item's query heads (rows >= GC
+//    stay zero) and its K/V page tiles into a 3-stage ring of 64 KB (K and V
+//    complete on separate mbarriers, so QK^T starts while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
+//    in page order: QK^T(j), then P.V(j) once P(j) is in shared memory.
+//  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
+//    softmax in the log2 domain with a per-head reference max shared by the
+//    CTA.  The reference only moves when some score exceeds it by more than
+//    2^8 (one bar.red.or per page decides), which rescales O in TMEM; the
+//    first page of an item takes the exact max.  The warps agree through a
+//    small shared-memory exchange on mbarriers (bounded waits, no bar.sync).  P is rounded to BF16 and
+//    written transposed into a K-major operand; the row sums accumulate the
+//    rounded values, so the normalisation matches the weights the MMA used.
+//    V rows past the context in the last page are zeroed before P.V reads
+//    them (P is 0 there, but 0 * NaN is NaN).
+//  * warps 6-9, one thread per head dim: the epilogue of the previous item
+//    (O / l from TMEM, double-buffered) overlaps the next item's pages; it
+//    writes `out` (one split) or normalised partials (o, lse) for the combine.
+// With one new token per sequence a work unit is a KV head (p.NT == 1: the
+// "% p.NT" terms below are 0 and the "/ p.NT" terms the unit itself).
+#include "pa_launch.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTmaWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
+constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
+constexpr int kThreads = 10 * 32;
+constexpr int kStages = 3;
+constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
+constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
+constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
+constexpr int kStageBytes = 4 * kBox;      // K lo, K hi, V lo, V hi of a page
+constexpr int kN = 16;                     // MMA N: query heads of an item, padded
+constexpr int kAtom = kN * 128;            // 16 rows x 128 bytes
+constexpr int kOpBytes = 2 * kAtom;        // Q or P operand: two 64-element atoms
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// shared memory (offsets from a 1024-aligned base)
+constexpr int kRing = 0;
+constexpr int kQ = kRing + kStages * kStageBytes;  // [kSlots] query operands
+constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
+constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax-warp exchange
+constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O buffer
+constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][kInfoInts]: item records
+constexpr int kBars = kInfo + kSlots * 8 * 4;
+constexpr int kNumBars = 3 * kStages + 2 * kSlots + 2 + 4 * 2 + 1;
+constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
+constexpr int kSmemLimit = 232448;
+static_assert(kSmem <= kSmemLimit, "decode shared memory exceeds the per-CTA limit");
+
+// TMEM columns
+constexpr uint32_t kColS = 0;   // S^T: 16 columns
+constexpr uint32_t kColO = 16;  // O^T[2]: 16 columns each
+constexpr uint32_t kTmemCols = 64;
+
+struct Bars {
+  uint64_t* k_full;    // [kStages]
+  uint64_t* v_full;    // [kStages]
+  uint64_t* kv_empty;  // [kStages]
+  uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
+  uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
+  uint64_t* s_full;    // S^T of the current page
+  uint64_t* p_full;    // P of the current page
+  uint64_t* o_full;    // [2] last P.V of the item done
+  uint64_t* o_free;    // [2] epilogue read O and (m, l)
+  uint64_t* ml_full;   // [2] (m, l) of the item published
+  uint64_t* x_full;    // [2] softmax-warp exchange slots (one arrival per warp)
+  uint64_t* mma_done;  // drain at exit
+};
+
+// Item record in shared memory, written by the TMA warp, read by every role.
+enum : int {
+  kICtx = 0,   // context length of the sequence
+  kIPg0 = 1,   // first page of the item
+  kIPg1 = 2,   // end page (== kIPg0 when the item has no pages to read)
+  kIFlag = 3,  // 0 ok, 1 invalid block-table entry, 2 invalid context length
+  kISeq = 4,   // sequence
+  kIUnit = 5,  // KV head * NG + head group
+  kIDest = 6,  // -1: out; else the partial record (split index, or 2 * CTA + cut side)
+  kIDone = 7,  // no more items
+  kInfoInts = 8
+};
+
+// A work item: pages [pg0, pg1) of unit (s, unit) whose result goes to `dest`.
+struct Work {
+  int s, unit, ctx, pg0, pg1, dest;
+};
+
+__device__ __forceinline__ bool ctx_ok(int ctx, const DecodeParams& p) {
+  return ctx >= 0 && ctx <= p.max_pages * kPage;
+}
+
+__device__ __forceinline__ int pages_of(int ctx, const DecodeParams& p) {
+  return ctx_ok(ctx, p) ? (ctx + kPage - 1) / kPage : 0;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// NH: query-head columns the softmax and epilogue handle (8 or 16, >= GC).
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBars);
+  Bars B;
+  B.k_full = bar;
+  B.v_full = B.k_full + kStages;
+  B.kv_empty = B.v_full + kStages;
+  B.q_full = B.kv_empty + kStages;
+  B.q_empty = B.q_full + kSlots;
+  B.s_full = B.q_empty + kSlots;
+  B.p_full = B.s_full + 1;
+  B.o_full = B.p_full + 1;
+  B.o_free = B.o_full + 2;
+  B.ml_full = B.o_free + 2;
+  B.x_full = B.ml_full + 2;
+  B.mma_done = B.x_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
+  int* info = reinterpret_cast<int*>(smem + kInfo);
+  const int GC = p.G / p.NT;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&B.k_full[i], 1);
+      mbar_init(&B.v_full[i], 1);
+      mbar_init(&B.kv_empty[i], 1);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_empty[i], 1 + 4 + 4);  // MMA, 4 softmax warps, 4 epilogue warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.o_full[i], 1);
+      mbar_init(&B.o_free[i], 128);
+      mbar_init(&B.ml_full[i], 1);
+      mbar_init(&B.x_full[i], 4);
+    }
+    mbar_init(B.s_full, 1);
+    mbar_init(B.p_full, 128);
+    mbar_init(B.mma_done, 1);
+    fence_mbar_init();
+  }
+  // query rows >= GC and unused P rows must read as zero: clear the operands
+  for (int o = threadIdx.x * 16; o < (kSlots + 1) * kOpBytes; o += kThreads * 16)
+    sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // a combine launched as a programmatic dependent may start its prologue now;
+  // it reads partials only after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+      prefetch_tensor_map(&tm_q);
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    // ---- work generator (warp-uniform state).  Fixed splits: items
+    // i = blockIdx.x + k * gridDim.x of (split, sequence, unit).  Page-balanced:
+    // the CTAs form groups of UPS (one CTA per unit = KV head x head group);
+    // the sequences' pages laid end to end (n_s pages for sequence s, W in
+    // total) are divided evenly among the groups, and the CTA with unit j of a
+    // group takes unit j of every sequence in the group's range [lo, hi) --
+    // so the CTAs of a group read the same pages at about the same time.  A
+    // sequence cut by lo or hi leaves partial records for the balanced
+    // combine; an empty sequence (or one with an invalid length) belongs to
+    // the group whose range holds its position (the last group for W).
+    const int UPS = p.Hkv * p.NT;  // units per sequence
+    int gi = blockIdx.x;           // fixed: next item index
+    int bs = p.B, bn = 0, bctx = 0;  // balanced: sequence, its pages, its context length
+    int64_t bP = 0, lo = 0, hi = 0, W = 0;
+    const int ngroups = gridDim.x / UPS, grp = blockIdx.x / UPS, unit_j = blockIdx.x % UPS;
+    int cbase = -64, cval = 0;     // 32 context lengths starting at cbase (lane's in cval)
+    const bool last_grp = grp == ngroups - 1;
+    auto ctx_at = [&](int sq) -> int {
+      if (sq < cbase || sq >= cbase + 32) {
+        cbase = sq;
+        cval = cbase + lane < p.B ? __ldg(p.context_lens + cbase + lane) : 0;
+      }
+      return __shfl_sync(0xffffffffu, cval, sq - cbase);
+    };
+    if (p.balanced && grp < ngroups) {
+      // lane l holds the page counts of sequences 16l .. 16l+15 (B <= 512;
+      // the host guarantees W < 2^31).  Loads of a clamped index are
+      // unconditional, so they issue together.
+      constexpr int R = kBalMaxSeqs / 32;
+      int np[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) np[r] = __ldg(p.context_lens + min(lane * R + r, p.B - 1));
+      int lsum = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        np[r] = lane * R + r < p.B ? pages_of(np[r], p) : 0;
+        lsum += np[r];
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      W = __shfl_sync(0xffffffffu, incl, 31);
+      lo = W * grp / ngroups;
+      hi = W * (grp + 1) / ngroups;
+      // first sequence the group touches: it reaches past lo, or it is empty
+      // and sits at or after lo
+      int start = incl - lsum, hit_r = -1, hit_start = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const bool hit = lane * R + r < p.B &&
+                         (start + np[r] > lo || (np[r] == 0 && start >= lo));
+        if (hit && hit_r < 0) {
+          hit_r = r;
+          hit_start = start;
+        }
+        start += np[r];
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, hit_r >= 0);
+      if (m) {
+        const int f = __ffs(m) - 1;
+        bs = f * R + __shfl_sync(0xffffffffu, hit_r, f);
+        bP = __shfl_sync(0xffffffffu, hit_start, f);
+        bctx = ctx_at(bs);
+        bn = pages_of(bctx, p);
+      }
+    }
+    auto gen_next = [&](Work& w) -> bool {
+      if (!p.balanced) {
+        if (gi >= p.num_items) return false;
+        const int U = p.B * UPS;
+        const int jsp = gi / U, u = gi - jsp * U;
+        w.s = u / UPS;
+        w.unit = u - w.s * UPS;
+        w.ctx = __ldg(p.context_lens + w.s);
+        w.pg0 = jsp * p.pps;
+        w.pg1 = max(w.pg0, min(pages_of(w.ctx, p), w.pg0 + p.pps));
+        w.dest = p.S == 1 ? -1 : jsp;
+        gi += gridDim.x;
+        return true;
+      }
+      if (grp >= ngroups || bs >= p.B) return false;
+      if (bn == 0) {
+        if (bP >= hi && !(last_grp && bP == W)) {
+          bs = p.B;
+          return false;
+        }
+        w.pg0 = 0;
+        w.pg1 = 0;
+        w.dest = -1;
+      } else {
+        if (bP >= hi || lo >= hi) {  // past the range, or an empty range
+          bs = p.B;
+          return false;
+        }
+        const int64_t a = max(bP, lo), b = min(bP + bn, hi);
+        w.pg0 = (int)(a - bP);
+        w.pg1 = (int)(b - bP);
+        w.dest = (a == bP && b == bP + bn) ? -1 : 2 * (int)blockIdx.x + (bP <= lo ? 0 : 1);
+      }
+      w.s = bs;
+      w.unit = unit_j;
+      w.ctx = bctx;
+      bP += bn;
+      ++bs;
+      if (bs < p.B) {
+        bctx = ctx_at(bs);
+        bn = pages_of(bctx, p);
+      }
+      return true;
+    };
+    // this lane's block-table entry among the first 32 pages of an item
+    // (it does not wait for the context length: entries past the sequence's
+    // pages are in the row and are never used)
+    auto first_pid = [&](const Work& w) -> int {
+      const int pg = w.pg0 + lane;
+      return pg < p.max_pages ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
+    };
+    Work nx;
+    bool have = gen_next(nx);
+    int nx_pid = have ? first_pid(nx) : 0;
+    uint32_t gp = 0, n = 0;
+    // per item slot: parity of its last use if that use loaded a query operand, else -1
+    int q_pending[kSlots];
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) q_pending[k] = -1;
+    bool ok = true;
+    for (; ok; ++n) {
+      const Work w = nx;
+      const int pid0 = nx_pid;
+      const bool item = have;
+      int flag = 0, npg = 0;
+      if (item) {
+        // validate every page of the item; the next item's metadata loads
+        // while this one's pages are issued
+        const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
+        bool bad = w.pg0 + lane < w.pg1 && (pid0 < 0 || pid0 >= p.num_pages);
+        for (int pg = w.pg0 + 32 + lane; pg < w.pg1; pg += 32) {
+          const int pid = __ldg(bt + pg);
+          bad |= pid < 0 || pid >= p.num_pages;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        flag = !ctx_ok(w.ctx, p) ? 2 : (bad ? 1 : 0);
+        npg = flag ? 0 : w.pg1 - w.pg0;
+        have = gen_next(nx);
+        if (have) nx_pid = first_pid(nx);
+      }
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
+      if (lane == 0) {
+        int* rec = info + kInfoInts * slot;
+        rec[kICtx] = w.ctx;
+        rec[kIPg0] = w.pg0;
+        rec[kIPg1] = w.pg0 + npg;
+        rec[kIFlag] = flag;
+        rec[kISeq] = w.s;
+        rec[kIUnit] = w.unit;
+        rec[kIDest] = w.dest;
+        rec[kIDone] = item ? 0 : 1;
+        if (npg > 0) {
+          const int qrow = w.s * p.Hq + (w.unit / p.NT) * p.G + (w.unit % p.NT) * GC;
+          uint8_t* qd = smem + kQ + slot * kOpBytes;
+          mbar_arrive_expect_tx(&B.q_full[slot], 2 * GC * 128);
+          tma_load_2d(qd, &tm_q, 0, qrow, &B.q_full[slot], pol);
+          tma_load_2d(qd + kAtom, &tm_q, 64, qrow, &B.q_full[slot], pol);
+          q_pending[slot] = (int)((n / kSlots) & 1);
+        } else {
+          mbar_arrive(&B.q_full[slot]);
+          q_pending[slot] = -1;
+        }
+      }
+      if (!item) break;
+      const int x = (w.unit / p.NT) * kHeadDim;
+      const int32_t* bt = p.block_table + (int64_t)w.s * p.max_pages;
+      for (int c = 0; ok && c < npg; c += 32) {
+        const int pid_l = c == 0 ? pid0 : (c + lane < npg ? __ldg(bt + w.pg0 + c + lane) : 0);
+        const int cnt = min(32, npg - c);
+        for (int k = 0; k < cnt; ++k) {
+          const int page = __shfl_sync(0xffffffffu, pid_l, k);
+          int lok = 1;
+          if (lane == 0) {
+            const int st = gp % kStages;
+            lok = mbar_wait(&B.kv_empty[st], ((gp / kStages) & 1) ^ 1, p.status);
+            if (lok) {
+              uint8_t* dst = smem + kRing + st * kStageBytes;
+              const int y = page * kPage;
+              mbar_arrive_expect_tx(&B.k_full[st], 2 * kBox);
+              tma_load_2d(dst, &tm_k, x, y, &B.k_full[st], pol);
+              tma_load_2d(dst + kBox, &tm_k, x + 64, y, &B.k_full[st], pol);
+              mbar_arrive_expect_tx(&B.v_full[st], 2 * kBox);
+              tma_load_2d(dst + 2 * kBox, &tm_v, x, y, &B.v_full[st], pol);
+              tma_load_2d(dst + 3 * kBox, &tm_v, x + 64, y, &B.v_full[st], pol);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, lok, 0) != 0;
+          if (!ok) break;
+          ++gp;
+        }
+      }
+    }
+    // drain: copies still in flight (only after a timeout elsewhere) must land
+    // before the CTA exits
+    if (lane == 0) {
+      for (uint32_t g = gp > kStages ? gp - kStages : 0; g < gp; ++g) {
+        mbar_wait(&B.k_full[g % kStages], (g / kStages) & 1, nullptr);
+        mbar_wait(&B.v_full[g % kStages], (g / kStages) & 1, nullptr);
+      }
+      for (int k = 0; k < kSlots; ++k)
+        if (q_pending[k] >= 0) mbar_wait(&B.q_full[k], (uint32_t)q_pending[k], nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = umma_idesc_bf16(128, kN, false, false);
+      const uint32_t idesc_pv = umma_idesc_bf16(128, kN, true, false);
+      uint32_t gp = 0, nb = 0;
+      bool ok = true;
+      for (uint32_t n = 0; ok; ++n) {
+        const int slot = n % kSlots;
+        if (!(ok = mbar_wait(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
+        const int* rec = info + kInfoInts * slot;
+        if (rec[kIDone]) break;
+        const int npg = rec[kIPg1] - rec[kIPg0];
+        if (npg <= 0) {
+          mbar_arrive(&B.q_empty[slot]);
+          continue;
+        }
+        const int ob = nb & 1;
+        const uint32_t q_addr = smem_u32(smem + kQ + slot * kOpBytes);
+        for (int j = 0; j < npg; ++j, ++gp) {
+          const int st = gp % kStages;
+          const uint32_t ph = (gp / kStages) & 1;
+          if (!(ok = mbar_wait(&B.k_full[st], ph, p.status))) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(B.s_full);
+          if (j == npg - 1) umma_commit(&B.q_empty[slot]);
+          if (!(ok = mbar_wait(B.p_full, gp & 1, p.status))) break;
+          if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
+          if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
+          tc_fence_after();
+          const uint32_t v_addr = k_addr + 2 * kBox;
+          const uint32_t p_addr = smem_u32(smem + kP);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
+            const uint64_t bd = umma_sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&B.kv_empty[st]);
+        }
+        if (!ok) break;
+        umma_commit(&B.o_full[ob]);
+        ++nb;
+      }
+      // every MMA this thread issued completes before TMEM is released
+      umma_commit(B.mma_done);
+      mbar_wait(B.mma_done, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ softmax, thread = key
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int key = quarter * 32 + lane;
+    const int wi = warp - kSoftWarp0;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float* xbuf = reinterpret_cast<float*>(smem + kX);
+    float* ml = reinterpret_cast<float*>(smem + kML);
+    const float c = p.scale_log2;
+    // P^T operand, K-major over keys: row g (head), 64-key atoms, 128-byte swizzle
+    const int kc = (key & 63) >> 3;
+    const uint32_t p_key = (uint32_t)((key >> 6) * kAtom + (key & 7) * 2);
+    // Exchange among the four softmax warps: lane 0 of each warp publishes up
+    // to 16 floats in slot (ex & 1) and arrives; every warp then waits (bounded)
+    // and reads all four rows.  A slot is rewritten two exchanges later, after
+    // every warp has arrived at the exchange in between (so has read it).
+    uint32_t ex = 0;
+    auto exchange = [&](const float (&v)[NH], int nv) -> const float* {
+      float* slot = xbuf + (ex & 1) * 4 * kN;
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < NH; ++k)
+          if (k < nv) slot[wi * kN + k] = v[k];
+        mbar_arrive(&B.x_full[ex & 1]);
+      }
+      const bool r = mbar_wait_warp(&B.x_full[ex & 1], (ex >> 1) & 1, p.status);
+      ++ex;
+      return r ? slot : nullptr;
+    };
+    uint32_t gp = 0, nb = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
+      const int* rec = info + kInfoInts * slot;
+      if (rec[kIDone]) break;
+      const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+      const int npg = pg1 - pg0;
+      if (npg <= 0) continue;
+      const int ob = nb & 1;
+      float m[NH], ls[NH];
+#pragma unroll
+      for (int g = 0; g < NH; ++g) {
+        m[g] = -INFINITY;
+        ls[g] = 0.f;
+      }
+      for (int j = 0; j < npg; ++j, ++gp) {
+        const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
+        const bool kv = key < nvalid;
+        if (!(ok = mbar_wait_warp(B.s_full, gp & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t sr[16];
+        tmem_ld16(tmem + lane_base + kColS, sr);
+        tmem_wait_ld();
+        float d[NH];
+        bool need = j == 0;
+        if (!need) {
+          bool v = false;
+#pragma unroll
+          for (int g = 0; g < NH; ++g) {
+            d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
+            if (g < GC) v |= kv && d[g] > kRescaleThreshold;
+          }
+          float vote[NH];
+          vote[0] = __any_sync(0xffffffffu, v) ? 1.f : 0.f;
+          const float* x = exchange(vote, 1);
+          if (!(ok = x != nullptr)) break;
+          need = (x[0] + x[kN]) + (x[2 * kN] + x[3 * kN]) > 0.f;  // uniform over the 4 warps
+        }
+        if (need) {
+          // exact per-head max of this page; the reference becomes max(m, it)
+          float wm[NH];
+#pragma unroll
+          for (int g = 0; g < NH; ++g)
+            wm[g] = g < GC ? warp_max(kv ? __uint_as_float(sr[g]) * c : -INFINITY) : 0.f;
+          const float* x = exchange(wm, GC);
+          if (!(ok = x != nullptr)) break;
+          float alpha[NH];
+#pragma unroll
+          for (int g = 0; g < NH; ++g) {
+            alpha[g] = 1.f;
+            if (g < GC) {
+              const float M = fmaxf(fmaxf(x[g], x[kN + g]), fmaxf(x[2 * kN + g], x[3 * kN + g]));
+              const float mn = fmaxf(m[g], M);  // finite: the page has a visible key
+              if (j > 0) alpha[g] = fast_exp2(m[g] - mn);
+              m[g] = mn;
+              ls[g] *= alpha[g];
+            }
+            d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
+          }
+          if (j > 0) {
+            // O^T holds P.V of the item's earlier pages: the commit that
+            // published S of this page came after the previous P.V finished
+            uint32_t orow[16];
+            const uint32_t o_cols = tmem + lane_base + kColO + ob * kN;
+            tmem_ld16(o_cols, orow);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < NH; ++g)
+              orow[g] = __float_as_uint(__uint_as_float(orow[g]) * alpha[g]);
+            tmem_st16(o_cols, orow);
+          }
+        }
+        // P(j) into the operand: P.V(j - 1) has finished reading it (it completed
+        // before the commit that published S of this page)
+        const uint32_t pbase = smem_u32(smem + kP) + p_key;
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          if (g < GC) {
+            const float pv = kv ? fast_exp2(d[g]) : 0.f;
+            const uint16_t pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+            ls[g] += __uint_as_float((uint32_t)pbf << 16);
+            sts16(pbase + (g >> 3) * 1024 + (g & 7) * 128 + ((kc ^ (g & 7)) << 4), pbf);
+          }
+        }
+        if (nvalid < kPage) {
+          // the sequence's last page: zero the V rows past the context
+          const int st = gp % kStages;
+          if (!(ok = mbar_wait_warp(&B.v_full[st], (gp / kStages) & 1, p.status))) break;
+          if (!kv) {
+            const uint32_t vr = smem_u32(smem + kRing + st * kStageBytes + 2 * kBox) + key * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              sts128(vr + ch * 16, 0u, 0u, 0u, 0u);
+              sts128(vr + kBox + ch * 16, 0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        if (need && j > 0) tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(B.p_full);
+      }
+      if (!ok) break;
+      // item end: row sums over the 128 keys, published with the max
+      float wl[NH];
+#pragma unroll
+      for (int g = 0; g < NH; ++g) wl[g] = g < GC ? warp_sum(ls[g]) : 0.f;
+      const float* x = exchange(wl, GC);
+      if (!(ok = x != nullptr)) break;
+      if (wi == 0) {
+        if (!(ok = mbar_wait_warp(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
+        if (lane < GC) {
+          float mm = 0.f;
+#pragma unroll
+          for (int g = 0; g < NH; ++g)
+            if (lane == g) mm = m[g];
+          ml[(ob * kN + lane) * 2] = mm;
+          ml[(ob * kN + lane) * 2 + 1] =
+              (x[lane] + x[kN + lane]) + (x[2 * kN + lane] + x[3 * kN + lane]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.ml_full[ob]);
+      }
+      ++nb;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue, thread = head dim
+    const int quarter = warp & 3;
+    const int dim = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float* ml = reinterpret_cast<const float*>(smem + kML);
+    uint32_t nb = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
+      const int* rec = info + kInfoInts * slot;
+      if (rec[kIDone]) break;
+      const int pg0 = rec[kIPg0], pg1 = rec[kIPg1], flag = rec[kIFlag];
+      const int sq = rec[kISeq], unit = rec[kIUnit], dest = rec[kIDest];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+      const int64_t row0 = (int64_t)sq * p.Hq + (unit / p.NT) * p.G + (unit % p.NT) * GC;
+      float res[NH], lse[NH];
+      if (pg1 - pg0 <= 0) {
+        // nothing visible (lse -inf), or an invalid sequence (lse +inf: the
+        // combine zeroes the row)
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          res[g] = 0.f;
+          lse[g] = flag ? INFINITY : -INFINITY;
+        }
+        if (flag && warp == kEpiWarp0 && lane == 0 && p.status)
+          atomicOr(p.status, flag == 1 ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
+      } else {
+        const int ob = nb & 1;
+        if (!(ok = mbar_wait_warp(&B.ml_full[ob], (nb >> 1) & 1, p.status))) break;
+        if (!(ok = mbar_wait_warp(&B.o_full[ob], (nb >> 1) & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t orow[16];
+        tmem_ld16(tmem + lane_base + kColO + ob * kN, orow);
+        tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < NH; ++g) {
+          const float mm = ml[(ob * kN + g) * 2], L = ml[(ob * kN + g) * 2 + 1];
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          res[g] = __uint_as_float(orow[g]) * inv;
+          lse[g] = L > 0.f ? (mm + __log2f(L)) * kLn2 : -INFINITY;
+        }
+        tc_fence_before();
+        mbar_arrive(&B.o_free[ob]);
+        ++nb;
+      }
+#pragma unroll
+      for (int g = 0; g < NH; ++g) {
+        if (g < GC) {
+          const int64_t row = row0 + g;
+          if (dest < 0) {
+            if (p.out_f32)
+              reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[g];
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.out)[row * kHeadDim + dim] =
+                  __float2bfloat16_rn(res[g]);
+          } else if (p.balanced) {
+            p.bal_o[((int64_t)dest * kN + g) * kHeadDim + dim] = res[g];
+            if (dim == 0) p.bal_lse[dest * kN + g] = lse[g];
+          } else {
+            p.part_o[(row * p.S + dest) * kHeadDim + dim] = res[g];
+            if (dim == 0) p.part_lse[row * p.S + dest] = lse[g];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int NH>
+cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
+                      const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
+  if (grid < 1) return cudaSuccess;
+  decode_kernel<NH><<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_plain(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_q, const DecodeParams& p, int gc,
+                                int num_sms, cudaStream_t stream) {
+  if (gc < 1 || gc > kN) return cudaErrorInvalidValue;
+  return gc <= 8 ? launch_nh<8>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_nh<16>(tm_k, tm_v, tm_q, p, num_sms, stream);
+}
+
+}  // namespace pa

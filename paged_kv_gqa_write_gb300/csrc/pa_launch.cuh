@@ -29,13 +29,19 @@ cudaError_t launch_kv_write(const KvWriteParams& p, int num_sms, cudaStream_t st
 cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t stream);
 
 // Decode: persistent flash-decoding kernel over (split, sequence, kv head,
-// head group) items.  tm_k / tm_v are 2-D tensor maps over the caches viewed
+// token group) items.  tm_k / tm_v are 2-D tensor maps over the caches viewed
 // as [num_pages * 128 rows, Hkv * 128 columns] bf16 with 128-byte swizzle and
 // a 64 x 128 box; tm_q is a 2-D map over q viewed as [B * Hq rows, 128
 // columns] with a 64 x gc box (gc = query heads per item, <= 16).
+// With p.k_scale set the caches are e4m3 (uint8 maps, 128 x 128 boxes); with
+// p.L > 1, tm_q is a 3-D map over [tokens][Hq][128] with a 64 x G x Lg box.
 cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
                           cudaStream_t stream);
+// The bf16, one-token-per-sequence kernel launch_decode dispatches to.
+cudaError_t launch_decode_plain(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_q, const DecodeParams& p, int gc,
+                                int num_sms, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
