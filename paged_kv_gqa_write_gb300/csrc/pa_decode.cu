@@ -59,7 +59,6 @@ constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert, one thread per
 constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
 constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
-constexpr int kStageBytes = 4 * kBox;      // K lo, K hi, V lo, V hi of a page
 constexpr int kN = 16;                     // MMA N: query heads of an item, padded
 constexpr int kAtom = kN * 128;            // 16 rows x 128 bytes
 constexpr int kOpBytes = 2 * kAtom;        // Q or P operand: two 64-element atoms
@@ -67,28 +66,33 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Shared memory (offsets from a 1024-aligned base).  BF16 cache: a 3-stage
-// ring of K/V operand pages loaded by TMA.  FP8 cache: a 2-stage ring of e4m3
-// pages (32 KB each) loaded by TMA, converted by warps 10-13 into a 2-stage
-// ring of F16 operand pages (the tensor core reads F16; every e4m3 value is
-// exact in it).
+// ring of K/V operand pages loaded by TMA.  FP8 cache: a 4-stage ring of e4m3
+// pages (32 KB each) loaded by TMA; the converter warps rewrite each page's K
+// as F16 into one of two tensor-memory buffers (QK^T takes A from TMEM) and
+// its V as F16 into a 2-stage shared-memory ring (the tensor core reads F16;
+// every e4m3 value is exact in it).
 constexpr int kBox8 = 128 * kPage;         // 128 one-byte dims x 128 tokens = 16 KB
 template <bool FP8, int NH = 16>
 struct Layout {
-  static constexpr int kStages = FP8 ? 2 : 3;   // operand pages (K lo, K hi, V lo, V hi)
-  static constexpr int kStages8 = FP8 ? 2 : 0;  // e4m3 pages (K, V)
+  // operand stages: bf16 K lo, K hi, V lo, V hi; FP8 V lo, V hi (K is in TMEM)
+  static constexpr int kStages = FP8 ? 2 : 3;
+  static constexpr int kStageBytes = FP8 ? 2 * kBox : 4 * kBox;
+  static constexpr int kStages8 = FP8 ? 4 : 0;  // e4m3 pages (K, V)
   // converter warps: 8 (K and V converted side by side) where the registers
   // allow it (the 8-column softmax), else 4 (K, then V)
   static constexpr int kConvWarps = FP8 ? (NH == 8 ? 8 : 4) : 0;
   static constexpr int kThreads = (10 + kConvWarps) * 32;
   static constexpr int kRing = 0;
   static constexpr int kRing8 = kRing + kStages * kStageBytes;
+  static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;  // FP8: + two 64-column K buffers
   static constexpr int kQ = kRing8 + kStages8 * 2 * kBox8;  // [kSlots] query operands
   static constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
   static constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax exchange
   static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O
   static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][8]: item records
   static constexpr int kBars = kInfo + kSlots * 8 * 4;
-  static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * kSlots + 2 + 4 * 2 + 1;
+  static constexpr int kNumBars =
+      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 + 4 * 2 + 1;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 };
 constexpr int kSmemLimit = 232448;
@@ -98,7 +102,7 @@ static_assert(Layout<true>::kSmem <= kSmemLimit, "FP8 decode shared memory excee
 // TMEM columns
 constexpr uint32_t kColS = 0;   // S^T: 16 columns
 constexpr uint32_t kColO = 16;  // O^T[2]: 16 columns each
-constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kColK = 64;  // FP8: K[2] as F16 pairs, 64 columns each (lane = key)
 
 struct Bars {
   uint64_t* k_full;    // [kStages] operand page: K ready (TMA, or the FP8 converters)
@@ -106,6 +110,7 @@ struct Bars {
   uint64_t* kv_empty;  // [kStages] P.V of the page done
   uint64_t* kv8_full;  // [kStages8] FP8: e4m3 page landed
   uint64_t* kv8_empty; // [kStages8] FP8: e4m3 page converted
+  uint64_t* k_free;    // [kStages] FP8: QK^T done with the TMEM K buffer
   uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
   uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
   uint64_t* s_full;    // S^T of the current page
@@ -162,6 +167,17 @@ __device__ __forceinline__ int unit_columns(const DecodeParams& p, int unit) {
   return min(p.Lg, p.L - t0) * p.G;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 (lane = row, element pairs per
+// column), issued by one thread.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 4 e4m3 codes (bytes 0..3 of w) -> 4 F16 values (exact): two F16 pairs.
 __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
@@ -189,7 +205,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using Lay = Layout<FP8, NH>;
   constexpr int kConvWarps = Lay::kConvWarps;
-  constexpr int kStages = Lay::kStages;
+  constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStageBytes;
   constexpr int kStages8 = FP8 ? Lay::kStages8 : 1;  // (the bf16 kernel has no e4m3 ring)
   constexpr int kRing = Lay::kRing, kRing8 = Lay::kRing8, kQ = Lay::kQ, kP = Lay::kP;
   constexpr int kX = Lay::kX, kML = Lay::kML, kInfo = Lay::kInfo, kBars = Lay::kBars;
@@ -204,7 +220,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   B.kv_empty = B.v_full + kStages;
   B.kv8_full = B.kv_empty + kStages;
   B.kv8_empty = B.kv8_full + Lay::kStages8;  // (none in the bf16 kernel)
-  B.q_full = B.kv8_empty + Lay::kStages8;
+  B.k_free = B.kv8_empty + Lay::kStages8;
+  B.q_full = B.k_free + (FP8 ? kStages : 0);
   B.q_empty = B.q_full + kSlots;
   B.s_full = B.q_empty + kSlots;
   B.p_full = B.s_full + 1;
@@ -227,6 +244,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       mbar_init(&B.kv8_full[i], 1);
       mbar_init(&B.kv8_empty[i], kConvWarps);
     }
+    if (FP8)
+      for (int i = 0; i < kStages; ++i) mbar_init(&B.k_free[i], 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&B.q_full[i], 1);
       // MMA, 4 softmax warps, 4 epilogue warps (, the converter warps)
@@ -249,7 +268,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, Lay::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -572,11 +591,21 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           if (!(ok = mbar_wait(&B.k_full[st], ph, p.status))) break;
           tc_fence_after();
           const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
+          if constexpr (FP8) {
+            // A = K from the TMEM buffer the converters filled
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            umma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+              umma_ts(tmem + kColS, tmem + kColK + st * 64 + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&B.k_free[st]);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+              umma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(B.s_full);
           if (j == npg - 1) umma_commit(&B.q_empty[slot]);
@@ -584,7 +613,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
           if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
           tc_fence_after();
-          const uint32_t v_addr = k_addr + 2 * kBox;
+          const uint32_t v_addr = FP8 ? k_addr : k_addr + 2 * kBox;
           const uint32_t p_addr = smem_u32(smem + kP);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -605,16 +634,20 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     __syncwarp();
   } else if (warp >= kConvWarp0) {
     // ------------------------------------------------------------ FP8 converters, thread = key
-    // Each page: wait for its e4m3 tiles and for the operand page to be free
-    // (P.V of the previous page done), then rewrite K and V as F16 in the
-    // swizzled layout the bf16 path gets from TMA; K is published first so
-    // that QK^T starts while V converts.
+    // Each page: wait for its e4m3 tiles; K (once QK^T is done with the TMEM
+    // buffer two pages back) goes to tensor memory as F16 pairs, one lane per
+    // key, 64 columns; V (once P.V is done with the shared-memory stage two
+    // pages back) goes to shared memory as F16 in the swizzled layout the bf16
+    // path gets from TMA.  With eight converter warps, warps 10-13 take K and
+    // 14-17 V; with four, each warp takes both for its 32 keys.
     if constexpr (FP8) {
       const int ct = threadIdx.x - kConvWarp0 * 32;
-      const int row = ct & 127;                       // key 0..127
+      const int quarter = warp & 3;                   // TMEM lanes this warp may access
+      const int row = quarter * 32 + lane;            // key 0..127
       const int sw = row & 7;                         // 128-byte swizzle of the row
-      // with 8 converter warps, warps 10-13 convert K and 14-17 V
-      const int t_lo = kConvWarps == 8 ? (ct >> 7) : 0, t_hi = kConvWarps == 8 ? t_lo + 1 : 2;
+      const bool do_k = kConvWarps == 8 ? ct < 128 : true;
+      const bool do_v = kConvWarps == 8 ? ct >= 128 : true;
+      const uint32_t k_lanes = tmem + ((uint32_t)(quarter * 32) << 16) + kColK;
       uint32_t gp = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
@@ -627,22 +660,48 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         if (lane == 0) mbar_arrive(&B.q_empty[slot]);
         for (int j = 0; j < npg; ++j, ++gp) {
           const int st8 = gp % kStages8, st = gp % kStages;
+          const uint32_t ph = ((gp / kStages) & 1) ^ 1;  // the buffer's previous use
           if (!(ok = mbar_wait_warp(&B.kv8_full[st8], (gp / kStages8) & 1, p.status))) break;
-          if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((gp / kStages) & 1) ^ 1, p.status))) break;
           const uint32_t src = smem_u32(smem + kRing8 + st8 * 2 * kBox8) + row * 128;
-          const uint32_t dst = smem_u32(smem + kRing + st * kStageBytes) + row * 128;
-          for (int t = t_lo; t < t_hi; ++t) {  // K, then V
+          if (do_k) {
+            if (!(ok = mbar_wait_warp(&B.k_free[st], ph, p.status))) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // dims 64h .. 64h + 63: columns 32h .. 32h + 31
+              uint32_t w[32];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint4 lo, hi;
+                e4m3x16_to_f16(lds128(src + (((4 * h + c) ^ sw) << 4)), lo, hi);
+                w[8 * c] = lo.x;
+                w[8 * c + 1] = lo.y;
+                w[8 * c + 2] = lo.z;
+                w[8 * c + 3] = lo.w;
+                w[8 * c + 4] = hi.x;
+                w[8 * c + 5] = hi.y;
+                w[8 * c + 6] = hi.z;
+                w[8 * c + 7] = hi.w;
+              }
+              tmem_st32(k_lanes + st * 64 + 32 * h, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.k_full[st]);
+          }
+          if (do_v) {
+            if (!(ok = mbar_wait_warp(&B.kv_empty[st], ph, p.status))) break;
+            const uint32_t dst = smem_u32(smem + kRing + st * kStageBytes) + row * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // dims 16c .. 16c + 15
               uint4 lo, hi;
-              e4m3x16_to_f16(lds128(src + t * kBox8 + ((c ^ sw) << 4)), lo, hi);
-              const uint32_t d = dst + t * 2 * kBox + (c >> 2) * kBox;
+              e4m3x16_to_f16(lds128(src + kBox8 + ((c ^ sw) << 4)), lo, hi);
+              const uint32_t d = dst + (c >> 2) * kBox;
               sts128(d + (((2 * (c & 3)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
               sts128(d + (((2 * (c & 3) + 1) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(t == 0 ? &B.k_full[st] : &B.v_full[st]);
+            if (lane == 0) mbar_arrive(&B.v_full[st]);
           }
           if (lane == 0) mbar_arrive(&B.kv8_empty[st8]);
         }
@@ -802,7 +861,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           const int st = gp % kStages;
           if (!(ok = mbar_wait_warp(&B.v_full[st], (gp / kStages) & 1, p.status))) break;
           if (!kv) {
-            const uint32_t vr = smem_u32(smem + kRing + st * kStageBytes + 2 * kBox) + key * 128;
+            const uint32_t vr =
+                smem_u32(smem + kRing + st * kStageBytes + (FP8 ? 0 : 2 * kBox)) + key * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
               sts128(vr + ch * 16, 0u, 0u, 0u, 0u);
@@ -928,7 +988,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, Lay::kTmemCols);
   }
 }
 
