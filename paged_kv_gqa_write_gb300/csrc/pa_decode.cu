@@ -86,13 +86,13 @@ struct Layout {
   static constexpr int kRing8 = kRing + kStages * kStageBytes;
   static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;  // FP8: + two 64-column K buffers
   static constexpr int kQ = kRing8 + kStages8 * 2 * kBox8;  // [kSlots] query operands
-  static constexpr int kP = kQ + kSlots * kOpBytes;         // P operand
-  static constexpr int kX = kP + kOpBytes;                  // float [2][4][16]: softmax exchange
+  static constexpr int kP = kQ + kSlots * kOpBytes;         // P operands [2]
+  static constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][16]: softmax exchange
   static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O
   static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][8]: item records
   static constexpr int kBars = kInfo + kSlots * 8 * 4;
   static constexpr int kNumBars =
-      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 + 4 * 2 + 1;
+      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 };
 constexpr int kSmemLimit = 232448;
@@ -100,8 +100,8 @@ static_assert(Layout<false>::kSmem <= kSmemLimit, "decode shared memory exceeds 
 static_assert(Layout<true>::kSmem <= kSmemLimit, "FP8 decode shared memory exceeds the limit");
 
 // TMEM columns
-constexpr uint32_t kColS = 0;   // S^T: 16 columns
-constexpr uint32_t kColO = 16;  // O^T[2]: 16 columns each
+constexpr uint32_t kColS = 0;   // S^T[2]: 16 columns each (page parity)
+constexpr uint32_t kColO = 32;  // O^T[2]: 16 columns each (item parity)
 constexpr uint32_t kColK = 64;  // FP8: K[2] as F16 pairs, 64 columns each (lane = key)
 
 struct Bars {
@@ -113,8 +113,9 @@ struct Bars {
   uint64_t* k_free;    // [kStages] FP8: QK^T done with the TMEM K buffer
   uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
   uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
-  uint64_t* s_full;    // S^T of the current page
-  uint64_t* p_full;    // P of the current page
+  uint64_t* s_full;    // [2] S^T of a page (by page parity)
+  uint64_t* p_full;    // [2] P of a page
+  uint64_t* pv_done;   // every P.V, in page order (the softmax's O rescale waits on it)
   uint64_t* o_full;    // [2] last P.V of the item done
   uint64_t* o_free;    // [2] epilogue read O and (m, l)
   uint64_t* ml_full;   // [2] (m, l) of the item published
@@ -224,8 +225,9 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   B.q_full = B.k_free + (FP8 ? kStages : 0);
   B.q_empty = B.q_full + kSlots;
   B.s_full = B.q_empty + kSlots;
-  B.p_full = B.s_full + 1;
-  B.o_full = B.p_full + 1;
+  B.p_full = B.s_full + 2;
+  B.pv_done = B.p_full + 2;
+  B.o_full = B.pv_done + 1;
   B.o_free = B.o_full + 2;
   B.ml_full = B.o_free + 2;
   B.x_full = B.ml_full + 2;
@@ -257,14 +259,17 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       mbar_init(&B.ml_full[i], 1);
       mbar_init(&B.x_full[i], 4);
     }
-    mbar_init(B.s_full, 1);
-    mbar_init(B.p_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.s_full[i], 1);
+      mbar_init(&B.p_full[i], 128);
+    }
+    mbar_init(B.pv_done, 1);
     mbar_init(B.mma_done, 1);
     fence_mbar_init();
   }
   // query rows past every item's box and unused P rows read as zero: clear the
   // operands (columns past an item's GC are computed and never used)
-  for (int o = threadIdx.x * 16; o < (kSlots + 1) * kOpBytes; o += kThreads * 16)
+  for (int o = threadIdx.x * 16; o < (kSlots + 2) * kOpBytes; o += kThreads * 16)
     sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
@@ -585,36 +590,46 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         }
         const int ob = nb & 1;
         const uint32_t q_addr = smem_u32(smem + kQ + slot * kOpBytes);
-        for (int j = 0; j < npg; ++j, ++gp) {
-          const int st = gp % kStages;
-          const uint32_t ph = (gp / kStages) & 1;
-          if (!(ok = mbar_wait(&B.k_full[st], ph, p.status))) break;
+        // QK^T of page g into S buffer g & 1 (free: the softmax read page
+        // g - 2's scores before publishing its P, which the loop below waited for)
+        auto qk = [&](uint32_t g) -> bool {
+          const int st = g % kStages;
+          if (!mbar_wait(&B.k_full[st], (g / kStages) & 1, p.status)) return false;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
+          const uint32_t s_cols = tmem + kColS + (g & 1) * kN;
           if constexpr (FP8) {
             // A = K from the TMEM buffer the converters filled
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              umma_ts(tmem + kColS, tmem + kColK + st * 64 + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+              umma_ts(s_cols, tmem + kColK + st * 64 + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
             }
             umma_commit(&B.k_free[st]);
           } else {
+            const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              umma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+              umma_bf16_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
             }
           }
-          umma_commit(B.s_full);
+          umma_commit(&B.s_full[g & 1]);
+          return true;
+        };
+        if (!(ok = qk(gp))) break;  // the item's first page
+        for (int j = 0; j < npg; ++j, ++gp) {
+          // the next page's QK^T runs on the tensor core during this page's softmax
+          if (j + 1 < npg && !(ok = qk(gp + 1))) break;
           if (j == npg - 1) umma_commit(&B.q_empty[slot]);
-          if (!(ok = mbar_wait(B.p_full, gp & 1, p.status))) break;
+          const int st = gp % kStages;
+          const uint32_t ph = (gp / kStages) & 1;
+          if (!(ok = mbar_wait(&B.p_full[gp & 1], (gp >> 1) & 1, p.status))) break;
           if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
           if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
           tc_fence_after();
-          const uint32_t v_addr = FP8 ? k_addr : k_addr + 2 * kBox;
-          const uint32_t p_addr = smem_u32(smem + kP);
+          const uint32_t v_addr = smem_u32(smem + kRing + st * kStageBytes) + (FP8 ? 0 : 2 * kBox);
+          const uint32_t p_addr = smem_u32(smem + kP + (gp & 1) * kOpBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
@@ -622,6 +637,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
             umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&B.kv_empty[st]);
+          umma_commit(B.pv_done);
         }
         if (!ok) break;
         umma_commit(&B.o_full[ob]);
@@ -781,10 +797,10 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
           for (int g = 0; g < NH; ++g) vis |= (kpos < lim[g] ? 1u : 0u) << g;
         }
         auto visible = [&](int g) -> bool { return MULTI ? ((vis >> g) & 1u) != 0 : kv; };
-        if (!(ok = mbar_wait_warp(B.s_full, gp & 1, p.status))) break;
+        if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
         tc_fence_after();
         uint32_t sr[16];
-        tmem_ld16(tmem + lane_base + kColS, sr);
+        tmem_ld16(tmem + lane_base + kColS + (gp & 1) * kN, sr);
         tmem_wait_ld();
         float d[NH];
         bool need = j == 0;
@@ -825,8 +841,11 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
             d[g] = fmaf(__uint_as_float(sr[g]), c, -m[g]);
           }
           if (j > 0) {
-            // O^T holds P.V of the item's earlier pages: the commit that
-            // published S of this page came after the previous P.V finished
+            // O^T holds P.V of the item's earlier pages once the previous
+            // page's P.V is done (this page's QK^T was issued before it; the
+            // one before it finished ahead of this page's scores)
+            if (!(ok = mbar_wait_warp(B.pv_done, (gp - 1) & 1, p.status))) break;
+            tc_fence_after();
             uint32_t orow[16];
             const uint32_t o_cols = tmem + lane_base + kColO + ob * kN;
             tmem_ld16(o_cols, orow);
@@ -837,9 +856,9 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
             tmem_st16(o_cols, orow);
           }
         }
-        // P(j) into the operand: P.V(j - 1) has finished reading it (it completed
-        // before the commit that published S of this page)
-        const uint32_t pbase = smem_u32(smem + kP) + p_key;
+        // P(j) into operand buffer j & 1: P.V(j - 2) has finished reading it (it
+        // was issued before QK^T(j), whose commit published these scores)
+        const uint32_t pbase = smem_u32(smem + kP + (gp & 1) * kOpBytes) + p_key;
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
           if (g < GC) {
@@ -873,7 +892,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         fence_proxy_async_smem();
         if (need && j > 0) tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(B.p_full);
+        mbar_arrive(&B.p_full[gp & 1]);
       }
       if (!ok) break;
       // item end: row sums over the 128 keys, published with the max
