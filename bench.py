@@ -170,7 +170,7 @@ def decode_traffic_from_profile():
     try:
         # the decode path: its kernel, the combines and the shared device helpers
         blob = b"".join(open(os.path.join(csrc, f), "rb").read()
-                        for f in ("pa_decode_plain.cu", "pa_combine.cu", "pa_common.cuh"))
+                        for f in ("pa_decode.cu", "pa_combine.cu", "pa_common.cuh"))
         h = hashlib.sha256(blob).hexdigest()[:16]
         vals = {}
         for line in open(prof):

@@ -1,7 +1,6 @@
 // pa_decode.cu -- paged GQA decode attention, flash-decoding split-K, with the
-// two contractions on the 5th-generation tensor cores: the general kernel
-// (several new tokens per sequence, and the FP8 cache).  A bf16 cache with one
-// new token per sequence runs the same design from pa_decode_plain.cu.
+// two contractions on the 5th-generation tensor cores; one kernel template for
+// a bf16 or an FP8 (e4m3) cache and one or several new tokens per sequence.
 //
 // Computes, for every sequence s and query head g (KV head h = g / G):
 //   out[s][g] = softmax(scale * q[s][g] . K_t) V_t over t < context_lens[s],
@@ -26,23 +25,30 @@
 //    (128-byte swizzle), and the FP32 pipes only run the softmax.
 //  * warp 0: validates each item's block-table range (the next item's
 //    metadata is loaded while the current item's pages are issued), stages
-//    up to four items ahead, TMA-loads each item's query rows (a 3-D box of
-//    Lg tokens x G heads; rows past it stay zero) and its K/V page tiles into a 3-stage ring of 64 KB (K and V
-//    complete on separate mbarriers, so QK^T starts while V is in flight).  warp 1: owns TMEM (S, O[2]) and issues the MMAs
-//    in page order: QK^T(j), then P.V(j) once P(j) is in shared memory.
+//    up to four items ahead, TMA-loads each item's query rows (G heads, or a
+//    3-D box of Lg tokens x G heads; rows past it stay zero) and its K/V page
+//    tiles into a 3-stage ring of 64 KB (K and V complete on separate
+//    mbarriers, so QK^T starts while V is in flight).
+//  * warp 1: owns TMEM (S[2], O[2]) and issues the MMAs: QK^T(j + 1) before
+//    P.V(j), into the other of two S buffers, so the tensor core computes the
+//    next page's scores while the softmax works on this page's; P.V(j) once
+//    P(j) is in its shared-memory buffer (two, by page parity).
 //  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
 //    softmax in the log2 domain with a per-head reference max shared by the
 //    CTA.  The reference only moves when some score exceeds it by more than
-//    2^8 (one bar.red.or per page decides), which rescales O in TMEM; the
-//    first page of an item takes the exact max.  The warps agree through a
-//    small shared-memory exchange on mbarriers (bounded waits, no bar.sync).  P is rounded to BF16 and
-//    written transposed into a K-major operand; the row sums accumulate the
-//    rounded values, so the normalisation matches the weights the MMA used.
-//    V rows past the context in the last page are zeroed before P.V reads
-//    them (P is 0 there, but 0 * NaN is NaN).
+//    2^8 (a vote exchanged among the four warps decides), which rescales O in
+//    TMEM after the previous P.V; the first page of an item takes the exact
+//    max.  The warps agree through a small shared-memory exchange on
+//    mbarriers (bounded waits, no bar.sync).  P is rounded to BF16 (F16 for
+//    the FP8 cache) and written transposed into a K-major operand; the row
+//    sums accumulate the rounded values, so the normalisation matches the
+//    weights the MMA used.  V rows past the context in the last page are
+//    zeroed before P.V reads them (P is 0 there, but 0 * NaN is NaN).
 //  * warps 6-9, one thread per head dim: the epilogue of the previous item
 //    (O / l from TMEM, double-buffered) overlaps the next item's pages; it
 //    writes `out` (one split) or normalised partials (o, lse) for the combine.
+//  * FP8 cache: TMA lands e4m3 pages; converter warps rewrite K as F16 into
+//    tensor memory (QK^T takes A from TMEM) and V as F16 into shared memory.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -1041,10 +1047,8 @@ cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   if (p.k_scale)  // FP8 cache
     return gc <= 8 ? launch_multi<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
                    : launch_multi<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
-  // bf16 cache, one new token per sequence: the kernel of pa_decode_plain.cu
-  if (p.L == 1) return launch_decode_plain(tm_k, tm_v, tm_q, p, gc, num_sms, stream);
-  return gc <= 8 ? launch_nh<8, false, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                 : launch_nh<16, false, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  return gc <= 8 ? launch_multi<8, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                 : launch_multi<16, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace pa

@@ -38,10 +38,6 @@ cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
                           cudaStream_t stream);
-// The bf16, one-token-per-sequence kernel launch_decode dispatches to.
-cudaError_t launch_decode_plain(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const CUtensorMap& tm_q, const DecodeParams& p, int gc,
-                                int num_sms, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
