@@ -107,6 +107,9 @@ typedef struct pa_dims {
  * token offsets are built in shared memory). */
 #define PA_MAX_CHUNKED_SEQS 16384
 
+/* Largest Hq + 2 Hkv that pa_qk_norm_rope_write takes. */
+#define PA_MAX_PROLOGUE_HEADS 384
+
 /* num_splits value for pa_decode's page-balanced schedule (see pa_decode). */
 #define PA_SPLITS_BALANCED (-1)
 /* Largest batch the page-balanced schedule takes. */
@@ -151,7 +154,9 @@ int pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cac
  *   status: exactly as pa_kv_write (K is written normed and rotated, rounded
  *   to bf16; V bit for bit).  Positions are context_lens[s] - chunk_lens[s] + j.
  * Returns PA_ERR_DIMS for eps < 0, rope_base <= 0, rope_scale <= 0 or a
- * non-finite value; every pointer must be 16-byte aligned.
+ * non-finite value, PA_ERR_HEADS when Hq + 2 Hkv > PA_MAX_PROLOGUE_HEADS (a
+ * token's row is staged whole in shared memory); every pointer must be
+ * 16-byte aligned.
  */
 int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
                           float eps, float rope_base, float rope_scale, float q_scale,

@@ -26,6 +26,7 @@ PA_SPLITS_BALANCED = -1
 PA_BALANCED_MAX_SEQS = 512
 PA_TOPK_MAX_K = 32
 PA_MAX_Q_LEN = 16
+PA_MAX_PROLOGUE_HEADS = 384
 (PA_ERR_NULL_POINTER, PA_ERR_HEAD_DIM, PA_ERR_PAGE_SIZE, PA_ERR_HEADS, PA_ERR_DIMS,
  PA_ERR_ALIGNMENT, PA_ERR_OUT_DTYPE, PA_ERR_WORKSPACE, PA_ERR_SPLITS, PA_ERR_TOO_MANY_SEQS,
  PA_ERR_TENSOR_MAP, PA_ERR_NO_DEVICE, PA_ERR_NOALLOC_TOO_LARGE) = range(-1, -14, -1)

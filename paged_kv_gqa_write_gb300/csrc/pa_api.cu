@@ -373,7 +373,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 104; }
+int32_t pa_abi_version(void) { return 105; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -472,6 +472,7 @@ int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k
   if (num_tokens < 0) return PA_ERR_DIMS;
   if (!chunk_lens && num_tokens != d.num_seqs) return PA_ERR_DIMS;
   if (chunk_lens && d.num_seqs > PA_MAX_CHUNKED_SEQS) return PA_ERR_TOO_MANY_SEQS;
+  if (d.num_q_heads + 2 * d.num_kv_heads > PA_MAX_PROLOGUE_HEADS) return PA_ERR_HEADS;
   if (!(eps >= 0.f) || !(rope_base > 0.f) || !(rope_scale > 0.f) || !std::isfinite(eps) ||
       !std::isfinite(rope_base) || !std::isfinite(rope_scale) || !std::isfinite(q_scale))
     return PA_ERR_DIMS;
@@ -497,8 +498,17 @@ int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k
   p.status = status;
   p.eps = eps;
   p.q_scale = q_scale;
-  p.log2_base = std::log2((double)rope_base);
-  p.rope_scale = rope_scale;
+  {
+    const double log2_base = std::log2((double)rope_base);
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < 64; ++i) {
+      const double f = std::exp2(-2.0 * i / kHeadDim * log2_base) / (double)rope_scale;
+      const double g = f / two_pi;
+      p.freq[i] = f;
+      p.turn_hi[i] = (float)g;
+      p.turn_lo[i] = (float)(g - (double)p.turn_hi[i]);
+    }
+  }
   p.B = d.num_seqs;
   p.T = num_tokens;
   p.Hq = d.num_q_heads;

@@ -353,18 +353,30 @@ __device__ __forceinline__ bool block_chunk_offsets(const int32_t* chunk_lens, i
     sum += c > 0 ? c : 0;
     off[i] = sum;
   }
-  scratch[tid] = sum;
+  // exclusive prefix of the per-thread sums: a scan within each warp, then one
+  // over the warp totals (blockDim.x is a multiple of 32, at most 1024)
+  const int lane = tid & 31, w = tid >> 5, nw = nt >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) scratch[w] = incl;
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < nt; ++i) {
-      int v = scratch[i];
-      scratch[i] = run;
-      run += v;
+  if (w == 0) {
+    const int v = lane < nw ? scratch[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += t;
     }
+    if (lane < nw) scratch[lane] = x - v;
   }
   __syncthreads();
-  for (int i = lo; i < hi; ++i) off[i] += scratch[tid];
+  const int base = scratch[w] + incl - sum;
+  for (int i = lo; i < hi; ++i) off[i] += base;
   return __syncthreads_or(neg) != 0;
 }
 
@@ -447,8 +459,11 @@ struct PrologueParams {
   const int32_t* chunk_lens;    // may be null (one token per sequence)
   int32_t* status;
   float eps, q_scale;
-  double log2_base, rope_scale;  // RoPE: log2 of the frequency base, scale divisor
   int32_t B, T, Hq, Hkv, num_pages, max_pages;
+  // RoPE frequencies of the 64 pairs, base^(-2i/D) / scale: in radians per
+  // position (double) and in turns per position as an unevaluated float pair
+  double freq[64];
+  float turn_hi[64], turn_lo[64];
 };
 
 // Exact top-k over rows of logits.

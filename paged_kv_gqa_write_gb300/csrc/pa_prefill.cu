@@ -55,9 +55,10 @@ constexpr int kMaxList = 64;                  // scheduled items per CTA
 constexpr int kQ = 0;                         // Q_A, Q_B
 constexpr int kK = kQ + 2 * kTileBytes;
 constexpr int kV = kK + kRingK * kTileBytes;
-constexpr int kList = kV + kRingV * kTileBytes;  // schedule [kMaxList][3] int
-constexpr int kBars = kList + kMaxList * 3 * 4;
-constexpr int kNumBars = 2 + 2 * kRingK + 2 * kRingV + 4 * 2;
+constexpr int kListInts = 5;                  // per item: s, pair|head, tok0, chunk len, ctx
+constexpr int kList = kV + kRingV * kTileBytes;  // schedule [kMaxList][kListInts] int
+constexpr int kBars = kList + kMaxList * kListInts * 4;
+constexpr int kNumBars = 2 * 2 + 2 * kRingK + 2 * kRingV + 4 * 2;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
 constexpr int kMaxCost = 4096;                // schedule histogram buckets (ring scratch)
 // TMEM columns
@@ -67,7 +68,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Bars {
-  uint64_t* q_full;
+  uint64_t* q_full;   // [2] per query tile
   uint64_t* q_empty;
   uint64_t* k_full;   // [kRingK]
   uint64_t* k_empty;
@@ -94,14 +95,13 @@ __device__ __forceinline__ bool lengths_ok(const PrefillParams& p, int n, int ct
 }
 
 __device__ __forceinline__ Item make_item(const PrefillParams& p, int s, int pair, int g,
-                                          int tok0) {
+                                          int tok0, int n, int ctx) {
   Item it;
   it.s = s;
   it.g = g;
   it.h = g / p.G;
   it.pair = pair;
-  const int n = __ldg(p.chunk_lens + s);
-  it.ctx = __ldg(p.context_lens + s);
+  it.ctx = ctx;
   it.tok0 = tok0;
   it.len_ok = lengths_ok(p, n, it.ctx);
   it.prior = it.ctx - n;
@@ -165,10 +165,12 @@ __device__ int build_schedule(const PrefillParams& p, int* hist, int* list, int 
       for (int k = 0; k < 2; ++k) {
         const int64_t res = k ? N2 - 1 - c : c;
         for (int64_t pos = pos0 + ((res - pos0 % N2) % N2 + N2) % N2; pos < pos0 + p.Hq; pos += N2) {
-          const int r = (int)(pos / N);
-          list[3 * r] = s;
-          list[3 * r + 1] = (pr << 8) | (int)(pos - pos0);
-          list[3 * r + 2] = tok + pr * 256;
+          int* e = list + kListInts * (int)(pos / N);
+          e[0] = s;
+          e[1] = (pr << 8) | (int)(pos - pos0);
+          e[2] = tok + pr * 256;
+          e[3] = n;
+          e[4] = ctx;
         }
       }
     }
@@ -186,8 +188,8 @@ struct ItemSource {
   __device__ bool get(const PrefillParams& p, int r, Item& it) {
     if (count >= 0) {
       if (r >= count) return false;
-      const int s_ = list[3 * r], qg = list[3 * r + 1];
-      it = make_item(p, s_, qg >> 8, qg & 255, list[3 * r + 2]);
+      const int* e = list + kListInts * r;
+      it = make_item(p, e[0], e[1] >> 8, e[1] & 255, e[2], e[3], e[4]);
       return true;
     }
     const int i = (int)blockIdx.x + r * (int)gridDim.x;
@@ -202,7 +204,8 @@ struct ItemSource {
     }
     if (s >= p.B) return false;
     const int pr = pair - pairs_before;
-    it = make_item(p, s, pr, g, tok_before + pr * 256);
+    it = make_item(p, s, pr, g, tok_before + pr * 256, __ldg(p.chunk_lens + s),
+                   __ldg(p.context_lens + s));
     return true;
   }
 };
@@ -226,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBars);
   Bars B;
   B.q_full = bar;
-  B.q_empty = bar + 1;
-  B.k_full = bar + 2;
+  B.q_empty = bar + 2;
+  B.k_full = bar + 4;
   B.k_empty = B.k_full + kRingK;
   B.v_full = B.k_empty + kRingK;
   B.v_empty = B.v_full + kRingV;
@@ -241,8 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(B.q_full, 1);
-    mbar_init(B.q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&B.q_full[t], 1);
+      mbar_init(&B.q_empty[t], 1);
+    }
     for (int i = 0; i < kRingK; ++i) {
       mbar_init(&B.k_full[i], 1);
       mbar_init(&B.k_empty[i], 1);
@@ -285,21 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensor_map(map);
       const uint64_t pol_kv = l2_policy_evict_last();  // reused by other tiles/heads
       const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t items = 0, tiles = 0;
+      uint32_t tiles = 0;
+      uint32_t qitems[2] = {0, 0};  // items in which each query tile had key tiles
       bool ok = true;
       Item it;
       for (int r = 0; ok && src.get(p, r, it); ++r) {
         if (it.nmax == 0) continue;
-        if (is_k) {
-          if (!(ok = mbar_wait(B.q_empty, (items & 1) ^ 1, p.status))) break;
-          mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
-          for (int t = 0; t < 2; ++t) {
-            tma_load_3d(smem + kQ + t * kTileBytes, &tm_q, 0, it.g, it.tok0 + t * 128, B.q_full, pol_q);
-            tma_load_3d(smem + kQ + t * kTileBytes + kBox, &tm_q, 64, it.g, it.tok0 + t * 128,
-                        B.q_full, pol_q);
-          }
-        }
-        ++items;
         const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
         for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
           int page = __ldg(bt + kt);
@@ -310,6 +306,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[slot], kTileBytes);
           tma_load_2d(ring + slot * kTileBytes, map, x, y, &full[slot], pol_kv);
           tma_load_2d(ring + slot * kTileBytes + kBox, map, x + 64, y, &full[slot], pol_kv);
+          if (is_k && kt == 0) {
+            // each query tile's Q once its buffer is free (after the previous
+            // item's last QK^T of that tile); the first K tile goes ahead of it
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (it.nkt[t] == 0) continue;
+              if (!(ok = mbar_wait(&B.q_empty[t], (qitems[t] & 1) ^ 1, p.status))) break;
+              ++qitems[t];
+              mbar_arrive_expect_tx(&B.q_full[t], kTileBytes);
+              tma_load_3d(smem + kQ + t * kTileBytes, &tm_q, 0, it.g, it.tok0 + t * 128,
+                          &B.q_full[t], pol_q);
+              tma_load_3d(smem + kQ + t * kTileBytes + kBox, &tm_q, 64, it.g, it.tok0 + t * 128,
+                          &B.q_full[t], pol_q);
+            }
+            if (!ok) break;
+          }
         }
       }
     }
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, 128, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, 128, false, true);
-      uint32_t items = 0, tiles = 0;
+      uint32_t tiles = 0;
       uint32_t gt[2] = {0, 0};     // key tiles each query tile has been through (all items)
       uint32_t gitems[2] = {0, 0};  // items in which each query tile had key tiles
       bool ok = true;
@@ -359,15 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it;
       for (int r = 0; ok && src.get(p, r, it); ++r) {
         if (it.nmax == 0) continue;
-        if (!(ok = mbar_wait(B.q_full, items & 1, p.status))) break;
-        ++items;
-        for (int t = 0; t < 2; ++t) gitems[t] += it.nkt[t] > 0 ? 1u : 0u;
         const uint32_t k0 = tiles;
         if (!(ok = wait_k(k0))) break;
-        for (int t = 0; t < 2; ++t)
-          if (it.nkt[t] > 0) qk(t, k0);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (it.nkt[t] == 0) continue;
+          ++gitems[t];
+          if (!(ok = mbar_wait(&B.q_full[t], (gitems[t] - 1) & 1, p.status))) break;
+          tc_fence_after();
+          qk(t, k0);
+          if (it.nkt[t] == 1) umma_commit(&B.q_empty[t]);
+        }
+        if (!ok) break;
         umma_commit(&B.k_empty[k0 % kRingK]);
-        if (it.nmax == 1) umma_commit(B.q_empty);
         for (int j = 0; j < it.nmax && ok; ++j) {
           const uint32_t kidx = k0 + j;
           const bool next = j + 1 < it.nmax;
@@ -378,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = wait_k(kidx + 1))) break;
               k_ready = true;
               qk(0, kidx + 1);
+              if (j + 2 == it.nkt[0]) umma_commit(&B.q_empty[0]);
             }
           }
           if (j < it.nkt[1]) {
@@ -387,11 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < it.nkt[1]) {
             if (!k_ready && !(ok = wait_k(kidx + 1))) break;
             qk(1, kidx + 1);
+            if (j + 2 == it.nkt[1]) umma_commit(&B.q_empty[1]);
           }
-          if (next) {
-            umma_commit(&B.k_empty[(kidx + 1) % kRingK]);
-            if (j + 2 == it.nmax) umma_commit(B.q_empty);
-          }
+          if (next) umma_commit(&B.k_empty[(kidx + 1) % kRingK]);
         }
         tiles += it.nmax;
       }
@@ -421,26 +434,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nkt = it.nkt[qtile];
       const uint32_t k0 = tiles;
       if (it.nmax > 0) tiles += it.nmax;
-      // sequence validity: lengths and every referenced block-table entry
-      bool bad = !it.len_ok;
-      if (!bad) {
-        const int used = (it.ctx + kPage - 1) / kPage;
-        const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
-        bool b = false;
-        for (int e = lane; e < used; e += 32) {
-          const int pg = __ldg(bt + e);
-          b |= (pg < 0 || pg >= p.num_pages);
-        }
-        bad = __any_sync(0xffffffffu, b);
-      }
-      if (bad && qtile == 0 && t == 0 && it.pair == 0 && it.g == 0 && p.status)
-        atomicOr(p.status, it.len_ok ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
+      const bool reporter = qtile == 0 && t == 0 && it.pair == 0 && it.g == 0 && p.status;
       const int nrows = it.nrows[qtile];
       const int64_t tok = (int64_t)it.tok0 + qtile * 128 + row;
       const bool row_out = row < nrows && tok < p.T;
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
                      ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
       if (nkt == 0) {
+        // tile A has key tiles unless the lengths are invalid
+        if (!it.len_ok && reporter) atomicOr(p.status, PA_STATUS_BAD_LENGTH);
         if (row_out)  // lengths invalid: zero rows
           for (int cc = 0; cc < (p.out_f32 ? 32 : 16); ++cc)
             reinterpret_cast<uint4*>(dst)[cc] = make_uint4(0, 0, 0, 0);
@@ -452,6 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the first P.V to read the last page zeroes its tail: tile A's if it reaches it
       const bool zero_mine = vtail != 0 && nkt - 1 == last_page &&
                              (qtile == 0 || it.nkt[0] - 1 != last_page);
+      // block-table entries of the context: the first 32 loaded now, checked
+      // after the key tiles (off the path to the first tile)
+      const int used = (it.ctx + kPage - 1) / kPage;
+      const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
+      const int pg_first = lane < used ? __ldg(bt + lane) : 0;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt < nkt; ++kt, ++gt) {
         if (!(ok = mbar_wait_warp(&B.s_full[qtile], gt & 1, p.status))) break;
@@ -572,6 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&B.p_full[qtile]);
       }
       if (!ok) break;
+      bool pg_bad = pg_first < 0 || pg_first >= p.num_pages;
+      for (int e = lane + 32; e < used; e += 32) {
+        const int pg = __ldg(bt + e);
+        pg_bad |= (pg < 0 || pg >= p.num_pages);
+      }
+      const bool bad = __any_sync(0xffffffffu, pg_bad);
+      if (bad && reporter) atomicOr(p.status, PA_STATUS_BAD_PAGE);
       // ---- epilogue: O / l for this row
       if (!(ok = mbar_wait_warp(&B.o_done[qtile], (gt - 1) & 1, p.status))) break;
       tc_fence_after();

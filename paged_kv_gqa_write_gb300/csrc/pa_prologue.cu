@@ -11,21 +11,45 @@
 // "Model structure, top down": decode_fwd runs Q/K norm -> RoPE before the KV
 // cache write; FP32 RMSNorm weights.
 //
-// Memory bound and small (decode: B tokens): a warp takes a token and 8 of
-// its Hq + 2 Hkv heads, resolves the token's slot and validity (as the KV
-// write does) while those heads' rows load, computes the (cos, sin) pairs of
-// its position -- the angle pos * base^(-2i/D) / scale reduced modulo 2 pi in
-// double precision so that long contexts keep full accuracy -- and runs the
-// heads.
-// A lane holds 4 of a head's 128 values: the RMS is one warp reduction, and
-// NeoX pairs (i, i+64) sit in lanes l and l+16, one shuffle apart.
+// Memory bound: each token's fused QKV row (Hq + 2 Hkv heads of 256 bytes,
+// contiguous) is read once and Q, K and V rows are written once.  A CTA takes
+// a contiguous run of tokens.  Its loader warp streams each token's row into a
+// ring of shared-memory stages with one bulk copy, and while the copy is in
+// flight it resolves the token's sequence, validity and cache slot and the
+// (cos, sin) pairs of its position -- once per token, for all heads.  Eight
+// compute warps take the heads of the staged token (head w, w + 8, ...) and
+// write the results with coalesced stores.  Rows in flight per SM (the ring
+// depth times the resident CTAs) cover the HBM latency.
+//
+// The host computes the 64 frequencies in double precision.  The angle is
+// carried in turns (angle / 2 pi): pos times the frequency in turns as an
+// unevaluated float pair, whose product is exact up to the low
+// word's rounding, so the whole turns drop out exactly and the remainder in
+// [-1/2, 1/2] goes to sincospif.  Single precision throughout (the GPU's
+// double-precision rate is a small fraction of its float rate); positions
+// whose turn count leaves too few fraction bits take a double-precision path.
+//
+// A compute lane holds 4 of a head's 128 values: the RMS is one warp
+// reduction, and NeoX pairs (i, i+64) sit in lanes l and l+16, one shuffle
+// apart.
 #include "pa_launch.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kChunk = 8;  // heads per warp, all loaded before the token's slot is resolved
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = (kComputeWarps + 1) * 32;  // warp 0: loader
+constexpr int kMaxStages = 4;
+constexpr int kStageBudget = 200 * 1024;            // shared memory for the row ring
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+// per stage: the token's cache slot (-1: invalid sequence, nothing written)
+// and the cos / sin of its 64 rotary pairs
+struct StageInfo {
+  long long slot;
+  int32_t valid, pad;
+  float cs[2][64];
+};
 
 __device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
   const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
@@ -36,15 +60,48 @@ __device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
   return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
-__global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueParams p) {
-  extern __shared__ int32_t pro_smem[];
-  int32_t* off = pro_smem;                                 // [B] chunk offsets
-  int32_t* scratch = pro_smem + (p.chunk_lens ? p.B : 0);  // [kThreads]
-  __shared__ double freq[64];
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// contiguous global -> shared bulk copy (16-byte aligned, a multiple of 16 bytes)
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 3)
+    prologue_kernel(const __grid_constant__ PrologueParams p, int per_cta, int stages) {
+  extern __shared__ __align__(16) uint8_t pro_smem[];
+  const int heads = p.Hq + 2 * p.Hkv;
+  const uint32_t row_bytes = (uint32_t)heads * (kHeadDim * 2);
+  uint8_t* rows = pro_smem;                                           // [stages][row_bytes]
+  StageInfo* info = reinterpret_cast<StageInfo*>(rows + stages * row_bytes);  // [stages]
+  uint64_t* full = reinterpret_cast<uint64_t*>(info + stages);        // [stages]
+  uint64_t* empty = full + stages;                                    // [stages]
+  int32_t* off = reinterpret_cast<int32_t*>(empty + stages);          // [B] chunk offsets
+  int32_t* scratch = off + (p.chunk_lens ? p.B : 0);                  // [kThreads]
+  __shared__ double freq[64];                 // base^(-2i/D) / scale, radians per position
+  __shared__ float turn_hi[64], turn_lo[64];  // the same in turns, as hi + lo floats
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the 64 frequencies base^(-2i/D) / scale, once per CTA
-  if (threadIdx.x < 64)
-    freq[threadIdx.x] = exp2(-2.0 * threadIdx.x / kHeadDim * p.log2_base) / p.rope_scale;
+  if (threadIdx.x < 64) {
+    freq[threadIdx.x] = p.freq[threadIdx.x];
+    turn_hi[threadIdx.x] = p.turn_hi[threadIdx.x];
+    turn_lo[threadIdx.x] = p.turn_lo[threadIdx.x];
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 32);
+      mbar_init(&empty[i], kComputeWarps);
+    }
+    fence_mbar_init();
+  }
   if (p.chunk_lens) {
     const bool neg = block_chunk_offsets(p.chunk_lens, p.B, off, scratch);
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) {
@@ -54,99 +111,139 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueParams
   } else {
     __syncthreads();
   }
-  const int heads = p.Hq + 2 * p.Hkv;
-  const int chunks = (heads + kChunk - 1) / kChunk;  // head chunks per token
-  const int64_t units = (int64_t)p.T * chunks;
-  const int warps = gridDim.x * (kThreads / 32);
-  // a warp per (token, chunk of kChunk heads); lane l holds values 4l .. 4l+3 of each head
-  for (int64_t u = (int64_t)blockIdx.x * (kThreads / 32) + warp; u < units; u += warps) {
-    const int token = (int)(u / chunks);
-    const int h0 = (int)(u - (int64_t)token * chunks) * kChunk;
-    const int h1 = min(heads, h0 + kChunk);
-    const uint2* row = p.qkv + (int64_t)token * heads * (kHeadDim / 4);
-    // the chunk's rows load while the token's slot is resolved
-    uint2 raw[kChunk];
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k)
-      raw[k] = h0 + k < h1 ? __ldg(row + (h0 + k) * (kHeadDim / 4) + lane) : make_uint2(0u, 0u);
-    int s, j, n;
-    if (p.chunk_lens) {
-      s = seq_of_token(off, p.B, token);
-      j = s < p.B ? token - (s ? off[s - 1] : 0) : 0;
-      n = s < p.B ? p.chunk_lens[s] : 0;
-    } else {
-      s = token;
-      j = 0;
-      n = 1;
-    }
-    int err = PA_STATUS_BAD_TOKENS;  // a token past sum(chunk_lens): flagged above
-    int ctx = 0;
-    if (s < p.B) {
-      ctx = p.context_lens[s];
-      err = warp_check_sequence(p.block_table, s, ctx, n, p.num_pages, p.max_pages);
-      if (err && lane == 0 && p.status) atomicOr(p.status, err);
-    }
-    const bool valid = err == 0;
-    const int pos = valid ? ctx - n + j : 0;
-    const int64_t slot =
-        valid ? (int64_t)p.block_table[(int64_t)s * p.max_pages + pos / kPage] * kPage + pos % kPage
-              : 0;
-    // angles of pairs lane and lane + 32: pos * f_i reduced to [-pi, pi] in
-    // double precision (three operations; long contexts reach thousands of
-    // radians), then the single-precision sine and cosine of the remainder
-    constexpr double kTwoPi = 6.283185307179586476925286766559;
-    float c_lo, s_lo, c_hi, s_hi;
-    {
-      const double a0 = (double)pos * freq[lane], a1 = (double)pos * freq[lane + 32];
-      sincosf((float)fma(-rint(a0 * (1.0 / kTwoPi)), kTwoPi, a0), &s_lo, &c_lo);
-      sincosf((float)fma(-rint(a1 * (1.0 / kTwoPi)), kTwoPi, a1), &s_hi, &c_hi);
-    }
-    // this lane's values 4l .. 4l+3 belong to pair (4l .. 4l+3) mod 64
-    const int i0 = (lane & 15) * 4;
-    float cq[4], sq[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = i0 + e;
-      const float cl = __shfl_sync(0xffffffffu, c_lo, i & 31);
-      const float ch = __shfl_sync(0xffffffffu, c_hi, i & 31);
-      const float sl = __shfl_sync(0xffffffffu, s_lo, i & 31);
-      const float sh = __shfl_sync(0xffffffffu, s_hi, i & 31);
-      cq[e] = i < 32 ? cl : ch;
-      sq[e] = (i < 32 ? sl : sh) * (lane < 16 ? -1.f : 1.f);
-    }
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const int hh = h0 + k;
-      if (hh >= h1) break;
-      const uint2 w4 = raw[k];
-      if (hh >= p.Hq + p.Hkv) {  // V: copied bit for bit
-        if (valid) p.v_cache[(slot * p.Hkv + (hh - p.Hq - p.Hkv)) * (kHeadDim / 4) + lane] = w4;
-        continue;
+  const int t0 = blockIdx.x * per_cta, t1 = min(p.T, t0 + per_cta);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loader
+    const uint64_t pol = l2_policy_evict_first();  // each row is read once
+    const float gmax = fmaxf(turn_hi[0], turn_hi[63]);  // the frequencies are monotone in i
+    int last_s = -1, last_err = 0, last_ctx = 0, last_n = 0, pg = 0;
+    for (int token = t0, i = 0; token < t1; ++token, ++i) {
+      const int st = i % stages;
+      if (!mbar_wait_warp(&empty[st], ((i / stages) & 1) ^ 1, p.status)) break;
+      if (lane == 0) {
+        mbar_expect_tx(&full[st], row_bytes);
+        bulk_load(rows + st * row_bytes, reinterpret_cast<const uint8_t*>(p.qkv) +
+                  (int64_t)token * row_bytes, row_bytes, &full[st], pol);
       }
-      const bool is_q = hh < p.Hq;
-      const float4 x = bf16x4_to_float4(w4);
-      float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
-      const float4 w = __ldg(reinterpret_cast<const float4*>(is_q ? p.wq : p.wk) + lane);
-      const float4 y = make_float4(x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w);
-      // NeoX pairs (i, i + 64): lane l < 16 holds the first halves, l + 16 the second
-      const float4 z = make_float4(__shfl_xor_sync(0xffffffffu, y.x, 16),
-                                   __shfl_xor_sync(0xffffffffu, y.y, 16),
-                                   __shfl_xor_sync(0xffffffffu, y.z, 16),
-                                   __shfl_xor_sync(0xffffffffu, y.w, 16));
-      const float4 o = make_float4(fmaf(sq[0], z.x, y.x * cq[0]), fmaf(sq[1], z.y, y.y * cq[1]),
-                                   fmaf(sq[2], z.z, y.z * cq[2]), fmaf(sq[3], z.w, y.w * cq[3]));
-      if (is_q) {
-        // (an invalid sequence's rows are zero, like its attention output)
-        const float qs = p.q_scale;
-        p.q_out[((int64_t)token * p.Hq + hh) * (kHeadDim / 4) + lane] =
-            valid ? float4_to_bf16x4(make_float4(o.x * qs, o.y * qs, o.z * qs, o.w * qs))
-                  : make_uint2(0u, 0u);
-      } else if (valid) {
-        p.k_cache[(slot * p.Hkv + (hh - p.Hq)) * (kHeadDim / 4) + lane] = float4_to_bf16x4(o);
+      // the token's sequence and offset in its chunk
+      int s, j;
+      if (p.chunk_lens) {
+        s = seq_of_token(off, p.B, token);
+        j = s < p.B ? token - (s ? off[s - 1] : 0) : 0;
+      } else {
+        s = token;
+        j = 0;
       }
+      const int32_t* bt = p.block_table + (int64_t)s * p.max_pages;
+      if (s < p.B && s != last_s) {
+        // a new sequence: its length and first 32 block-table entries load
+        // together; then lengths and every referenced entry are checked
+        last_s = s;
+        last_n = p.chunk_lens ? off[s] - (s ? off[s - 1] : 0) : 1;
+        last_ctx = p.context_lens[s];
+        pg = lane < p.max_pages ? bt[lane] : 0;
+        const int ctx = last_ctx, n = last_n;
+        if (ctx < 0 || n > ctx || ctx > p.max_pages * kPage) {
+          last_err = PA_STATUS_BAD_LENGTH;
+        } else {
+          const int used = (ctx + kPage - 1) / kPage;
+          bool bad = lane < used && (pg < 0 || pg >= p.num_pages);
+          for (int e = lane + 32; e < used; e += 32) {
+            const int q = bt[e];
+            bad |= (q < 0 || q >= p.num_pages);
+          }
+          last_err = __any_sync(0xffffffffu, bad) ? PA_STATUS_BAD_PAGE : 0;
+        }
+        if (last_err && lane == 0 && p.status) atomicOr(p.status, last_err);
+      }
+      // a token past sum(chunk_lens) (flagged above) is invalid
+      const bool valid = s < p.B && last_err == 0;
+      const int pos = valid ? last_ctx - last_n + j : 0;
+      // the slot's page: from the entries loaded with the sequence when among them
+      const int pi = pos / kPage;
+      const int page_sh = __shfl_sync(0xffffffffu, pg, pi & 31);
+      StageInfo& in = info[st];
+      if (lane == 0) {
+        const int page = pi < 32 ? page_sh : (valid ? bt[pi] : 0);
+        in.slot = valid ? (long long)page * kPage + pos % kPage : -1ll;
+        in.valid = valid;
+      }
+      // angles of pairs lane and lane + 32, reduced to [-1/2, 1/2] turns
+      float c_lo, s_lo, c_hi, s_hi;
+      const float fpos = (float)pos;
+      if (pos < (1 << 24) && fpos * gmax < 4194304.f) {
+        // pos is exact in a float and pos * g < 2^22 turns: hi - rint(hi) is
+        // exact and the fraction keeps at least 2^-24 resolution
+        auto frac = [&](int q) {
+          const float hi = fpos * turn_hi[q];
+          const float lo = fmaf(fpos, turn_lo[q], fmaf(fpos, turn_hi[q], -hi));
+          return (hi - rintf(hi)) + lo;
+        };
+        sincospif(2.f * frac(lane), &s_lo, &c_lo);
+        sincospif(2.f * frac(lane + 32), &s_hi, &c_hi);
+      } else {
+        // very long positions: the product and its reduction in double precision
+        const double a0 = (double)pos * freq[lane], a1 = (double)pos * freq[lane + 32];
+        sincosf((float)fma(-rint(a0 * (1.0 / kTwoPi)), kTwoPi, a0), &s_lo, &c_lo);
+        sincosf((float)fma(-rint(a1 * (1.0 / kTwoPi)), kTwoPi, a1), &s_hi, &c_hi);
+      }
+      in.cs[0][lane] = c_lo;
+      in.cs[0][lane + 32] = c_hi;
+      in.cs[1][lane] = s_lo;
+      in.cs[1][lane + 32] = s_hi;
+      mbar_arrive(&full[st]);  // with the row's bytes, completes the stage
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int cw = warp - 1;
+    const float4 wq = __ldg(reinterpret_cast<const float4*>(p.wq) + lane);
+    const float4 wk = __ldg(reinterpret_cast<const float4*>(p.wk) + lane);
+    const int i0 = (lane & 15) * 4;  // this lane's values 4l .. 4l+3 belong to pairs i0 .. i0+3
+    const float sgn = lane < 16 ? -1.f : 1.f;
+    for (int token = t0, i = 0; token < t1; ++token, ++i) {
+      const int st = i % stages;
+      if (!mbar_wait_warp(&full[st], (i / stages) & 1, p.status)) break;
+      const StageInfo& in = info[st];
+      const long long slot = in.slot;
+      const bool valid = in.valid != 0;
+      const float4 cq = *reinterpret_cast<const float4*>(&in.cs[0][i0]);
+      float4 sq = *reinterpret_cast<const float4*>(&in.cs[1][i0]);
+      sq = make_float4(sq.x * sgn, sq.y * sgn, sq.z * sgn, sq.w * sgn);
+      const uint2* row = reinterpret_cast<const uint2*>(rows + st * row_bytes);
+      for (int hh = cw; hh < heads; hh += kComputeWarps) {
+        const uint2 w4 = row[hh * (kHeadDim / 4) + lane];
+        if (hh >= p.Hq + p.Hkv) {  // V: copied bit for bit
+          if (valid) p.v_cache[(slot * p.Hkv + (hh - p.Hq - p.Hkv)) * (kHeadDim / 4) + lane] = w4;
+          continue;
+        }
+        const bool is_q = hh < p.Hq;
+        const float4 x = bf16x4_to_float4(w4);
+        float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
+        const float4 w = is_q ? wq : wk;
+        const float4 y = make_float4(x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w);
+        // NeoX pairs (i, i + 64): lane l < 16 holds the first halves, l + 16 the second
+        const float4 z = make_float4(__shfl_xor_sync(0xffffffffu, y.x, 16),
+                                     __shfl_xor_sync(0xffffffffu, y.y, 16),
+                                     __shfl_xor_sync(0xffffffffu, y.z, 16),
+                                     __shfl_xor_sync(0xffffffffu, y.w, 16));
+        const float4 o = make_float4(fmaf(sq.x, z.x, y.x * cq.x), fmaf(sq.y, z.y, y.y * cq.y),
+                                     fmaf(sq.z, z.z, y.z * cq.z), fmaf(sq.w, z.w, y.w * cq.w));
+        if (is_q) {
+          // (an invalid sequence's rows are zero, like its attention output)
+          const float qs = p.q_scale;
+          p.q_out[((int64_t)token * p.Hq + hh) * (kHeadDim / 4) + lane] =
+              valid ? float4_to_bf16x4(make_float4(o.x * qs, o.y * qs, o.z * qs, o.w * qs))
+                    : make_uint2(0u, 0u);
+        } else if (valid) {
+          p.k_cache[(slot * p.Hkv + (hh - p.Hq)) * (kHeadDim / 4) + lane] = float4_to_bf16x4(o);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
   }
 }
@@ -155,18 +252,29 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const PrologueParams
 
 cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
-  const int64_t units = (int64_t)p.T * ((p.Hq + 2 * p.Hkv + kChunk - 1) / kChunk);
-  int64_t blocks64 = (units + kThreads / 32 - 1) / (kThreads / 32);
-  int blocks = (int)(blocks64 < INT32_MAX ? blocks64 : INT32_MAX);
-  const int cap = num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  const size_t smem = p.chunk_lens ? (size_t)(p.B + kThreads) * sizeof(int32_t) : 0;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(prologue_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  prologue_kernel<<<blocks, kThreads, smem, stream>>>(p);
+  const size_t row_bytes = (size_t)(p.Hq + 2 * p.Hkv) * kHeadDim * 2;
+  int stages = (int)(kStageBudget / (row_bytes + sizeof(StageInfo)));
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 1) stages = 1;
+  const size_t smem = stages * (row_bytes + sizeof(StageInfo) + 2 * sizeof(uint64_t)) +
+                      (p.chunk_lens ? (size_t)(p.B + kThreads) * sizeof(int32_t) : 0);
+  int max_smem = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (smem + 2048 > (size_t)max_smem) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  // resident CTAs per SM by shared memory (at most the 3 the registers allow)
+  int per_sm = (int)((228 * 1024) / (smem + 2048));
+  if (per_sm > 3) per_sm = 3;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t slots = (int64_t)num_sms * per_sm;
+  const int per_cta = (int)((p.T + slots - 1) / slots);
+  const int blocks = (p.T + per_cta - 1) / per_cta;
+  prologue_kernel<<<blocks, kThreads, smem, stream>>>(p, per_cta, stages);
   return cudaGetLastError();
 }
 

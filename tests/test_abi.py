@@ -53,11 +53,12 @@ def test_python_constants_match_header(pa):
     assert h["PA_SPLITS_BALANCED"] == pa.PA_SPLITS_BALANCED
     assert h["PA_BALANCED_MAX_SEQS"] == pa.PA_BALANCED_MAX_SEQS
     assert h["PA_MAX_Q_LEN"] == pa.PA_MAX_Q_LEN
+    assert h["PA_MAX_PROLOGUE_HEADS"] == pa.PA_MAX_PROLOGUE_HEADS
     assert h["PA_STATUS_Q_RANGE"] == pa.PA_STATUS_Q_RANGE
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
-    assert pa.pa_abi_version() == 104
+    assert pa.pa_abi_version() == 105
 
 
 def test_status_strings(pa):
@@ -122,6 +123,9 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert pro(qkv=None) == h["PA_ERR_NULL_POINTER"]
     assert pro(qkv=MIS) == h["PA_ERR_ALIGNMENT"]
     assert pro(n=0, cl=FAKE) == 0
+    wide = _dims(pa, num_q_heads=352, num_kv_heads=32)  # G = 11, 416 heads in a row
+    assert lib.pa_qk_norm_rope_write(FAKE, FAKE, FAKE, 1e-6, 1e6, 1.0, 1.0, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, None, 2, wide, None, None) == h["PA_ERR_HEADS"]
     tk = lambda rows=2, vocab=100, k=8, stride=100, ptr=FAKE: lib.pa_topk(
         ptr, stride, rows, vocab, k, FAKE, FAKE, FAKE, 1 << 20, None)
     assert tk(k=0) == h["PA_ERR_DIMS"] and tk(k=33) == h["PA_ERR_DIMS"]
