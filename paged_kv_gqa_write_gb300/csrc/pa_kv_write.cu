@@ -5,7 +5,8 @@
 // (TensorSharp), section 11: ScatterKv writes each token at slot
 // blockId * blockSize + offset.  A pure byte copy, bound by launch latency at
 // decode sizes and by HBM at prefill sizes: one warp per token moves the
-// token's Hkv*256-byte K row and V row with 16-byte accesses.
+// token's Hkv*256-byte K row and V row with 16-byte accesses, issuing the row
+// loads before it resolves the token's slot so the two latencies overlap.
 //
 // The FP8 variant quantizes instead of copying (an "fp8_e4m3" KV cache, as in
 // the SGLang measurement quoted by the "Qwen4-Exp QSA trafia na Ascend..."
@@ -54,50 +55,66 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
   }
   const int warps_per_block = blockDim.x >> 5;
   const int row_chunks = p.Hkv * (kHeadDim * 2 / 16);  // 16-byte chunks per token row
+  // output chunks per row: a bf16 chunk is copied, an FP8 chunk takes two inputs
+  const int out_chunks = FP8 ? row_chunks / 2 : row_chunks;
+  constexpr int kIn = FP8 ? 2 : 1;   // input chunks per output chunk
+  constexpr int kU = FP8 ? 2 : 4;    // output chunks per lane in flight
   for (int token = blockIdx.x * warps_per_block + (threadIdx.x >> 5); token < p.T;
        token += gridDim.x * warps_per_block) {
-    int s, j, n;
-    if (p.chunk_lens) {
-      s = seq_of_token(off, p.B, token);
-      if (s >= p.B) continue;  // more tokens than sum(chunk_lens): flagged above
-      j = token - (s ? off[s - 1] : 0);
-      n = p.chunk_lens[s];
-    } else {
-      s = token;
-      j = 0;
-      n = 1;
-    }
-    const int ctx = p.context_lens[s];
-    const int err = warp_check_sequence(p.block_table, s, ctx, n, p.num_pages, p.max_pages);
-    if (err) {
-      if (lane == 0 && p.status) atomicOr(p.status, err);
-      continue;
-    }
-    const int pos = ctx - n + j;
-    const int page = p.block_table[(int64_t)s * p.max_pages + pos / kPage];
-    const int64_t slot = (int64_t)page * kPage + pos % kPage;
     const uint4* ks = p.k_new + (int64_t)token * row_chunks;
     const uint4* vs = p.v_new + (int64_t)token * row_chunks;
-    if constexpr (FP8) {
-      // 16 elements (32 input bytes, 16 output bytes) per step
-      uint4* kd = p.k_cache + slot * (row_chunks / 2);
-      uint4* vd = p.v_cache + slot * (row_chunks / 2);
-      for (int c = lane; c < row_chunks / 2; c += 32) {
-        const int h = c / (kHeadDim / 16);
-        const float sk = __ldg(p.k_scale + h), sv = __ldg(p.v_scale + h);
-        const uint4 k0 = __ldg(ks + 2 * c), k1 = __ldg(ks + 2 * c + 1);
-        const uint4 v0 = __ldg(vs + 2 * c), v1 = __ldg(vs + 2 * c + 1);
-        kd[c] = quantize16(k0, k1, sk);
-        vd[c] = quantize16(v0, v1, sv);
+    int64_t slot = -1;  // resolved while the first rows load
+    for (int c0 = 0; c0 < out_chunks; c0 += 32 * kU) {
+      uint4 a[kU][kIn], b[kU][kIn];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < out_chunks) {
+#pragma unroll
+          for (int e = 0; e < kIn; ++e) {
+            a[u][e] = __ldg(ks + kIn * c + e);
+            b[u][e] = __ldg(vs + kIn * c + e);
+          }
+        }
       }
-    } else {
-      uint4* kd = p.k_cache + slot * row_chunks;
-      uint4* vd = p.v_cache + slot * row_chunks;
-      for (int c = lane; c < row_chunks; c += 32) {
-        uint4 a = __ldg(ks + c);
-        uint4 b = __ldg(vs + c);
-        kd[c] = a;
-        vd[c] = b;
+      if (c0 == 0) {
+        int s, j, n;
+        if (p.chunk_lens) {
+          s = seq_of_token(off, p.B, token);
+          if (s >= p.B) break;  // more tokens than sum(chunk_lens): flagged above
+          j = token - (s ? off[s - 1] : 0);
+          n = p.chunk_lens[s];
+        } else {
+          s = token;
+          j = 0;
+          n = 1;
+        }
+        const int ctx = p.context_lens[s];
+        const int err = warp_check_sequence(p.block_table, s, ctx, n, p.num_pages, p.max_pages);
+        if (err) {
+          if (lane == 0 && p.status) atomicOr(p.status, err);
+          break;
+        }
+        const int pos = ctx - n + j;
+        const int page = p.block_table[(int64_t)s * p.max_pages + pos / kPage];
+        slot = (int64_t)page * kPage + pos % kPage;
+      }
+      uint4* kd = p.k_cache + slot * out_chunks;
+      uint4* vd = p.v_cache + slot * out_chunks;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < out_chunks) {
+          if constexpr (FP8) {
+            // 16 elements (32 input bytes, 16 output bytes) per chunk
+            const int h = c / (kHeadDim / 16);
+            kd[c] = quantize16(a[u][0], a[u][1], __ldg(p.k_scale + h));
+            vd[c] = quantize16(b[u][0], b[u][1], __ldg(p.v_scale + h));
+          } else {
+            kd[c] = a[u][0];
+            vd[c] = b[u][0];
+          }
+        }
       }
     }
   }

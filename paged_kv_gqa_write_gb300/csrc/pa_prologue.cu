@@ -17,9 +17,10 @@
 // ring of shared-memory stages with one bulk copy, and while the copy is in
 // flight it resolves the token's sequence, validity and cache slot and the
 // (cos, sin) pairs of its position -- once per token, for all heads.  Eight
-// compute warps take the heads of the staged token (head w, w + 8, ...) and
-// write the results with coalesced stores.  Rows in flight per SM (the ring
-// depth times the resident CTAs) cover the HBM latency.
+// compute warps take the staged token's Q and K heads, two per warp at a time,
+// and write the results with coalesced stores; the V rows leave the stage with
+// one bulk store.  Rows in flight per SM (the ring depth times the resident
+// CTAs) cover the HBM latency.
 //
 // The host computes the 64 frequencies in double precision.  The angle is
 // carried in turns (angle / 2 pi): pos times the frequency in turns as an
@@ -29,9 +30,9 @@
 // double-precision rate is a small fraction of its float rate); positions
 // whose turn count leaves too few fraction bits take a double-precision path.
 //
-// A compute lane holds 4 of a head's 128 values: the RMS is one warp
-// reduction, and NeoX pairs (i, i+64) sit in lanes l and l+16, one shuffle
-// apart.
+// A compute lane holds 8 of a head's 128 values, both members of four NeoX
+// pairs (i, i+64): the RMS is a 16-lane reduction and the rotation needs no
+// data from other lanes.
 #include "pa_launch.cuh"
 
 namespace pa {
@@ -196,55 +197,75 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int cw = warp - 1;
-    const float4 wq = __ldg(reinterpret_cast<const float4*>(p.wq) + lane);
-    const float4 wk = __ldg(reinterpret_cast<const float4*>(p.wk) + lane);
-    const int i0 = (lane & 15) * 4;  // this lane's values 4l .. 4l+3 belong to pairs i0 .. i0+3
-    const float sgn = lane < 16 ? -1.f : 1.f;
+    // Half-warp h of a warp takes head 2m + h of the token's Q and K heads
+    // (pair m = cw, cw + 8, ...).  Its lane li holds values i0 .. i0+3 and
+    // i0+64 .. i0+67 (i0 = 4 li): each NeoX pair (i, i + 64) in one lane.
+    const int cw = warp - 1, hl = lane >> 4, li = lane & 15, i0 = 4 * li;
+    const float4 wq_lo = __ldg(reinterpret_cast<const float4*>(p.wq + i0));
+    const float4 wq_hi = __ldg(reinterpret_cast<const float4*>(p.wq + i0 + 64));
+    const float4 wk_lo = __ldg(reinterpret_cast<const float4*>(p.wk + i0));
+    const float4 wk_hi = __ldg(reinterpret_cast<const float4*>(p.wk + i0 + 64));
+    const int nqk = p.Hq + p.Hkv;
     for (int token = t0, i = 0; token < t1; ++token, ++i) {
       const int st = i % stages;
       if (!mbar_wait_warp(&full[st], (i / stages) & 1, p.status)) break;
       const StageInfo& in = info[st];
       const long long slot = in.slot;
       const bool valid = in.valid != 0;
-      const float4 cq = *reinterpret_cast<const float4*>(&in.cs[0][i0]);
-      float4 sq = *reinterpret_cast<const float4*>(&in.cs[1][i0]);
-      sq = make_float4(sq.x * sgn, sq.y * sgn, sq.z * sgn, sq.w * sgn);
-      const uint2* row = reinterpret_cast<const uint2*>(rows + st * row_bytes);
-      for (int hh = cw; hh < heads; hh += kComputeWarps) {
-        const uint2 w4 = row[hh * (kHeadDim / 4) + lane];
-        if (hh >= p.Hq + p.Hkv) {  // V: copied bit for bit
-          if (valid) p.v_cache[(slot * p.Hkv + (hh - p.Hq - p.Hkv)) * (kHeadDim / 4) + lane] = w4;
-          continue;
-        }
-        const bool is_q = hh < p.Hq;
-        const float4 x = bf16x4_to_float4(w4);
-        float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
-        const float4 w = is_q ? wq : wk;
-        const float4 y = make_float4(x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w);
-        // NeoX pairs (i, i + 64): lane l < 16 holds the first halves, l + 16 the second
-        const float4 z = make_float4(__shfl_xor_sync(0xffffffffu, y.x, 16),
-                                     __shfl_xor_sync(0xffffffffu, y.y, 16),
-                                     __shfl_xor_sync(0xffffffffu, y.z, 16),
-                                     __shfl_xor_sync(0xffffffffu, y.w, 16));
-        const float4 o = make_float4(fmaf(sq.x, z.x, y.x * cq.x), fmaf(sq.y, z.y, y.y * cq.y),
-                                     fmaf(sq.z, z.z, y.z * cq.z), fmaf(sq.w, z.w, y.w * cq.w));
-        if (is_q) {
-          // (an invalid sequence's rows are zero, like its attention output)
-          const float qs = p.q_scale;
-          p.q_out[((int64_t)token * p.Hq + hh) * (kHeadDim / 4) + lane] =
-              valid ? float4_to_bf16x4(make_float4(o.x * qs, o.y * qs, o.z * qs, o.w * qs))
-                    : make_uint2(0u, 0u);
-        } else if (valid) {
-          p.k_cache[(slot * p.Hkv + (hh - p.Hq)) * (kHeadDim / 4) + lane] = float4_to_bf16x4(o);
-        }
+      const uint8_t* row = rows + st * row_bytes;
+      // V is copied bit for bit: one bulk store of the token's Hkv V rows,
+      // which are contiguous in the staged row and in the cache slot
+      const bool v_store = cw == 0 && lane == 0 && valid;
+      if (v_store) {
+        asm volatile(
+            "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+            "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(
+                reinterpret_cast<uint8_t*>(p.v_cache) + slot * p.Hkv * (kHeadDim * 2))),
+            "r"(smem_u32(row + nqk * (kHeadDim * 2))), "r"((uint32_t)p.Hkv * (kHeadDim * 2))
+            : "memory");
       }
+      const float4 c4 = *reinterpret_cast<const float4*>(&in.cs[0][i0]);
+      const float4 s4 = *reinterpret_cast<const float4*>(&in.cs[1][i0]);
+      for (int m = cw; 2 * m < nqk; m += kComputeWarps) {
+        const int hh = 2 * m + hl;
+        const bool live = hh < nqk;
+        const uint8_t* hrow = row + (live ? hh : 0) * (kHeadDim * 2);
+        const uint2 ra = *reinterpret_cast<const uint2*>(hrow + 8 * li);
+        const uint2 rb = *reinterpret_cast<const uint2*>(hrow + 128 + 8 * li);
+        const float4 xa = bf16x4_to_float4(ra), xb = bf16x4_to_float4(rb);
+        float ss = xa.x * xa.x + xa.y * xa.y + xa.z * xa.z + xa.w * xa.w +
+                   xb.x * xb.x + xb.y * xb.y + xb.z * xb.z + xb.w * xb.w;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const bool is_q = hh < p.Hq;
+        const float sc = rsqrtf(ss * (1.f / kHeadDim) + p.eps) * (is_q ? p.q_scale : 1.f);
+        const float4 wa = is_q ? wq_lo : wk_lo, wb = is_q ? wq_hi : wk_hi;
+        const float4 ta = make_float4(xa.x * wa.x, xa.y * wa.y, xa.z * wa.z, xa.w * wa.w);
+        const float4 tb = make_float4(xb.x * wb.x, xb.y * wb.y, xb.z * wb.z, xb.w * wb.w);
+        // (x_i, x_{i+64}) -> (x_i cos - x_{i+64} sin, x_{i+64} cos + x_i sin), times the scale
+        const float4 oa = make_float4(fmaf(ta.x, c4.x, -tb.x * s4.x) * sc, fmaf(ta.y, c4.y, -tb.y * s4.y) * sc,
+                                      fmaf(ta.z, c4.z, -tb.z * s4.z) * sc, fmaf(ta.w, c4.w, -tb.w * s4.w) * sc);
+        const float4 ob = make_float4(fmaf(tb.x, c4.x, ta.x * s4.x) * sc, fmaf(tb.y, c4.y, ta.y * s4.y) * sc,
+                                      fmaf(tb.z, c4.z, ta.z * s4.z) * sc, fmaf(tb.w, c4.w, ta.w * s4.w) * sc);
+        if (!live) continue;
+        uint2* dst;
+        if (is_q) {
+          dst = p.q_out + ((int64_t)token * p.Hq + hh) * (kHeadDim / 4);
+        } else {
+          if (!valid) continue;
+          dst = p.k_cache + (slot * p.Hkv + (hh - p.Hq)) * (kHeadDim / 4);
+        }
+        // (an invalid sequence's Q rows are zero, like its attention output)
+        dst[li] = valid ? float4_to_bf16x4(oa) : make_uint2(0u, 0u);
+        dst[16 + li] = valid ? float4_to_bf16x4(ob) : make_uint2(0u, 0u);
+      }
+      // the V store must have read the stage before it is refilled
+      if (v_store) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
+    // the V stores complete before the CTA exits
+    if (cw == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 }
 
