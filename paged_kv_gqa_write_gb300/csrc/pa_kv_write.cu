@@ -83,20 +83,36 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
           s = seq_of_token(off, p.B, token);
           if (s >= p.B) break;  // more tokens than sum(chunk_lens): flagged above
           j = token - (s ? off[s - 1] : 0);
-          n = p.chunk_lens[s];
+          n = off[s] - (s ? off[s - 1] : 0);  // the token's sequence has n >= 1 tokens
         } else {
           s = token;
           j = 0;
           n = 1;
         }
+        // the context length and the first 32 block-table entries load together
+        const int32_t* bt = p.block_table + (int64_t)s * p.max_pages;
         const int ctx = p.context_lens[s];
-        const int err = warp_check_sequence(p.block_table, s, ctx, n, p.num_pages, p.max_pages);
+        const int pg = lane < p.max_pages ? bt[lane] : 0;
+        int err = 0;
+        if (ctx < 0 || n > ctx || ctx > p.max_pages * kPage) {
+          err = PA_STATUS_BAD_LENGTH;
+        } else {
+          const int used = (ctx + kPage - 1) / kPage;
+          bool bad = lane < used && (pg < 0 || pg >= p.num_pages);
+          for (int e = lane + 32; e < used; e += 32) {
+            const int q = bt[e];
+            bad |= (q < 0 || q >= p.num_pages);
+          }
+          err = __any_sync(0xffffffffu, bad) ? PA_STATUS_BAD_PAGE : 0;
+        }
         if (err) {
           if (lane == 0 && p.status) atomicOr(p.status, err);
           break;
         }
         const int pos = ctx - n + j;
-        const int page = p.block_table[(int64_t)s * p.max_pages + pos / kPage];
+        const int pi = pos / kPage;
+        const int page_sh = __shfl_sync(0xffffffffu, pg, pi & 31);
+        const int page = pi < 32 ? page_sh : bt[pi];
         slot = (int64_t)page * kPage + pos % kPage;
       }
       uint4* kd = p.k_cache + slot * out_chunks;
