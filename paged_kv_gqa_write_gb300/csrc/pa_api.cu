@@ -16,7 +16,7 @@ using pa::kHeadDim;
 using pa::kPage;
 
 constexpr int kMaxGroup = 16;    // query heads per KV head
-constexpr int kMaxColumns = 16;  // (token, query head) columns of one decode work item
+constexpr int kMaxColumns = 32;  // (token, query head) columns of one decode work item
 
 int check_dims(const pa_dims& d) {
   if (d.head_dim != kHeadDim) return PA_ERR_HEAD_DIM;
@@ -34,7 +34,7 @@ int check_dims(const pa_dims& d) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Token groups of a decode step with L new tokens per sequence: a work item
-// takes Lg tokens x G query heads <= 16 MMA columns.  NT = the fewest groups
+// takes Lg tokens x G query heads <= 32 MMA columns.  NT = the fewest groups
 // that fit, Lg = the tokens of the largest (groups as even as possible).
 void token_groups(int G, int L, int* NT, int* Lg) {
   const int per = kMaxColumns / G;  // >= 1 (G <= 16)
@@ -111,12 +111,15 @@ size_t workspace_bytes_for(const pa_dims& d, int L, int splits) {
   return align256(rows * splits * kHeadDim * sizeof(float)) + align256(rows * splits * sizeof(float));
 }
 
-// Partial records of the page-balanced schedule: two per decode CTA, 16 head
-// slots of 128 floats plus the lse.
+// Partial records of the page-balanced schedule: two per decode CTA, up to
+// kMaxColumns column slots of 128 floats plus the lse.
 size_t balanced_ws_bytes(int grid) {
-  return align256((size_t)2 * grid * 16 * kHeadDim * sizeof(float)) +
-         align256((size_t)2 * grid * 16 * sizeof(float));
+  return align256((size_t)2 * grid * kMaxColumns * kHeadDim * sizeof(float)) +
+         align256((size_t)2 * grid * kMaxColumns * sizeof(float));
 }
+
+// Record columns of the decode kernel for items of gc columns: the MMA width.
+int record_columns(int gc) { return gc > 16 ? 32 : 16; }
 
 // Units (KV head x token group) per sequence; the page-balanced schedule runs
 // groups of that many CTAs.
@@ -337,7 +340,8 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
   p.grid = pl.grid;
   p.bal_o = pl.balanced ? reinterpret_cast<float*>(ws) : nullptr;
   p.bal_lse = pl.balanced ? reinterpret_cast<float*>(
-                                ws + align256((size_t)2 * pl.grid * 16 * kHeadDim * sizeof(float)))
+                                ws + align256((size_t)2 * pl.grid * kMaxColumns * kHeadDim *
+                                              sizeof(float)))
                           : nullptr;
   cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G * Lg, sms, st);
   if (e != cudaSuccess) return launch_result(e);
@@ -355,6 +359,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
     c.NT = NT;
     c.Lg = Lg;
     c.grid = pl.grid;
+    c.NC = record_columns(G * Lg);
     c.out_f32 = p.out_f32;
     return launch_result(pa::launch_bal_combine(c, st));
   }

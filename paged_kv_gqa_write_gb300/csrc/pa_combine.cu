@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
       const int gg = g0 + lane;
       const int lo = gg < ng ? sh_lo[gg] : INT32_MAX, hi = gg < ng ? sh_lo[gg + 1] : INT32_MAX;
       const bool has = gg < ng && lo < P + n && lo != hi;
-      const float v = has ? p.bal_lse[(2 * (gg * UPS + j) + (P <= lo ? 0 : 1)) * 16 + g] : -INFINITY;
+      const float v = has ? p.bal_lse[(2 * (gg * UPS + j) + (P <= lo ? 0 : 1)) * p.NC + g] : -INFINITY;
       inval |= v == INFINITY;
       M = fmaxf(M, v);
       if (!__any_sync(0xffffffffu, gg < ng && lo < P + n)) break;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
         const int lo = gg < ng ? sh_lo[gg] : INT32_MAX, hi = gg < ng ? sh_lo[gg + 1] : INT32_MAX;
         const bool has = gg < ng && lo < P + n && lo != hi;
         const int rec = 2 * (gg * UPS + j) + (P <= lo ? 0 : 1);
-        const float v = has ? p.bal_lse[rec * 16 + g] : -INFINITY;
+        const float v = has ? p.bal_lse[rec * p.NC + g] : -INFINITY;
         const float w = v == -INFINITY ? 0.f : expf(v - M);
         Lsum += w;
         unsigned mk = __ballot_sync(0xffffffffu, w != 0.f);
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
           const float wk = __shfl_sync(0xffffffffu, w, k);
           const int rk = __shfl_sync(0xffffffffu, rec, k);
           const float4 x =
-              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)rk * 16 + g) * kHeadDim)[lane];
+              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)rk * p.NC + g) * kHeadDim)[lane];
           acc.x = fmaf(wk, x.x, acc.x);
           acc.y = fmaf(wk, x.y, acc.y);
           acc.z = fmaf(wk, x.z, acc.z);

@@ -487,6 +487,7 @@ struct BalCombineParams {
   int32_t B, Hq, G, max_pages;
   int32_t L, NT, Lg;            // new tokens per sequence, token groups, tokens per group
   int32_t grid;                 // CTAs of the decode launch
+  int32_t NC;                   // column slots per record (the decode kernel's MMA width)
   int32_t out_f32;
 };
 

@@ -12,20 +12,22 @@
 // Design (GB300; HBM bound: every K/V byte is read once):
 //  * Persistent grid, one CTA per SM.  A work item is (split j, sequence s,
 //    KV head h, token group): a contiguous range of at most `pps` pages and
-//    the GC = Lg * G <= 16 (token, query head) columns of the G query heads
+//    the GC = Lg * G <= 32 (token, query head) columns of the G query heads
 //    that share the KV head, for Lg of the sequence's L new tokens (L = 1:
-//    the plain decode, one column per head).  Items are dealt round-robin;
+//    the plain decode, one column per head).  With several new tokens the
+//    columns of all of them share each K/V page as long as they fit, so the
+//    pages are read once per KV head, not once per token.  Items are dealt round-robin;
 //    split boundaries depend only on logical positions.
 //  * Per page the two products are transposed so that the 128 keys (or the
-//    128 head dims) fill the 128 rows of one tcgen05.mma and the query heads,
-//    padded to 16, are its N:
+//    128 head dims) fill the 128 rows of one tcgen05.mma and the columns,
+//    padded to 16 or 32, are its N:
 //      S^T[key][g] = K[key][:] . Q[g][:]        (A = K tile, K-major)
 //      O^T[d][g]  += V[:][d] . P[g][:]          (A = V tile, MN-major)
 //    so the K/V tiles are read by the tensor core straight from the TMA ring
 //    (128-byte swizzle), and the FP32 pipes only run the softmax.
 //  * warp 0: validates each item's block-table range (the next item's
 //    metadata is loaded while the current item's pages are issued), stages
-//    up to four items ahead, TMA-loads each item's query rows (G heads, or a
+//    up to four items ahead (two with 32 columns), TMA-loads each item's query rows (G heads, or a
 //    3-D box of Lg tokens x G heads; rows past it stay zero) and its K/V page
 //    tiles into a 3-stage ring of 64 KB (K and V complete on separate
 //    mbarriers, so QK^T starts while V is in flight).
@@ -62,12 +64,8 @@ constexpr int kMmaWarp = 1;
 constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
 constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
 constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert, one thread per key row
-constexpr int kSlots = 4;                  // item slots: how far the TMA warp runs ahead
 constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
-constexpr int kN = 16;                     // MMA N: query heads of an item, padded
-constexpr int kAtom = kN * 128;            // 16 rows x 128 bytes
-constexpr int kOpBytes = 2 * kAtom;        // Q or P operand: two 64-element atoms
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -80,6 +78,16 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kBox8 = 128 * kPage;         // 128 one-byte dims x 128 tokens = 16 KB
 template <bool FP8, int NH = 16>
 struct Layout {
+  // MMA N: the item's (token, query head) columns, padded to 16 or 32
+  static constexpr int kN = NH > 16 ? 32 : 16;
+  static constexpr int kAtom = kN * 128;     // kN rows x 128 bytes
+  static constexpr int kOpBytes = 2 * kAtom; // Q or P operand: two 64-element atoms
+  // item slots: how far the TMA warp runs ahead (two with the wide operands,
+  // which the shared-memory budget allows no more of)
+  static constexpr int kSlots = kN == 32 ? 2 : 4;
+  // tensor-memory columns: S^T[2] and O^T[2], kN each; FP8: K[2] as F16
+  // pairs, 64 columns each (lane = key)
+  static constexpr uint32_t kColS = 0, kColO = 2 * kN, kColK = 4 * kN;
   // operand stages: bf16 K lo, K hi, V lo, V hi; FP8 V lo, V hi (K is in TMEM)
   static constexpr int kStages = FP8 ? 2 : 3;
   static constexpr int kStageBytes = FP8 ? 2 * kBox : 4 * kBox;
@@ -90,25 +98,33 @@ struct Layout {
   static constexpr int kThreads = (10 + kConvWarps) * 32;
   static constexpr int kRing = 0;
   static constexpr int kRing8 = kRing + kStages * kStageBytes;
-  static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;  // FP8: + two 64-column K buffers
+  static constexpr uint32_t kTmemCols = FP8 ? 256 : 4 * kN;  // FP8: + two 64-column K buffers
   static constexpr int kQ = kRing8 + kStages8 * 2 * kBox8;  // [kSlots] query operands
   static constexpr int kP = kQ + kSlots * kOpBytes;         // P operands [2]
-  static constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][16]: softmax exchange
-  static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][16][2]: (m, l) per O
+  static constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][kN]: softmax exchange
+  static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][kN][2]: (m, l) per O
   static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][8]: item records
   static constexpr int kBars = kInfo + kSlots * 8 * 4;
   static constexpr int kNumBars =
-      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1;
+      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
+      (kN == 32 ? 2 : 0);  // 32 columns: a second pair of exchange slots
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 };
 constexpr int kSmemLimit = 232448;
 static_assert(Layout<false>::kSmem <= kSmemLimit, "decode shared memory exceeds the limit");
 static_assert(Layout<true>::kSmem <= kSmemLimit, "FP8 decode shared memory exceeds the limit");
+static_assert(Layout<false, 32>::kSmem <= kSmemLimit, "wide decode shared memory exceeds the limit");
+static_assert(Layout<true, 32>::kSmem <= kSmemLimit, "wide FP8 decode shared memory exceeds the limit");
 
-// TMEM columns
-constexpr uint32_t kColS = 0;   // S^T[2]: 16 columns each (page parity)
-constexpr uint32_t kColO = 32;  // O^T[2]: 16 columns each (item parity)
-constexpr uint32_t kColK = 64;  // FP8: K[2] as F16 pairs, 64 columns each (lane = key)
+// TMEM loads and stores of one lane's kN columns
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 32) tmem_st32(taddr, r); else tmem_st16(taddr, r);
+}
 
 struct Bars {
   uint64_t* k_full;    // [kStages] operand page: K ready (TMA, or the FP8 converters)
@@ -201,7 +217,7 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4& lo, uint4& hi) {
   e4m3x4_to_f16x4(c.w, hi.z, hi.w);
 }
 
-// NH: columns the softmax and epilogue handle (8 or 16, >= any item's GC).
+// NH: columns the softmax and epilogue handle (8, 16 or 32, >= any item's GC).
 // FP8: the cache holds e4m3 codes with per-KV-head scales.  MULTI: more than
 // one new token per sequence (per-column causal masks, (token, head) columns);
 // without it every column is a query head that sees the whole context.
@@ -217,6 +233,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   constexpr int kRing = Lay::kRing, kRing8 = Lay::kRing8, kQ = Lay::kQ, kP = Lay::kP;
   constexpr int kX = Lay::kX, kML = Lay::kML, kInfo = Lay::kInfo, kBars = Lay::kBars;
   constexpr int kNumBars = Lay::kNumBars, kThreads = Lay::kThreads;
+  constexpr int kN = Lay::kN, kAtom = Lay::kAtom, kOpBytes = Lay::kOpBytes, kSlots = Lay::kSlots;
+  constexpr uint32_t kColS = Lay::kColS, kColO = Lay::kColO, kColK = Lay::kColK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,7 +255,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   B.o_free = B.o_full + 2;
   B.ml_full = B.o_free + 2;
   B.x_full = B.ml_full + 2;
-  B.mma_done = B.x_full + 2;
+  B.mma_done = B.x_full + (kN == 32 ? 4 : 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
   int* info = reinterpret_cast<int*>(smem + kInfo);
 
@@ -259,15 +277,17 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       // MMA, 4 softmax warps, 4 epilogue warps (, the converter warps)
       mbar_init(&B.q_empty[i], 1 + 4 + 4 + kConvWarps);
     }
+    // 32 columns: two groups of 128 softmax threads, each also its columns' epilogue
+    constexpr uint32_t kColThreads = kN == 32 ? 256 : 128;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.o_full[i], 1);
-      mbar_init(&B.o_free[i], 128);
+      mbar_init(&B.o_free[i], kColThreads);
       mbar_init(&B.ml_full[i], 1);
-      mbar_init(&B.x_full[i], 4);
     }
+    for (int i = 0; i < (kN == 32 ? 4 : 2); ++i) mbar_init(&B.x_full[i], 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], 128);
+      mbar_init(&B.p_full[i], kColThreads);
     }
     mbar_init(B.pv_done, 1);
     mbar_init(B.mma_done, 1);
@@ -729,6 +749,231 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         }
       }
     }
+  } else if (kN == 32) {
+    // ------------------------------------------------------------ 32 columns: softmax + epilogue
+    // Warps 2-5 take columns 0-15, warps 6-9 columns 16-31, each group as the
+    // 16-column softmax does (thread = key, its own exchange slots), and at
+    // the item's end the same threads (thread = head dim) write their
+    // columns' outputs.
+    const int sg = (warp - kSoftWarp0) >> 2;  // column group
+    const int wi = (warp - kSoftWarp0) & 3;
+    const int quarter = warp & 3;             // TMEM lanes this warp may access
+    const int key = quarter * 32 + lane;      // also the head dim in the epilogue
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    constexpr int kH = 16;                    // columns per group
+    float* xbuf = reinterpret_cast<float*>(smem + kX) + sg * 2 * 4 * kH;
+    uint64_t* xf = B.x_full + 2 * sg;
+    float c = p.scale_log2;
+    const int kc = (key & 63) >> 3;
+    const uint32_t p_key = (uint32_t)((key >> 6) * kAtom + (key & 7) * 2);
+    uint32_t ex = 0;
+    auto exchange = [&](const float (&v)[kH], int nv) -> const float* {
+      float* slot = xbuf + (ex & 1) * 4 * kH;
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kH; ++k)
+          if (k < nv) slot[wi * kH + k] = v[k];
+        mbar_arrive(&xf[ex & 1]);
+      }
+      const bool r = mbar_wait_warp(&xf[ex & 1], (ex >> 1) & 1, p.status);
+      ++ex;
+      return r ? slot : nullptr;
+    };
+    uint32_t gp = 0, nb = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int slot = n % kSlots;
+      if (!(ok = mbar_wait_warp(&B.q_full[slot], (n / kSlots) & 1, p.status))) break;
+      const int* rec = info + kInfoInts * slot;
+      if (rec[kIDone]) break;
+      const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1], unit = rec[kIUnit];
+      const int flag = rec[kIFlag], sq = rec[kISeq], dest = rec[kIDest];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.q_empty[slot]);
+      const int npg = pg1 - pg0;
+      const int GC = MULTI ? unit_columns(p, unit) : p.G;
+      const int GL = min(max(GC - kH * sg, 0), kH);  // this group's columns
+      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
+      // column g = tl * G + head (token t0 + tl) sees key positions below lim[gl]
+      int lim[kH];
+      {
+        int t = (unit % p.NT) * p.Lg + (kH * sg) / p.G, hg = (kH * sg) % p.G;
+#pragma unroll
+        for (int gl = 0; gl < kH; ++gl) {
+          lim[gl] = gl < GL ? ctx - (p.L - 1 - t) : 0;
+          if (++hg == p.G) {
+            hg = 0;
+            ++t;
+          }
+        }
+      }
+      float res[kH], lse[kH];
+      if (npg <= 0) {
+        // nothing visible (lse -inf), or an invalid sequence (lse +inf: the
+        // combine zeroes the row)
+#pragma unroll
+        for (int gl = 0; gl < kH; ++gl) {
+          res[gl] = 0.f;
+          lse[gl] = flag ? INFINITY : -INFINITY;
+        }
+        if (flag && sg == 0 && wi == 0 && lane == 0 && p.status)
+          atomicOr(p.status, flag == 1 ? PA_STATUS_BAD_PAGE : PA_STATUS_BAD_LENGTH);
+      } else {
+        const int ob = nb & 1;
+        float m[kH], ls[kH];
+#pragma unroll
+        for (int gl = 0; gl < kH; ++gl) {
+          m[gl] = -INFINITY;
+          ls[gl] = 0.f;
+        }
+        for (int j = 0; j < npg; ++j, ++gp) {
+          const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
+          const bool kv = key < nvalid;
+          const int kpos = (pg0 + j) * kPage + key;
+          uint32_t vis = 0;
+#pragma unroll
+          for (int gl = 0; gl < kH; ++gl) vis |= (kpos < lim[gl] ? 1u : 0u) << gl;
+          auto visible = [&](int gl) -> bool { return ((vis >> gl) & 1u) != 0; };
+          if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
+          tc_fence_after();
+          uint32_t sr[kH];
+          tmem_ld16(tmem + lane_base + kColS + (gp & 1) * kN + kH * sg, sr);
+          tmem_wait_ld();
+          float d[kH];
+          bool need = j == 0;
+          if (!need) {
+            bool v = false;
+#pragma unroll
+            for (int gl = 0; gl < kH; ++gl) {
+              d[gl] = fmaf(__uint_as_float(sr[gl]), c, -m[gl]);
+              if (gl < GL) v |= visible(gl) && d[gl] > kRescaleThreshold;
+            }
+            float vote[kH];
+            vote[0] = __any_sync(0xffffffffu, v) ? 1.f : 0.f;
+            const float* x = exchange(vote, 1);
+            if (!(ok = x != nullptr)) break;
+            need = (x[0] + x[kH]) + (x[2 * kH] + x[3 * kH]) > 0.f;  // uniform over the group
+          }
+          if (need) {
+            float wm[kH];
+#pragma unroll
+            for (int gl = 0; gl < kH; ++gl)
+              wm[gl] = gl < GL ? warp_max(visible(gl) ? __uint_as_float(sr[gl]) * c : -INFINITY) : 0.f;
+            const float* x = exchange(wm, GL);
+            if (!(ok = x != nullptr)) break;
+            float alpha[kH];
+#pragma unroll
+            for (int gl = 0; gl < kH; ++gl) {
+              alpha[gl] = 1.f;
+              if (gl < GL) {
+                const float M = fmaxf(fmaxf(x[gl], x[kH + gl]), fmaxf(x[2 * kH + gl], x[3 * kH + gl]));
+                const float mn = fmaxf(m[gl], M);
+                if (j > 0 && mn != -INFINITY) alpha[gl] = fast_exp2(m[gl] - mn);
+                m[gl] = mn;
+                ls[gl] *= alpha[gl];
+              }
+              d[gl] = fmaf(__uint_as_float(sr[gl]), c, -m[gl]);
+            }
+            if (j > 0) {
+              if (!(ok = mbar_wait_warp(B.pv_done, (gp - 1) & 1, p.status))) break;
+              tc_fence_after();
+              uint32_t orow[kH];
+              const uint32_t o_cols = tmem + lane_base + kColO + ob * kN + kH * sg;
+              tmem_ld16(o_cols, orow);
+              tmem_wait_ld();
+#pragma unroll
+              for (int gl = 0; gl < kH; ++gl)
+                orow[gl] = __float_as_uint(__uint_as_float(orow[gl]) * alpha[gl]);
+              tmem_st16(o_cols, orow);
+            }
+          }
+          const uint32_t pbase = smem_u32(smem + kP + (gp & 1) * kOpBytes) + p_key;
+#pragma unroll
+          for (int gl = 0; gl < kH; ++gl) {
+            if (gl < GL) {
+              const int g = kH * sg + gl;
+              const float pv = visible(gl) ? fast_exp2(d[gl]) : 0.f;
+              uint16_t pbf;
+              if constexpr (FP8) {
+                const __half ph = __float2half_rn(pv);
+                pbf = __half_as_ushort(ph);
+                ls[gl] += __half2float(ph);
+              } else {
+                pbf = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+                ls[gl] += __uint_as_float((uint32_t)pbf << 16);
+              }
+              sts16(pbase + (g >> 3) * 1024 + (g & 7) * 128 + ((kc ^ (g & 7)) << 4), pbf);
+            }
+          }
+          if (nvalid < kPage && sg == 0) {
+            // the sequence's last page: zero the V rows past the context
+            const int st = gp % kStages;
+            if (!(ok = mbar_wait_warp(&B.v_full[st], (gp / kStages) & 1, p.status))) break;
+            if (!kv) {
+              const uint32_t vr =
+                  smem_u32(smem + kRing + st * kStageBytes + (FP8 ? 0 : 2 * kBox)) + key * 128;
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch) {
+                sts128(vr + ch * 16, 0u, 0u, 0u, 0u);
+                sts128(vr + kBox + ch * 16, 0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          if (need && j > 0) tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&B.p_full[gp & 1]);
+        }
+        if (!ok) break;
+        // item end: the column sums over the 128 keys, then this group's
+        // epilogue once the last P.V is done (thread = head dim)
+        float wl[kH];
+#pragma unroll
+        for (int gl = 0; gl < kH; ++gl) wl[gl] = gl < GL ? warp_sum(ls[gl]) : 0.f;
+        const float* x = exchange(wl, GL);
+        if (!(ok = x != nullptr)) break;
+        const float vsc = FP8 ? __ldg(p.v_scale + unit / p.NT) : 1.f;  // FP8: V scale
+        if (!(ok = mbar_wait_warp(&B.o_full[ob], (nb >> 1) & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t orow[kH];
+        tmem_ld16(tmem + lane_base + kColO + ob * kN + kH * sg, orow);
+        tmem_wait_ld();
+#pragma unroll
+        for (int gl = 0; gl < kH; ++gl) {
+          const float L = (x[gl] + x[kH + gl]) + (x[2 * kH + gl] + x[3 * kH + gl]);
+          const float inv = L > 0.f ? vsc / L : 0.f;
+          res[gl] = __uint_as_float(orow[gl]) * inv;
+          lse[gl] = L > 0.f ? (m[gl] + __log2f(L)) * kLn2 : -INFINITY;
+        }
+        tc_fence_before();
+        mbar_arrive(&B.o_free[ob]);
+        ++nb;
+      }
+      // output row of column g: token t0 + g / G, query head h G + g % G
+      const int dim = key;
+      const int64_t tok0 = (int64_t)sq * p.L + (unit % p.NT) * p.Lg;
+      const int head0 = (unit / p.NT) * p.G;
+#pragma unroll
+      for (int gl = 0; gl < kH; ++gl) {
+        if (gl < GL) {
+          const int g = kH * sg + gl;
+          const int64_t row = (tok0 + g / p.G) * p.Hq + head0 + g % p.G;
+          if (dest < 0) {
+            if (p.out_f32)
+              reinterpret_cast<float*>(p.out)[row * kHeadDim + dim] = res[gl];
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.out)[row * kHeadDim + dim] =
+                  __float2bfloat16_rn(res[gl]);
+          } else if (p.balanced) {
+            p.bal_o[((int64_t)dest * kN + g) * kHeadDim + dim] = res[gl];
+            if (dim == 0) p.bal_lse[dest * kN + g] = lse[gl];
+          } else {
+            p.part_o[(row * p.S + dest) * kHeadDim + dim] = res[gl];
+            if (dim == 0) p.part_lse[row * p.S + dest] = lse[gl];
+          }
+        }
+      }
+    }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ softmax, thread = key
     const int quarter = warp & 3;  // TMEM lanes this warp may access
@@ -742,7 +987,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     const int kc = (key & 63) >> 3;
     const uint32_t p_key = (uint32_t)((key >> 6) * kAtom + (key & 7) * 2);
     // Exchange among the four softmax warps: lane 0 of each warp publishes up
-    // to 16 floats in slot (ex & 1) and arrives; every warp then waits (bounded)
+    // to kN floats in slot (ex & 1) and arrives; every warp then waits (bounded)
     // and reads all four rows.  A slot is rewritten two exchanges later, after
     // every warp has arrived at the exchange in between (so has read it).
     uint32_t ex = 0;
@@ -772,7 +1017,6 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       if (npg <= 0) continue;
       const int GC = MULTI ? unit_columns(p, unit) : p.G;
       if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
-      // MULTI: column g (token t0 + g / G) sees key positions below lim[g]
       int lim[NH];
       if constexpr (MULTI) {
         int t = (unit % p.NT) * p.Lg, hg = 0;
@@ -796,7 +1040,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
         const bool kv = key < nvalid;  // within the sequence's context
         const int kpos = (pg0 + j) * kPage + key;
-        // MULTI: visible columns of this key, bit g
+        // MULTI: visible columns of this key, bit g -- the tokens
+        // tl > kpos - ctx + L - 1 - t0, i.e. the columns from (u + 1) G on
         uint32_t vis = 0;
         if constexpr (MULTI) {
 #pragma unroll
@@ -805,8 +1050,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         auto visible = [&](int g) -> bool { return MULTI ? ((vis >> g) & 1u) != 0 : kv; };
         if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
         tc_fence_after();
-        uint32_t sr[16];
-        tmem_ld16(tmem + lane_base + kColS + (gp & 1) * kN, sr);
+        uint32_t sr[kN];
+        tmem_ld_cols(tmem + lane_base + kColS + (gp & 1) * kN, sr);
         tmem_wait_ld();
         float d[NH];
         bool need = j == 0;
@@ -852,14 +1097,14 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
             // one before it finished ahead of this page's scores)
             if (!(ok = mbar_wait_warp(B.pv_done, (gp - 1) & 1, p.status))) break;
             tc_fence_after();
-            uint32_t orow[16];
+            uint32_t orow[kN];
             const uint32_t o_cols = tmem + lane_base + kColO + ob * kN;
-            tmem_ld16(o_cols, orow);
+            tmem_ld_cols(o_cols, orow);
             tmem_wait_ld();
 #pragma unroll
             for (int g = 0; g < NH; ++g)
               orow[g] = __float_as_uint(__uint_as_float(orow[g]) * alpha[g]);
-            tmem_st16(o_cols, orow);
+            tmem_st_cols(o_cols, orow);
           }
         }
         // P(j) into operand buffer j & 1: P.V(j - 2) has finished reading it (it
@@ -961,8 +1206,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         if (!(ok = mbar_wait_warp(&B.ml_full[ob], (nb >> 1) & 1, p.status))) break;
         if (!(ok = mbar_wait_warp(&B.o_full[ob], (nb >> 1) & 1, p.status))) break;
         tc_fence_after();
-        uint32_t orow[16];
-        tmem_ld16(tmem + lane_base + kColO + ob * kN, orow);
+        uint32_t orow[kN];
+        tmem_ld_cols(tmem + lane_base + kColO + ob * kN, orow);
         tmem_wait_ld();
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
@@ -1034,8 +1279,12 @@ template <int NH, bool FP8>
 cudaError_t launch_multi(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          const CUtensorMap& tm_q, const DecodeParams& p, int num_sms,
                          cudaStream_t stream) {
-  return p.L > 1 ? launch_nh<NH, FP8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                 : launch_nh<NH, FP8, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  if constexpr (NH > 16) {
+    return launch_nh<NH, FP8, true>(tm_k, tm_v, tm_q, p, num_sms, stream);  // only L > 1 is this wide
+  } else {
+    return p.L > 1 ? launch_nh<NH, FP8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                   : launch_nh<NH, FP8, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  }
 }
 
 }  // namespace
@@ -1043,12 +1292,14 @@ cudaError_t launch_multi(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
 cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
                           cudaStream_t stream) {
-  if (gc < 1 || gc > kN) return cudaErrorInvalidValue;
+  if (gc < 1 || gc > 32) return cudaErrorInvalidValue;
   if (p.k_scale)  // FP8 cache
-    return gc <= 8 ? launch_multi<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                   : launch_multi<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
-  return gc <= 8 ? launch_multi<8, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
-                 : launch_multi<16, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
+    return gc <= 8    ? launch_multi<8, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+           : gc <= 16 ? launch_multi<16, true>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                      : launch_multi<32, true>(tm_k, tm_v, tm_q, p, num_sms, stream);
+  return gc <= 8    ? launch_multi<8, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
+         : gc <= 16 ? launch_multi<16, false>(tm_k, tm_v, tm_q, p, num_sms, stream)
+                    : launch_multi<32, false>(tm_k, tm_v, tm_q, p, num_sms, stream);
 }
 
 }  // namespace pa
