@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int UPS = (p.Hq / p.G) * p.NT;
   const int ng = p.grid / UPS;
-  const int b = blockIdx.x + 1;
+  // a boundary's rows (L * Hq) are spread over cpb CTAs, one row per warp
+  const int nrows = p.L * p.Hq, wpc = blockDim.x >> 5;
+  const int cpb = (nrows + wpc - 1) / wpc;
+  const int b = blockIdx.x / cpb + 1, part = blockIdx.x - (b - 1) * cpb;
   if (warp == 0) {
     // prologue, overlapping the decode kernel: locate the sequence at
     // boundary b.  Lane l holds the page counts of sequences 16l .. 16l+15
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
   const int P = sh_P, n = sh_n;
   // the groups b-1 .. that touched pages [P, P + n), 32 at a time: lane k
   // holds group b-1+k of the current chunk (its record loads run in parallel)
-  for (int r = warp; r < p.L * p.Hq; r += blockDim.x >> 5) {
+  for (int r = part * wpc + warp; r < nrows && r < (part + 1) * wpc; r += wpc) {
     const int t = r / p.Hq, hd = r - t * p.Hq;
     const int j = (hd / p.G) * p.NT + t / p.Lg, g = (t % p.Lg) * p.G + hd % p.G;
     float M = -INFINITY;
@@ -196,16 +199,29 @@ __global__ void __launch_bounds__(1024) bal_combine_kernel(const BalCombineParam
         Lsum += w;
         unsigned mk = __ballot_sync(0xffffffffu, w != 0.f);
         while (mk) {
-          const int k = __ffs(mk) - 1;
+          // two records at a time: both loads issue before either is used
+          const int k0 = __ffs(mk) - 1;
           mk &= mk - 1;
-          const float wk = __shfl_sync(0xffffffffu, w, k);
-          const int rk = __shfl_sync(0xffffffffu, rec, k);
-          const float4 x =
-              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)rk * p.NC + g) * kHeadDim)[lane];
-          acc.x = fmaf(wk, x.x, acc.x);
-          acc.y = fmaf(wk, x.y, acc.y);
-          acc.z = fmaf(wk, x.z, acc.z);
-          acc.w = fmaf(wk, x.w, acc.w);
+          const int k1 = mk ? __ffs(mk) - 1 : k0;
+          const bool two = mk != 0;
+          if (two) mk &= mk - 1;
+          const float w0 = __shfl_sync(0xffffffffu, w, k0);
+          const float w1 = two ? __shfl_sync(0xffffffffu, w, k1) : 0.f;
+          const int r0 = __shfl_sync(0xffffffffu, rec, k0), r1 = __shfl_sync(0xffffffffu, rec, k1);
+          const float4 x0 =
+              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)r0 * p.NC + g) * kHeadDim)[lane];
+          const float4 x1 =
+              reinterpret_cast<const float4*>(p.bal_o + ((int64_t)r1 * p.NC + g) * kHeadDim)[lane];
+          acc.x = fmaf(w0, x0.x, acc.x);
+          acc.y = fmaf(w0, x0.y, acc.y);
+          acc.z = fmaf(w0, x0.z, acc.z);
+          acc.w = fmaf(w0, x0.w, acc.w);
+          if (two) {  // (warp-uniform)
+            acc.x = fmaf(w1, x1.x, acc.x);
+            acc.y = fmaf(w1, x1.y, acc.y);
+            acc.z = fmaf(w1, x1.z, acc.z);
+            acc.w = fmaf(w1, x1.w, acc.w);
+          }
         }
         if (!__any_sync(0xffffffffu, gg < ng && lo < P + n)) break;
       }
@@ -237,8 +253,11 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
 cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream) {
   const int ng = p.grid / ((p.Hq / p.G) * p.NT);
   if (ng <= 1) return cudaSuccess;
-  const int warps = p.L * p.Hq < 32 ? p.L * p.Hq : 32;
-  cudaError_t e = launch_dependent(bal_combine_kernel, p, ng - 1, 32 * warps, stream);
+  // one row per warp: up to 16 warps per CTA, ceil(rows / warps) CTAs per boundary
+  const int rows = p.L * p.Hq;
+  const int warps = rows < 16 ? rows : 16;
+  const int cpb = (rows + warps - 1) / warps;
+  cudaError_t e = launch_dependent(bal_combine_kernel, p, (ng - 1) * cpb, 32 * warps, stream);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
