@@ -48,6 +48,10 @@ def parse_args():
                     help="decode batch (pool = 32 pages per sequence); smaller values are "
                          "for profiling captures, the benchmark workload is 128")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-leg", choices=["prefill", "fp8", "prologue", "topk", "multi"],
+                    default=None,
+                    help="run one benchmark leg's calls a few times (FP8 and multi-token legs at "
+                         "--batch sequences) for an ncu capture, then exit; prints no bench line")
     return ap.parse_args()
 
 
@@ -176,7 +180,8 @@ def decode_traffic_from_profile():
         for line in open(prof):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip().strip("`")
+                # the value's first word (a hash in backquotes, or a number)
+                vals[k.strip()] = v.strip().split()[0].strip("`") if v.strip() else ""
         if vals.get("source_sha256_16") != h:
             return None
         # captured on the batch-16 case; traffic scales with the units processed
@@ -305,13 +310,13 @@ def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
             "l2": "flushed between steps"}
 
 
-def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3):
+def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3, batch=64):
     """Multi-token decode (64 sequences x 4096 tokens, 4 new tokens each, 40/8
     heads): the 256 new tokens' KV write, then pa_decode_multi -- and the same
     attention through pa_prefill_chunk for comparison.  Bytes: the K+V of every
     context read once (1.07 GB; the working set is far larger than L2)."""
     q_len = 4
-    case = W.multi_token_decode(device="cuda", pool_device="cuda", q_len=q_len)
+    case = W.multi_token_decode(device="cuda", pool_device="cuda", q_len=q_len, B=batch)
     kv_bytes = int(case.context_lens.sum()) * case.Hkv * D * 2 * 2
     out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -359,12 +364,12 @@ def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3):
     return res
 
 
-def run_fp8(pa, W, torch, hbm, steps=30, warmup=3):
+def run_fp8(pa, W, torch, hbm, steps=30, warmup=3, batch=128):
     """FP8 (e4m3) KV cache on the headline shape (128 sequences x 4096 tokens,
     40/8 heads): the new token's quantizing write, then pa_decode_fp8 over
     1.07 GB of e4m3 K+V (the working set is far larger than L2)."""
     case = W.qwen3_14b_decode_b128(device="cuda", pool_device="cuda", with_new=True,
-                                   poison=False)
+                                   poison=False, batch=batch)
     Hkv = case.Hkv
     g = torch.Generator(device="cuda").manual_seed(11)
     ks = torch.rand(Hkv, generator=g, device="cuda") * 0.02 + 0.02
@@ -397,7 +402,7 @@ def run_fp8(pa, W, torch, hbm, steps=30, warmup=3):
     torch.cuda.synchronize()
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
     gbs = kv_bytes / (ms * 1e-3) / 1e9
-    return {"workload": "qwen3-14b-decode-b128-ctx4096-fp8-kv", "kv_bytes": kv_bytes, "ms": ms,
+    return {"workload": f"qwen3-14b-decode-b{batch}-ctx4096-fp8-kv", "kv_bytes": kv_bytes, "ms": ms,
             "gbs": gbs, "frac": gbs / hbm, "bf16_equivalent_gbs": 2 * gbs,
             "status": int(st.item()), "step": "pa_kv_write_fp8 (1 token/seq) + pa_decode_fp8",
             "l2": "working set > L2"}
@@ -527,6 +532,22 @@ def run_ours(args):
     __graft_entry__.build()
     import paged_kv_gqa_write_gb300 as pa
     import workloads as W
+
+    if args.profile_leg:
+        hbm_p = peaks()[0]
+        if args.profile_leg == "prefill":
+            r = run_prefill(pa, W, torch, steps=2, warmup=1)
+        elif args.profile_leg == "fp8":
+            r = run_fp8(pa, W, torch, hbm_p, steps=2, warmup=1, batch=args.batch)
+        elif args.profile_leg == "prologue":
+            r = run_prologue(pa, W, torch, hbm_p, steps=2, warmup=1)
+        elif args.profile_leg == "topk":
+            r = run_topk(pa, torch, hbm_p, steps=2, warmup=1)
+        else:
+            r = run_multi_token(pa, W, torch, hbm_p, steps=2, warmup=1, batch=args.batch)
+        print(json.dumps({"profile_leg": args.profile_leg, "batch": args.batch,
+                          "status": r.get("status", 0)}), flush=True)
+        return
 
     dev = torch.device("cuda", torch.cuda.current_device())
     case = W.qwen3_14b_decode_b128(device=dev, with_new=True, pool_device=dev, batch=B)
