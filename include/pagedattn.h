@@ -219,7 +219,7 @@ int32_t pa_decode_auto_splits(pa_dims dims);
  * "prefill_fwd" ("Qwen3-14B", pypto-lib doc) with every chunk q_len long,
  * run on the decode kernel: token j of sequence s sits at position
  * context_lens[s] - q_len + j and attends to keys 0 .. that position.  Each
- * decode work item stacks (token, query head) pairs of one KV head -- up to 16
+ * decode work item stacks (token, query head) pairs of one KV head -- up to 32
  * of them -- in the columns of its tensor-core products, so a K/V page is read
  * once for all the tokens it serves.
  *   q              bf16 [B * q_len, Hq, D], token-major in sequence order
@@ -361,7 +361,7 @@ size_t pa_topk_workspace_size(int32_t rows, int32_t vocab, int32_t k);
  * the library holds that array until the process exits.  A call whose split
  * count (num_splits, or the automatic choice for 0) needs more scratch than
  * that -- (B * Hq * splits * 516 bytes, rounded up; the page-balanced
- * schedule needs about 2.6 MB) -- returns PA_ERR_NOALLOC_TOO_LARGE without
+ * schedule needs about 5 MB on 152 SMs) -- returns PA_ERR_NOALLOC_TOO_LARGE without
  * launching; num_splits = 1 needs none.
  *
  * Setup: the first call made with a given device current looks up the
