@@ -47,8 +47,10 @@ def test_ragged_batch_all_rows(cuda_lib, q_len, splits):
     assert_close(out, _oracle_after_write(case), what=f"q_len={q_len} splits={splits}")
 
 
-@pytest.mark.parametrize("Hq,Hkv,q_len", [(40, 8, 4), (64, 8, 2), (16, 1, 3), (32, 2, 5)])
+@pytest.mark.parametrize("Hq,Hkv,q_len", [(40, 8, 4), (64, 8, 2), (16, 1, 3), (32, 2, 5), (40, 8, 7)])
 def test_head_layouts(cuda_lib, Hq, Hkv, q_len):
+    """G query heads per KV head: items of up to 32 (token, head) columns; 40/8
+    with q_len 7 takes one 20-column and one 15-column token group."""
     ctx = [700, 129, 2000]
     case = W.custom_case(720 + Hq, ctx, Hq=Hq, Hkv=Hkv, chunk_lens=[q_len] * 3, with_new=True)
     c = case.to("cuda")
