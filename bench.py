@@ -597,24 +597,28 @@ def run_ours(args):
     # kv_write + decode, + a combine for the balanced schedule or fixed splits > 1
     launches_per_step = 2 + (1 if (balanced or splits > 1) else 0)
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
-    hq = case.q.cpu().pin_memory()
-    hk = case.k_new.cpu().pin_memory()
-    hv = case.v_new.cpu().pin_memory()
-    hbt = case.block_table.cpu().pin_memory()
-    hctx = case.context_lens.cpu().pin_memory()
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed.
+    # A step's inputs (q, the new K/V rows, the block table, the lengths) sit in
+    # one pinned staging buffer and go up in one copy; the output comes back.
+    parts = (case.q, case.k_new, case.v_new, case.block_table, case.context_lens)
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    hstage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dstage = torch.empty(total, dtype=torch.uint8, device=dev)
+    dviews = []
+    for t, o in zip(parts, offs):
+        n = t.numel() * t.element_size()
+        hstage[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+        dviews.append(dstage[o:o + n].view(t.dtype).view(t.shape))
+    dq, dk, dv, dbt, dctx = dviews
     hout = torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory()
-    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new)
-    dbt, dctx = torch.empty_like(case.block_table), torch.empty_like(case.context_lens)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hctx))
+    h2d = total
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dbt.copy_(hbt, non_blocking=True)
-        dctx.copy_(hctx, non_blocking=True)
+        dstage.copy_(hstage, non_blocking=True)
         pa.pa_kv_write(dk, dv, case.k_cache, case.v_cache, dbt, dctx, None, status=status,
                        stream=stream)
         pa.pa_decode(dq, case.k_cache, case.v_cache, dbt, dctx, case.scale, out=out,
