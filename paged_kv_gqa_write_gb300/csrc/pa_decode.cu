@@ -1040,8 +1040,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         const int nvalid = min(ctx - (pg0 + j) * kPage, kPage);  // >= 1
         const bool kv = key < nvalid;  // within the sequence's context
         const int kpos = (pg0 + j) * kPage + key;
-        // MULTI: visible columns of this key, bit g -- the tokens
-        // tl > kpos - ctx + L - 1 - t0, i.e. the columns from (u + 1) G on
+        // MULTI: visible columns of this key, bit g
         uint32_t vis = 0;
         if constexpr (MULTI) {
 #pragma unroll
