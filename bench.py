@@ -190,11 +190,19 @@ def decode_traffic_from_profile():
         return None
 
 
-def cpu_oracle_rate(case, seconds, rank0=True):
+def spread(ms_list):
+    """Median, p10 and p90 (ms) of per-step event times."""
+    v = sorted(ms_list)
+    at = lambda q: v[min(len(v) - 1, int(q * (len(v) - 1) + 0.5))]
+    return {"median_ms": statistics.median(v), "p10_ms": at(0.1), "p90_ms": at(0.9)}
+
+
+def cpu_oracle_rate(case, seconds, rank0=True, threads=None):
     """Time the FP64 oracle on whole decode steps of `case` (host copies) until
-    `seconds` have passed; returns (GB/s of K+V processed, threads, sample text)."""
+    `seconds` have passed; returns (GB/s of K+V processed, threads, sample text).
+    `threads`: OpenMP threads (default: all host cores)."""
     import oracle
-    nt = oracle.max_threads()
+    nt = threads or oracle.max_threads()
     kb = case.k_cache.cpu()
     vb = case.v_cache.cpu()
     q = case.q.cpu()
@@ -301,8 +309,10 @@ def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
         step()
         b.record()
     torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    sp = spread([a.elapsed_time(b) for a, b in ev])
+    ms = sp["median_ms"]
     return {"workload": name, "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv,
+            "spread": sp,
             "kv_bytes": kv_bytes, "ms": ms, "gbs": kv_bytes / (ms * 1e-3) / 1e9,
             "seqs_per_s": case.B / (ms * 1e-3), "status": int(st.item()),
             "schedule": "page-balanced" if sched == 0 else f"{sched} fixed splits",
@@ -356,9 +366,10 @@ def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3, batch=64):
             fn()
             b.record()
         torch.cuda.synchronize()
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        sp = spread([a.elapsed_time(b) for a, b in ev])
+        ms = sp["median_ms"]
         gbs = kv_bytes / (ms * 1e-3) / 1e9
-        res[name] = {"ms": ms, "gbs": gbs, "frac": gbs / hbm,
+        res[name] = {"ms": ms, "spread": sp, "gbs": gbs, "frac": gbs / hbm,
                      "tokens_per_s": case.T / (ms * 1e-3)}
     res["status"] = int(st.item())
     return res
@@ -400,9 +411,11 @@ def run_fp8(pa, W, torch, hbm, steps=30, warmup=3, batch=128):
         step()
         b.record()
     torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    sp = spread([a.elapsed_time(b) for a, b in ev])
+    ms = sp["median_ms"]
     gbs = kv_bytes / (ms * 1e-3) / 1e9
     return {"workload": f"qwen3-14b-decode-b{batch}-ctx4096-fp8-kv", "kv_bytes": kv_bytes, "ms": ms,
+            "spread": sp,
             "gbs": gbs, "frac": gbs / hbm, "bf16_equivalent_gbs": 2 * gbs,
             "status": int(st.item()), "step": "pa_kv_write_fp8 (1 token/seq) + pa_decode_fp8",
             "l2": "working set > L2"}
@@ -438,9 +451,10 @@ def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
             step()
             b.record()
         torch.cuda.synchronize()
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        sp = spread([a.elapsed_time(b) for a, b in ev])
+        ms = sp["median_ms"]
         nbytes = case.T * (case.Hq + 2 * case.Hkv) * D * 2 * 2
-        out[name] = {"tokens": case.T, "us": ms * 1e3, "bytes": nbytes,
+        out[name] = {"tokens": case.T, "us": ms * 1e3, "spread": sp, "bytes": nbytes,
                      "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
                      "status": int(st.item())}
     out["step"] = "pa_qk_norm_rope_write"
@@ -475,11 +489,12 @@ def run_topk(pa, torch, hbm, steps=50, warmup=5):
         step()
         b.record()
     torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    sp = spread([a.elapsed_time(b) for a, b in ev])
+    ms = sp["median_ms"]
     nbytes = 16 * 151936 * 4
     ref = torch.topk(logits, 32, dim=1)
     exact = bool(torch.equal(ref.indices.to(torch.int32), idx)) and bool(torch.equal(ref.values, vals))
-    return {"workload": "topk-b16-v151936-k32", "us": ms * 1e3, "bytes": nbytes,
+    return {"workload": "topk-b16-v151936-k32", "us": ms * 1e3, "spread": sp, "bytes": nbytes,
             "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
             "matches_torch_topk": exact, "step": "pa_topk (slice select + merge)",
             "l2": "flushed between steps"}
@@ -514,8 +529,10 @@ def run_prefill(pa, W, torch, steps=20, warmup=3):
         step()
         b.record()
     torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    sp = spread([a.elapsed_time(b) for a, b in ev])
+    ms = sp["median_ms"]
     return {"workload": PREFILL_WORKLOAD, "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms,
+            "spread": sp,
             "gflop_causal": flops / 1e9, "status": int(st.item()),
             "step": "pa_kv_write (4096 tokens) + pa_prefill_chunk", "l2": "flushed between steps"}
 
@@ -689,7 +706,9 @@ def run_ours(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, nt, sample = cpu_oracle_rate(case, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample}
+        v1, _, sample1 = cpu_oracle_rate(case, max(1.0, args.cpu_seconds / 4), threads=1)
+        cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample,
+               "single_thread": {"value": v1, "unit": UNIT, "sample": sample1}}
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -709,7 +728,8 @@ def run_ours(args):
                      "frac": achieved / hbm, "traffic": decode_traffic_from_profile(),
                      "kernel": "pa_decode (decode_kernel + combine_kernel)",
                      "peak_source": f"{src} hbm_gbs (burst)",
-                     "ms_per_launch": dec_ms},
+                     "ms_per_launch": dec_ms,
+                     "launch_spread": spread([a.elapsed_time(b) for a, b in dec_ev])},
         "e2e": None if e2e_ms is None else {
             "value": KV_BYTES * ws / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
