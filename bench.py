@@ -273,7 +273,7 @@ class L2Flush:
         self.r.sum()
 
 
-def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
+def run_decode_config(pa, W, torch, name, steps=50, warmup=10):
     """One of the smaller decode configurations, timed per step with an L2
     flush in between (their K+V is about the size of L2)."""
     if name == "qwen3-14b-decode-b16":
@@ -320,7 +320,7 @@ def run_decode_config(pa, W, torch, name, steps=30, warmup=3):
             "l2": "flushed between steps"}
 
 
-def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3, batch=64):
+def run_multi_token(pa, W, torch, hbm, steps=50, warmup=10, batch=64):
     """Multi-token decode (64 sequences x 4096 tokens, 4 new tokens each, 40/8
     heads): the 256 new tokens' KV write, then pa_decode_multi -- and the same
     attention through pa_prefill_chunk for comparison.  Bytes: the K+V of every
@@ -375,7 +375,7 @@ def run_multi_token(pa, W, torch, hbm, steps=30, warmup=3, batch=64):
     return res
 
 
-def run_fp8(pa, W, torch, hbm, steps=30, warmup=3, batch=128):
+def run_fp8(pa, W, torch, hbm, steps=50, warmup=10, batch=128):
     """FP8 (e4m3) KV cache on the headline shape (128 sequences x 4096 tokens,
     40/8 heads): the new token's quantizing write, then pa_decode_fp8 over
     1.07 GB of e4m3 K+V (the working set is far larger than L2)."""
@@ -421,7 +421,7 @@ def run_fp8(pa, W, torch, hbm, steps=30, warmup=3, batch=128):
             "l2": "working set > L2"}
 
 
-def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
+def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
     """pa_qk_norm_rope_write (Q/K RMSNorm -> NeoX RoPE -> KV write) on the decode
     batch (128 tokens) and on the 8 x 512 prefill chunk, with a clean L2 flush
     between steps.  Bytes: the fused QKV rows read, Q and the K/V rows written."""
@@ -462,7 +462,7 @@ def run_prologue(pa, W, torch, hbm, steps=30, warmup=3):
     return out
 
 
-def run_topk(pa, torch, hbm, steps=50, warmup=5):
+def run_topk(pa, torch, hbm, steps=50, warmup=10):
     """Exact top-32 of 16 rows of 151936 logits (the Qwen3-14B real vocabulary in
     rows padded to 152064), the selector's batch-16 configuration; L2 flushed
     between steps.  Bytes: the logits read once."""
@@ -500,7 +500,7 @@ def run_topk(pa, torch, hbm, steps=50, warmup=5):
             "l2": "flushed between steps"}
 
 
-def run_prefill(pa, W, torch, steps=20, warmup=3):
+def run_prefill(pa, W, torch, steps=50, warmup=10):
     """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
     case = W.chunked_prefill(device="cuda", pool_device="cuda")
     flops = 0.0
