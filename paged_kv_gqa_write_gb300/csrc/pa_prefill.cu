@@ -61,6 +61,7 @@ constexpr int kBars = kList + kMaxList * kListInts * 4;
 constexpr int kNumBars = 2 * 2 + 2 * kRingK + 2 * kRingV + 4 * 2;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
 constexpr int kMaxCost = 4096;                // schedule histogram buckets (ring scratch)
+constexpr int kMaxSchedSeqs = (kRingV * kTileBytes / 4 - 1) / 4;  // sequences the schedule stages
 // TMEM columns
 constexpr uint32_t kColS = 0;     // S_A, S_B: 128 columns each (P in their first 64)
 constexpr uint32_t kColO = 256;   // O_A, O_B: 128 columns each
@@ -128,60 +129,139 @@ __device__ __forceinline__ int pair_cost(const PrefillParams& p, int n, int ctx,
 // Greedy longest-first schedule: all items sorted by key-tile count
 // (descending; ties in (sequence, pair, head) order), dealt to CTAs in a snake
 // (0..N-1, N-1..0, ...).  Writes this CTA's items in order and returns their
-// count, or -1 when the launch is too large for the table (round-robin then).
-__device__ int build_schedule(const PrefillParams& p, int* hist, int* list, int N, int c) {
+// count, or -1 on every CTA when the launch is too large for the table
+// (round-robin then).  Built by the 32 lanes of one warp, which all call it
+// and get the same result: a pair at a time on one thread, the walk took most
+// of the kernel's start-up.
+//   scratch: 3 * kMaxCost ints (pairs per cost, first sorted position of each
+//            cost, pairs of each cost placed so far)
+//   seqs:    4 * B + 1 ints (chunk lengths, context lengths, first pair of
+//            each sequence [B + 1], first packed token of each sequence)
+__device__ int build_schedule(const PrefillParams& p, int* scratch, int* seqs, int* list, int N,
+                              int c, int lane) {
+  constexpr unsigned kAll = 0xffffffffu;
   const int maxc = 2 * p.max_pages + 1;
-  if (maxc > kMaxCost || p.Hq > 256) return -1;
-  int* start = hist + kMaxCost;
-  for (int b = 0; b < maxc; ++b) hist[b] = 0;
-  int64_t pairs = 0;
-  for (int s = 0; s < p.B; ++s) {
-    const int n = __ldg(p.chunk_lens + s), ctx = __ldg(p.context_lens + s);
-    for (int pr = 0; pr * 256 < n; ++pr) {
-      ++hist[pair_cost(p, n, ctx, pr)];
-      ++pairs;
-    }
-  }
-  const int64_t items = pairs * p.Hq;
-  int rows = 0;  // snake rows that hold an item for this CTA
-  for (int64_t r = 0;; ++r) {
-    const int64_t pos = r * N + ((r & 1) ? N - 1 - c : c);
-    if (pos >= items) break;
-    if (++rows > kMaxList) return -1;
-  }
-  // Past the check above every position fits in 32 bits (items <= (kMaxList +
-  // 1) * N).  The walk runs on one thread before any CTA starts its first
-  // item, so its divisions are 32-bit: with 64-bit ones (a long software
-  // routine) the kernel's start-up measured 18 us instead of 8.
-  int acc = 0;
-  for (int b = maxc - 1; b >= 0; --b) {
-    start[b] = acc;
-    acc += hist[b] * p.Hq;
+  if (maxc > kMaxCost || p.Hq > 256 || p.B > kMaxSchedSeqs) return -1;
+  int* hist = scratch;
+  int* start = scratch + kMaxCost;
+  int* taken = scratch + 2 * kMaxCost;
+  int* sn = seqs;
+  int* sc = seqs + p.B;
+  int* spf = seqs + 2 * p.B;
+  int* stk = seqs + 3 * p.B + 1;
+  for (int b = lane; b < maxc; b += 32) {
     hist[b] = 0;
+    taken[b] = 0;
   }
-  const int N2 = 2 * N;
-  int tok = 0;
-  for (int s = 0; s < p.B; ++s) {
-    const int n = __ldg(p.chunk_lens + s), ctx = __ldg(p.context_lens + s);
-    for (int pr = 0; pr * 256 < n; ++pr) {
-      const int cost = pair_cost(p, n, ctx, pr);
-      const int pos0 = start[cost] + (hist[cost]++) * p.Hq;
-      for (int k = 0; k < 2; ++k) {
-        // this CTA's positions of the snake: pos = res (mod 2N)
-        const int res = k ? N2 - 1 - c : c;
-        int d = (res - pos0) % N2;
-        if (d < 0) d += N2;
-        for (int pos = pos0 + d; pos < pos0 + p.Hq; pos += N2) {
-          int* e = list + kListInts * (pos / N);
-          e[0] = s;
-          e[1] = (pr << 8) | (pos - pos0);
-          e[2] = tok + pr * 256;
-          e[3] = n;
-          e[4] = ctx;
-        }
+  // lengths, then the pair and token prefix sums, 32 sequences at a time
+  int64_t pbase = 0, tbase = 0;
+  for (int s0 = 0; s0 < p.B; s0 += 32) {
+    const int s = s0 + lane;
+    int n = 0, ctx = 0;
+    if (s < p.B) {
+      n = __ldg(p.chunk_lens + s);
+      ctx = __ldg(p.context_lens + s);
+      sn[s] = n;
+      sc[s] = ctx;
+    }
+    const int np = n > 0 ? n / 256 + (n % 256 != 0) : 0;  // < 2^24
+    const int64_t tk = n > 0 ? n : 0;
+    int inp = np;
+    int64_t itk = tk;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(kAll, inp, o);
+      const int64_t b = __shfl_up_sync(kAll, itk, o);
+      if (lane >= o) {
+        inp += a;
+        itk += b;
       }
     }
-    tok += n > 0 ? n : 0;
+    if (s < p.B) {
+      spf[s] = (int)min(pbase + inp - np, (int64_t)INT32_MAX);
+      stk[s] = (int)min(tbase + itk - tk, (int64_t)INT32_MAX);  // T < 2^31 for valid lengths
+    }
+    pbase += __shfl_sync(kAll, inp, 31);
+    tbase += __shfl_sync(kAll, itk, 31);
+  }
+  // the table holds kMaxList items per CTA; the same test on every CTA
+  const int64_t items = pbase * p.Hq;
+  if (items > (int64_t)kMaxList * N) return -1;
+  const int pairs = (int)pbase;  // from here on every count fits in 32 bits
+  if (lane == 0) spf[p.B] = pairs;
+  __syncwarp();
+  // pair q's sequence: the last s with spf[s] <= q (sequences without pairs
+  // have spf[s] == spf[s + 1])
+  auto seq_of = [&](int q) {
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (spf[mid] <= q) lo = mid; else hi = mid;
+    }
+    return lo;
+  };
+  for (int q = lane; q < pairs; q += 32) {
+    const int s = seq_of(q);
+    atomicAdd(&hist[pair_cost(p, sn[s], sc[s], q - spf[s])], 1);
+  }
+  __syncwarp();
+  // first sorted position of each cost: costs in decreasing order, Hq items
+  // per pair (a scan over the buckets from the top, 32 at a time)
+  int acc = 0;
+  for (int b0 = maxc - 1; b0 >= 0; b0 -= 32) {
+    const int b = b0 - lane;
+    const int v = b >= 0 ? hist[b] * p.Hq : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(kAll, inc, o);
+      if (lane >= o) inc += a;
+    }
+    if (b >= 0) start[b] = acc + inc - v;
+    acc += __shfl_sync(kAll, inc, 31);
+  }
+  __syncwarp();
+  // each pair's rank among the pairs of its cost, in (sequence, pair) order,
+  // 32 pairs at a time; its Hq items take the positions start + rank * Hq ...
+  const int N2 = 2 * N;
+  for (int q0 = 0; q0 < pairs; q0 += 32) {
+    const int q = q0 + lane;
+    const bool act = q < pairs;
+    int s = 0, pr = 0, cost = -1;
+    if (act) {
+      s = seq_of(q);
+      pr = q - spf[s];
+      cost = pair_cost(p, sn[s], sc[s], pr);
+    }
+    const unsigned grp = __match_any_sync(kAll, cost);
+    const int before = __popc(grp & ((1u << lane) - 1u));
+    const int rank = act ? taken[cost] + before : 0;
+    __syncwarp();
+    if (act && before == 0) taken[cost] += __popc(grp);
+    __syncwarp();
+    if (!act) continue;
+    const int pos0 = start[cost] + rank * p.Hq;
+    for (int k = 0; k < 2; ++k) {
+      // this CTA's positions of the snake: pos = res (mod 2N)
+      const int res = k ? N2 - 1 - c : c;
+      int d = (res - pos0) % N2;
+      if (d < 0) d += N2;
+      for (int pos = pos0 + d; pos < pos0 + p.Hq; pos += N2) {
+        int* e = list + kListInts * (pos / N);
+        e[0] = s;
+        e[1] = (pr << 8) | (pos - pos0);
+        e[2] = stk[s] + pr * 256;
+        e[3] = sn[s];
+        e[4] = sc[s];
+      }
+    }
+  }
+  __syncwarp();
+  int rows = 0;  // snake rows that hold an item for this CTA (<= kMaxList)
+  for (int r = 0; r <= kMaxList; ++r) {
+    const int64_t pos = (int64_t)r * N + ((r & 1) ? N - 1 - c : c);
+    if (pos >= items) break;
+    ++rows;
   }
   return rows;
 }
@@ -270,8 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B.o_free[i], 128);
     }
     fence_mbar_init();
+  }
+  if (warp == 0) {
     // the rings are idle until the first load: scratch for the schedule
-    *list_count = build_schedule(p, reinterpret_cast<int*>(smem + kK), list, gridDim.x, blockIdx.x);
+    const int count = build_schedule(p, reinterpret_cast<int*>(smem + kK),
+                                     reinterpret_cast<int*>(smem + kV), list, gridDim.x,
+                                     blockIdx.x, lane);
+    if (lane == 0) *list_count = count;
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -444,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool reporter = qtile == 0 && t == 0 && it.pair == 0 && it.g == 0 && p.status;
       const int nrows = it.nrows[qtile];
       const int64_t tok = (int64_t)it.tok0 + qtile * 128 + row;
-      const bool row_out = row < nrows && tok < p.T;
+      const bool row_out = row < nrows && tok >= 0 && tok < p.T;
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
                      ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
       if (nkt == 0) {
@@ -639,7 +724,8 @@ cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream) {
   static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
-  static_assert(2 * kMaxCost * 4 <= kRingK * kTileBytes, "schedule scratch must fit the K ring");
+  static_assert(3 * kMaxCost * 4 <= kRingK * kTileBytes, "schedule scratch must fit the K ring");
+  static_assert((4 * kMaxSchedSeqs + 1) * 4 <= kRingV * kTileBytes, "schedule lengths must fit the V ring");
   cudaError_t e =
       cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;

@@ -162,3 +162,34 @@ def test_scores_that_move_the_reference(cuda_lib, profile):
     assert st == 0
     ref, _, _ = _oracle_after_write(case)
     assert_close(out, ref, what=f"prefill {profile} scores")
+
+
+@pytest.mark.parametrize("extra", [-1, 2])
+def test_schedule_table_limit(cuda_lib, extra):
+    """Launches whose item count sits just below or just above what the
+    per-CTA schedule table holds (64 items per CTA on a grid of one CTA per
+    SM): below it every CTA takes its items from the table, above it every CTA
+    falls back to round-robin -- never a mix, which would leave items
+    unprocessed.  One pair of query tiles per sequence and 8 query heads, so
+    items = 8 * sequences; the output starts as NaN and every row must be
+    written."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B = 64 * sms // 8 + extra
+    chunk = [1 + s % 3 for s in range(B)]
+    ctx = [c + (37 * s) % 150 for s, c in enumerate(chunk)]
+    case = W.custom_case(612, ctx, Hq=8, Hkv=2, chunk_lens=chunk, with_new=True)
+    c = case.to("cuda")
+    st = dev_status()
+    cuda_lib.pa_kv_write(c.k_new, c.v_new, c.k_cache, c.v_cache, c.block_table, c.context_lens,
+                         c.chunk_lens, status=st)
+    out = torch.full((sum(chunk), 8, 128), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.pa_prefill_chunk(c.q, c.k_cache, c.v_cache, c.block_table, c.context_lens,
+                              c.chunk_lens, c.scale, out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert bool(torch.isfinite(out).all()), "rows left unwritten"
+    T = sum(chunk)
+    rows = sample_rows(T, 8, 200, seed=13, extra=[0, 8 * T - 1, 8 * (T // 2) + 3])
+    ref, _, _ = _oracle_after_write(case, rows=rows)
+    got = out.reshape(-1, 128)[torch.as_tensor(rows, device="cuda")]
+    assert_close(got, ref, what=f"schedule limit B={B}")
