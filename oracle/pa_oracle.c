@@ -23,7 +23,7 @@
  *    size-limit bullet: -1 padding is not a valid slot, fully masked rows
  *    produce zero output.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - query head g reads KV head g / (Hq/Hkv) (contiguous groups);
  *  - context_lens[s] counts tokens AFTER the write; chunk_lens[s] new tokens;
  *    new token j of sequence s sits at position context_lens[s]-chunk_lens[s]+j
@@ -53,7 +53,7 @@ static double bf16_to_f64(uint16_t b) {
  * FP8 KV cache ("fp8_e4m3" KV cache in the SGLang measurement of the
  * "Qwen4-Exp QSA trafia na Ascend..." blog; a quantized KV dtype is also the
  * --kv-cache-dtype option of the "Qwen 3" TensorSharp doc, section 11).
- * Readings (each also in the design doc): e4m3 is the e4m3fn encoding (sign, 4
+ * Readings: e4m3 is the e4m3fn encoding (sign, 4
  * exponent bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is
  * NaN; largest finite 448); every KV head h has one FP32 scale for K and one
  * for V; a cached value means code_value * scale; writing divides the bf16
@@ -410,7 +410,7 @@ int oracle_max_threads(void) {
  * "Q/K norm -> RoPE" before the KV cache write; "Deployment configuration":
  * FP32 RMSNorm weights.
  *
- * Readings (each also in the design doc):
+ * Readings where the pages are silent:
  *  - RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w, over the head's D values;
  *  - NeoX RoPE rotates the pair (x[i], x[i + D/2]), i < D/2, by the angle
  *    pos * f_i with f_i = base^(-2i/D) / scale:
@@ -522,7 +522,7 @@ int oracle_qk_norm_rope_write(const uint16_t* qkv, const float* wq, const float*
  * candidate values and token IDs.  The oracle is the plain definition: sort the
  * row's (value, index) pairs and take the first k.
  *
- * Readings (each also in the design doc):
+ * Readings where the pages are silent:
  *  - order: larger value first; NaN ranks above +inf (as torch.topk does);
  *    among equal values the smaller index comes first (the page fixes no tie
  *    order; this one is total, so the result is unique);
