@@ -381,6 +381,26 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                       void* out, int32_t out_dtype, int32_t num_splits, pa_dims dims,
                       int32_t* status, pa_stream_t stream);
 
+/*
+ * pa_wait_selftest -- run the kernels' bounded-wait failure path once, on
+ * purpose and without a fault.  The only device failure the pages report is a
+ * timeout (the "507018" timeout of oversized task-graph prototypes in the
+ * pypto-serving top-k PR, "Exactness Design"); here every mbarrier wait inside
+ * a kernel gives up after a limit, sets PA_STATUS_TIMEOUT, drains the copies
+ * it has in flight and returns, so the context stays usable.
+ *
+ * Launches one CTA of 64 threads on `stream` that waits, with the same wait
+ * routines (one warp-uniform, one single-thread), on a shared-memory mbarrier
+ * that nothing arrives on, giving up after limit_us microseconds (1 ..
+ * 5,000,000; the attention kernels use 2 s).  No bulk copy is in flight.
+ *   status   device int32, required: PA_STATUS_TIMEOUT is OR-ed in when the
+ *            waits give up (the expected outcome); PA_STATUS_BAD_LENGTH too if
+ *            a wait ever reported a phase that never completed.
+ * Returns PA_ERR_DIMS for a limit out of range, PA_ERR_NULL_POINTER for a NULL
+ * status, or a positive CUDA launch error.
+ */
+int pa_wait_selftest(uint32_t limit_us, int32_t* status, pa_stream_t stream);
+
 /* Human-readable text for a return code (negative PA_ERR_* or positive CUDA
  * error).  Never NULL; the string is static. */
 const char* pa_status_string(int32_t code);

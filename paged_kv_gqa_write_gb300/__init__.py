@@ -35,7 +35,7 @@ EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_a
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
             "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
-            "pa_decode_fp8")
+            "pa_decode_fp8", "pa_wait_selftest")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -96,6 +96,8 @@ def load(path: str = LIB_PATH):
     lib.pa_combine.argtypes = [vp, vp, i32, vp, i32, pa_dims, vp]
     lib.pa_decode_noalloc.restype = ctypes.c_int
     lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, i32, pa_dims, vp, vp]
+    lib.pa_wait_selftest.restype = ctypes.c_int
+    lib.pa_wait_selftest.argtypes = [ctypes.c_uint32, vp, vp]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [i32]
     lib.pa_abi_version.restype = i32
@@ -452,6 +454,8 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None
     if out is None:
         out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
     _need(out, "out", out.dtype, dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
     code = PA_F32 if out.dtype == torch.float32 else PA_BF16
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     rc = load().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
@@ -459,3 +463,16 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None
                                   _ptr(status), _stream(stream))
     _check("pa_decode_noalloc", rc)
     return out
+
+
+def pa_wait_selftest(limit_us=2000, status=None, stream=None):
+    """Run the kernels' bounded-wait failure path once: a wait on an mbarrier
+    that nothing arrives on gives up after limit_us and sets PA_STATUS_TIMEOUT
+    in `status` (a 1-element int32 device tensor, created when omitted).
+    Returns `status`."""
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _need(status, "status", torch.int32, status.device)
+    rc = load().pa_wait_selftest(int(limit_us), _ptr(status), _stream(stream))
+    _check("pa_wait_selftest", rc)
+    return status

@@ -261,6 +261,33 @@ bool encode_q_decode_map(CUtensorMap* map, const void* q, const pa_dims& d, int 
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? PA_OK : (int)e; }
 
+// Argument checks shared by pa_decode_multi (and so pa_decode), pa_decode_fp8
+// and pa_decode_noalloc, in order: dims, q_len, out_dtype, schedule request;
+// then, for a non-empty batch, the row count and the tensor pointers
+// (non-null, 16-byte aligned).  *empty is set when there is nothing to launch.
+int check_decode_args(const pa_dims& d, int32_t q_len, int32_t out_dtype, int32_t num_splits,
+                      const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* context_lens, const void* out,
+                      bool* empty) {
+  *empty = false;
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return PA_ERR_DIMS;
+  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
+  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
+  if (d.num_seqs == 0) {
+    *empty = true;
+    return PA_OK;
+  }
+  // rows of q / out are indexed in 32 bits on the device
+  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGNMENT;
+  return PA_OK;
+}
+
 // Top-k slicing: about two CTAs per SM over all rows, slices of at most 16384
 // entries (64 KB of keys in shared memory), a multiple of 4 long.
 void topk_plan(int rows, int vocab, int num_sms, int* slices, int* slice_len) {
@@ -378,7 +405,7 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 105; }
+int32_t pa_abi_version(void) { return 106; }
 
 const char* pa_status_string(int32_t code) {
   switch (code) {
@@ -584,17 +611,10 @@ int pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_table, const int32_t* context_lens, int32_t q_len,
                     float scale, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
                     int32_t num_splits, pa_dims d, int32_t* status, pa_stream_t stream) {
-  int rc = check_dims(d);
-  if (rc) return rc;
-  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return PA_ERR_DIMS;
-  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
-  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
-  if (d.num_seqs == 0) return PA_OK;
-  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
-    return PA_ERR_NULL_POINTER;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return PA_ERR_ALIGNMENT;
+  bool empty = false;
+  int rc = check_decode_args(d, q_len, out_dtype, num_splits, q, k_cache, v_cache, block_table,
+                             context_lens, out, &empty);
+  if (rc || empty) return rc;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   DecodePlan pl;
@@ -621,18 +641,12 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const
                   const int32_t* context_lens, int32_t q_len, float scale, void* out,
                   int32_t out_dtype, void* workspace, size_t ws_bytes, int32_t num_splits,
                   pa_dims d, int32_t* status, pa_stream_t stream) {
-  int rc = check_dims(d);
-  if (rc) return rc;
-  if (q_len < 1 || q_len > PA_MAX_Q_LEN) return PA_ERR_DIMS;
-  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
-  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
-  if (d.num_seqs == 0) return PA_OK;
-  if ((int64_t)d.num_seqs * q_len > INT32_MAX / d.num_q_heads) return PA_ERR_DIMS;
-  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !context_lens ||
-      !out)
-    return PA_ERR_NULL_POINTER;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
+  bool empty = false;
+  int rc = check_decode_args(d, q_len, out_dtype, num_splits, q, k_cache, v_cache, block_table,
+                             context_lens, out, &empty);
+  if (rc || empty) return rc;
+  if (!k_scale || !v_scale) return PA_ERR_NULL_POINTER;
+  if (((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
     return PA_ERR_ALIGNMENT;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
@@ -713,6 +727,13 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
       pa::launch_prefill(tm_k, tm_v, tm_q, p, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int pa_wait_selftest(uint32_t limit_us, int32_t* status, pa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 5000000u) return PA_ERR_DIMS;
+  if (!status) return PA_ERR_NULL_POINTER;
+  return launch_result(pa::launch_wait_selftest((uint64_t)limit_us * 1000u, status,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -757,15 +778,10 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
                                  const int32_t* block_table, const int32_t* context_lens,
                                  float scale, void* out, int32_t out_dtype, int32_t num_splits,
                                  pa_dims d, int32_t* status, pa_stream_t stream) {
-  int rc = check_dims(d);
-  if (rc) return rc;
-  if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
-  if (num_splits < PA_SPLITS_BALANCED) return PA_ERR_SPLITS;
-  if (d.num_seqs == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
-    return PA_ERR_NULL_POINTER;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return PA_ERR_ALIGNMENT;
+  bool empty = false;
+  int rc = check_decode_args(d, 1, out_dtype, num_splits, q, k_cache, v_cache, block_table,
+                             context_lens, out, &empty);
+  if (rc || empty) return rc;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   DecodePlan pl;

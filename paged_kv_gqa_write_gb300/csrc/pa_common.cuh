@@ -86,23 +86,35 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Waits for the phase with the given parity to complete; returns false (after
-// recording PA_STATUS_TIMEOUT) if it does not within the limits above.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+// recording PA_STATUS_TIMEOUT) if it does not within limit_ns of wall-clock
+// time or kMaxPolls polls.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int32_t* status,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
-    if ((i & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if ((i & 15u) == 0 && global_timer_ns() - t0 > limit_ns) break;
   }
   if (status) atomicOr(status, PA_STATUS_TIMEOUT);
   return false;
 }
 
+// The kernels' wait: the limit above (kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  return mbar_wait_for(bar, parity, status, kWaitLimitNs);
+}
+
 // Warp-uniform variant: every lane waits and all lanes agree on the outcome,
 // so a timeout never leaves a warp diverged before a .sync.aligned operation.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* status) {
-  const bool ok = mbar_wait(bar, parity, status);
+__device__ __forceinline__ bool mbar_wait_warp_for(uint64_t* bar, uint32_t parity,
+                                                   int32_t* status, uint64_t limit_ns) {
+  const bool ok = mbar_wait_for(bar, parity, status, limit_ns);
   return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* status) {
+  return mbar_wait_warp_for(bar, parity, status, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA

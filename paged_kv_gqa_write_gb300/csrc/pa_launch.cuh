@@ -47,6 +47,10 @@ cudaError_t launch_bal_combine(const BalCombineParams& p, cudaStream_t stream);
 // Exact top-k of logit rows: per-slice candidates, then a per-row merge.
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 
+// One CTA whose waiting warp waits, with the kernels' bounded wait, on an
+// mbarrier that nothing arrives on, giving up after limit_ns.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream);

@@ -58,7 +58,7 @@ def test_python_constants_match_header(pa):
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k
-    assert pa.pa_abi_version() == 105
+    assert pa.pa_abi_version() == 106
 
 
 def test_status_strings(pa):
@@ -154,3 +154,27 @@ def test_decode_multi_rejects_q_len_on_the_host(pa):
         assert rc == pa.PA_ERR_DIMS, (bad, rc)
         n = lib.pa_decode_multi_workspace_size(d, ctypes.c_int32(bad), ctypes.c_int32(1))
         assert n == ctypes.c_size_t(-1).value
+
+
+def test_host_checks_wait_selftest_and_noalloc(pa):
+    """pa_wait_selftest refuses a limit out of range or a NULL status, and
+    pa_decode_noalloc shares pa_decode's checks (including the 32-bit row
+    bound), all before any launch."""
+    lib, h = pa.load(), _header_defines()
+    assert lib.pa_wait_selftest(0, FAKE, None) == h["PA_ERR_DIMS"]
+    assert lib.pa_wait_selftest(5000001, FAKE, None) == h["PA_ERR_DIMS"]
+    assert lib.pa_wait_selftest(1000, None, None) == h["PA_ERR_NULL_POINTER"]
+    na = lambda d, q=FAKE, out=FAKE, dt=0, ns=0: lib.pa_decode_noalloc(
+        q, FAKE, FAKE, FAKE, FAKE, 1.0, out, dt, ns, d, None, None)
+    assert na(_dims(pa, head_dim=64)) == h["PA_ERR_HEAD_DIM"]
+    assert na(_dims(pa), dt=7) == h["PA_ERR_OUT_DTYPE"]
+    assert na(_dims(pa), ns=-2) == h["PA_ERR_SPLITS"]
+    assert na(_dims(pa), q=None) == h["PA_ERR_NULL_POINTER"]
+    assert na(_dims(pa), out=MIS) == h["PA_ERR_ALIGNMENT"]
+    assert na(_dims(pa, num_seqs=0)) == 0
+    # B * Hq rows beyond int32: refused like pa_decode (no scratch is needed
+    # with one split, so the size check alone would not catch it)
+    huge = _dims(pa, num_seqs=40_000_000, num_q_heads=128, num_kv_heads=8)
+    assert na(huge, ns=1) == h["PA_ERR_DIMS"]
+    assert lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, 0, None, 0, 1, huge, None,
+                         None) == h["PA_ERR_DIMS"]

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads as W
-from pa_testutil import ATOL, assert_close, dev_status
+from pa_testutil import ATOL, assert_close, dev_status, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -65,3 +65,30 @@ def test_rejects_sizes_beyond_the_scratch_array(cuda_lib):
                                            fake, cuda_lib.PA_F32, 32, big, None, None)
     assert rc == -13
     assert "PA_NOALLOC_SCRATCH_BYTES" in cuda_lib.pa_status_string(rc)
+
+
+def test_python_wrapper_balanced_matches_the_oracle(cuda_lib):
+    # the binding's pa_decode_noalloc with an explicit page-balanced schedule,
+    # twice in a row on different inputs, each checked against the FP64 oracle
+    cases = [W.custom_case(902, [4096, 3000, 17, 1, 2500, 129, 0, 640], Hq=40, Hkv=8,
+                           max_pages_per_seq=32),
+             W.custom_case(903, [100, 4096, 4096, 300], Hq=64, Hkv=8, max_pages_per_seq=32)]
+    for case in cases:
+        c = case.to("cuda")
+        out = torch.full((case.B, case.Hq, 128), float("nan"), dtype=torch.float32,
+                         device="cuda")
+        st = dev_status()
+        cuda_lib.pa_decode_noalloc(c.q, c.k_cache, c.v_cache, c.block_table, c.context_lens,
+                                   c.scale, out=out, num_splits=cuda_lib.PA_SPLITS_BALANCED,
+                                   status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert_close(out, oracle_decode(case), atol=ATOL, what="noalloc balanced vs oracle")
+
+
+def test_python_wrapper_rejects_other_out_dtypes(cuda_lib):
+    c = W.tiny_decode().to("cuda")
+    out = torch.empty(c.B, c.Hq, 128, dtype=torch.float16, device="cuda")
+    with pytest.raises(TypeError):
+        cuda_lib.pa_decode_noalloc(c.q, c.k_cache, c.v_cache, c.block_table, c.context_lens,
+                                   c.scale, out=out)
