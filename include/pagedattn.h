@@ -381,6 +381,20 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                       void* out, int32_t out_dtype, int32_t num_splits, pa_dims dims,
                       int32_t* status, pa_stream_t stream);
 
+/* Work items (sequence, pair of 128-token query tiles, query head) that each
+ * CTA pair of a pa_prefill_chunk launch schedules longest-first; launches
+ * with more than PA_PREFILL_SCHEDULE_ITEMS x pa_prefill_pairs() items deal
+ * them round-robin instead. */
+#define PA_PREFILL_SCHEDULE_ITEMS 64
+
+/*
+ * pa_prefill_pairs -- CTA pairs (clusters of two CTAs on two SMs) that a
+ * pa_prefill_chunk launch uses at most on the current device: the pairs that
+ * fit on the GPU at once.  Returns the count (>= 1), PA_ERR_NO_DEVICE, or a
+ * positive CUDA error.
+ */
+int32_t pa_prefill_pairs(void);
+
 /*
  * pa_wait_selftest -- run the kernels' bounded-wait failure path once, on
  * purpose and without a fault.  The only device failure the pages report is a

@@ -27,6 +27,7 @@ PA_BALANCED_MAX_SEQS = 512
 PA_TOPK_MAX_K = 32
 PA_MAX_Q_LEN = 16
 PA_MAX_PROLOGUE_HEADS = 384
+PA_PREFILL_SCHEDULE_ITEMS = 64
 (PA_ERR_NULL_POINTER, PA_ERR_HEAD_DIM, PA_ERR_PAGE_SIZE, PA_ERR_HEADS, PA_ERR_DIMS,
  PA_ERR_ALIGNMENT, PA_ERR_OUT_DTYPE, PA_ERR_WORKSPACE, PA_ERR_SPLITS, PA_ERR_TOO_MANY_SEQS,
  PA_ERR_TENSOR_MAP, PA_ERR_NO_DEVICE, PA_ERR_NOALLOC_TOO_LARGE) = range(-1, -14, -1)
@@ -35,7 +36,7 @@ EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_a
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
             "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
-            "pa_decode_fp8", "pa_wait_selftest")
+            "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -96,6 +97,8 @@ def load(path: str = LIB_PATH):
     lib.pa_combine.argtypes = [vp, vp, i32, vp, i32, pa_dims, vp]
     lib.pa_decode_noalloc.restype = ctypes.c_int
     lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, i32, pa_dims, vp, vp]
+    lib.pa_prefill_pairs.restype = i32
+    lib.pa_prefill_pairs.argtypes = []
     lib.pa_wait_selftest.restype = ctypes.c_int
     lib.pa_wait_selftest.argtypes = [ctypes.c_uint32, vp, vp]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -476,3 +479,11 @@ def pa_wait_selftest(limit_us=2000, status=None, stream=None):
     rc = load().pa_wait_selftest(int(limit_us), _ptr(status), _stream(stream))
     _check("pa_wait_selftest", rc)
     return status
+
+
+def pa_prefill_pairs() -> int:
+    """CTA pairs a pa_prefill_chunk launch uses at most on the current device."""
+    n = int(load().pa_prefill_pairs())
+    if n < 1:
+        raise PagedAttnError("pa_prefill_pairs", n)
+    return n

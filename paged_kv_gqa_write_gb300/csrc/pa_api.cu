@@ -701,7 +701,12 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   CUtensorMap tm_k, tm_v, tm_q;
-  if (!encode_cache_map(&tm_k, k_cache, d) || !encode_cache_map(&tm_v, v_cache, d))
+  // each CTA of a pair stages half a page tile: K as 64-key x 64-dim boxes,
+  // V as 128-key x 64-dim boxes
+  if (!encode_2d(&tm_k, k_cache, (uint64_t)d.num_kv_heads * kHeadDim,
+                 (uint64_t)d.num_pages * kPage, (uint64_t)d.num_kv_heads * kHeadDim * 2, 64, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_cache_map(&tm_v, v_cache, d))
     return PA_ERR_TENSOR_MAP;
   // q as [num_tokens, Hq, 128]: a box is 128 tokens of one head, 64 dims wide.
   if (!encode_3d(&tm_q, q, kHeadDim, d.num_q_heads, (uint64_t)num_tokens, 64, 128,
@@ -725,6 +730,14 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   p.out_f32 = out_dtype == PA_F32;
   return launch_result(
       pa::launch_prefill(tm_k, tm_v, tm_q, p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t pa_prefill_pairs(void) {
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  int pairs = 0;
+  const cudaError_t e = pa::prefill_pairs(sms, &pairs);
+  return e == cudaSuccess ? pairs : launch_result(e);
 }
 
 int pa_wait_selftest(uint32_t limit_us, int32_t* status, pa_stream_t stream) {

@@ -51,6 +51,10 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 // mbarrier that nothing arrives on, giving up after limit_ns.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t stream);
 
+// CTA pairs a prefill launch uses at most on the current device (the pairs
+// that can be resident at once), cached per device.
+cudaError_t prefill_pairs(int num_sms, int* pairs);
+
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream);

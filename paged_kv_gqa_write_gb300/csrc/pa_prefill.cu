@@ -1,5 +1,6 @@
 // pa_prefill.cu -- causal chunked-prefill attention over the paged cache on
-// the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// the 5th-generation tensor cores, one CTA pair (a cluster of two CTAs on two
+// SMs) per work item, with pair MMAs (tcgen05 cta_group::2, M = 256).
 //
 // "Qwen3-14B" (pypto-lib), "prefill_fwd": per layer the KV cache update is
 // followed by causal attention over token-major packed inputs
@@ -9,35 +10,50 @@
 // own sequence, read from the paged cache (prior context plus the chunk,
 // which pa_kv_write has already stored).
 //
-// Work item: (sequence, pair of consecutive 128-token query tiles A and B,
-// query head).  Both tiles share every K/V page tile the CTA loads, so each
-// 64 KB of K/V feeds four 128x128x128 BF16 products (S_A, S_B, P_A.V, P_B.V):
-// with one query tile per load the kernel would be bound by L2 bandwidth
-// (~72 GB/s per SM), with two it needs half that.
-//  * warp 0 (one lane) loads the two Q tiles (3-D TMA map over [T, Hq, 128])
-//    and the K page tiles into a 3-deep ring; warp 10 (one lane) the V page
-//    tiles into a 2-deep ring (128-byte swizzle, the layout the tensor core
-//    reads).
-//  * warp 1 (one lane) issues tcgen05.mma (M=128, N=128, K=16 steps) in the
-//    order P_A(j).V(j), S_A(j+1), P_B(j).V(j), S_B(j+1), so that each softmax
-//    group overlaps the other's MMAs.  P_t(j) is read from tensor memory (it
-//    overwrites the first 64 columns of S_t(j) as packed BF16 pairs); V is an
-//    MN-major shared-memory operand.  The MMAs of one thread execute in issue
-//    order, so P_t(j) is consumed before S_t(j+1) is written.  The warp owns
-//    the TMEM allocation (S_A, S_B, O_A, O_B: 512 columns).
-//  * warps 2-5 (tile A) and 6-9 (tile B): one thread per query row.  Per key
-//    tile: tcgen05.ld of the score row, causal mask (only on tiles that cross
-//    the row's position), online softmax in the log2 domain (max of the raw
-//    scores, one FMA + exp2 per element), P into TMEM.  O_t is rescaled in
-//    TMEM only when the max grows by more than 2^8 (the final O / l is
-//    unchanged by the choice of reference max).  Epilogue: O_t / l per row.
-// Key pages entirely above a tile's last query position are never loaded for
-// it (causal tile skipping); V rows past the sequence's context in its last
-// page are zeroed in shared memory before use (P is 0 there, but 0 * NaN is
-// NaN).  Items are dealt to the persistent CTAs in decreasing order of
-// key-tile count, snaking across CTAs (a greedy longest-first balance every
-// CTA computes from the lengths); very large launches fall back to
-// round-robin.
+// Work item: (sequence, pair of consecutive 128-token query tiles, query
+// head).  CTA r of the pair owns query tile r: its 128 rows of Q, S, P and O.
+// Per key page tile (one "step") the even CTA issues two pair products:
+//   S = Q K^T   M = 256 (both tiles), N = 128 keys, K = 128 dims
+//   O += P V    M = 256, N = 128 dims, K = 128 keys
+// Each CTA stages only half of the page tile: keys 64r..64r+63 of K (the
+// half of S's N columns the pair product takes from it) and dims 64r..64r+63
+// of V (the half of O's N columns), so one 64 KB page tile feeds four
+// 128x128x128 products while each SM reads 32 KB of it.
+//  * warp 0 (one lane): Q tiles (double-buffered: the next item's tile loads
+//    during this one) and K halves (3-stage ring: stage j % 3 is free once
+//    S(j - 3) is done).  Both CTAs' loads complete on the even CTA's
+//    barriers (paired TMA), which its S issuer waits on.
+//  * warp 10 (one lane): V halves (3-stage ring, free once P.V(j - 3) is
+//    done), completing locally.
+//  * warp 1: both CTAs allocate tensor memory together (S0, S1, S2, O).  In
+//    the even CTA one lane issues the S products and one lane of warp 11 the
+//    P.V products: each issuer's waits and commits overlap the other's
+//    products in the tensor core's queue.  S is triple-buffered, so the
+//    scores of the next steps are computed while the softmax works, and P(j)
+//    is written back over S(j) (A operand from tensor memory), so the
+//    softmax runs up to three steps ahead of P.V; S(j + 3) is issued only
+//    once P.V(j) has completed.  In the odd CTA warp 1 relays "P ready" to
+//    the even CTA (below).
+//  * warps 2-9: softmax and epilogue, two threads per query row (warps w and
+//    w + 4 share the row's tensor-memory lanes; each takes 64 of the 128
+//    columns).  Per step: tcgen05.ld of the score half-row, causal mask (only
+//    on tiles that cross the row's position), online softmax in the log2
+//    domain against a running reference that moves only when a score exceeds
+//    it by 2^8 (the two halves agree on it through shared memory; O is then
+//    rescaled in tensor memory), P rounded to BF16 pairs into the first 32
+//    of the half's own 64 S columns, and the row sum taken over the rounded
+//    weights the MMA uses.  The warps then wait for this
+//    CTA's V half, zero its rows past the context on the sequence's last page
+//    (P is 0 there, but 0 * NaN is NaN), and arrive on the P barrier.
+// "P ready" crosses the pair once per step: the odd CTA's warps arrive on a
+// local barrier and its relay thread, having acquired their writes, arrives
+// with cluster-scope release on the even CTA's barrier, so the P.V product
+// (which reads both CTAs' P and V halves) is ordered after every write.
+// Key pages entirely above both tiles' last query positions are never loaded
+// (causal tile skipping); the lower tile sees its pair's last page fully
+// masked.  Items are dealt to the pairs in decreasing order of key-tile
+// count, snaking across pairs (a greedy longest-first balance every CTA
+// computes from the lengths); very large launches fall back to round-robin.
 #include <type_traits>
 
 #include "pa_launch.cuh"
@@ -45,48 +61,64 @@
 namespace pa {
 namespace {
 
+constexpr int kSoftWarp0 = 2;                 // softmax warps 2 .. 9
+constexpr int kSoftmaxWarps = 8;
 constexpr int kVWarp = 10;                    // V producer
-constexpr int kThreads = (kVWarp + 1) * 32;
-constexpr int kTileBytes = 128 * 128 * 2;     // 32 KB: one 128x128 bf16 tile
-constexpr int kBox = 16384;                   // 64-column half of a tile
-constexpr int kRingK = 2, kRingV = 3;
-constexpr int kMaxList = 64;                  // scheduled items per CTA
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int kQ = 0;                         // Q_A, Q_B
-constexpr int kK = kQ + 2 * kTileBytes;
-constexpr int kV = kK + kRingK * kTileBytes;
+constexpr int kPvWarp = 11;                   // P.V issuer (even CTA)
+constexpr int kThreads = (kPvWarp + 1) * 32;
+constexpr int kQBytes = 128 * 128 * 2;        // one query tile (two 64-column boxes)
+constexpr int kQBox = 16384;
+constexpr int kKBytes = 64 * 128 * 2;         // this CTA's K half: 64 keys x 128 dims
+constexpr int kKBox = 8192;                   // 64 keys x 64 dims
+constexpr int kVBytes = 128 * 64 * 2;         // this CTA's V half: 128 keys x 64 dims
+// the K and V rings have as many stages as there are S buffers, so that S(j)
+// done frees K stage j % 3 and P.V(j) done frees V stage j % 3
+constexpr int kNumS = 3, kRingK = kNumS, kRingV = kNumS;
+constexpr int kMaxList = PA_PREFILL_SCHEDULE_ITEMS;  // scheduled items per pair
+// shared memory layout (offsets from a 1024-aligned base; identical in both
+// CTAs: a pair MMA reads both at the same offsets)
+constexpr int kQ = 0;
+constexpr int kK = kQ + 2 * kQBytes;
+constexpr int kV = kK + kRingK * kKBytes;
+constexpr int kX = kV + kRingV * kVBytes;     // row exchange between the two halves: [2][128] float
 constexpr int kListInts = 5;                  // per item: s, pair|head, tok0, chunk len, ctx
-constexpr int kList = kV + kRingV * kTileBytes;  // schedule [kMaxList][kListInts] int
+constexpr int kList = kX + 2 * 128 * 4;       // schedule [kMaxList][kListInts] int
 constexpr int kBars = kList + kMaxList * kListInts * 4;
-constexpr int kNumBars = 2 * 2 + 2 * kRingK + 2 * kRingV + 4 * 2;
+constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 4 * kNumS + 1;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
-constexpr int kMaxCost = 4096;                // schedule histogram buckets (ring scratch)
-constexpr int kMaxSchedSeqs = (kRingV * kTileBytes / 4 - 1) / 4;  // sequences the schedule stages
-// TMEM columns
-constexpr uint32_t kColS = 0;     // S_A, S_B: 128 columns each (P in their first 64)
-constexpr uint32_t kColO = 256;   // O_A, O_B: 128 columns each
+constexpr int kMaxCost = 4096;                // schedule histogram buckets (K ring scratch)
+constexpr int kMaxSchedSeqs = (kRingV * kVBytes / 4 - 1) / 4;  // sequences the schedule stages
+// TMEM columns (the same in both CTAs)
+constexpr uint32_t kColS = 0;     // S0, S1, S2: 128 columns each, by step mod 3; P(j) over S(j)
+constexpr uint32_t kColO = 384;   // O: 128 columns
+// P(j) as BF16 pairs inside S(j): keys 0-63 (half 0) in columns 0-31, keys
+// 64-127 (half 1) in columns 64-95, each half writing over its own scores
+__host__ __device__ constexpr uint32_t p_col(int kstep) {
+  return kstep < 4 ? kstep * 8 : 64 + (kstep - 4) * 8;
+}
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint16_t kPairMask = 3;             // both CTAs of the cluster
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // copies land in microseconds
 
 struct Bars {
-  uint64_t* q_full;   // [2] per query tile
-  uint64_t* q_empty;
-  uint64_t* k_full;   // [kRingK]
-  uint64_t* k_empty;
-  uint64_t* v_full;   // [kRingV]
-  uint64_t* v_empty;
-  uint64_t* s_full;   // [2] per query tile
-  uint64_t* p_full;
-  uint64_t* o_done;
-  uint64_t* o_free;
+  uint64_t* q_full;   // [2] even CTA: both CTAs' query tiles landed
+  uint64_t* q_empty;  // [2] the item's last S product read the tile
+  uint64_t* k_full;   // [3] even CTA: both K halves landed
+  uint64_t* v_full;   // [3] this CTA's V half landed
+  uint64_t* s_full;   // [3] S(g) in buffer g % 3 done (and K stage g % 3 free)
+  uint64_t* p_full;   // [3] even CTA: P(g) written in both CTAs, V(g) halves in place
+  uint64_t* p_local;  // [3] odd CTA: its softmax warps' P(g), for the relay
+  uint64_t* o_done;   // [3] P.V(g) done: O holds every step <= g, V stage g % 3 free
+  uint64_t* drain;    // every MMA issued (by both issuers) has completed
 };
 
 struct Item {
   int s, g, h, pair;
-  int tok0;          // packed index of tile A's first query token
-  int nrows[2];      // query rows of tiles A, B (<= 128; B may be 0)
-  int nkt[2];        // key tiles each query tile visits (0: none / lengths invalid)
-  int nmax;          // key tiles the pair loads
+  int tok0;          // packed index of the pair's first query token
+  int nrows[2];      // query rows of tiles 0, 1 (<= 128; tile 1 may be 0)
+  int nkt[2];        // key tiles each query tile sees (0: none / lengths invalid)
+  int nmax;          // key tiles (steps) the pair runs
   int prior, ctx;
   bool len_ok;
 };
@@ -115,22 +147,24 @@ __device__ __forceinline__ Item make_item(const PrefillParams& p, int s, int pai
   return it;
 }
 
+// Key tiles a pair runs: its two query tiles go through the key tiles in
+// lockstep (one M = 256 product per step), so the longer tile's count.
 __device__ __forceinline__ int pair_cost(const PrefillParams& p, int n, int ctx, int pair) {
   if (!lengths_ok(p, n, ctx)) return 0;
   int c = 0;
   for (int t = 0; t < 2; ++t) {
     const int q0 = pair * 256 + t * 128;
     const int nr = min(128, n - q0);
-    if (nr > 0) c += (ctx - n + q0 + nr - 1) / kPage + 1;
+    if (nr > 0) c = max(c, (ctx - n + q0 + nr - 1) / kPage + 1);
   }
   return c;
 }
 
 // Greedy longest-first schedule: all items sorted by key-tile count
-// (descending; ties in (sequence, pair, head) order), dealt to CTAs in a snake
-// (0..N-1, N-1..0, ...).  Writes this CTA's items in order and returns their
-// count, or -1 on every CTA when the launch is too large for the table
-// (round-robin then).  Built by the 32 lanes of one warp, which all call it
+// (descending; ties in (sequence, pair, head) order), dealt to the N CTA pairs
+// in a snake (0..N-1, N-1..0, ...).  Writes pair c's items in order and
+// returns their count, or -1 on every CTA when the launch is too large for
+// the table (round-robin then).  Both CTAs of a pair build the same list.  Built by the 32 lanes of one warp, which all call it
 // and get the same result: a pair at a time on one thread, the walk took most
 // of the kernel's start-up.
 //   scratch: 3 * kMaxCost ints (pairs per cost, first sorted position of each
@@ -140,7 +174,7 @@ __device__ __forceinline__ int pair_cost(const PrefillParams& p, int n, int ctx,
 __device__ int build_schedule(const PrefillParams& p, int* scratch, int* seqs, int* list, int N,
                               int c, int lane) {
   constexpr unsigned kAll = 0xffffffffu;
-  const int maxc = 2 * p.max_pages + 1;
+  const int maxc = p.max_pages + 2;
   if (maxc > kMaxCost || p.Hq > 256 || p.B > kMaxSchedSeqs) return -1;
   int* hist = scratch;
   int* start = scratch + kMaxCost;
@@ -267,10 +301,12 @@ __device__ int build_schedule(const PrefillParams& p, int* scratch, int* seqs, i
 }
 
 // Item source shared by all roles: the schedule table, or round-robin over
-// (sequence, pair, head) when the table is unavailable.
+// (sequence, pair, head) across the N pairs when the table is unavailable.
+// A source walks its items in increasing r.
 struct ItemSource {
   const int* list;
   int count;  // -1: round-robin
+  int c, N;   // this pair, pairs in the launch
   int s = 0, pairs_before = 0, tok_before = 0;
   __device__ bool get(const PrefillParams& p, int r, Item& it) {
     if (count >= 0) {
@@ -279,7 +315,9 @@ struct ItemSource {
       it = make_item(p, e[0], e[1] >> 8, e[1] & 255, e[2], e[3], e[4]);
       return true;
     }
-    const int i = (int)blockIdx.x + r * (int)gridDim.x;
+    const int64_t i64 = (int64_t)c + (int64_t)r * N;
+    if (i64 > INT32_MAX) return false;
+    const int i = (int)i64;
     const int pair = i / p.Hq, g = i - pair * p.Hq;
     while (s < p.B) {
       const int n = __ldg(p.chunk_lens + s);
@@ -295,16 +333,27 @@ struct ItemSource {
                    __ldg(p.context_lens + s));
     return true;
   }
+  // Next item with key tiles (r advanced past it); false at the end.
+  __device__ bool next_with_tiles(const PrefillParams& p, int& r, Item& it) {
+    while (get(p, r, it)) {
+      ++r;
+      if (it.nmax > 0) return true;
+    }
+    return false;
+  }
 };
 
-// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 BF16 (lane = row, pairs per column).
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// Waits for the last phase of each barrier that saw `issued` loads spread
+// round-robin over `n` barriers (no wait for barriers that saw none): every
+// copy in flight lands before the shared memory is released.
+__device__ __forceinline__ void drain_loads(uint64_t* bars, int n, uint32_t issued, int32_t* status,
+                                            bool cluster_scope) {
+  for (int i = 0; i < n; ++i) {
+    const uint32_t cnt = issued > (uint32_t)i ? (issued - 1 - i) / n + 1 : 0;
+    if (cnt == 0) continue;
+    if (cluster_scope) mbar_wait_cl_for(&bars[i], (cnt - 1) & 1, status, kDrainLimitNs);
+    else mbar_wait_for(&bars[i], (cnt - 1) & 1, status, kDrainLimitNs);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -318,278 +367,297 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.q_full = bar;
   B.q_empty = bar + 2;
   B.k_full = bar + 4;
-  B.k_empty = B.k_full + kRingK;
-  B.v_full = B.k_empty + kRingK;
-  B.v_empty = B.v_full + kRingV;
-  B.s_full = B.v_empty + kRingV;
-  B.p_full = B.s_full + 2;
-  B.o_done = B.p_full + 2;
-  B.o_free = B.o_done + 2;
+  B.v_full = B.k_full + kRingK;
+  B.s_full = B.v_full + kRingV;
+  B.p_full = B.s_full + kNumS;
+  B.p_local = B.p_full + kNumS;
+  B.o_done = B.p_local + kNumS;
+  B.drain = B.o_done + kNumS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
   int* list_count = reinterpret_cast<int*>(tmem_slot + 1);
   int* list = reinterpret_cast<int*>(smem + kList);
+  float* xch = reinterpret_cast<float*>(smem + kX);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // query tile of the pair this CTA owns
+  const bool even = rank == 0;              // issues the pair MMAs
+  const int npairs = (int)cluster_count_x(), pair_id = (int)cluster_id_x();
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&B.q_full[t], 1);
       mbar_init(&B.q_empty[t], 1);
     }
-    for (int i = 0; i < kRingK; ++i) {
-      mbar_init(&B.k_full[i], 1);
-      mbar_init(&B.k_empty[i], 1);
-    }
-    for (int i = 0; i < kRingV; ++i) {
-      mbar_init(&B.v_full[i], 1);
-      mbar_init(&B.v_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRingK; ++i) mbar_init(&B.k_full[i], 1);
+    for (int i = 0; i < kRingV; ++i) mbar_init(&B.v_full[i], 1);
+    for (int i = 0; i < kNumS; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], 128);
+      mbar_init(&B.p_full[i], kSoftmaxWarps + 1);  // this CTA's warps + the odd CTA's relay
+      mbar_init(&B.p_local[i], kSoftmaxWarps);
       mbar_init(&B.o_done[i], 1);
-      mbar_init(&B.o_free[i], 128);
     }
+    mbar_init(B.drain, 2);  // one commit from each issuer
     fence_mbar_init();
   }
   if (warp == 0) {
     // the rings are idle until the first load: scratch for the schedule
     const int count = build_schedule(p, reinterpret_cast<int*>(smem + kK),
-                                     reinterpret_cast<int*>(smem + kV), list, gridDim.x,
-                                     blockIdx.x, lane);
+                                     reinterpret_cast<int*>(smem + kV), list, npairs, pair_id,
+                                     lane);
     if (lane == 0) *list_count = count;
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
+  // both CTAs' barriers are initialised before any paired copy, multicast
+  // commit or remote arrival targets them
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  ItemSource src{list, *list_count};
+  ItemSource src{list, *list_count, pair_id, npairs};
 
   if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 0: Q and K tiles; warp 10: V tiles.  Each runs ahead as far as its ring allows.
     if (lane == 0) {
       const bool is_k = warp == 0;
-      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-      const int ring_n = is_k ? kRingK : kRingV;
-      uint64_t* full = is_k ? B.k_full : B.v_full;
-      uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-      uint8_t* ring = smem + (is_k ? kK : kV);
       if (is_k) prefetch_tensor_map(&tm_q);
-      prefetch_tensor_map(map);
-      const uint64_t pol_kv = l2_policy_evict_last();  // reused by other tiles/heads
+      prefetch_tensor_map(is_k ? &tm_k : &tm_v);
+      const uint64_t pol_kv = l2_policy_evict_last();  // reused by the other heads' items
       const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t tiles = 0;
-      uint32_t qitems[2] = {0, 0};  // items in which each query tile had key tiles
+      uint32_t tiles = 0, qitems = 0;
       bool ok = true;
       Item it;
-      for (int r = 0; ok && src.get(p, r, it); ++r) {
-        if (it.nmax == 0) continue;
+      int r = 0;
+      while (ok && src.next_with_tiles(p, r, it)) {
         const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
+        if (is_k) {
+          // this CTA's query tile, once the item two back released the buffer
+          const int qb = qitems & 1;
+          if (!(ok = mbar_wait_cl(&B.q_empty[qb], ((qitems >> 1) & 1) ^ 1, p.status))) break;
+          ++qitems;
+          if (even) mbar_arrive_expect_tx(&B.q_full[qb], 2 * kQBytes);
+          const uint32_t qbar = mapa_shared(smem_u32(&B.q_full[qb]), 0);
+          const int z = it.tok0 + (int)rank * 128;
+          tma_load_3d_pair(smem + kQ + qb * kQBytes, &tm_q, 0, it.g, z, qbar, pol_q);
+          tma_load_3d_pair(smem + kQ + qb * kQBytes + kQBox, &tm_q, 64, it.g, z, qbar, pol_q);
+        }
         for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
           int page = __ldg(bt + kt);
           if (page < 0 || page >= p.num_pages) page = 0;  // sequence reported invalid
-          const int slot = tiles % ring_n;
-          const int x = it.h * kHeadDim, y = page * kPage;
-          if (!(ok = mbar_wait(&empty[slot], ((tiles / ring_n) & 1) ^ 1, p.status))) break;
-          mbar_arrive_expect_tx(&full[slot], kTileBytes);
-          tma_load_2d(ring + slot * kTileBytes, map, x, y, &full[slot], pol_kv);
-          tma_load_2d(ring + slot * kTileBytes + kBox, map, x + 64, y, &full[slot], pol_kv);
-          if (is_k && kt == 0) {
-            // each query tile's Q once its buffer is free (after the previous
-            // item's last QK^T of that tile); the first K tile goes ahead of it
-            for (int t = 0; t < 2 && ok; ++t) {
-              if (it.nkt[t] == 0) continue;
-              if (!(ok = mbar_wait(&B.q_empty[t], (qitems[t] & 1) ^ 1, p.status))) break;
-              ++qitems[t];
-              mbar_arrive_expect_tx(&B.q_full[t], kTileBytes);
-              tma_load_3d(smem + kQ + t * kTileBytes, &tm_q, 0, it.g, it.tok0 + t * 128,
-                          &B.q_full[t], pol_q);
-              tma_load_3d(smem + kQ + t * kTileBytes + kBox, &tm_q, 64, it.g, it.tok0 + t * 128,
-                          &B.q_full[t], pol_q);
-            }
-            if (!ok) break;
+          const int y = page * kPage;
+          if (is_k) {
+            // stage tiles % 3 is free once S(tiles - 3) is done
+            const int st = tiles % kRingK;
+            if (tiles >= (uint32_t)kRingK &&
+                !(ok = mbar_wait_cl(&B.s_full[st], ((tiles / kRingK) & 1) ^ 1, p.status)))
+              break;
+            if (even) mbar_arrive_expect_tx(&B.k_full[st], 2 * kKBytes);
+            const uint32_t kbar = mapa_shared(smem_u32(&B.k_full[st]), 0);
+            uint8_t* dst = smem + kK + st * kKBytes;
+            tma_load_2d_pair(dst, &tm_k, it.h * kHeadDim, y + (int)rank * 64, kbar, pol_kv);
+            tma_load_2d_pair(dst + kKBox, &tm_k, it.h * kHeadDim + 64, y + (int)rank * 64, kbar,
+                             pol_kv);
+          } else {
+            // stage tiles % 3 is free once P.V(tiles - 3) is done
+            const int st = tiles % kRingV;
+            if (tiles >= (uint32_t)kRingV &&
+                !(ok = mbar_wait_cl(&B.o_done[st], ((tiles / kRingV) & 1) ^ 1, p.status)))
+              break;
+            mbar_arrive_expect_tx(&B.v_full[st], kVBytes);
+            tma_load_2d(smem + kV + st * kVBytes, &tm_v, it.h * kHeadDim + (int)rank * 64, y,
+                        &B.v_full[st], pol_kv);
           }
         }
       }
+      // copies still in flight (only after a timeout) land before teardown;
+      // the even CTA's barriers count both CTAs' Q and K halves
+      if (!is_k) drain_loads(B.v_full, kRingV, tiles, p.status, false);
+      else if (even) {
+        drain_loads(B.q_full, 2, qitems, p.status, true);
+        drain_loads(B.k_full, kRingK, tiles, p.status, true);
+      }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_qk = umma_idesc_bf16(128, 128, false, false);
-      const uint32_t idesc_pv = umma_idesc_bf16(128, 128, false, true);
-      uint32_t tiles = 0;
-      uint32_t gt[2] = {0, 0};     // key tiles each query tile has been through (all items)
-      uint32_t gitems[2] = {0, 0};  // items in which each query tile had key tiles
+  } else if (warp == 1 || warp == kPvWarp) {
+    if (even && lane == 0 && warp == 1) {
+      // ---------------------------------------------------------- S issuer (even CTA)
+      const uint32_t idesc_qk = umma_idesc_bf16(256, 128, false, false);  // Q, K: K-major
+      uint32_t g = 0, qi = 0;
       bool ok = true;
-      auto qk = [&](int t, uint32_t kidx) {
-        const uint32_t q_addr = smem_u32(smem + kQ + t * kTileBytes);
-        const uint32_t k_addr = smem_u32(smem + kK + (kidx % kRingK) * kTileBytes);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = umma_sdesc_sw128(q_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_sdesc_sw128(k_addr + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + kColS + t * 128, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&B.s_full[t]);
-      };
-      auto pv = [&](int t, uint32_t kidx, bool first) -> bool {
-        if (!mbar_wait(&B.p_full[t], gt[t] & 1, p.status)) return false;
-        if (!mbar_wait(&B.v_full[kidx % kRingV], (kidx / kRingV) & 1, p.status)) return false;
-        if (first && gitems[t] > 1 && !mbar_wait(&B.o_free[t], gitems[t] & 1, p.status))
-          return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + kV + (kidx % kRingV) * kTileBytes);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t bd = umma_sdesc_sw128(v_addr + k * 2048, kBox, 1024);
-          umma_bf16_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + k * 8, bd, idesc_pv,
-                       (first && k == 0) ? 0u : 1u);
-        }
-        umma_commit(&B.o_done[t]);
-        ++gt[t];
-        return true;
-      };
-      auto wait_k = [&](uint32_t kidx) -> bool {
-        const bool r = mbar_wait(&B.k_full[kidx % kRingK], (kidx / kRingK) & 1, p.status);
-        tc_fence_after();
-        return r;
-      };
       Item it;
-      for (int r = 0; ok && src.get(p, r, it); ++r) {
-        if (it.nmax == 0) continue;
-        const uint32_t k0 = tiles;
-        if (!(ok = wait_k(k0))) break;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (it.nkt[t] == 0) continue;
-          ++gitems[t];
-          if (!(ok = mbar_wait(&B.q_full[t], (gitems[t] - 1) & 1, p.status))) break;
+      int r = 0;
+      while (ok && src.next_with_tiles(p, r, it)) {
+        const int qb = qi & 1;
+        if (!(ok = mbar_wait_cl(&B.q_full[qb], (qi >> 1) & 1, p.status))) break;
+        const uint32_t qa = smem_u32(smem + kQ + qb * kQBytes);
+        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
+          const int sb = g % kNumS;
+          if (!(ok = mbar_wait_cl(&B.k_full[sb], (g / kNumS) & 1, p.status))) break;
+          // S buffer sb holds P(g - 3): free once P.V(g - 3) is done
+          if (g >= (uint32_t)kNumS &&
+              !(ok = mbar_wait_cl(&B.o_done[sb], ((g / kNumS) & 1) ^ 1, p.status)))
+            break;
           tc_fence_after();
-          qk(t, k0);
-          if (it.nkt[t] == 1) umma_commit(&B.q_empty[t]);
+          const uint32_t ka = smem_u32(smem + kK + sb * kKBytes);
+          const uint32_t d = tmem + kColS + sb * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = umma_sdesc_sw128(qa + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_sdesc_sw128(ka + (k >> 2) * kKBox + (k & 3) * 32, 16, 1024);
+            umma_bf16_ss_pair(d, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          }
+          umma_commit_pair(&B.s_full[sb], kPairMask);
         }
         if (!ok) break;
-        umma_commit(&B.k_empty[k0 % kRingK]);
-        for (int j = 0; j < it.nmax && ok; ++j) {
-          const uint32_t kidx = k0 + j;
-          const bool next = j + 1 < it.nmax;
-          bool k_ready = false;
-          if (j < it.nkt[0]) {
-            if (!(ok = pv(0, kidx, j == 0))) break;
-            if (j + 1 < it.nkt[0]) {
-              if (!(ok = wait_k(kidx + 1))) break;
-              k_ready = true;
-              qk(0, kidx + 1);
-              if (j + 2 == it.nkt[0]) umma_commit(&B.q_empty[0]);
-            }
+        umma_commit_pair(&B.q_empty[qb], kPairMask);
+        ++qi;
+      }
+      // every product issued completes before the columns are released
+      umma_commit_pair(B.drain, kPairMask);
+    } else if (even && lane == 0) {
+      // ---------------------------------------------------------- P.V issuer (even CTA)
+      const uint32_t idesc_pv = umma_idesc_bf16(256, 128, false, true);   // P (TMEM), V MN-major
+      uint32_t g = 0;
+      bool ok = true;
+      Item it;
+      int r = 0;
+      while (ok && src.next_with_tiles(p, r, it)) {
+        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
+          // both CTAs' P (tensor memory) and V halves are in place
+          const int sb = g % kNumS;
+          if (!(ok = mbar_wait_cl(&B.p_full[sb], (g / kNumS) & 1, p.status))) break;
+          tc_fence_after();
+          const uint32_t va = smem_u32(smem + kV + sb * kVBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t bd = umma_sdesc_sw128(va + k * 2048, kVBytes, 1024);
+            umma_bf16_ts_pair(tmem + kColO, tmem + kColS + sb * 128 + p_col(k), bd, idesc_pv,
+                              (kt > 0 || k > 0) ? 1u : 0u);
           }
-          if (j < it.nkt[1]) {
-            if (!(ok = pv(1, kidx, j == 0))) break;
-          }
-          umma_commit(&B.v_empty[kidx % kRingV]);
-          if (j + 1 < it.nkt[1]) {
-            if (!k_ready && !(ok = wait_k(kidx + 1))) break;
-            qk(1, kidx + 1);
-            if (j + 2 == it.nkt[1]) umma_commit(&B.q_empty[1]);
-          }
-          if (next) umma_commit(&B.k_empty[(kidx + 1) % kRingK]);
+          umma_commit_pair(&B.o_done[sb], kPairMask);
         }
-        tiles += it.nmax;
+      }
+      umma_commit_pair(B.drain, kPairMask);
+    } else if (!even && lane == 0 && warp == 1) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      // This CTA's softmax warps arrive on p_local; once their P and V writes
+      // are acquired here, one cluster-scope release arrival hands them to the
+      // even CTA's P.V issuer.
+      const uint32_t p_full_even[kNumS] = {mapa_shared(smem_u32(&B.p_full[0]), 0),
+                                           mapa_shared(smem_u32(&B.p_full[1]), 0),
+                                           mapa_shared(smem_u32(&B.p_full[2]), 0)};
+      uint32_t g = 0;
+      Item it;
+      int r = 0;
+      bool ok = true;
+      while (ok && src.next_with_tiles(p, r, it)) {
+        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
+          if (!(ok = mbar_wait(&B.p_local[g % kNumS], (g / kNumS) & 1, p.status))) break;
+          mbar_arrive_cluster(p_full_even[g % kNumS]);
+        }
       }
     }
     __syncwarp();
+    if (warp == 1 && lane == 0) mbar_wait_cl_for(B.drain, 0, p.status, kWaitLimitNs);
+    __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax (query tile A or B)
-    const int qtile = (warp - 2) >> 2;       // 0: warps 2-5 (tile A), 1: warps 6-9 (tile B)
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    // ------------------------------------------------------------ softmax + epilogue
+    // two threads per row of tile `rank`: warps w and w + 4 share TMEM lanes
+    // 32 (w % 4) .. +31; half 0 takes columns 0-63, half 1 columns 64-127
+    const int quarter = warp & 3;
+    const int half = (warp - kSoftWarp0) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int t = (warp - 2 - 4 * qtile) * 32 + lane;  // 0..127 within the group
-    const uint32_t s_cols = tmem + lane_base + kColS + qtile * 128;
-    const uint32_t o_cols = tmem + lane_base + kColO + qtile * 128;
+    const int t = (warp - kSoftWarp0) * 32 + lane;  // 0..255 within the group
+    const int xbar = 1 + quarter;                   // named barrier of this row quarter's two warps
+    const uint32_t o_cols = tmem + lane_base + kColO + half * 64;
+    float* x_mine = xch + half * 128 + row;
+    const float* x_other = xch + (1 - half) * 128 + row;
     const float c = p.scale_log2;
-    if (blockIdx.x == 0 && warp == 2 && p.status) {
+    if (blockIdx.x == 0 && warp == kSoftWarp0 && p.status) {
       int sum = 0;
       for (int e = lane; e < p.B; e += 32) sum += max(__ldg(p.chunk_lens + e), 0);
 #pragma unroll
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       if (lane == 0 && sum != p.T) atomicOr(p.status, PA_STATUS_BAD_TOKENS);
     }
-    uint32_t tiles = 0, gt = 0;
+    // After a wait gives up (PA_STATUS_TIMEOUT) the warps skip every later
+    // wait but still walk all items and steps, so the two warps of a row
+    // quarter keep meeting at the same named barriers and reach the end.
+    uint32_t g = 0;  // steps so far (all items)
     bool ok = true;
     Item it;
-    for (int r = 0; ok && src.get(p, r, it); ++r) {
-      const int nkt = it.nkt[qtile];
-      const uint32_t k0 = tiles;
-      if (it.nmax > 0) tiles += it.nmax;
-      const bool reporter = qtile == 0 && t == 0 && it.pair == 0 && it.g == 0 && p.status;
-      const int nrows = it.nrows[qtile];
-      const int64_t tok = (int64_t)it.tok0 + qtile * 128 + row;
-      const bool row_out = row < nrows && tok >= 0 && tok < p.T;
+    for (int r = 0; src.get(p, r, it); ++r) {
+      const bool reporter = even && t == 0 && it.pair == 0 && it.g == 0 && p.status;
+      const int nrows = it.nrows[rank];
+      const int64_t tok = (int64_t)it.tok0 + rank * 128 + row;
+      const bool row_valid = row < nrows;
+      const bool row_out = row_valid && tok >= 0 && tok < p.T;
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
-                     ((tok * p.Hq + it.g) * kHeadDim) * (p.out_f32 ? 4 : 2);
-      if (nkt == 0) {
-        // tile A has key tiles unless the lengths are invalid
+                     ((tok * p.Hq + it.g) * kHeadDim + half * 64) * (p.out_f32 ? 4 : 2);
+      if (it.nmax == 0) {
+        // lengths invalid: zero rows
         if (!it.len_ok && reporter) atomicOr(p.status, PA_STATUS_BAD_LENGTH);
-        if (row_out)  // lengths invalid: zero rows
-          for (int cc = 0; cc < (p.out_f32 ? 32 : 16); ++cc)
+        if (row_out)
+          for (int cc = 0; cc < (p.out_f32 ? 16 : 8); ++cc)
             reinterpret_cast<uint4*>(dst)[cc] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      const int pos = it.prior + it.pair * 256 + qtile * 128 + min(row, nrows - 1);  // query position
+      const int pos = it.prior + it.pair * 256 + (int)rank * 128 + row;  // this row's position
       const int last_page = (it.ctx - 1) / kPage;
       const int vtail = it.ctx % kPage;  // rows >= vtail of the last page are past the context
-      // the first P.V to read the last page zeroes its tail: tile A's if it reaches it
-      const bool zero_mine = vtail != 0 && nkt - 1 == last_page &&
-                             (qtile == 0 || it.nkt[0] - 1 != last_page);
+      const bool zero_tail = vtail != 0 && it.nmax - 1 == last_page;
       // block-table entries of the context: the first 32 loaded now, checked
       // after the key tiles (off the path to the first tile)
       const int used = (it.ctx + kPage - 1) / kPage;
       const int32_t* bt = p.block_table + (int64_t)it.s * p.max_pages;
       const int pg_first = lane < used ? __ldg(bt + lane) : 0;
-      float m = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < nkt; ++kt, ++gt) {
-        if (!(ok = mbar_wait_warp(&B.s_full[qtile], gt & 1, p.status))) break;
+      float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+      for (int kt = 0; kt < it.nmax; ++kt, ++g) {
+        if (ok) ok = mbar_wait_warp_cl(&B.s_full[g % kNumS], (g / kNumS) & 1, p.status);
         tc_fence_after();
+        const uint32_t s_cols = tmem + lane_base + kColS + (g % kNumS) * 128 + half * 64;
         // causal mask only where the tile crosses pos: masked scores take no part
-        const int key0 = kt * kPage;
-        const int nvis = min(max(pos - key0 + 1, 0), kPage);  // visible keys of this row
+        const int key0 = kt * kPage + half * 64;
+        const int nvis = row_valid ? min(max(pos - key0 + 1, 0), 64) : 0;  // visible keys of this half
         // warp-uniform choices: the TMEM loads and stores below are .sync.aligned
-        const bool diag = __any_sync(0xffffffffu, nvis < kPage);
+        // (both warps of a quarter hold the same rows, so they choose alike)
+        const bool diag = __any_sync(0xffffffffu, nvis < 64);
         const float2 c2 = make_float2(c, c);
         if (__any_sync(0xffffffffu, m == -INFINITY)) {
           // the row's first key tile: the exact max of c * s over the visible keys
           float mx = -INFINITY;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t sr[32];
             tmem_ld32(s_cols + cc * 32, sr);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float t = __uint_as_float(sr[e]) * c;
-              mx = fmaxf(mx, cc * 32 + e < nvis ? t : -INFINITY);
+              const float v = __uint_as_float(sr[e]) * c;
+              mx = fmaxf(mx, cc * 32 + e < nvis ? v : -INFINITY);
             }
           }
+          *x_mine = mx;
+          named_bar_sync(xbar, 64);
+          mx = fmaxf(mx, *x_other);
+          named_bar_sync(xbar, 64);  // the slot is free for the next exchange
           if (m == -INFINITY) m = mx;
         }
         // One pass, speculatively against the running reference m: p = 2^(c s - m),
         // tracking the largest exponent.  The reference moves (and the tile is
-        // redone) only when some visible score exceeds it by more than 2^8.
+        // redone) only when some visible score of the row exceeds it by more than 2^8.
         float alpha = 1.f;
         bool rescale = false;
-        uint32_t pw[64];  // P as BF16 pairs
+        uint32_t pw[32];  // P as BF16 pairs (this half's 64 keys)
         float2 sum2;
         auto pass = [&](float m_ref, auto masked) -> float {
           const float2 nm2 = make_float2(-m_ref, -m_ref);
           float dmax = -INFINITY;
           sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t sr[32];
             tmem_ld32(s_cols + cc * 32, sr);
             tmem_wait_ld();
@@ -603,18 +671,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d2.y = k0e + 1 < nvis ? d2.y : -INFINITY;
               }
               dmax = fmaxf(dmax, fmaxf(d2.x, d2.y));
-              const float2 p2 = make_float2(fast_exp2(d2.x), fast_exp2(d2.y));
-              sum2 = __fadd2_rn(sum2, p2);
-              pw[cc * 16 + e] = pack_bf16x2(p2.x, p2.y);
+              const uint32_t w = pack_bf16x2(fast_exp2(d2.x), fast_exp2(d2.y));
+              pw[cc * 16 + e] = w;
+              // the normaliser adds the weights as rounded, as the MMA uses them
+              sum2 = __fadd2_rn(sum2, bf16x2_to_float2(w));
             }
           }
           return dmax;
         };
         const float m_use = m == -INFINITY ? 0.f : m;  // nothing visible yet: every p = 0
-        const float dmax = diag ? pass(m_use, std::true_type{}) : pass(m_use, std::false_type{});
-        const bool over = dmax > kRescaleThreshold;
-        if (__any_sync(0xffffffffu, over)) {
-          // rare: move this row's reference up to its tile max and redo the tile
+        float dmax = diag ? pass(m_use, std::true_type{}) : pass(m_use, std::false_type{});
+        if (named_bar_red_or(dmax > kRescaleThreshold, xbar, 64)) {
+          // rare: the row's reference moves up to the larger of the two halves'
+          // maxima, and both halves redo the tile against it
+          *x_mine = dmax;
+          named_bar_sync(xbar, 64);
+          dmax = fmaxf(dmax, *x_other);
+          const bool over = dmax > kRescaleThreshold;
           const float m_new = over ? m_use + dmax : m_use;
           if (over) {
             alpha = fast_exp2(-dmax);
@@ -623,37 +696,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (diag) pass(m_new, std::true_type{}); else pass(m_new, std::false_type{});
         }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pw[cc * 16 + e];
-          tmem_st16(s_cols + cc * 16, w);
-        }
         l = l * alpha + (sum2.x + sum2.y);
-        if (zero_mine && kt == nkt - 1) {
-          // zero V rows past the context in the last page before P.V reads them
-          const uint32_t kidx = k0 + kt;
-          const int vs = kidx % kRingV;
-          if (!(ok = mbar_wait_warp(&B.v_full[vs], (kidx / kRingV) & 1, p.status))) break;
-          const int rr = vtail + t;
-          if (rr < kPage) {
-            const uint32_t vb = smem_u32(smem + kV + vs * kTileBytes) + rr * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              sts128(vb + ch * 16, 0u, 0u, 0u, 0u);
-              sts128(vb + kBox + ch * 16, 0u, 0u, 0u, 0u);
-            }
-          }
-          fence_proxy_async_smem();
-        }
+        // P over this half's scores (all of them read above)
+        tmem_st32(s_cols, pw);
         // warp-uniform: lanes that need no rescale take alpha = 1 (exact)
         if (__any_sync(0xffffffffu, rescale) && kt > 0) {
-          // O holds P.V up to the previous key tile: wait for it, then scale
-          if (!(ok = mbar_wait_warp(&B.o_done[qtile], (gt - 1) & 1, p.status))) break;
+          // O must hold every earlier step: P.V(g - 1) done.  (S(g) complete
+          // means P.V(g - 3) is, so this barrier is at most one phase behind.)
+          const uint32_t g1 = g - 1;
+          if (ok) ok = mbar_wait_warp_cl(&B.o_done[g1 % kNumS], (g1 / kNumS) & 1, p.status);
           tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t orow[32];
             tmem_ld32(o_cols + cc * 32, orow);
             tmem_wait_ld();
@@ -662,11 +716,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_cols + cc * 32, orow);
           }
         }
+        // this CTA's V half of the step: landed, and zeroed past the context
+        const int vs = g % kRingV;
+        if (ok) ok = mbar_wait_warp_cl(&B.v_full[vs], (g / kRingV) & 1, p.status);
+        if (zero_tail && kt == it.nmax - 1) {
+          const int rr = vtail + (t >> 1);
+          if (rr < kPage) {
+            const uint32_t vb = smem_u32(smem + kV + vs * kVBytes) + rr * 128 + (t & 1) * 64;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) sts128(vb + ch * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&B.p_full[qtile]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(even ? &B.p_full[g % kNumS] : &B.p_local[g % kNumS]);
       }
-      if (!ok) break;
       bool pg_bad = pg_first < 0 || pg_first >= p.num_pages;
       for (int e = lane + 32; e < used; e += 32) {
         const int pg = __ldg(bt + e);
@@ -674,13 +740,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool bad = __any_sync(0xffffffffu, pg_bad);
       if (bad && reporter) atomicOr(p.status, PA_STATUS_BAD_PAGE);
-      // ---- epilogue: O / l for this row
-      if (!(ok = mbar_wait_warp(&B.o_done[qtile], (gt - 1) & 1, p.status))) break;
+      // ---- epilogue: O / l for this half-row, once the item's last P.V is done
+      named_bar_sync(xbar, 64);  // the partner's last reads of the slot are done
+      *x_mine = l;
+      named_bar_sync(xbar, 64);
+      const float lrow = l + *x_other;
+      named_bar_sync(xbar, 64);  // the slot is free for the next item
+      const uint32_t gl = g - 1;
+      if (ok) ok = mbar_wait_warp_cl(&B.o_done[gl % kNumS], (gl / kNumS) & 1, p.status);
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       // an invalid sequence may have read a substitute page: select zeros
       const uint32_t keep = bad ? 0u : 0xffffffffu;
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t o0[32];
         tmem_ld32(o_cols + cc * 32, o0);
         tmem_wait_ld();
@@ -706,34 +778,77 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&B.o_free[qtile]);
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
 }  // namespace
 
+cudaError_t prefill_pairs(int num_sms, int* pairs) {
+  static int pairs_cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && pairs_cache[dev] > 0) {
+    *pairs = pairs_cache[dev];
+    return cudaSuccess;
+  }
+  if ((e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem)) != cudaSuccess)
+    return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.gridDim = dim3(2 * (num_sms / 2 > 0 ? num_sms / 2 : 1));
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg)) != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  if (dev >= 0 && dev < 64) pairs_cache[dev] = n;
+  *pairs = n;
+  return cudaSuccess;
+}
+
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
                            cudaStream_t stream) {
   static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
-  static_assert(3 * kMaxCost * 4 <= kRingK * kTileBytes, "schedule scratch must fit the K ring");
-  static_assert((4 * kMaxSchedSeqs + 1) * 4 <= kRingV * kTileBytes, "schedule lengths must fit the V ring");
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  static_assert(3 * kMaxCost * 4 <= kRingK * kKBytes, "schedule scratch must fit the K ring");
+  static_assert((4 * kMaxSchedSeqs + 1) * 4 <= kRingV * kVBytes, "schedule lengths must fit the V ring");
+  // persistent: one CTA per SM, as many pairs as can be resident at once
+  // (tensor memory and shared memory are sized for one CTA per SM)
+  int pairs = 0;
+  cudaError_t e = prefill_pairs(num_sms, &pairs);
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM (tensor memory and shared memory are sized for one)
   const int64_t max_items = ((int64_t)p.T / 256 + p.B) * p.Hq;
-  const int grid = (int)(max_items < num_sms ? max_items : num_sms);
-  if (grid < 1) return cudaSuccess;
-  prefill_kernel<<<grid, kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, p);
+  const int grid_pairs = (int)(max_items < pairs ? max_items : pairs);
+  if (grid_pairs < 1) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.gridDim = dim3(2 * grid_pairs);
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, tm_q, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

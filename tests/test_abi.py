@@ -55,6 +55,7 @@ def test_python_constants_match_header(pa):
     assert h["PA_MAX_Q_LEN"] == pa.PA_MAX_Q_LEN
     assert h["PA_MAX_PROLOGUE_HEADS"] == pa.PA_MAX_PROLOGUE_HEADS
     assert h["PA_STATUS_Q_RANGE"] == pa.PA_STATUS_Q_RANGE
+    assert h["PA_PREFILL_SCHEDULE_ITEMS"] == pa.PA_PREFILL_SCHEDULE_ITEMS
     for k, v in h.items():
         if k.startswith("PA_ERR_"):
             assert getattr(pa, k) == v, k

@@ -167,14 +167,14 @@ def test_scores_that_move_the_reference(cuda_lib, profile):
 @pytest.mark.parametrize("extra", [-1, 2])
 def test_schedule_table_limit(cuda_lib, extra):
     """Launches whose item count sits just below or just above what the
-    per-CTA schedule table holds (64 items per CTA on a grid of one CTA per
-    SM): below it every CTA takes its items from the table, above it every CTA
-    falls back to round-robin -- never a mix, which would leave items
-    unprocessed.  One pair of query tiles per sequence and 8 query heads, so
-    items = 8 * sequences; the output starts as NaN and every row must be
-    written."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    B = 64 * sms // 8 + extra
+    per-pair schedule table holds (PA_PREFILL_SCHEDULE_ITEMS items per CTA
+    pair, pa_prefill_pairs() pairs): below it every pair takes its items from
+    the table, above it every pair falls back to round-robin -- never a mix,
+    which would leave items unprocessed.  One pair of query tiles per sequence
+    and 8 query heads, so items = 8 * sequences; the output starts as NaN and
+    every row must be written."""
+    pairs = cuda_lib.pa_prefill_pairs()
+    B = cuda_lib.PA_PREFILL_SCHEDULE_ITEMS * pairs // 8 + extra
     chunk = [1 + s % 3 for s in range(B)]
     ctx = [c + (37 * s) % 150 for s, c in enumerate(chunk)]
     case = W.custom_case(612, ctx, Hq=8, Hkv=2, chunk_lens=chunk, with_new=True)
