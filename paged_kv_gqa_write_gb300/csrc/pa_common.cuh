@@ -173,6 +173,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// Hand this thread's shared::cta writes (and those it has synchronised with,
+// e.g. its warp's after __syncwarp) to a consumer in another CTA: a release
+// fence at cluster scope restricted to shared::cta accesses, then a relaxed
+// arrival on the barrier at shared::cluster address `caddr`.  The restricted
+// fence does not wait for global memory, so it costs about as much as a
+// local arrival; the consumer's cluster-scope acquire pairs with it.
+__device__ __forceinline__ void mbar_arrive_cluster_smem(uint32_t caddr) {
+  asm volatile("fence.sync_restrict::shared::cta.release.cluster;" ::: "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+               : "memory");
+}
+
 // Arrive (release at cluster scope) on the barrier at shared::cluster address `caddr`.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)

@@ -32,8 +32,7 @@
 //    scores of the next steps are computed while the softmax works, and P(j)
 //    is written back over S(j) (A operand from tensor memory), so the
 //    softmax runs up to three steps ahead of P.V; S(j + 3) is issued only
-//    once P.V(j) has completed.  In the odd CTA warp 1 relays "P ready" to
-//    the even CTA (below).
+//    once P.V(j) has completed.
 //  * warps 2-9: softmax and epilogue, two threads per query row (warps w and
 //    w + 4 share the row's tensor-memory lanes; each takes 64 of the 128
 //    columns).  Per step: tcgen05.ld of the score half-row, causal mask (only
@@ -42,13 +41,17 @@
 //    it by 2^8 (the two halves agree on it through shared memory; O is then
 //    rescaled in tensor memory), P rounded to BF16 pairs into the first 32
 //    of the half's own 64 S columns, and the row sum taken over the rounded
-//    weights the MMA uses.  The warps then wait for this
-//    CTA's V half, zero its rows past the context on the sequence's last page
-//    (P is 0 there, but 0 * NaN is NaN), and arrive on the P barrier.
-// "P ready" crosses the pair once per step: the odd CTA's warps arrive on a
-// local barrier and its relay thread, having acquired their writes, arrives
-// with cluster-scope release on the even CTA's barrier, so the P.V product
-// (which reads both CTAs' P and V halves) is ordered after every write.
+//    weights the MMA uses.  The warps then wait for this CTA's V half, zero
+//    its rows past the context on the sequence's last page (P is 0 there,
+//    but 0 * NaN is NaN), and arrive on the even CTA's P barrier: the P.V
+//    product reads both CTAs' P and V halves.
+// "P ready" crosses the pair once per step.  Each odd-CTA warp completes its
+// tensor-memory stores (tcgen05.wait::st, then tcgen05.fence before the
+// thread synchronisation), makes its shared-memory writes visible to the
+// tensor core (fence.proxy.async), and arrives on the even CTA's barrier
+// after a cluster-scope release restricted to shared memory: a full
+// cluster-scope release waits for global memory and cost about 0.6 us per
+// arrival, the restricted one about as much as a local arrival.
 // Key pages entirely above both tiles' last query positions are never loaded
 // (causal tile skipping); the lower tile sees its pair's last page fully
 // masked.  Items are dealt to the pairs in decreasing order of key-tile
@@ -84,7 +87,7 @@ constexpr int kX = kV + kRingV * kVBytes;     // row exchange between the two ha
 constexpr int kListInts = 5;                  // per item: s, pair|head, tok0, chunk len, ctx
 constexpr int kList = kX + 2 * 128 * 4;       // schedule [kMaxList][kListInts] int
 constexpr int kBars = kList + kMaxList * kListInts * 4;
-constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 4 * kNumS + 1;
+constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 3 * kNumS + 1;
 constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
 constexpr int kMaxCost = 4096;                // schedule histogram buckets (K ring scratch)
 constexpr int kMaxSchedSeqs = (kRingV * kVBytes / 4 - 1) / 4;  // sequences the schedule stages
@@ -108,7 +111,6 @@ struct Bars {
   uint64_t* v_full;   // [3] this CTA's V half landed
   uint64_t* s_full;   // [3] S(g) in buffer g % 3 done (and K stage g % 3 free)
   uint64_t* p_full;   // [3] even CTA: P(g) written in both CTAs, V(g) halves in place
-  uint64_t* p_local;  // [3] odd CTA: its softmax warps' P(g), for the relay
   uint64_t* o_done;   // [3] P.V(g) done: O holds every step <= g, V stage g % 3 free
   uint64_t* drain;    // every MMA issued (by both issuers) has completed
 };
@@ -370,8 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.v_full = B.k_full + kRingK;
   B.s_full = B.v_full + kRingV;
   B.p_full = B.s_full + kNumS;
-  B.p_local = B.p_full + kNumS;
-  B.o_done = B.p_local + kNumS;
+  B.o_done = B.p_full + kNumS;
   B.drain = B.o_done + kNumS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
   int* list_count = reinterpret_cast<int*>(tmem_slot + 1);
@@ -391,8 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kRingV; ++i) mbar_init(&B.v_full[i], 1);
     for (int i = 0; i < kNumS; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], kSoftmaxWarps + 1);  // this CTA's warps + the odd CTA's relay
-      mbar_init(&B.p_local[i], kSoftmaxWarps);
+      mbar_init(&B.p_full[i], 2 * kSoftmaxWarps);  // the softmax warps of both CTAs
       mbar_init(&B.o_done[i], 1);
     }
     mbar_init(B.drain, 2);  // one commit from each issuer
@@ -539,24 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       umma_commit_pair(B.drain, kPairMask);
-    } else if (!even && lane == 0 && warp == 1) {
-      // ---------------------------------------------------------- relay (odd CTA)
-      // This CTA's softmax warps arrive on p_local; once their P and V writes
-      // are acquired here, one cluster-scope release arrival hands them to the
-      // even CTA's P.V issuer.
-      const uint32_t p_full_even[kNumS] = {mapa_shared(smem_u32(&B.p_full[0]), 0),
-                                           mapa_shared(smem_u32(&B.p_full[1]), 0),
-                                           mapa_shared(smem_u32(&B.p_full[2]), 0)};
-      uint32_t g = 0;
-      Item it;
-      int r = 0;
-      bool ok = true;
-      while (ok && src.next_with_tiles(p, r, it)) {
-        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
-          if (!(ok = mbar_wait(&B.p_local[g % kNumS], (g / kNumS) & 1, p.status))) break;
-          mbar_arrive_cluster(p_full_even[g % kNumS]);
-        }
-      }
     }
     __syncwarp();
     if (warp == 1 && lane == 0) mbar_wait_cl_for(B.drain, 0, p.status, kWaitLimitNs);
@@ -572,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - kSoftWarp0) * 32 + lane;  // 0..255 within the group
     const int xbar = 1 + quarter;                   // named barrier of this row quarter's two warps
     const uint32_t o_cols = tmem + lane_base + kColO + half * 64;
+    const uint32_t p_full_even[kNumS] = {mapa_shared(smem_u32(&B.p_full[0]), 0),
+                                         mapa_shared(smem_u32(&B.p_full[1]), 0),
+                                         mapa_shared(smem_u32(&B.p_full[2]), 0)};
     float* x_mine = xch + half * 128 + row;
     const float* x_other = xch + (1 - half) * 128 + row;
     const float c = p.scale_log2;
@@ -731,7 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(even ? &B.p_full[g % kNumS] : &B.p_local[g % kNumS]);
+        if (lane == 0) {
+          if (even) mbar_arrive(&B.p_full[g % kNumS]);
+          else mbar_arrive_cluster_smem(p_full_even[g % kNumS]);
+        }
       }
       bool pg_bad = pg_first < 0 || pg_first >= p.num_pages;
       for (int e = lane + 32; e < used; e += 32) {
