@@ -712,6 +712,12 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   if (!encode_3d(&tm_q, q, kHeadDim, d.num_q_heads, (uint64_t)num_tokens, 64, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return PA_ERR_TENSOR_MAP;
+  // out as [num_tokens, Hq, 128] for the BF16 output tiles' TMA stores
+  CUtensorMap tm_o = {};
+  if (out_dtype == PA_BF16 &&
+      !encode_3d(&tm_o, out, kHeadDim, d.num_q_heads, (uint64_t)num_tokens, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return PA_ERR_TENSOR_MAP;
   pa::PrefillParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.block_table = block_table;
@@ -729,7 +735,7 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   p.max_pages = d.max_pages_per_seq;
   p.out_f32 = out_dtype == PA_F32;
   return launch_result(
-      pa::launch_prefill(tm_k, tm_v, tm_q, p, sms, reinterpret_cast<cudaStream_t>(stream)));
+      pa::launch_prefill(tm_k, tm_v, tm_q, tm_o, p, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t pa_prefill_pairs(void) {

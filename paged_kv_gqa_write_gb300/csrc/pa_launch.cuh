@@ -55,8 +55,10 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_
 // that can be resident at once), cached per device.
 cudaError_t prefill_pairs(int num_sms, int* pairs);
 
+// tm_o: 3-D map over a BF16 out [T][Hq][128] with 64 x 1 x 128 boxes and
+// 128-byte swizzle (unused, any contents, for FP32 output).
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                           const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
-                           cudaStream_t stream);
+                           const CUtensorMap& tm_q, const CUtensorMap& tm_o,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream);
 
 }  // namespace pa

@@ -52,6 +52,10 @@
 // after a cluster-scope release restricted to shared memory: a full
 // cluster-scope release waits for global memory and cost about 0.6 us per
 // arrival, the restricted one about as much as a local arrival.
+// Epilogue: O / l per row.  A full 128-row tile with BF16 output is staged in
+// shared memory (128-byte swizzle) and written by one TMA tensor store that
+// runs on while the warps start the next item; partial tiles and FP32 output
+// are written row by row.
 // Key pages entirely above both tiles' last query positions are never loaded
 // (causal tile skipping); the lower tile sees its pair's last page fully
 // masked.  Items are dealt to the pairs in decreasing order of key-tile
@@ -83,7 +87,10 @@ constexpr int kMaxList = PA_PREFILL_SCHEDULE_ITEMS;  // scheduled items per pair
 constexpr int kQ = 0;
 constexpr int kK = kQ + 2 * kQBytes;
 constexpr int kV = kK + kRingK * kKBytes;
-constexpr int kX = kV + kRingV * kVBytes;     // row exchange between the two halves: [2][128] float
+constexpr int kOut = kV + kRingV * kVBytes;   // BF16 output tile staging: 2 boxes of 128 x 64
+constexpr int kOutBytes = 128 * 128 * 2;
+constexpr int kOutBox = 16384;
+constexpr int kX = kOut + kOutBytes;          // row exchange between the two halves: [2][128] float
 constexpr int kListInts = 5;                  // per item: s, pair|head, tok0, chunk len, ctx
 constexpr int kList = kX + 2 * 128 * 4;       // schedule [kMaxList][kListInts] int
 constexpr int kBars = kList + kMaxList * kListInts * 4;
@@ -360,7 +367,8 @@ __device__ __forceinline__ void drain_loads(uint64_t* bars, int n, uint32_t issu
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_q, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                   const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -740,6 +748,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       // an invalid sequence may have read a substitute page: select zeros
       const uint32_t keep = bad ? 0u : 0xffffffffu;
+      // a full tile of BF16 rows: staged and stored by TMA (uniform over the CTA)
+      const int64_t tile0 = (int64_t)it.tok0 + rank * 128;
+      if (!p.out_f32 && nrows == 128 && tile0 + 128 <= p.T) {
+        // the previous tile's store has finished reading the staging area
+        if (t == 0) bulk_wait_read_all();
+        named_bar_sync(5, 32 * kSoftmaxWarps);
+        const uint32_t o_row = smem_u32(smem + kOut) + half * kOutBox + row * 128;
+        const uint32_t sw = (uint32_t)(row & 7);
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o0[32];
+          tmem_ld32(o_cols + cc * 32, o0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float* f = reinterpret_cast<const float*>(o0) + 8 * e;
+            sts128(o_row + (((uint32_t)(cc * 4 + e) ^ sw) << 4),
+                   pack_bf16x2(f[0] * inv, f[1] * inv) & keep, pack_bf16x2(f[2] * inv, f[3] * inv) & keep,
+                   pack_bf16x2(f[4] * inv, f[5] * inv) & keep, pack_bf16x2(f[6] * inv, f[7] * inv) & keep);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(5, 32 * kSoftmaxWarps);
+        if (t == 0) {
+          tma_store_3d(&tm_o, smem + kOut, 0, it.g, (int32_t)tile0);
+          tma_store_3d(&tm_o, smem + kOut + kOutBox, 64, it.g, (int32_t)tile0);
+          bulk_commit_group();
+        }
+        continue;
+      }
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t o0[32];
         tmem_ld32(o_cols + cc * 32, o0);
@@ -768,6 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  // the output stores complete before the CTA exits
+  if (warp == kSoftWarp0 && lane == 0) bulk_wait_all();
   tc_fence_before();
   cluster_sync_all();
   if (warp == 1) {
@@ -810,8 +849,8 @@ cudaError_t prefill_pairs(int num_sms, int* pairs) {
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                           const CUtensorMap& tm_q, const PrefillParams& p, int num_sms,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tm_q, const CUtensorMap& tm_o,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
   static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
   static_assert(3 * kMaxCost * 4 <= kRingK * kKBytes, "schedule scratch must fit the K ring");
   static_assert((4 * kMaxSchedSeqs + 1) * 4 <= kRingV * kVBytes, "schedule lengths must fit the V ring");
@@ -835,7 +874,7 @@ cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cfg.gridDim = dim3(2 * grid_pairs);
-  e = cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, tm_q, p);
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, tm_q, tm_o, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
