@@ -26,13 +26,14 @@
 //  * warp 10 (one lane): V halves (3-stage ring, free once P.V(j - 3) is
 //    done), completing locally.
 //  * warp 1: both CTAs allocate tensor memory together (S0, S1, S2, O).  In
-//    the even CTA one lane issues the S products and one lane of warp 11 the
-//    P.V products: each issuer's waits and commits overlap the other's
-//    products in the tensor core's queue.  S is triple-buffered, so the
-//    scores of the next steps are computed while the softmax works, and P(j)
-//    is written back over S(j) (A operand from tensor memory), so the
-//    softmax runs up to three steps ahead of P.V; S(j + 3) is issued only
-//    once P.V(j) has completed.
+//    the even CTA one lane of warp 1 and one of warp 11 issue the MMAs,
+//    taking alternate steps: each issues P.V(j) and then S(j + 3), so each
+//    one's waits and commits overlap the other's products in the tensor
+//    core's queue.  S is triple-buffered, so the scores of the next steps are
+//    computed while the softmax works, and P(j) is written back over S(j) (A
+//    operand from tensor memory), so the softmax runs up to three steps ahead
+//    of P.V; one thread's products execute in issue order, so S(j + 3)
+//    follows P.V(j) without waiting for it.
 //  * warps 2-9: softmax and epilogue, two threads per query row (warps w and
 //    w + 4 share the row's tensor-memory lanes; each takes 64 of the 128
 //    columns).  Per step: tcgen05.ld of the score half-row, causal mask (only
@@ -45,6 +46,10 @@
 //    its rows past the context on the sequence's last page (P is 0 there,
 //    but 0 * NaN is NaN), and arrive on the even CTA's P barrier: the P.V
 //    product reads both CTAs' P and V halves.
+// Waits on barriers completed by tensor-core commits (multicast to both CTAs)
+// or by copies take acquire at CTA scope, as for a single CTA; the waits on
+// the even CTA's P barrier, which the odd CTA's threads arrive on, take it at
+// cluster scope.  (A cluster-scope acquire cost 0.1-0.2 us per wait.)
 // "P ready" crosses the pair once per step.  Each odd-CTA warp completes its
 // tensor-memory stores (tcgen05.wait::st, then tcgen05.fence before the
 // thread synchronisation), makes its shared-memory writes visible to the
@@ -394,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&B.q_full[t], 1);
-      mbar_init(&B.q_empty[t], 1);
+      mbar_init(&B.q_empty[t], 2);  // one commit from each MMA issuer
     }
     for (int i = 0; i < kRingK; ++i) mbar_init(&B.k_full[i], 1);
     for (int i = 0; i < kRingV; ++i) mbar_init(&B.v_full[i], 1);
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (is_k) {
           // this CTA's query tile, once the item two back released the buffer
           const int qb = qitems & 1;
-          if (!(ok = mbar_wait_cl(&B.q_empty[qb], ((qitems >> 1) & 1) ^ 1, p.status))) break;
+          if (!(ok = mbar_wait(&B.q_empty[qb], ((qitems >> 1) & 1) ^ 1, p.status))) break;
           ++qitems;
           if (even) mbar_arrive_expect_tx(&B.q_full[qb], 2 * kQBytes);
           const uint32_t qbar = mapa_shared(smem_u32(&B.q_full[qb]), 0);
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage tiles % 3 is free once S(tiles - 3) is done
             const int st = tiles % kRingK;
             if (tiles >= (uint32_t)kRingK &&
-                !(ok = mbar_wait_cl(&B.s_full[st], ((tiles / kRingK) & 1) ^ 1, p.status)))
+                !(ok = mbar_wait(&B.s_full[st], ((tiles / kRingK) & 1) ^ 1, p.status)))
               break;
             if (even) mbar_arrive_expect_tx(&B.k_full[st], 2 * kKBytes);
             const uint32_t kbar = mapa_shared(smem_u32(&B.k_full[st]), 0);
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage tiles % 3 is free once P.V(tiles - 3) is done
             const int st = tiles % kRingV;
             if (tiles >= (uint32_t)kRingV &&
-                !(ok = mbar_wait_cl(&B.o_done[st], ((tiles / kRingV) & 1) ^ 1, p.status)))
+                !(ok = mbar_wait(&B.o_done[st], ((tiles / kRingV) & 1) ^ 1, p.status)))
               break;
             mbar_arrive_expect_tx(&B.v_full[st], kVBytes);
             tma_load_2d(smem + kV + st * kVBytes, &tm_v, it.h * kHeadDim + (int)rank * 64, y,
@@ -488,25 +493,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1 || warp == kPvWarp) {
-    if (even && lane == 0 && warp == 1) {
-      // ---------------------------------------------------------- S issuer (even CTA)
+    if (even && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers (even CTA)
+      // Two threads take alternate steps g (thread par takes g % 2 == par):
+      // each issues P.V(g) and then S(g + 3), into the buffer that holds P(g).
+      // One thread's products execute in issue order, so S(g + 3) runs after
+      // P.V(g) has read P(g) without waiting for it, and the tensor core's
+      // queue holds P.V(g), S(g + 3), P.V(g + 1), S(g + 4), ...  P.V(g) first
+      // waits for P.V(g - 1) (the other thread's) to complete, which orders
+      // the accumulation into O.  Thread 0 issues S(0..2) up front.
+      const uint32_t par = warp == 1 ? 0u : 1u;
       const uint32_t idesc_qk = umma_idesc_bf16(256, 128, false, false);  // Q, K: K-major
-      uint32_t g = 0, qi = 0;
+      const uint32_t idesc_pv = umma_idesc_bf16(256, 128, false, true);   // P (TMEM), V MN-major
       bool ok = true;
-      Item it;
-      int r = 0;
-      while (ok && src.next_with_tiles(p, r, it)) {
+      // S cursor: step gq of item iq (key tile jq), its query tile's ordinal qi
+      ItemSource sq = src;
+      int rq = 0, jq = 0;
+      Item iq;
+      bool hq = sq.next_with_tiles(p, rq, iq);
+      uint32_t gq = 0, qi = 0, q_waited = ~0u;
+      auto next_qk = [&](bool issue) {
         const int qb = qi & 1;
-        if (!(ok = mbar_wait_cl(&B.q_full[qb], (qi >> 1) & 1, p.status))) break;
-        const uint32_t qa = smem_u32(smem + kQ + qb * kQBytes);
-        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
-          const int sb = g % kNumS;
-          if (!(ok = mbar_wait_cl(&B.k_full[sb], (g / kNumS) & 1, p.status))) break;
-          // S buffer sb holds P(g - 3): free once P.V(g - 3) is done
-          if (g >= (uint32_t)kNumS &&
-              !(ok = mbar_wait_cl(&B.o_done[sb], ((g / kNumS) & 1) ^ 1, p.status)))
-            break;
+        if (issue) {
+          if (q_waited != qi) {
+            if (!(ok = mbar_wait(&B.q_full[qb], (qi >> 1) & 1, p.status))) return;
+            q_waited = qi;
+          }
+          const int sb = gq % kNumS;
+          if (!(ok = mbar_wait(&B.k_full[sb], (gq / kNumS) & 1, p.status))) return;
           tc_fence_after();
+          const uint32_t qa = smem_u32(smem + kQ + qb * kQBytes);
           const uint32_t ka = smem_u32(smem + kK + sb * kKBytes);
           const uint32_t d = tmem + kColS + sb * 128;
 #pragma unroll
@@ -517,35 +533,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit_pair(&B.s_full[sb], kPairMask);
         }
-        if (!ok) break;
-        umma_commit_pair(&B.q_empty[qb], kPairMask);
-        ++qi;
-      }
-      // every product issued completes before the columns are released
-      umma_commit_pair(B.drain, kPairMask);
-    } else if (even && lane == 0) {
-      // ---------------------------------------------------------- P.V issuer (even CTA)
-      const uint32_t idesc_pv = umma_idesc_bf16(256, 128, false, true);   // P (TMEM), V MN-major
+        ++gq;
+        if (++jq == iq.nmax) {
+          // the query tile is free once both threads' S products of the item
+          // are done: each thread commits when its cursor leaves the item
+          umma_commit_pair(&B.q_empty[qb], kPairMask);
+          ++qi;
+          jq = 0;
+          hq = sq.next_with_tiles(p, rq, iq);
+        }
+      };
+      for (int i = 0; i < kNumS && hq && ok; ++i) next_qk(par == 0);
+      // P.V cursor
+      ItemSource sp = src;
+      int rp = 0;
+      Item ip;
       uint32_t g = 0;
-      bool ok = true;
-      Item it;
-      int r = 0;
-      while (ok && src.next_with_tiles(p, r, it)) {
-        for (int kt = 0; kt < it.nmax; ++kt, ++g) {
-          // both CTAs' P (tensor memory) and V halves are in place
-          const int sb = g % kNumS;
-          if (!(ok = mbar_wait_cl(&B.p_full[sb], (g / kNumS) & 1, p.status))) break;
-          tc_fence_after();
-          const uint32_t va = smem_u32(smem + kV + sb * kVBytes);
+      while (ok && sp.next_with_tiles(p, rp, ip)) {
+        for (int kt = 0; kt < ip.nmax && ok; ++kt, ++g) {
+          const bool mine = (g & 1u) == par;
+          if (mine) {
+            // both CTAs' P (tensor memory) and V halves are in place, and
+            // P.V(g - 1) has accumulated into O
+            const int sb = g % kNumS;
+            if (!(ok = mbar_wait_cl(&B.p_full[sb], (g / kNumS) & 1, p.status))) break;
+            if (g > 0) {
+              const uint32_t g1 = g - 1;
+              if (!(ok = mbar_wait(&B.o_done[g1 % kNumS], (g1 / kNumS) & 1, p.status))) break;
+            }
+            tc_fence_after();
+            const uint32_t va = smem_u32(smem + kV + sb * kVBytes);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t bd = umma_sdesc_sw128(va + k * 2048, kVBytes, 1024);
-            umma_bf16_ts_pair(tmem + kColO, tmem + kColS + sb * 128 + p_col(k), bd, idesc_pv,
-                              (kt > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t bd = umma_sdesc_sw128(va + k * 2048, kVBytes, 1024);
+              umma_bf16_ts_pair(tmem + kColO, tmem + kColS + sb * 128 + p_col(k), bd, idesc_pv,
+                                (kt > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit_pair(&B.o_done[sb], kPairMask);
           }
-          umma_commit_pair(&B.o_done[sb], kPairMask);
+          // S(g + 3): by the thread that issued P.V(g)
+          if (hq) next_qk(mine);
         }
       }
+      // every product issued completes before the columns are released
       umma_commit_pair(B.drain, kPairMask);
     }
     __syncwarp();
@@ -608,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg_first = lane < used ? __ldg(bt + lane) : 0;
       float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
       for (int kt = 0; kt < it.nmax; ++kt, ++g) {
-        if (ok) ok = mbar_wait_warp_cl(&B.s_full[g % kNumS], (g / kNumS) & 1, p.status);
+        if (ok) ok = mbar_wait_warp(&B.s_full[g % kNumS], (g / kNumS) & 1, p.status);
         tc_fence_after();
         const uint32_t s_cols = tmem + lane_base + kColS + (g % kNumS) * 128 + half * 64;
         // causal mask only where the tile crosses pos: masked scores take no part
@@ -697,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O must hold every earlier step: P.V(g - 1) done.  (S(g) complete
           // means P.V(g - 3) is, so this barrier is at most one phase behind.)
           const uint32_t g1 = g - 1;
-          if (ok) ok = mbar_wait_warp_cl(&B.o_done[g1 % kNumS], (g1 / kNumS) & 1, p.status);
+          if (ok) ok = mbar_wait_warp(&B.o_done[g1 % kNumS], (g1 / kNumS) & 1, p.status);
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
@@ -711,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // this CTA's V half of the step: landed, and zeroed past the context
         const int vs = g % kRingV;
-        if (ok) ok = mbar_wait_warp_cl(&B.v_full[vs], (g / kRingV) & 1, p.status);
+        if (ok) ok = mbar_wait_warp(&B.v_full[vs], (g / kRingV) & 1, p.status);
         if (zero_tail && kt == it.nmax - 1) {
           const int rr = vtail + (t >> 1);
           if (rr < kPage) {
@@ -743,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lrow = l + *x_other;
       named_bar_sync(xbar, 64);  // the slot is free for the next item
       const uint32_t gl = g - 1;
-      if (ok) ok = mbar_wait_warp_cl(&B.o_done[gl % kNumS], (gl / kNumS) & 1, p.status);
+      if (ok) ok = mbar_wait_warp(&B.o_done[gl % kNumS], (gl / kNumS) & 1, p.status);
       tc_fence_after();
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       // an invalid sequence may have read a substitute page: select zeros
