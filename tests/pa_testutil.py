@@ -12,6 +12,18 @@ ATOL = 5e-3
 REL_L2 = 8e-3
 
 
+# (test, what, max|err|, bound) of every comparison made through the helpers
+# below; tests/conftest.py prints them at the end of the run and, when
+# PA_MAXERR_LOG names a file, writes them there as JSON.
+ERRORS = []
+
+
+def _record(what, mx, bound):
+    import os
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    ERRORS.append((test, what, float(mx), float(bound)))
+
+
 def dev_status():
     return torch.zeros(1, dtype=torch.int32, device="cuda")
 
@@ -35,6 +47,7 @@ def assert_close(gpu, ref, atol=ATOL, what=""):
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - ref)
     mx = float(err.max()) if err.size else 0.0
+    _record(what, mx, atol)
     assert mx <= atol, f"{what}: max|err| {mx:.3e} > {atol:.1e} at {np.unravel_index(err.argmax(), err.shape)}"
     denom = np.linalg.norm(ref)
     if denom > 0:
@@ -49,7 +62,10 @@ def assert_close_bf16(gpu, ref, what=""):
     g = gpu.detach().float().cpu().double().numpy().reshape(ref.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     bound = ATOL + np.abs(ref) * 2.0 ** -8
-    bad = np.abs(g - ref) > bound
+    err = np.abs(g - ref)
+    # recorded: the worst error as a fraction of its element's bound
+    _record(what + " (bf16 out, err / bound)", float((err / bound).max()) if err.size else 0.0, 1.0)
+    bad = err > bound
     assert not bad.any(), f"{what}: {bad.sum()} elements beyond bf16 bound"
 
 
