@@ -301,6 +301,27 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
                      pa_stream_t stream);
 
 /*
+ * pa_prefill_chunk_fp8 -- pa_prefill_chunk over an FP8 (e4m3) cache, the
+ * prefill step ("Qwen3-14B" pypto-lib doc, prefill_fwd: KV cache update, then
+ * causal attention) with the "fp8_e4m3" KV cache dtype the SGLang launch in
+ * the "Qwen4-Exp QSA..." blog selects.  The chunk's own K/V must already be
+ * in the cache (pa_kv_write_fp8).  As in pa_decode_fp8, the e4m3 pages are
+ * converted on the chip to F16, which holds every e4m3 value exactly, and q
+ * to F16 (|q| must stay below 65520: larger elements set PA_STATUS_Q_RANGE and
+ * make the output undefined); P is rounded to F16 for the P.V product.  The
+ * scores are q . K * k_scale[h] * scale and the output is multiplied by
+ * v_scale[h].  Arguments, limits, status bits and errors as pa_prefill_chunk;
+ * k_scale and v_scale (float32 [Hkv], device) must be non-null
+ * (PA_ERR_NULL_POINTER) and 4-byte aligned (PA_ERR_ALIGNMENT).
+ */
+int pa_prefill_chunk_fp8(const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale,
+                         const int32_t* block_table, const int32_t* context_lens,
+                         const int32_t* chunk_lens, int32_t num_tokens, float scale,
+                         void* out, int32_t out_dtype, pa_dims dims, int32_t* status,
+                         pa_stream_t stream);
+
+/*
  * pa_combine -- merge num_splits partial attention states per (sequence, head).
  *   part_o         float32 [B, Hq, num_splits, D]; state i normalised by its own
  *                  softmax sum

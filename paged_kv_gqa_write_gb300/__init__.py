@@ -36,7 +36,7 @@ EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_a
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
             "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
-            "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs")
+            "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs", "pa_prefill_chunk_fp8")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -93,6 +93,9 @@ def load(path: str = LIB_PATH):
     lib.pa_decode_auto_splits.argtypes = [pa_dims]
     lib.pa_prefill_chunk.restype = ctypes.c_int
     lib.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, f32, vp, i32, pa_dims, vp, vp]
+    lib.pa_prefill_chunk_fp8.restype = ctypes.c_int
+    lib.pa_prefill_chunk_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, i32,
+                                         pa_dims, vp, vp]
     lib.pa_combine.restype = ctypes.c_int
     lib.pa_combine.argtypes = [vp, vp, i32, vp, i32, pa_dims, vp]
     lib.pa_decode_noalloc.restype = ctypes.c_int
@@ -411,12 +414,47 @@ def pa_prefill_chunk(q, k_cache, v_cache, block_table, context_lens, chunk_lens,
     if out is None:
         out = torch.empty(T, Hq, D, dtype=out_dtype, device=dev)
     _need(out, "out", out.dtype, dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
     code = PA_F32 if out.dtype == torch.float32 else PA_BF16
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     rc = load().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                  _ptr(context_lens), _ptr(chunk_lens), int(T), scale, _ptr(out),
                                  code, d, _ptr(status), _stream(stream))
     _check("pa_prefill_chunk", rc)
+    return out
+
+
+def pa_prefill_chunk_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                         chunk_lens, scale=None, out=None, out_dtype=torch.bfloat16, status=None,
+                         stream=None):
+    """Causal chunked prefill over an FP8 (e4m3) cache [num_pages, 128, Hkv, 128] with
+    per-KV-head float32 scales.  q: [T, Hq, 128] bf16 token-major."""
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need_fp8_cache(k_cache, "k_cache", dev)
+    _need_fp8_cache(v_cache, "v_cache", dev)
+    _need(k_scale, "k_scale", torch.float32, dev)
+    _need(v_scale, "v_scale", torch.float32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    T, Hq, D = q.shape
+    d = _cache_dims(Hq, k_cache, block_table)
+    if out is None:
+        out = torch.empty(T, Hq, D, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    rc = load().pa_prefill_chunk_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(block_table), _ptr(context_lens),
+                                     _ptr(chunk_lens), int(T), scale, _ptr(out), code, d,
+                                     _ptr(status), _stream(stream))
+    _check("pa_prefill_chunk_fp8", rc)
     return out
 
 

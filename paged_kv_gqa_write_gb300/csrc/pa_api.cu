@@ -683,10 +683,31 @@ int pa_combine(const float* part_o, const float* part_lse, int32_t num_splits, v
   return launch_result(pa::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
-                     const int32_t* block_table, const int32_t* context_lens,
-                     const int32_t* chunk_lens, int32_t num_tokens, float scale, void* out,
-                     int32_t out_dtype, pa_dims d, int32_t* status, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// An FP8 (e4m3) cache viewed as [num_pages * 128 rows, Hkv * 128 one-byte
+// columns] with the given box and swizzle.
+bool encode_cache_u8(CUtensorMap* map, const void* cache, const pa_dims& d, uint32_t box_cols,
+                     uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d.num_kv_heads * kHeadDim, (cuuint64_t)d.num_pages * kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)d.num_kv_heads * kHeadDim};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// pa_prefill_chunk over a bf16 cache (k_scale == nullptr) or an FP8 one.
+int prefill_impl(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                 const float* v_scale, const int32_t* block_table, const int32_t* context_lens,
+                 const int32_t* chunk_lens, int32_t num_tokens, float scale, void* out,
+                 int32_t out_dtype, pa_dims d, int32_t* status, pa_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_OUT_DTYPE;
@@ -695,19 +716,27 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   if (num_tokens == 0 || d.num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !chunk_lens || !out)
     return PA_ERR_NULL_POINTER;
+  const bool fp8 = k_scale != nullptr;
+  if (fp8 && !v_scale) return PA_ERR_NULL_POINTER;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGNMENT;
+  if (fp8 && ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u))
     return PA_ERR_ALIGNMENT;
   if ((int64_t)num_tokens * d.num_q_heads * kHeadDim > ((int64_t)1 << 40)) return PA_ERR_DIMS;
   const int sms = device_sms();
   if (sms <= 0) return PA_ERR_NO_DEVICE;
   CUtensorMap tm_k, tm_v, tm_q;
-  // each CTA of a pair stages half a page tile: K as 64-key x 64-dim boxes,
-  // V as 128-key x 64-dim boxes
-  if (!encode_2d(&tm_k, k_cache, (uint64_t)d.num_kv_heads * kHeadDim,
-                 (uint64_t)d.num_pages * kPage, (uint64_t)d.num_kv_heads * kHeadDim * 2, 64, 64,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_cache_map(&tm_v, v_cache, d))
-    return PA_ERR_TENSOR_MAP;
+  // each CTA of a pair stages half a page tile: K as 64-key boxes (64 dims
+  // wide, or all 128 one-byte dims of an e4m3 row), V as 128-key x 64-dim
+  // boxes
+  const bool maps_ok =
+      fp8 ? encode_cache_u8(&tm_k, k_cache, d, kHeadDim, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                encode_cache_u8(&tm_v, v_cache, d, 64, kPage, CU_TENSOR_MAP_SWIZZLE_64B)
+          : encode_2d(&tm_k, k_cache, (uint64_t)d.num_kv_heads * kHeadDim,
+                      (uint64_t)d.num_pages * kPage, (uint64_t)d.num_kv_heads * kHeadDim * 2, 64,
+                      64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                encode_cache_map(&tm_v, v_cache, d);
+  if (!maps_ok) return PA_ERR_TENSOR_MAP;
   // q as [num_tokens, Hq, 128]: a box is 128 tokens of one head, 64 dims wide.
   if (!encode_3d(&tm_q, q, kHeadDim, d.num_q_heads, (uint64_t)num_tokens, 64, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -734,8 +763,32 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   p.out_f32 = out_dtype == PA_F32;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   return launch_result(
       pa::launch_prefill(tm_k, tm_v, tm_q, tm_o, p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* context_lens,
+                     const int32_t* chunk_lens, int32_t num_tokens, float scale, void* out,
+                     int32_t out_dtype, pa_dims d, int32_t* status, pa_stream_t stream) {
+  return prefill_impl(q, k_cache, v_cache, nullptr, nullptr, block_table, context_lens,
+                      chunk_lens, num_tokens, scale, out, out_dtype, d, status, stream);
+}
+
+int pa_prefill_chunk_fp8(const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* context_lens, const int32_t* chunk_lens,
+                         int32_t num_tokens, float scale, void* out, int32_t out_dtype,
+                         pa_dims d, int32_t* status, pa_stream_t stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL_POINTER;
+  return prefill_impl(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                      chunk_lens, num_tokens, scale, out, out_dtype, d, status, stream);
 }
 
 int32_t pa_prefill_pairs(void) {

@@ -504,6 +504,39 @@ __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
 }
 
 // ---------------------------------------------------------------- numerics
+// Two floats -> two F16 (round to nearest even) in one 32-bit word, lo first.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two F16 in one 32-bit word -> two floats (exact).
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
+  float2 f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(w));
+  return f;
+}
+
+// 4 e4m3 codes (bytes 0..3 of w) -> 4 F16 values (exact): two F16 pairs.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 16 e4m3 codes -> 16 F16 values (exact), as two 16-byte chunks.
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4& lo, uint4& hi) {
+  e4m3x4_to_f16x4(c.x, lo.x, lo.y);
+  e4m3x4_to_f16x4(c.y, lo.z, lo.w);
+  e4m3x4_to_f16x4(c.z, hi.x, hi.y);
+  e4m3x4_to_f16x4(c.w, hi.z, hi.w);
+}
+
 // Two bf16 in one 32-bit word -> two floats (exact).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -719,6 +752,8 @@ struct PrefillParams {
   int32_t B, T, Hq, Hkv, G;
   int32_t num_pages, max_pages;
   int32_t out_f32;
+  const float* k_scale;         // FP8 cache: [Hkv] scales of the K and V codes
+  const float* v_scale;
 };
 
 }  // namespace pa

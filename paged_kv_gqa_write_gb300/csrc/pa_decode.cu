@@ -201,22 +201,6 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
-// 4 e4m3 codes (bytes 0..3 of w) -> 4 F16 values (exact): two F16 pairs.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
-// 16 e4m3 codes -> 16 F16 values (exact), as two 16-byte chunks.
-__device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4& lo, uint4& hi) {
-  e4m3x4_to_f16x4(c.x, lo.x, lo.y);
-  e4m3x4_to_f16x4(c.y, lo.z, lo.w);
-  e4m3x4_to_f16x4(c.z, hi.x, hi.y);
-  e4m3x4_to_f16x4(c.w, hi.z, hi.w);
-}
-
 // NH: columns the softmax and epilogue handle (8, 16 or 32, >= any item's GC).
 // FP8: the cache holds e4m3 codes with per-KV-head scales.  MULTI: more than
 // one new token per sequence (per-column causal masks, (token, head) columns);

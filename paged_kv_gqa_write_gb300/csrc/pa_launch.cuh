@@ -56,7 +56,10 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_
 cudaError_t prefill_pairs(int num_sms, int* pairs);
 
 // tm_o: 3-D map over a BF16 out [T][Hq][128] with 64 x 1 x 128 boxes and
-// 128-byte swizzle (unused, any contents, for FP32 output).
+// 128-byte swizzle (unused, any contents, for FP32 output).  p.k_scale
+// non-null selects the FP8-cache kernel: tm_k and tm_v are then maps over the
+// e4m3 caches, K with 128-byte x 64-row boxes (128-byte swizzle) and V with
+// 64-byte x 128-row boxes (64-byte swizzle).
 cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const CUtensorMap& tm_o,
                            const PrefillParams& p, int num_sms, cudaStream_t stream);

@@ -77,32 +77,54 @@ constexpr int kSoftWarp0 = 2;                 // softmax warps 2 .. 9
 constexpr int kSoftmaxWarps = 8;
 constexpr int kVWarp = 10;                    // V producer
 constexpr int kPvWarp = 11;                   // P.V issuer (even CTA)
-constexpr int kThreads = (kPvWarp + 1) * 32;
+constexpr int kConvWarp0 = 12;                // FP8 cache: converter warps 12 .. 15
 constexpr int kQBytes = 128 * 128 * 2;        // one query tile (two 64-column boxes)
 constexpr int kQBox = 16384;
 constexpr int kKBytes = 64 * 128 * 2;         // this CTA's K half: 64 keys x 128 dims
 constexpr int kKBox = 8192;                   // 64 keys x 64 dims
 constexpr int kVBytes = 128 * 64 * 2;         // this CTA's V half: 128 keys x 64 dims
-// the K and V rings have as many stages as there are S buffers, so that S(j)
-// done frees K stage j % 3 and P.V(j) done frees V stage j % 3
-constexpr int kNumS = 3, kRingK = kNumS, kRingV = kNumS;
+constexpr int kK8Bytes = 64 * 128;            // the same K half as e4m3 codes
+constexpr int kV8Bytes = 128 * 64;            // the same V half as e4m3 codes
+constexpr int kNumS = 3;                      // S buffers in tensor memory
 constexpr int kMaxList = PA_PREFILL_SCHEDULE_ITEMS;  // scheduled items per pair
-// shared memory layout (offsets from a 1024-aligned base; identical in both
-// CTAs: a pair MMA reads both at the same offsets)
-constexpr int kQ = 0;
-constexpr int kK = kQ + 2 * kQBytes;
-constexpr int kV = kK + kRingK * kKBytes;
-constexpr int kOut = kV + kRingV * kVBytes;   // BF16 output tile staging: 2 boxes of 128 x 64
 constexpr int kOutBytes = 128 * 128 * 2;
 constexpr int kOutBox = 16384;
-constexpr int kX = kOut + kOutBytes;          // row exchange between the two halves: [2][128] float
 constexpr int kListInts = 5;                  // per item: s, pair|head, tok0, chunk len, ctx
-constexpr int kList = kX + 2 * 128 * 4;       // schedule [kMaxList][kListInts] int
-constexpr int kBars = kList + kMaxList * kListInts * 4;
-constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 3 * kNumS + 1;
-constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
-constexpr int kMaxCost = 4096;                // schedule histogram buckets (K ring scratch)
-constexpr int kMaxSchedSeqs = (kRingV * kVBytes / 4 - 1) / 4;  // sequences the schedule stages
+constexpr int kMaxCost = 4096;                // schedule histogram buckets
+constexpr int kSchedBytes = 3 * kMaxCost * 4; // the schedule's scratch ...
+constexpr int kSeqBytes = 48 * 1024;          // ... and its staged lengths
+constexpr int kMaxSchedSeqs = (kSeqBytes / 4 - 1) / 4;  // sequences the schedule stages
+// Shared memory layout (offsets from a 1024-aligned base; identical in both
+// CTAs: a pair MMA reads both at the same offsets).  BF16 cache: 3-stage K
+// and V operand rings, S(j) done frees K stage j % 3 and P.V(j) done V stage
+// j % 3.  FP8 cache: 2-stage F16 operand rings, filled by the converter warps
+// from 3-stage rings of e4m3 halves.
+template <bool FP8>
+struct Lay {
+  static constexpr int kThreads = (FP8 ? kConvWarp0 + 4 : kPvWarp + 1) * 32;
+  static constexpr int kRingK = FP8 ? 2 : 3, kRingV = FP8 ? 2 : 3;  // operand stages
+  static constexpr int kRing8 = FP8 ? 3 : 0;                        // e4m3 stages
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kQBytes;
+  static constexpr int kV = kK + kRingK * kKBytes;
+  static constexpr int kK8 = kV + kRingV * kVBytes;
+  static constexpr int kV8 = kK8 + kRing8 * kK8Bytes;
+  static constexpr int kOut = kV8 + kRing8 * kV8Bytes;  // BF16 output tile staging: 2 boxes of 128 x 64
+  static constexpr int kX = kOut + kOutBytes;           // row exchange between the two halves: [2][128] float
+  static constexpr int kList = kX + 2 * 128 * 4;        // schedule [kMaxList][kListInts] int
+  static constexpr int kBars = kList + kMaxList * kListInts * 4;
+  // q_full, q_empty, k_full, v_full, s_full, p_full, o_done, drain; FP8:
+  // q16_full, k16_full, v16_full, k8_full, k8_empty, v8_full, v8_empty
+  static constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 3 * kNumS + 1 +
+                                  (FP8 ? 2 + kRingK + kRingV + 4 * kRing8 : 0);
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
+  // the rings are idle until the first load: scratch for the schedule
+  static constexpr int kSched = kK;
+  static constexpr int kSeqs = FP8 ? kK8 : kV;
+  static_assert(kSched + kSchedBytes <= kSeqs, "schedule scratch must fit the operand rings");
+  static_assert(kSeqs + kSeqBytes <= kOut, "schedule lengths must fit the rings");
+  static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
+};
 // TMEM columns (the same in both CTAs)
 constexpr uint32_t kColS = 0;     // S0, S1, S2: 128 columns each, by step mod 3; P(j) over S(j)
 constexpr uint32_t kColO = 384;   // O: 128 columns
@@ -125,6 +147,14 @@ struct Bars {
   uint64_t* p_full;   // [3] even CTA: P(g) written in both CTAs, V(g) halves in place
   uint64_t* o_done;   // [3] P.V(g) done: O holds every step <= g, V stage g % 3 free
   uint64_t* drain;    // every MMA issued (by both issuers) has completed
+  // FP8 cache (q_full then completes per CTA: each loads its own tile)
+  uint64_t* q16_full;  // [2] even CTA: both CTAs' query tiles converted to F16
+  uint64_t* k16_full;  // [2] even CTA: both CTAs' K halves converted to F16
+  uint64_t* v16_full;  // [2] this CTA's V half converted to F16
+  uint64_t* k8_full;   // [3] this CTA's e4m3 K half landed
+  uint64_t* k8_empty;  // [3] ... converted
+  uint64_t* v8_full;   // [3] this CTA's e4m3 V half landed
+  uint64_t* v8_empty;  // [3] ... converted
 };
 
 struct Item {
@@ -370,27 +400,38 @@ __device__ __forceinline__ void drain_loads(uint64_t* bars, int n, uint32_t issu
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool FP8>
+__global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillParams p) {
+  using L = Lay<FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBars);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBars);
   Bars B;
   B.q_full = bar;
   B.q_empty = bar + 2;
   B.k_full = bar + 4;
-  B.v_full = B.k_full + kRingK;
-  B.s_full = B.v_full + kRingV;
+  B.v_full = B.k_full + L::kRingK;
+  B.s_full = B.v_full + L::kRingV;
   B.p_full = B.s_full + kNumS;
   B.o_done = B.p_full + kNumS;
   B.drain = B.o_done + kNumS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
+  if constexpr (FP8) {
+    B.q16_full = B.drain + 1;
+    B.k16_full = B.q16_full + 2;
+    B.v16_full = B.k16_full + L::kRingK;
+    B.k8_full = B.v16_full + L::kRingV;
+    B.k8_empty = B.k8_full + L::kRing8;
+    B.v8_full = B.k8_empty + L::kRing8;
+    B.v8_empty = B.v8_full + L::kRing8;
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + L::kNumBars * 8);
   int* list_count = reinterpret_cast<int*>(tmem_slot + 1);
-  int* list = reinterpret_cast<int*>(smem + kList);
-  float* xch = reinterpret_cast<float*>(smem + kX);
+  int* list = reinterpret_cast<int*>(smem + L::kList);
+  float* xch = reinterpret_cast<float*>(smem + L::kX);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // query tile of the pair this CTA owns
@@ -401,20 +442,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B.q_full[t], 1);
       mbar_init(&B.q_empty[t], 2);  // one commit from each MMA issuer
     }
-    for (int i = 0; i < kRingK; ++i) mbar_init(&B.k_full[i], 1);
-    for (int i = 0; i < kRingV; ++i) mbar_init(&B.v_full[i], 1);
+    for (int i = 0; i < L::kRingK; ++i) mbar_init(&B.k_full[i], 1);
+    for (int i = 0; i < L::kRingV; ++i) mbar_init(&B.v_full[i], 1);
     for (int i = 0; i < kNumS; ++i) {
       mbar_init(&B.s_full[i], 1);
       mbar_init(&B.p_full[i], 2 * kSoftmaxWarps);  // the softmax warps of both CTAs
       mbar_init(&B.o_done[i], 1);
     }
     mbar_init(B.drain, 2);  // one commit from each issuer
+    if constexpr (FP8) {
+      for (int i = 0; i < 2; ++i) mbar_init(&B.q16_full[i], 8);  // 4 converter warps x 2 CTAs
+      for (int i = 0; i < L::kRingK; ++i) mbar_init(&B.k16_full[i], 8);
+      for (int i = 0; i < L::kRingV; ++i) mbar_init(&B.v16_full[i], 4);
+      for (int i = 0; i < L::kRing8; ++i) {
+        mbar_init(&B.k8_full[i], 1);
+        mbar_init(&B.k8_empty[i], 4);
+        mbar_init(&B.v8_full[i], 1);
+        mbar_init(&B.v8_empty[i], 4);
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
     // the rings are idle until the first load: scratch for the schedule
-    const int count = build_schedule(p, reinterpret_cast<int*>(smem + kK),
-                                     reinterpret_cast<int*>(smem + kV), list, npairs, pair_id,
+    const int count = build_schedule(p, reinterpret_cast<int*>(smem + L::kSched),
+                                     reinterpret_cast<int*>(smem + L::kSeqs), list, npairs, pair_id,
                                      lane);
     if (lane == 0) *list_count = count;
   }
@@ -449,46 +501,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qb = qitems & 1;
           if (!(ok = mbar_wait(&B.q_empty[qb], ((qitems >> 1) & 1) ^ 1, p.status))) break;
           ++qitems;
-          if (even) mbar_arrive_expect_tx(&B.q_full[qb], 2 * kQBytes);
-          const uint32_t qbar = mapa_shared(smem_u32(&B.q_full[qb]), 0);
           const int z = it.tok0 + (int)rank * 128;
-          tma_load_3d_pair(smem + kQ + qb * kQBytes, &tm_q, 0, it.g, z, qbar, pol_q);
-          tma_load_3d_pair(smem + kQ + qb * kQBytes + kQBox, &tm_q, 64, it.g, z, qbar, pol_q);
+          uint8_t* qdst = smem + L::kQ + qb * kQBytes;
+          if constexpr (FP8) {
+            // each CTA's own barrier: its converter warps rewrite the tile as F16
+            mbar_arrive_expect_tx(&B.q_full[qb], kQBytes);
+            tma_load_3d(qdst, &tm_q, 0, it.g, z, &B.q_full[qb], pol_q);
+            tma_load_3d(qdst + kQBox, &tm_q, 64, it.g, z, &B.q_full[qb], pol_q);
+          } else {
+            if (even) mbar_arrive_expect_tx(&B.q_full[qb], 2 * kQBytes);
+            const uint32_t qbar = mapa_shared(smem_u32(&B.q_full[qb]), 0);
+            tma_load_3d_pair(qdst, &tm_q, 0, it.g, z, qbar, pol_q);
+            tma_load_3d_pair(qdst + kQBox, &tm_q, 64, it.g, z, qbar, pol_q);
+          }
         }
         for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
           int page = __ldg(bt + kt);
           if (page < 0 || page >= p.num_pages) page = 0;  // sequence reported invalid
           const int y = page * kPage;
-          if (is_k) {
+          if constexpr (FP8) {
+            // e4m3 halves: K keys 64 rank .. + 63 (128 one-byte dims), V dims
+            // 64 rank .. + 63 of the 128 keys; stage tiles % 3 is free once the
+            // converter warps have read it
+            const int st = tiles % L::kRing8;
+            const uint32_t ph = ((tiles / L::kRing8) & 1) ^ 1;
+            uint64_t* empty = is_k ? &B.k8_empty[st] : &B.v8_empty[st];
+            uint64_t* full = is_k ? &B.k8_full[st] : &B.v8_full[st];
+            if (tiles >= (uint32_t)L::kRing8 && !(ok = mbar_wait(empty, ph, p.status))) break;
+            if (is_k) {
+              mbar_arrive_expect_tx(full, kK8Bytes);
+              tma_load_2d(smem + L::kK8 + st * kK8Bytes, &tm_k, it.h * kHeadDim,
+                          y + (int)rank * 64, full, pol_kv);
+            } else {
+              mbar_arrive_expect_tx(full, kV8Bytes);
+              tma_load_2d(smem + L::kV8 + st * kV8Bytes, &tm_v, it.h * kHeadDim + (int)rank * 64,
+                          y, full, pol_kv);
+            }
+          } else if (is_k) {
             // stage tiles % 3 is free once S(tiles - 3) is done
-            const int st = tiles % kRingK;
-            if (tiles >= (uint32_t)kRingK &&
-                !(ok = mbar_wait(&B.s_full[st], ((tiles / kRingK) & 1) ^ 1, p.status)))
+            const int st = tiles % L::kRingK;
+            if (tiles >= (uint32_t)L::kRingK &&
+                !(ok = mbar_wait(&B.s_full[st], ((tiles / L::kRingK) & 1) ^ 1, p.status)))
               break;
             if (even) mbar_arrive_expect_tx(&B.k_full[st], 2 * kKBytes);
             const uint32_t kbar = mapa_shared(smem_u32(&B.k_full[st]), 0);
-            uint8_t* dst = smem + kK + st * kKBytes;
+            uint8_t* dst = smem + L::kK + st * kKBytes;
             tma_load_2d_pair(dst, &tm_k, it.h * kHeadDim, y + (int)rank * 64, kbar, pol_kv);
             tma_load_2d_pair(dst + kKBox, &tm_k, it.h * kHeadDim + 64, y + (int)rank * 64, kbar,
                              pol_kv);
           } else {
             // stage tiles % 3 is free once P.V(tiles - 3) is done
-            const int st = tiles % kRingV;
-            if (tiles >= (uint32_t)kRingV &&
-                !(ok = mbar_wait(&B.o_done[st], ((tiles / kRingV) & 1) ^ 1, p.status)))
+            const int st = tiles % L::kRingV;
+            if (tiles >= (uint32_t)L::kRingV &&
+                !(ok = mbar_wait(&B.o_done[st], ((tiles / L::kRingV) & 1) ^ 1, p.status)))
               break;
             mbar_arrive_expect_tx(&B.v_full[st], kVBytes);
-            tma_load_2d(smem + kV + st * kVBytes, &tm_v, it.h * kHeadDim + (int)rank * 64, y,
+            tma_load_2d(smem + L::kV + st * kVBytes, &tm_v, it.h * kHeadDim + (int)rank * 64, y,
                         &B.v_full[st], pol_kv);
           }
         }
       }
       // copies still in flight (only after a timeout) land before teardown;
       // the even CTA's barriers count both CTAs' Q and K halves
-      if (!is_k) drain_loads(B.v_full, kRingV, tiles, p.status, false);
-      else if (even) {
+      if constexpr (FP8) {
+        drain_loads(is_k ? B.k8_full : B.v8_full, L::kRing8, tiles, p.status, false);
+        if (is_k) drain_loads(B.q_full, 2, qitems, p.status, false);
+      } else if (!is_k) {
+        drain_loads(B.v_full, L::kRingV, tiles, p.status, false);
+      } else if (even) {
         drain_loads(B.q_full, 2, qitems, p.status, true);
-        drain_loads(B.k_full, kRingK, tiles, p.status, true);
+        drain_loads(B.k_full, L::kRingK, tiles, p.status, true);
       }
     }
     __syncwarp();
@@ -503,8 +585,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // waits for P.V(g - 1) (the other thread's) to complete, which orders
       // the accumulation into O.  Thread 0 issues S(0..2) up front.
       const uint32_t par = warp == 1 ? 0u : 1u;
-      const uint32_t idesc_qk = umma_idesc_bf16(256, 128, false, false);  // Q, K: K-major
-      const uint32_t idesc_pv = umma_idesc_bf16(256, 128, false, true);   // P (TMEM), V MN-major
+      // Q, K: K-major; P (TMEM), V MN-major; F16 operands for the FP8 cache
+      const uint32_t idesc_qk = FP8 ? umma_idesc_f16(256, 128, false, false)
+                                    : umma_idesc_bf16(256, 128, false, false);
+      const uint32_t idesc_pv = FP8 ? umma_idesc_f16(256, 128, false, true)
+                                    : umma_idesc_bf16(256, 128, false, true);
       bool ok = true;
       // S cursor: step gq of item iq (key tile jq), its query tile's ordinal qi
       ItemSource sq = src;
@@ -516,14 +601,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qb = qi & 1;
         if (issue) {
           if (q_waited != qi) {
-            if (!(ok = mbar_wait(&B.q_full[qb], (qi >> 1) & 1, p.status))) return;
+            // FP8: both CTAs' tiles rewritten as F16 by their converter warps
+            if (!(ok = FP8 ? mbar_wait_cl(&B.q16_full[qb], (qi >> 1) & 1, p.status)
+                           : mbar_wait(&B.q_full[qb], (qi >> 1) & 1, p.status)))
+              return;
             q_waited = qi;
           }
-          const int sb = gq % kNumS;
-          if (!(ok = mbar_wait(&B.k_full[sb], (gq / kNumS) & 1, p.status))) return;
+          const int sb = gq % kNumS, kb = gq % L::kRingK;
+          const uint32_t kph = (gq / L::kRingK) & 1;
+          if (!(ok = FP8 ? mbar_wait_cl(&B.k16_full[kb], kph, p.status)
+                         : mbar_wait(&B.k_full[kb], kph, p.status)))
+            return;
           tc_fence_after();
-          const uint32_t qa = smem_u32(smem + kQ + qb * kQBytes);
-          const uint32_t ka = smem_u32(smem + kK + sb * kKBytes);
+          const uint32_t qa = smem_u32(smem + L::kQ + qb * kQBytes);
+          const uint32_t ka = smem_u32(smem + L::kK + kb * kKBytes);
           const uint32_t d = tmem + kColS + sb * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -562,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait(&B.o_done[g1 % kNumS], (g1 / kNumS) & 1, p.status))) break;
             }
             tc_fence_after();
-            const uint32_t va = smem_u32(smem + kV + sb * kVBytes);
+            const uint32_t va = smem_u32(smem + L::kV + (g % L::kRingV) * kVBytes);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t bd = umma_sdesc_sw128(va + k * 2048, kVBytes, 1024);
@@ -581,6 +672,113 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (warp == 1 && lane == 0) mbar_wait_cl_for(B.drain, 0, p.status, kWaitLimitNs);
     __syncwarp();
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ FP8 converters
+    // Four warps (128 threads) per CTA, per item: this CTA's query tile from
+    // BF16 to F16 in place (thread = row), then per step this CTA's e4m3 K
+    // half (thread = key, 64 dims) and V half (thread = key) to F16, in the
+    // swizzled layouts the BF16 path gets from TMA (e4m3 values are exact in
+    // F16).  K and V stages are reused two steps later, once S(j - 2) and
+    // P.V(j - 2) are done.  The even CTA's issuer waits for both CTAs' Q and
+    // K (remote arrivals from the odd CTA); V is this CTA's, behind the
+    // softmax's P barrier.
+    if constexpr (FP8) {
+      const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
+      uint32_t q16_even[2], k16_even[L::kRingK];
+      for (int i = 0; i < 2; ++i) q16_even[i] = mapa_shared(smem_u32(&B.q16_full[i]), 0);
+      for (int i = 0; i < L::kRingK; ++i) k16_even[i] = mapa_shared(smem_u32(&B.k16_full[i]), 0);
+      auto arrive_even = [&](uint64_t* local, uint32_t remote) {
+        __syncwarp();
+        if (lane == 0) {
+          if (even) mbar_arrive(local);
+          else mbar_arrive_cluster_smem(remote);
+        }
+      };
+      uint32_t tiles = 0, qitems = 0;
+      bool ok = true;
+      Item it;
+      int r = 0;
+      while (src.next_with_tiles(p, r, it)) {
+        // ---- Q: row ct of this CTA's tile, 16 chunks of 8 values, in place
+        const int qb = qitems & 1;
+        if (ok) ok = mbar_wait_warp(&B.q_full[qb], (qitems >> 1) & 1, p.status);
+        ++qitems;
+        {
+          const uint32_t qrow = smem_u32(smem + L::kQ + qb * kQBytes) + ct * 128;
+          bool big = false;
+#pragma unroll 4
+          for (int c = 0; c < 16; ++c) {
+            const uint32_t a = qrow + (c >> 3) * kQBox + ((((uint32_t)c & 7) ^ (ct & 7)) << 4);
+            const uint4 v = lds128(a);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = bf16x2_to_float2(wv[e]);
+              big |= fabsf(f.x) >= 65520.f || fabsf(f.y) >= 65520.f;
+              o[e] = pack_f16x2(f.x, f.y);
+            }
+            sts128(a, o[0], o[1], o[2], o[3]);
+          }
+          if (__any_sync(0xffffffffu, big) && lane == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_Q_RANGE);
+        }
+        fence_proxy_async_smem();
+        arrive_even(&B.q16_full[qb], q16_even[qb]);
+        for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
+          const int st8 = tiles % L::kRing8;
+          const uint32_t ph8 = (tiles / L::kRing8) & 1;
+          // ---- K: key ct % 64, dims 64 (ct / 64) .. + 63 -> box ct / 64 of the stage
+          const int kb = tiles % L::kRingK;
+          if (ok) ok = mbar_wait_warp(&B.k8_full[st8], ph8, p.status);
+          if (tiles >= (uint32_t)L::kRingK) {
+            const uint32_t s2 = tiles - L::kRingK;  // S(tiles - 2) done: the stage is free
+            if (ok) ok = mbar_wait_warp(&B.s_full[s2 % kNumS], (s2 / kNumS) & 1, p.status);
+          }
+          {
+            const int key = ct & 63, hb = ct >> 6, sw = key & 7;
+            const uint32_t src8 = smem_u32(smem + L::kK8 + st8 * kK8Bytes) + key * 128;
+            const uint32_t dst = smem_u32(smem + L::kK + kb * kKBytes) + hb * kKBox + key * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {  // dims 64 hb + 16 c .. + 15
+              uint4 lo, hi;
+              e4m3x16_to_f16(lds128(src8 + ((((uint32_t)(4 * hb + c)) ^ sw) << 4)), lo, hi);
+              sts128(dst + ((((uint32_t)(2 * c)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
+              sts128(dst + ((((uint32_t)(2 * c + 1)) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
+            }
+          }
+          fence_proxy_async_smem();
+          arrive_even(&B.k16_full[kb], k16_even[kb]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.k8_empty[st8]);
+          // ---- V: key ct, this CTA's 64 dims
+          const int vb = tiles % L::kRingV;
+          if (ok) ok = mbar_wait_warp(&B.v8_full[st8], ph8, p.status);
+          if (tiles >= (uint32_t)L::kRingV) {
+            const uint32_t g2 = tiles - L::kRingV;  // P.V(tiles - 2) done: the stage is free
+            if (ok) ok = mbar_wait_warp(&B.o_done[g2 % kNumS], (g2 / kNumS) & 1, p.status);
+          }
+          {
+            const int key = ct, sw = key & 7, sw8 = (key >> 1) & 3;  // 64-byte rows, 64-byte swizzle
+            const uint32_t src8 = smem_u32(smem + L::kV8 + st8 * kV8Bytes) + key * 64;
+            const uint32_t dst = smem_u32(smem + L::kV + vb * kVBytes) + key * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {  // dims 16 c .. + 15 of the half
+              uint4 lo, hi;
+              e4m3x16_to_f16(lds128(src8 + ((((uint32_t)c) ^ sw8) << 4)), lo, hi);
+              sts128(dst + ((((uint32_t)(2 * c)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
+              sts128(dst + ((((uint32_t)(2 * c + 1)) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&B.v16_full[vb]);
+            mbar_arrive(&B.v8_empty[st8]);
+          }
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     // two threads per row of tile `rank`: warps w and w + 4 share TMEM lanes
@@ -597,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          mapa_shared(smem_u32(&B.p_full[2]), 0)};
     float* x_mine = xch + half * 128 + row;
     const float* x_other = xch + (1 - half) * 128 + row;
-    const float c = p.scale_log2;
+    float c = p.scale_log2;  // FP8: times the item's k_scale
     if (blockIdx.x == 0 && warp == kSoftWarp0 && p.status) {
       int sum = 0;
       for (int e = lane; e < p.B; e += 32) sum += max(__ldg(p.chunk_lens + e), 0);
@@ -627,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(dst)[cc] = make_uint4(0, 0, 0, 0);
         continue;
       }
+      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + it.h);
       const int pos = it.prior + it.pair * 256 + (int)rank * 128 + row;  // this row's position
       const int last_page = (it.ctx - 1) / kPage;
       const int vtail = it.ctx % kPage;  // rows >= vtail of the last page are past the context
@@ -694,10 +893,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d2.y = k0e + 1 < nvis ? d2.y : -INFINITY;
               }
               dmax = fmaxf(dmax, fmaxf(d2.x, d2.y));
-              const uint32_t w = pack_bf16x2(fast_exp2(d2.x), fast_exp2(d2.y));
+              // P as the MMA's operand type (F16 with the FP8 cache's F16 V)
+              const float p0 = fast_exp2(d2.x), p1 = fast_exp2(d2.y);
+              const uint32_t w = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
               pw[cc * 16 + e] = w;
               // the normaliser adds the weights as rounded, as the MMA uses them
-              sum2 = __fadd2_rn(sum2, bf16x2_to_float2(w));
+              sum2 = __fadd2_rn(sum2, FP8 ? f16x2_to_float2(w) : bf16x2_to_float2(w));
             }
           }
           return dmax;
@@ -740,12 +941,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // this CTA's V half of the step: landed, and zeroed past the context
-        const int vs = g % kRingV;
-        if (ok) ok = mbar_wait_warp(&B.v_full[vs], (g / kRingV) & 1, p.status);
+        const int vs = g % L::kRingV;
+        if (ok) ok = mbar_wait_warp(FP8 ? &B.v16_full[vs] : &B.v_full[vs], (g / L::kRingV) & 1,
+                                    p.status);
         if (zero_tail && kt == it.nmax - 1) {
           const int rr = vtail + (t >> 1);
           if (rr < kPage) {
-            const uint32_t vb = smem_u32(smem + kV + vs * kVBytes) + rr * 128 + (t & 1) * 64;
+            const uint32_t vb = smem_u32(smem + L::kV + vs * kVBytes) + rr * 128 + (t & 1) * 64;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) sts128(vb + ch * 16, 0u, 0u, 0u, 0u);
           }
@@ -775,7 +977,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t gl = g - 1;
       if (ok) ok = mbar_wait_warp(&B.o_done[gl % kNumS], (gl / kNumS) & 1, p.status);
       tc_fence_after();
-      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      // FP8: the V codes' scale comes in here
+      const float inv = lrow > 0.f ? (FP8 ? __ldg(p.v_scale + it.h) : 1.f) / lrow : 0.f;
       // an invalid sequence may have read a substitute page: select zeros
       const uint32_t keep = bad ? 0u : 0xffffffffu;
       // a full tile of BF16 rows: staged and stored by TMA (uniform over the CTA)
@@ -784,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous tile's store has finished reading the staging area
         if (t == 0) bulk_wait_read_all();
         named_bar_sync(5, 32 * kSoftmaxWarps);
-        const uint32_t o_row = smem_u32(smem + kOut) + half * kOutBox + row * 128;
+        const uint32_t o_row = smem_u32(smem + L::kOut) + half * kOutBox + row * 128;
         const uint32_t sw = (uint32_t)(row & 7);
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t o0[32];
@@ -801,8 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(5, 32 * kSoftmaxWarps);
         if (t == 0) {
-          tma_store_3d(&tm_o, smem + kOut, 0, it.g, (int32_t)tile0);
-          tma_store_3d(&tm_o, smem + kOut + kOutBox, 64, it.g, (int32_t)tile0);
+          tma_store_3d(&tm_o, smem + L::kOut, 0, it.g, (int32_t)tile0);
+          tma_store_3d(&tm_o, smem + L::kOut + kOutBox, 64, it.g, (int32_t)tile0);
           bulk_commit_group();
         }
         continue;
@@ -847,7 +1050,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t prefill_pairs(int num_sms, int* pairs) {
+namespace {
+
+// CTA pairs that can be resident at once for one variant (cached per device).
+template <bool FP8>
+cudaError_t pairs_of(int num_sms, int* pairs) {
+  using L = Lay<FP8>;
   static int pairs_cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -856,8 +1064,8 @@ cudaError_t prefill_pairs(int num_sms, int* pairs) {
     *pairs = pairs_cache[dev];
     return cudaSuccess;
   }
-  if ((e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kSmem)) != cudaSuccess)
     return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -867,27 +1075,26 @@ cudaError_t prefill_pairs(int num_sms, int* pairs) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kSmem;
   cfg.gridDim = dim3(2 * (num_sms / 2 > 0 ? num_sms / 2 : 1));
   int n = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, prefill_kernel<FP8>, &cfg)) != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) pairs_cache[dev] = n;
   *pairs = n;
   return cudaSuccess;
 }
 
-cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+template <bool FP8>
+cudaError_t launch_variant(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_q, const CUtensorMap& tm_o,
                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
-  static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
-  static_assert(3 * kMaxCost * 4 <= kRingK * kKBytes, "schedule scratch must fit the K ring");
-  static_assert((4 * kMaxSchedSeqs + 1) * 4 <= kRingV * kVBytes, "schedule lengths must fit the V ring");
+  using L = Lay<FP8>;
   // persistent: one CTA per SM, as many pairs as can be resident at once
   // (tensor memory and shared memory are sized for one CTA per SM)
   int pairs = 0;
-  cudaError_t e = prefill_pairs(num_sms, &pairs);
+  cudaError_t e = pairs_of<FP8>(num_sms, &pairs);
   if (e != cudaSuccess) return e;
   const int64_t max_items = ((int64_t)p.T / 256 + p.B) * p.Hq;
   const int grid_pairs = (int)(max_items < pairs ? max_items : pairs);
@@ -900,13 +1107,24 @@ cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kSmem;
   cfg.stream = stream;
   cfg.gridDim = dim3(2 * grid_pairs);
-  e = cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, tm_q, tm_o, p);
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel<FP8>, tm_k, tm_v, tm_q, tm_o, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prefill_pairs(int num_sms, int* pairs) { return pairs_of<false>(num_sms, pairs); }
+
+cudaError_t launch_prefill(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const CUtensorMap& tm_q, const CUtensorMap& tm_o,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
+  return p.k_scale ? launch_variant<true>(tm_k, tm_v, tm_q, tm_o, p, num_sms, stream)
+                   : launch_variant<false>(tm_k, tm_v, tm_q, tm_o, p, num_sms, stream);
 }
 
 }  // namespace pa

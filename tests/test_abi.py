@@ -114,6 +114,13 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 1.0, FAKE, 0, d, None, None) == h["PA_ERR_NULL_POINTER"]
     assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 3, d, None, None) == h["PA_ERR_OUT_DTYPE"]
     assert lib.pa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1.0, FAKE, 0, d, None, None) == 0
+    pf8 = lambda ks=FAKE, vs=FAKE, n=4, od=0: lib.pa_prefill_chunk_fp8(
+        FAKE, FAKE, FAKE, ks, vs, FAKE, FAKE, FAKE, n, 1.0, FAKE, od, d, None, None)
+    assert pf8(ks=None) == h["PA_ERR_NULL_POINTER"]
+    assert pf8(vs=None) == h["PA_ERR_NULL_POINTER"]
+    assert pf8(ks=ctypes.c_void_p(0x10002)) == h["PA_ERR_ALIGNMENT"]
+    assert pf8(od=3) == h["PA_ERR_OUT_DTYPE"]
+    assert pf8(n=0) == 0                                                          # nothing to do
     assert lib.pa_combine(FAKE, FAKE, 0, FAKE, 0, d, None) == h["PA_ERR_SPLITS"]
     pro = lambda eps=1e-6, base=1e6, scale=1.0, qkv=FAKE, n=2, cl=None: lib.pa_qk_norm_rope_write(
         qkv, FAKE, FAKE, eps, base, scale, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, cl, n, d, None, None)
