@@ -48,7 +48,7 @@ def parse_args():
                     help="decode batch (pool = 32 pages per sequence); smaller values are "
                          "for profiling captures, the benchmark workload is 128")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--profile-leg", choices=["prefill", "fp8", "prologue", "topk", "multi"],
+    ap.add_argument("--profile-leg", choices=["prefill", "prefill-fp8", "fp8", "prologue", "topk", "multi"],
                     default=None,
                     help="run one benchmark leg's calls a few times (FP8 and multi-token legs at "
                          "--batch sequences) for an ncu capture, then exit; prints no bench line")
@@ -500,8 +500,10 @@ def run_topk(pa, torch, hbm, steps=50, warmup=10):
             "l2": "flushed between steps"}
 
 
-def run_prefill(pa, W, torch, steps=50, warmup=10):
-    """Chunked prefill (8 x 512 new tokens): KV write then causal attention."""
+def run_prefill(pa, W, torch, steps=50, warmup=10, fp8=False):
+    """Chunked prefill (8 x 512 new tokens): KV write then causal attention.
+    fp8: the same over an FP8 (e4m3) cache with per-KV-head scales
+    (pa_kv_write_fp8 + pa_prefill_chunk_fp8)."""
     case = W.chunked_prefill(device="cuda", pool_device="cuda")
     flops = 0.0
     for s in range(case.B):
@@ -510,12 +512,25 @@ def run_prefill(pa, W, torch, steps=50, warmup=10):
         flops += case.Hq * 4 * D * sum(prior + j + 1 for j in range(n))
     out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if fp8:
+        g = torch.Generator(device="cuda").manual_seed(13)
+        ks = torch.rand(case.Hkv, generator=g, device="cuda") * 0.02 + 0.02
+        vs = torch.rand(case.Hkv, generator=g, device="cuda") * 0.02 + 0.02
+        k8 = (case.k_cache.float() / ks[None, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        v8 = (case.v_cache.float() / vs[None, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        del case.k_cache, case.v_cache
 
-    def step():
-        pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache, case.block_table,
-                       case.context_lens, case.chunk_lens, status=st)
-        pa.pa_prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table,
-                            case.context_lens, case.chunk_lens, case.scale, out=out, status=st)
+        def step():
+            pa.pa_kv_write_fp8(case.k_new, case.v_new, k8, v8, ks, vs, case.block_table,
+                               case.context_lens, case.chunk_lens, status=st)
+            pa.pa_prefill_chunk_fp8(case.q, k8, v8, ks, vs, case.block_table, case.context_lens,
+                                    case.chunk_lens, case.scale, out=out, status=st)
+    else:
+        def step():
+            pa.pa_kv_write(case.k_new, case.v_new, case.k_cache, case.v_cache, case.block_table,
+                           case.context_lens, case.chunk_lens, status=st)
+            pa.pa_prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table,
+                                case.context_lens, case.chunk_lens, case.scale, out=out, status=st)
 
     flush = L2Flush(torch)
     for _ in range(warmup):
@@ -531,10 +546,12 @@ def run_prefill(pa, W, torch, steps=50, warmup=10):
     torch.cuda.synchronize()
     sp = spread([a.elapsed_time(b) for a, b in ev])
     ms = sp["median_ms"]
-    return {"workload": PREFILL_WORKLOAD, "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms,
-            "spread": sp,
+    name = "pa_kv_write_fp8 (4096 tokens) + pa_prefill_chunk_fp8" if fp8 else \
+        "pa_kv_write (4096 tokens) + pa_prefill_chunk"
+    return {"workload": PREFILL_WORKLOAD + ("-fp8-kv" if fp8 else ""),
+            "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "spread": sp,
             "gflop_causal": flops / 1e9, "status": int(st.item()),
-            "step": "pa_kv_write (4096 tokens) + pa_prefill_chunk", "l2": "flushed between steps"}
+            "step": name, "l2": "flushed between steps"}
 
 
 def run_ours(args):
@@ -554,6 +571,8 @@ def run_ours(args):
         hbm_p = peaks()[0]
         if args.profile_leg == "prefill":
             r = run_prefill(pa, W, torch, steps=2, warmup=1)
+        elif args.profile_leg == "prefill-fp8":
+            r = run_prefill(pa, W, torch, steps=2, warmup=1, fp8=True)
         elif args.profile_leg == "fp8":
             r = run_fp8(pa, W, torch, hbm_p, steps=2, warmup=1, batch=args.batch)
         elif args.profile_leg == "prologue":
@@ -669,6 +688,15 @@ def run_ours(args):
             prefill["frac"] = prefill["tflops"] / bf16
         except Exception as e:  # report, do not hide
             prefill = {"error": str(e).splitlines()[0][:200]}
+    prefill_fp8 = None
+    if not args.no_prefill:
+        try:
+            prefill_fp8 = run_prefill(pa, W, torch, fp8=True)
+            prefill_fp8["peak_tflops"] = bf16
+            prefill_fp8["frac"] = prefill_fp8["tflops"] / bf16
+            prefill_fp8["peak_note"] = "F16 products: the F16 dense rate equals BF16's"
+        except Exception as e:  # report, do not hide
+            prefill_fp8 = {"error": str(e).splitlines()[0][:200]}
     prologue = None
     if not args.no_prefill:
         try:
@@ -736,6 +764,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "prefill_fp8_kv": prefill_fp8,
         "decode_configs": other,
         "prologue": prologue,
         "topk": topk,
