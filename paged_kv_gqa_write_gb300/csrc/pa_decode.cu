@@ -290,6 +290,11 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream (a KV write, say): everything above touches only this CTA's shared
+  // and tensor memory; every global access comes after that kernel has
+  // completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // a combine launched as a programmatic dependent may start its prologue now;
   // it reads partials only after this grid has completed
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1254,7 +1259,18 @@ cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CU
   if (e != cudaSuccess) return e;
   const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
   if (grid < 1) return cudaSuccess;
-  decode_kernel<NH, FP8, MULTI><<<grid, threads, smem, stream>>>(tm_k, tm_v, tm_q, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_kernel<NH, FP8, MULTI>, tm_k, tm_v, tm_q, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -42,6 +42,9 @@ __device__ __forceinline__ uint4 quantize16(uint4 a, uint4 b, float s) {
 
 template <bool FP8>
 __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
+  // an attention kernel launched next as a programmatic dependent may set up
+  // meanwhile; it reads nothing before this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ int32_t kvw_smem[];
   int32_t* off = kvw_smem;              // [B] when chunk_lens != null
   int32_t* scratch = kvw_smem + (p.chunk_lens ? p.B : 0);

@@ -463,6 +463,11 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
     }
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream (the chunk's KV write): the barrier set-up above touches only this
+  // CTA's shared memory; everything from here on comes after that kernel has
+  // completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == 0) {
     // the rings are idle until the first load: scratch for the schedule
     const int count = build_schedule(p, reinterpret_cast<int*>(smem + L::kSched),
@@ -1100,13 +1105,15 @@ cudaError_t launch_variant(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   const int grid_pairs = (int)(max_items < pairs ? max_items : pairs);
   if (grid_pairs < 1) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.blockDim = dim3(L::kThreads);
   cfg.dynamicSmemBytes = L::kSmem;
   cfg.stream = stream;

@@ -79,6 +79,9 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
 
 __global__ void __launch_bounds__(kThreads, 3)
     prologue_kernel(const __grid_constant__ PrologueParams p, int per_cta, int stages) {
+  // an attention kernel launched next as a programmatic dependent may set up
+  // meanwhile; it reads nothing before this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(16) uint8_t pro_smem[];
   const int heads = p.Hq + 2 * p.Hkv;
   const uint32_t row_bytes = (uint32_t)heads * (kHeadDim * 2);
