@@ -457,6 +457,39 @@ def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
         out[name] = {"tokens": case.T, "us": ms * 1e3, "spread": sp, "bytes": nbytes,
                      "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
                      "status": int(st.item())}
+        if not chunked:
+            # the decode step behind the prologue: pa_decode alone, and the
+            # prologue (128 tokens) then pa_decode, each timed the same way
+            dims = pa.make_dims(case.B, case.Hq, case.Hkv, case.num_pages, case.max_pages_per_seq)
+            wsp = torch.empty(max(1, pa.pa_decode_workspace_size(dims, 0)), dtype=torch.uint8,
+                              device="cuda")
+            dout = torch.empty(case.B, case.Hq, D, dtype=torch.bfloat16, device="cuda")
+
+            def dec():
+                pa.pa_decode(q_out, case.k_cache, case.v_cache, case.block_table,
+                             case.context_lens, 1.0, out=dout, workspace=wsp, num_splits=0,
+                             status=st)
+
+            def chain():
+                step()
+                dec()
+
+            res = {}
+            for leg, fn in (("pa_decode", dec), ("pa_qk_norm_rope_write + pa_decode", chain)):
+                for _ in range(warmup):
+                    fn()
+                torch.cuda.synchronize()
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(steps)]
+                for a, b in evs:
+                    flush()
+                    a.record()
+                    fn()
+                    b.record()
+                torch.cuda.synchronize()
+                res[leg] = spread([a.elapsed_time(b) for a, b in evs])["median_ms"] * 1e3
+            out[name]["decode_step_us"] = res
+            out[name]["prologue_cost_in_step_us"] = res["pa_qk_norm_rope_write + pa_decode"] - res["pa_decode"]
     out["step"] = "pa_qk_norm_rope_write"
     out["l2"] = "flushed between steps"
     return out
