@@ -663,6 +663,9 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(start.elapsed_time(end), ws)
     ms_per_step = elapsed_ms / args.steps
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    # a timed region of a few ms holds one or two samples at the sampler's
+    # 100 ms period: a second record spans every later leg (seconds of load)
+    clk_legs = ClockSampler(local).__enter__()
     # kv_write + decode, + a combine for the balanced schedule or fixed splits > 1
     launches_per_step = 2 + (1 if (balanced or splits > 1) else 0)
 
@@ -812,6 +815,9 @@ def run_ours(args):
                 other.append(r)
             except Exception as e:  # report, do not hide
                 other.append({"workload": name, "error": str(e).splitlines()[0][:200]})
+    clk_legs.__exit__(None, None, None)  # (the GPU idles during the CPU baseline)
+    clocks_legs = clk_legs.summary()
+    clocks_legs["span"] = "the e2e runs and every GPU leg after the headline's timed region"
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, nt, sample = cpu_oracle_rate(case, args.cpu_seconds)
@@ -848,6 +854,7 @@ def run_ours(args):
                                     "overlapping the previous and next steps' kernels"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "clocks_legs": clocks_legs,
         "prefill": prefill,
         "prefill_fp8_kv": prefill_fp8,
         "decode_configs": other,
