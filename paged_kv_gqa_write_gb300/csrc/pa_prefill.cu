@@ -852,8 +852,11 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
         // (both warps of a quarter hold the same rows, so they choose alike)
         const bool diag = __any_sync(0xffffffffu, nvis < 64);
         const float2 c2 = make_float2(c, c);
-        if (__any_sync(0xffffffffu, m == -INFINITY)) {
-          // the row's first key tile: the exact max of c * s over the visible keys
+        // BF16 P: the row's first key tile takes the exact max of c * s over the
+        // visible keys as the reference, so the largest weight is exactly 1 (with
+        // few keys per row its rounding error would dominate).  The FP8 cache's
+        // F16 P is 8x finer: its first tile runs against 0 (below).
+        if (!FP8 && __any_sync(0xffffffffu, m == -INFINITY)) {
           float mx = -INFINITY;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
@@ -909,22 +912,35 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
           return dmax;
         };
         const float m_use = m == -INFINITY ? 0.f : m;  // nothing visible yet: every p = 0
+        // FP8 cache, the row's first key tile (no reference yet): against 0, kept
+        // when the half's largest visible weight lies in [1, 2^8]; otherwise the
+        // row takes its exact max as the reference and redoes the tile
+        const bool first = FP8 && m == -INFINITY;  // the same for every row of the warp
         float dmax = diag ? pass(m_use, std::true_type{}) : pass(m_use, std::false_type{});
-        if (named_bar_red_or(dmax > kRescaleThreshold, xbar, 64)) {
+        const bool trig = dmax > kRescaleThreshold || (first && nvis > 0 && !(dmax >= 0.f));
+        if (named_bar_red_or(trig, xbar, 64)) {
           // rare: the row's reference moves up to the larger of the two halves'
           // maxima, and both halves redo the tile against it
           *x_mine = dmax;
           named_bar_sync(xbar, 64);
           dmax = fmaxf(dmax, *x_other);
-          const bool over = dmax > kRescaleThreshold;
-          const float m_new = over ? m_use + dmax : m_use;
-          if (over) {
-            alpha = fast_exp2(-dmax);
-            rescale = true;
+          float shift = dmax > kRescaleThreshold ? dmax : 0.f;
+          if (first) shift = dmax == -INFINITY ? 0.f : dmax;
+          const float m_new = m_use + shift;
+          if (shift != 0.f) {
+            if (!first) {
+              alpha = fast_exp2(-shift);
+              rescale = true;
+            }
             m = m_new;
           }
-          if (diag) pass(m_new, std::true_type{}); else pass(m_new, std::false_type{});
+          // warp-uniform: the pass holds .sync.aligned tensor-memory loads (a
+          // lane whose row keeps its reference recomputes the same weights)
+          if (__any_sync(0xffffffffu, shift != 0.f)) {
+            if (diag) pass(m_new, std::true_type{}); else pass(m_new, std::false_type{});
+          }
         }
+        if (m == -INFINITY) m = m_use;
         l = l * alpha + (sum2.x + sum2.y);
         // P over this half's scores (all of them read above)
         tmem_st32(s_cols, pw);
