@@ -279,6 +279,43 @@ def qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table,
     return q_out[:T], kc, vc, skipped
 
 
+def qk_norm_rope_write_fp8(qkv, q_norm_w, k_norm_w, k_cache, v_cache, k_scale, v_scale,
+                           block_table, context_lens, chunk_lens, num_q_heads, num_kv_heads,
+                           num_pages, max_pages_per_seq, eps=1e-6, rope_base=1e6,
+                           rope_scale=1.0, q_scale=1.0, page_size=128, head_dim=128):
+    """The prologue over an FP8 (e4m3) cache: the rows qk_norm_rope_write stores
+    (K normed, rotated and rounded to bf16; V as given), each quantized as
+    kv_write_fp8 quantizes a bf16 row -- element d of KV head h becomes the
+    e4m3 code of (float)x / scale[h], an FP32 quotient.  The "fp8_e4m3" KV
+    cache of the "Qwen4-Exp QSA" blog (DGX Spark note) written by the prologue
+    of "Qwen 3" (TensorSharp) section 3 / "Qwen3-14B" decode_fwd.  k_cache and
+    v_cache are uint8 [num_pages, page_size, Hkv, D]; returns (q_out float64,
+    k_cache', v_cache', skipped), the caches passed in unmodified.
+
+    A slot is written when the bf16 prologue, run on two scratch caches of
+    opposite fill (all-zero and all-ones bits), leaves the same row in both:
+    a stored row does not depend on what the slot held before."""
+    kc8 = _u8(k_cache).copy()
+    vc8 = _u8(v_cache).copy()
+    shape = kc8.shape
+    runs = []
+    for fill in (0x0000, 0xFFFF):
+        scratch = np.full(shape, fill, dtype=np.uint16)
+        runs.append(qk_norm_rope_write(
+            qkv, q_norm_w, k_norm_w, scratch, scratch, block_table, context_lens, chunk_lens,
+            num_q_heads, num_kv_heads, num_pages, max_pages_per_seq, eps=eps,
+            rope_base=rope_base, rope_scale=rope_scale, q_scale=q_scale, page_size=page_size,
+            head_dim=head_dim))
+    (q_out, k0, v0, skipped), (_, k1, v1, _) = runs
+    written = np.all(k0 == k1, axis=(-2, -1)) & np.all(v0 == v1, axis=(-2, -1))
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)[None, :, None]
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)[None, :, None]
+    for src, scl, dst in ((k0, ks, kc8), (v0, vs, vc8)):
+        rows = (src[written].astype(np.uint32) << 16).view(np.float32)  # exact bf16 values
+        dst[written] = e4m3_encode((rows / scl).astype(np.float32))
+    return q_out, kc8, vc8, skipped
+
+
 def topk(logits, k):
     """Exact top-k of each row of logits [rows, vocab] (float32): values and int32
     indices [rows, k], larger first, NaN above +inf, ties by smaller index."""

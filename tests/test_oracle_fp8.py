@@ -157,3 +157,62 @@ def test_attention_fp8_scale_identities():
         np.testing.assert_allclose(got[:, hs], float(vs[h]) * ref[:, hs], rtol=1e-12,
                                    atol=1e-14)
     assert not np.allclose(got, base)
+
+
+# ---- the prologue over an FP8 cache: the bf16 prologue's rows, quantized
+
+def _bits_f32(b):
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def _prologue_fp8_case(seed, ctx, chunk_lens=None, hq=8, hkv=2):
+    c = W.custom_case(seed, ctx, Hq=hq, Hkv=hkv, chunk_lens=chunk_lens)
+    qkv, wq, wk = W.prologue_inputs(c, seed)
+    g = np.random.default_rng(seed)
+    ks = (g.random(hkv) * 0.02 + 0.02).astype(np.float32)
+    vs = (g.random(hkv) * 0.02 + 0.02).astype(np.float32)
+    k8 = np.full(tuple(c.k_cache.shape), 0x5A, dtype=np.uint8)   # untouched-byte markers
+    v8 = np.full(tuple(c.v_cache.shape), 0xA5, dtype=np.uint8)
+    return c, qkv, wq.numpy(), wk.numpy(), ks, vs, k8, v8
+
+
+def _slots(c, chunk_lens, skip=()):
+    """(token index, page, offset) of the new tokens of valid sequences."""
+    out, tok = [], 0
+    for s in range(c.B):
+        n = 1 if chunk_lens is None else int(chunk_lens[s])
+        ctx = int(c.context_lens[s])
+        for j in range(n):
+            pos = ctx - n + j
+            if s not in skip:
+                out.append((tok, int(c.block_table[s, pos // 128]), pos % 128))
+            tok += 1
+    return out
+
+
+@pytest.mark.parametrize("ctx,chunk,bad", [([1, 200, 129], None, None),
+                                           ([300, 260, 5], [3, 130, 5], 1)])
+def test_prologue_fp8_quantizes_the_bf16_prologue_rows(ctx, chunk, bad):
+    c, qkv, wq, wk, ks, vs, k8, v8 = _prologue_fp8_case(611 + len(ctx), ctx, chunk)
+    if bad is not None:
+        c.block_table[bad, 1] = -1
+    cl = None if chunk is None else np.array(chunk, dtype=np.int32)
+    args = (c.block_table, c.context_lens, cl, c.Hq, c.Hkv, c.num_pages, c.max_pages_per_seq)
+    q8, kc8, vc8, sk8 = oracle.qk_norm_rope_write_fp8(qkv, wq, wk, k8, v8, ks, vs, *args)
+    q, kc, _, sk = oracle.qk_norm_rope_write(qkv, wq, wk, c.k_cache, c.v_cache, *args)
+    assert sk8 == sk == (0 if bad is None else 1)
+    assert np.array_equal(q8, q)
+    x = oracle._u16(qkv).reshape(c.T, c.Hq + 2 * c.Hkv, 128)
+    written = np.zeros(kc8.shape[:2], dtype=bool)
+    slots = _slots(c, chunk, skip=() if bad is None else (bad,))
+    assert slots
+    for tok, page, off in slots:
+        written[page, off] = True
+        # K: the bf16 prologue's row over k_scale (an FP32 quotient), then e4m3 by
+        # torch's float8_e4m3fn conversion
+        assert np.array_equal(kc8[page, off], _torch_encode(_bits_f32(kc[page, off]) / ks[:, None]))
+        # V: the input row over v_scale
+        v_in = _bits_f32(x[tok, c.Hq + c.Hkv:])
+        assert np.array_equal(vc8[page, off], _torch_encode(v_in / vs[:, None]))
+    # no other byte changes (an invalid sequence writes nothing)
+    assert np.all(kc8[~written] == 0x5A) and np.all(vc8[~written] == 0xA5)
