@@ -48,7 +48,8 @@ def parse_args():
                     help="decode batch (pool = 32 pages per sequence); smaller values are "
                          "for profiling captures, the benchmark workload is 128")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--profile-leg", choices=["prefill", "prefill-fp8", "fp8", "prologue", "topk", "multi"],
+    ap.add_argument("--profile-leg", choices=["prefill", "prefill-fp8", "fp8", "prologue", "topk", "multi",
+                                              "decode-b16", "decode-ragged"],
                     default=None,
                     help="run one benchmark leg's calls a few times (FP8 and multi-token legs at "
                          "--batch sequences) for an ncu capture, then exit; prints no bench line")
@@ -457,6 +458,35 @@ def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
         out[name] = {"tokens": case.T, "us": ms * 1e3, "spread": sp, "bytes": nbytes,
                      "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
                      "status": int(st.item())}
+        # the same prologue into an FP8 (e4m3) cache: K/V rows stored as codes
+        ks = torch.full((case.Hkv,), 0.03, dtype=torch.float32, device="cuda")
+        k8 = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device="cuda")
+        v8 = torch.zeros_like(k8)
+
+        def step8():
+            pa.pa_qk_norm_rope_write_fp8(qkv, wq, wk, k8, v8, ks, ks, case.block_table,
+                                         case.context_lens, case.chunk_lens if chunked else None,
+                                         q_scale=1.0 / math.sqrt(D), q_out=q_out, status=st)
+
+        for _ in range(warmup):
+            step8()
+        torch.cuda.synchronize()
+        ev8 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in ev8:
+            flush()
+            a.record()
+            step8()
+            b.record()
+        torch.cuda.synchronize()
+        sp8 = spread([a.elapsed_time(b) for a, b in ev8])
+        b8 = case.T * D * ((case.Hq + 2 * case.Hkv) * 2 + case.Hq * 2 + 2 * case.Hkv)
+        out[name]["fp8_cache"] = {"step": "pa_qk_norm_rope_write_fp8", "us": sp8["median_ms"] * 1e3,
+                                  "spread": sp8, "bytes": b8,
+                                  "gbs": b8 / (sp8["median_ms"] * 1e-3) / 1e9,
+                                  "frac": b8 / (sp8["median_ms"] * 1e-3) / 1e9 / hbm,
+                                  "status": int(st.item())}
+        del k8, v8
         if not chunked:
             # the decode step behind the prologue: pa_decode alone, and the
             # prologue (128 tokens) then pa_decode, each timed the same way
@@ -612,6 +642,10 @@ def run_ours(args):
             r = run_prologue(pa, W, torch, hbm_p, steps=2, warmup=1)
         elif args.profile_leg == "topk":
             r = run_topk(pa, torch, hbm_p, steps=2, warmup=1)
+        elif args.profile_leg == "decode-b16":
+            r = run_decode_config(pa, W, torch, "qwen3-14b-decode-b16", steps=2, warmup=1)
+        elif args.profile_leg == "decode-ragged":
+            r = run_decode_config(pa, W, torch, "qwen3-32b-ragged-b64", steps=2, warmup=1)
         else:
             r = run_multi_token(pa, W, torch, hbm_p, steps=2, warmup=1, batch=args.batch)
         print(json.dumps({"profile_leg": args.profile_leg, "batch": args.batch,

@@ -14,8 +14,9 @@
  *    KV ranges (flash-decoding) and merged by pa_combine.
  *  - pa_decode_multi: the same causal attention for q_len new tokens per
  *    sequence (every chunk q_len long), run as B * q_len decode queries.
- *  - pa_kv_write_fp8 / pa_decode_fp8: the same write and decode over an FP8
- *    (e4m3) cache with per-KV-head scales.
+ *  - pa_kv_write_fp8 / pa_qk_norm_rope_write_fp8 / pa_decode_fp8 /
+ *    pa_prefill_chunk_fp8: the same write, prologue, decode and prefill over
+ *    an FP8 (e4m3) cache with per-KV-head scales.
  *  - pa_prefill_chunk: "KV cache update -> causal attention" of prefill_fwd
  *    ("Qwen3-14B", "prefill_fwd"), inputs packed token-major with
  *    T = sum(chunk_lens); full causal attention without window or sinks
@@ -268,6 +269,29 @@ int pa_kv_write_fp8(const void* k_new, const void* v_new, void* k_cache, void* v
                     const float* k_scale, const float* v_scale, const int32_t* block_table,
                     const int32_t* context_lens, const int32_t* chunk_lens,
                     int32_t num_tokens, pa_dims dims, int32_t* status, pa_stream_t stream);
+
+/*
+ * pa_qk_norm_rope_write_fp8 -- pa_qk_norm_rope_write into an FP8 cache: the
+ * decode / prefill prologue ("Qwen 3" TensorSharp doc, section 3; "Qwen3-14B"
+ * pypto-lib doc, decode_fwd) writing an "fp8_e4m3" KV cache ("Qwen4-Exp QSA"
+ * blog, DGX Spark note; "Qwen 3" section 11, --kv-cache-dtype).  Each stored
+ * row is quantized as pa_kv_write_fp8 quantizes a bf16 row: K normed, rotated
+ * and rounded to bf16 as pa_qk_norm_rope_write stores it, V as given, element
+ * d of KV head h divided by k_scale[h] / v_scale[h] (FP32 quotient) and
+ * rounded to the nearest e4m3 code (ties to even, saturating at +-448).  The
+ * cache bytes equal those of pa_qk_norm_rope_write into a bf16 cache followed
+ * by pa_kv_write_fp8 of the rows it wrote; q_out, validity rules, status bits
+ * and the other arguments are those of pa_qk_norm_rope_write.
+ *   k_cache, v_cache  uint8 e4m3 codes [num_pages, P, Hkv, D], written in place
+ *   k_scale, v_scale  float32 [Hkv] device arrays, non-null and 4-byte aligned
+ */
+int pa_qk_norm_rope_write_fp8(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                              float eps, float rope_base, float rope_scale, float q_scale,
+                              void* q_out, void* k_cache, void* v_cache, const float* k_scale,
+                              const float* v_scale, const int32_t* block_table,
+                              const int32_t* context_lens, const int32_t* chunk_lens,
+                              int32_t num_tokens, pa_dims dims, int32_t* status,
+                              pa_stream_t stream);
 
 /*
  * pa_decode_fp8 -- pa_decode_multi over an FP8 cache (q_len = 1: single-token

@@ -36,7 +36,8 @@ EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_a
             "pa_prefill_chunk", "pa_combine", "pa_status_string", "pa_abi_version",
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
             "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
-            "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs", "pa_prefill_chunk_fp8")
+            "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs", "pa_prefill_chunk_fp8",
+            "pa_qk_norm_rope_write_fp8")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -71,6 +72,9 @@ def load(path: str = LIB_PATH):
     lib.pa_qk_norm_rope_write.restype = ctypes.c_int
     lib.pa_qk_norm_rope_write.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, vp,
                                           vp, i32, pa_dims, vp, vp]
+    lib.pa_qk_norm_rope_write_fp8.restype = ctypes.c_int
+    lib.pa_qk_norm_rope_write_fp8.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, i32, pa_dims, vp, vp]
     lib.pa_topk.restype = ctypes.c_int
     lib.pa_topk.argtypes = [vp, ctypes.c_int64, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.pa_topk_workspace_size.restype = sz
@@ -209,6 +213,42 @@ def pa_qk_norm_rope_write(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table
         _ptr(block_table), _ptr(context_lens), _ptr(chunk_lens), int(T), d, _ptr(status),
         _stream(stream))
     _check("pa_qk_norm_rope_write", rc)
+    return q_out
+
+
+def pa_qk_norm_rope_write_fp8(qkv, q_norm_w, k_norm_w, k_cache, v_cache, k_scale, v_scale,
+                              block_table, context_lens, chunk_lens=None, eps=1e-6,
+                              rope_base=1e6, rope_scale=1.0, q_scale=1.0, q_out=None,
+                              status=None, stream=None):
+    """The prologue into an FP8 (e4m3) cache [num_pages, 128, Hkv, 128] with
+    per-KV-head float32 scales; returns q_out [T, Hq, 128] bf16."""
+    dev = k_cache.device
+    _need(qkv, "qkv", torch.bfloat16, dev)
+    _need_fp8_cache(k_cache, "k_cache", dev)
+    _need_fp8_cache(v_cache, "v_cache", dev)
+    _need(k_scale, "k_scale", torch.float32, dev)
+    _need(v_scale, "v_scale", torch.float32, dev)
+    _need(q_norm_w, "q_norm_w", torch.float32, dev)
+    _need(k_norm_w, "k_norm_w", torch.float32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if chunk_lens is not None:
+        _need(chunk_lens, "chunk_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    Hkv = k_cache.shape[2]
+    T = qkv.shape[0]
+    Hq = qkv.reshape(T, -1).shape[1] // HEAD_DIM - 2 * Hkv
+    d = _cache_dims(Hq, k_cache, block_table)
+    if q_out is None:
+        q_out = torch.empty(T, Hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", torch.bfloat16, dev)
+    rc = load().pa_qk_norm_rope_write_fp8(
+        _ptr(qkv), _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base),
+        float(rope_scale), float(q_scale), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(context_lens), _ptr(chunk_lens),
+        int(T), d, _ptr(status), _stream(stream))
+    _check("pa_qk_norm_rope_write_fp8", rc)
     return q_out
 
 

@@ -493,12 +493,15 @@ int pa_kv_write_fp8(const void* k_new, const void* v_new, void* k_cache, void* v
                        context_lens, chunk_lens, num_tokens, d, status, stream);
 }
 
-int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
-                          float eps, float rope_base, float rope_scale, float q_scale,
-                          void* q_out, void* k_cache, void* v_cache,
-                          const int32_t* block_table, const int32_t* context_lens,
-                          const int32_t* chunk_lens, int32_t num_tokens, pa_dims d,
-                          int32_t* status, pa_stream_t stream) {
+namespace {
+
+// The prologue into a bf16 cache (k_scale == v_scale == null) or an FP8 one.
+int prologue_impl(const void* qkv, const float* q_norm_w, const float* k_norm_w, float eps,
+                  float rope_base, float rope_scale, float q_scale, void* q_out, void* k_cache,
+                  void* v_cache, const float* k_scale, const float* v_scale,
+                  const int32_t* block_table, const int32_t* context_lens,
+                  const int32_t* chunk_lens, int32_t num_tokens, pa_dims d, int32_t* status,
+                  pa_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_tokens < 0) return PA_ERR_DIMS;
@@ -524,6 +527,8 @@ int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k
   p.q_out = static_cast<uint2*>(q_out);
   p.k_cache = static_cast<uint2*>(k_cache);
   p.v_cache = static_cast<uint2*>(v_cache);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_table = block_table;
   p.context_lens = context_lens;
   p.chunk_lens = chunk_lens;
@@ -548,6 +553,34 @@ int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k
   p.num_pages = d.num_pages;
   p.max_pages = d.max_pages_per_seq;
   return launch_result(pa::launch_prologue(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int pa_qk_norm_rope_write(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                          float eps, float rope_base, float rope_scale, float q_scale,
+                          void* q_out, void* k_cache, void* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          const int32_t* chunk_lens, int32_t num_tokens, pa_dims d,
+                          int32_t* status, pa_stream_t stream) {
+  return prologue_impl(qkv, q_norm_w, k_norm_w, eps, rope_base, rope_scale, q_scale, q_out,
+                       k_cache, v_cache, nullptr, nullptr, block_table, context_lens,
+                       chunk_lens, num_tokens, d, status, stream);
+}
+
+int pa_qk_norm_rope_write_fp8(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                              float eps, float rope_base, float rope_scale, float q_scale,
+                              void* q_out, void* k_cache, void* v_cache, const float* k_scale,
+                              const float* v_scale, const int32_t* block_table,
+                              const int32_t* context_lens, const int32_t* chunk_lens,
+                              int32_t num_tokens, pa_dims d, int32_t* status,
+                              pa_stream_t stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL_POINTER;
+  if (((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
+    return PA_ERR_ALIGNMENT;
+  return prologue_impl(qkv, q_norm_w, k_norm_w, eps, rope_base, rope_scale, q_scale, q_out,
+                       k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                       chunk_lens, num_tokens, d, status, stream);
 }
 
 size_t pa_topk_workspace_size(int32_t rows, int32_t vocab, int32_t k) {

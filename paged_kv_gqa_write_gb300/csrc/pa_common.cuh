@@ -679,8 +679,10 @@ struct PrologueParams {
   const float* wq;              // [D] Q norm weight
   const float* wk;              // [D] K norm weight
   uint2* q_out;                 // [T, Hq, D] bf16
-  uint2* k_cache;               // [num_pages, 128, Hkv, D] bf16
+  uint2* k_cache;               // [num_pages, 128, Hkv, D] bf16, or e4m3 codes
   uint2* v_cache;
+  const float* k_scale;         // [Hkv] FP8 cache scales; null: bf16 cache
+  const float* v_scale;
   const int32_t* block_table;
   const int32_t* context_lens;
   const int32_t* chunk_lens;    // may be null (one token per sequence)

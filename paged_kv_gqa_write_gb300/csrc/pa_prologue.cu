@@ -33,6 +33,15 @@
 // A compute lane holds 8 of a head's 128 values, both members of four NeoX
 // pairs (i, i+64): the RMS is a 16-lane reduction and the rotation needs no
 // data from other lanes.
+//
+// Over an FP8 (e4m3) cache the same kernel quantizes what it stores: each K
+// value as the BF16 cache would hold it (rounded to bf16), and each V value
+// as given, divided by its KV head's scale (an FP32 quotient) and rounded to
+// the nearest e4m3 code, saturating -- the bytes pa_kv_write_fp8 would write
+// from those rows (an "fp8_e4m3" KV cache, "Qwen4-Exp QSA" blog, DGX Spark
+// note).  V then leaves through the compute warps instead of a bulk store.
+#include <cuda_fp8.h>
+
 #include "pa_launch.cuh"
 
 namespace pa {
@@ -61,6 +70,17 @@ __device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
   return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
+// 4 bf16 values over s -> 4 e4m3 codes (round to nearest even, saturating),
+// value i in byte i.
+__device__ __forceinline__ uint32_t quant4_e4m3(uint2 w, float s) {
+  const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)),
+                                               __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)),
+                                               __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
@@ -77,6 +97,7 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 3)
     prologue_kernel(const __grid_constant__ PrologueParams p, int per_cta, int stages) {
   // an attention kernel launched next as a programmatic dependent may set up
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       const uint8_t* row = rows + st * row_bytes;
       // V is copied bit for bit: one bulk store of the token's Hkv V rows,
       // which are contiguous in the staged row and in the cache slot
-      const bool v_store = cw == 0 && lane == 0 && valid;
+      const bool v_store = !FP8 && cw == 0 && lane == 0 && valid;
       if (v_store) {
         asm volatile(
             "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
@@ -256,11 +277,35 @@ __global__ void __launch_bounds__(kThreads, 3)
           dst = p.q_out + ((int64_t)token * p.Hq + hh) * (kHeadDim / 4);
         } else {
           if (!valid) continue;
+          if constexpr (FP8) {
+            // K as the bf16 cache would hold it, over the head's scale
+            const int h = hh - p.Hq;
+            const float ks = __ldg(p.k_scale + h);
+            uint32_t* kd = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_cache) +
+                                                       (slot * p.Hkv + h) * kHeadDim);
+            kd[li] = quant4_e4m3(float4_to_bf16x4(oa), ks);
+            kd[16 + li] = quant4_e4m3(float4_to_bf16x4(ob), ks);
+            continue;
+          }
           dst = p.k_cache + (slot * p.Hkv + (hh - p.Hq)) * (kHeadDim / 4);
         }
         // (an invalid sequence's Q rows are zero, like its attention output)
         dst[li] = valid ? float4_to_bf16x4(oa) : make_uint2(0u, 0u);
         dst[16 + li] = valid ? float4_to_bf16x4(ob) : make_uint2(0u, 0u);
+      }
+      if constexpr (FP8) {
+        // V heads over their scales: half-warp per head, lane li values 8 li .. 8 li + 7
+        if (valid) {
+          for (int m = cw; 2 * m < p.Hkv; m += kComputeWarps) {
+            const int h = 2 * m + hl;
+            if (h >= p.Hkv) continue;
+            const uint4 r = *reinterpret_cast<const uint4*>(row + (nqk + h) * (kHeadDim * 2) + 16 * li);
+            const float vs = __ldg(p.v_scale + h);
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.v_cache) +
+                                      (slot * p.Hkv + h) * kHeadDim + 8 * li) =
+                make_uint2(quant4_e4m3(make_uint2(r.x, r.y), vs), quant4_e4m3(make_uint2(r.z, r.w), vs));
+          }
+        }
       }
       // the V store must have read the stage before it is refilled
       if (v_store) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -288,8 +333,11 @@ cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t s
     e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem + 2048 > (size_t)max_smem) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  const bool fp8 = p.k_scale != nullptr;
+  e = fp8 ? cudaFuncSetAttribute(prologue_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem)
+          : cudaFuncSetAttribute(prologue_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
   if (e != cudaSuccess) return e;
   // resident CTAs per SM by shared memory (at most the 3 the registers allow)
   int per_sm = (int)((228 * 1024) / (smem + 2048));
@@ -298,7 +346,10 @@ cudaError_t launch_prologue(const PrologueParams& p, int num_sms, cudaStream_t s
   const int64_t slots = (int64_t)num_sms * per_sm;
   const int per_cta = (int)((p.T + slots - 1) / slots);
   const int blocks = (p.T + per_cta - 1) / per_cta;
-  prologue_kernel<<<blocks, kThreads, smem, stream>>>(p, per_cta, stages);
+  if (fp8)
+    prologue_kernel<true><<<blocks, kThreads, smem, stream>>>(p, per_cta, stages);
+  else
+    prologue_kernel<false><<<blocks, kThreads, smem, stream>>>(p, per_cta, stages);
   return cudaGetLastError();
 }
 

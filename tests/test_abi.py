@@ -131,6 +131,12 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert pro(qkv=None) == h["PA_ERR_NULL_POINTER"]
     assert pro(qkv=MIS) == h["PA_ERR_ALIGNMENT"]
     assert pro(n=0, cl=FAKE) == 0
+    pro8 = lambda ks=FAKE, vs=FAKE, n=2, eps=1e-6: lib.pa_qk_norm_rope_write_fp8(
+        FAKE, FAKE, FAKE, eps, 1e6, 1.0, 1.0, FAKE, FAKE, FAKE, ks, vs, FAKE, FAKE, None, n, d,
+        None, None)
+    assert pro8(ks=None) == h["PA_ERR_NULL_POINTER"] and pro8(vs=None) == h["PA_ERR_NULL_POINTER"]
+    assert pro8(vs=ctypes.c_void_p(0x10002)) == h["PA_ERR_ALIGNMENT"]
+    assert pro8(eps=-1.0) == h["PA_ERR_DIMS"] and pro8(n=3) == h["PA_ERR_DIMS"]
     wide = _dims(pa, num_q_heads=352, num_kv_heads=32)  # G = 11, 416 heads in a row
     assert lib.pa_qk_norm_rope_write(FAKE, FAKE, FAKE, 1e-6, 1e6, 1.0, 1.0, FAKE, FAKE, FAKE, FAKE,
                                      FAKE, None, 2, wide, None, None) == h["PA_ERR_HEADS"]
