@@ -424,13 +424,16 @@ def run_fp8(pa, W, torch, hbm, steps=50, warmup=10, batch=128):
 
 def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
     """pa_qk_norm_rope_write (Q/K RMSNorm -> NeoX RoPE -> KV write) on the decode
-    batch (128 tokens) and on the 8 x 512 prefill chunk, with a clean L2 flush
-    between steps.  Bytes: the fused QKV rows read, Q and the K/V rows written."""
+    batch (128 tokens), on the 8 x 512 prefill chunk and on the batch-16 decode,
+    with a clean L2 flush between steps.  Bytes: the fused QKV rows read, Q and
+    the K/V rows written.  For the decode batches also the decode step behind
+    it: pa_decode alone, the prologue then pa_decode, and pa_decode_prologue."""
     out = {}
     flush = L2Flush(torch)
     for name, case in (("decode-b128", W.qwen3_14b_decode_b128(device="cuda", pool_device="cuda",
                                                                 with_new=False)),
-                       ("prefill-b8-c512", W.chunked_prefill(device="cuda", pool_device="cuda"))):
+                       ("prefill-b8-c512", W.chunked_prefill(device="cuda", pool_device="cuda")),
+                       ("decode-b16", W.qwen3_14b_decode_b16(device="cuda", pool_device="cuda"))):
         qkv, wq, wk = W.prologue_inputs(case, 600, device="cuda")
         chunked = case.chunk_lens is not None
         q_out = torch.empty(case.T, case.Hq, D, dtype=torch.bfloat16, device="cuda")
@@ -504,8 +507,14 @@ def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
                 step()
                 dec()
 
+            def fused():
+                pa.pa_decode_prologue(qkv, wq, wk, case.k_cache, case.v_cache, case.block_table,
+                                      case.context_lens, q_scale=1.0 / math.sqrt(D), scale=1.0,
+                                      out=dout, workspace=wsp, num_splits=0, status=st)
+
             res = {}
-            for leg, fn in (("pa_decode", dec), ("pa_qk_norm_rope_write + pa_decode", chain)):
+            for leg, fn in (("pa_decode", dec), ("pa_qk_norm_rope_write + pa_decode", chain),
+                            ("pa_decode_prologue", fused)):
                 for _ in range(warmup):
                     fn()
                 torch.cuda.synchronize()
@@ -520,6 +529,7 @@ def run_prologue(pa, W, torch, hbm, steps=50, warmup=10):
                 res[leg] = spread([a.elapsed_time(b) for a, b in evs])["median_ms"] * 1e3
             out[name]["decode_step_us"] = res
             out[name]["prologue_cost_in_step_us"] = res["pa_qk_norm_rope_write + pa_decode"] - res["pa_decode"]
+            out[name]["fused_prologue_cost_in_step_us"] = res["pa_decode_prologue"] - res["pa_decode"]
     out["step"] = "pa_qk_norm_rope_write"
     out["l2"] = "flushed between steps"
     return out

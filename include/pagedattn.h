@@ -12,6 +12,8 @@
  *    [page, token, kv_head, dim]; K/V gathered per sequence from the block
  *    table and the sequence lengths ("Qwen 3", section 11).  Split across
  *    KV ranges (flash-decoding) and merged by pa_combine.
+ *  - pa_decode_prologue: pa_qk_norm_rope_write and pa_decode as one kernel
+ *    (decode_fwd's attention kernel with its in-kernel RoPE/QKV phase).
  *  - pa_decode_multi: the same causal attention for q_len new tokens per
  *    sequence (every chunk q_len long), run as B * q_len decode queries.
  *  - pa_kv_write_fp8 / pa_qk_norm_rope_write_fp8 / pa_decode_fp8 /
@@ -292,6 +294,33 @@ int pa_qk_norm_rope_write_fp8(const void* qkv, const float* q_norm_w, const floa
                               const int32_t* context_lens, const int32_t* chunk_lens,
                               int32_t num_tokens, pa_dims dims, int32_t* status,
                               pa_stream_t stream);
+
+/*
+ * pa_decode_prologue -- the decode step with its prologue in the attention
+ * kernel: "Qwen3-14B" (pypto-lib), "Model structure, top down" (decode_fwd:
+ * Q/K norm -> RoPE -> KV cache write -> paged attention; the CCE attention
+ * kernel there runs the RoPE/QKV step as its in-kernel phase 0).  For one
+ * new token per sequence: the query heads are normed, rotated and scaled from
+ * the fused projection row inside the kernel (never written out), the new
+ * token's K row (normed, rotated) and V row are written to its cache slot,
+ * and the token attends to its whole context, new token included.  The cache
+ * bytes and `out` equal those of pa_qk_norm_rope_write (chunk_lens NULL)
+ * followed by pa_decode with the same arguments, bit for bit, and so do the
+ * status bits (context_lens[s] == 0 flags PA_STATUS_BAD_LENGTH, as the
+ * prologue flags a token without a position, and gives a zero row).
+ *   qkv, q_norm_w, k_norm_w, eps, rope_base, rope_scale, q_scale: as
+ *                  pa_qk_norm_rope_write, num_tokens = num_seqs
+ *   k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
+ *   workspace, num_splits, status: as pa_decode (the same workspace size)
+ * Returns PA_ERR_HEADS when Hq / Hkv > 16; otherwise the checks of
+ * pa_qk_norm_rope_write and pa_decode.
+ */
+int pa_decode_prologue(const void* qkv, const float* q_norm_w, const float* k_norm_w, float eps,
+                       float rope_base, float rope_scale, float q_scale, void* k_cache,
+                       void* v_cache, const int32_t* block_table, const int32_t* context_lens,
+                       float scale, void* out, int32_t out_dtype, void* workspace,
+                       size_t workspace_bytes, int32_t num_splits, pa_dims dims,
+                       int32_t* status, pa_stream_t stream);
 
 /*
  * pa_decode_fp8 -- pa_decode_multi over an FP8 cache (q_len = 1: single-token

@@ -37,7 +37,7 @@ EXPORTED = ("pa_kv_write", "pa_decode", "pa_decode_workspace_size", "pa_decode_a
             "pa_decode_noalloc", "pa_qk_norm_rope_write", "pa_topk", "pa_topk_workspace_size",
             "pa_decode_multi", "pa_decode_multi_workspace_size", "pa_kv_write_fp8",
             "pa_decode_fp8", "pa_wait_selftest", "pa_prefill_pairs", "pa_prefill_chunk_fp8",
-            "pa_qk_norm_rope_write_fp8")
+            "pa_qk_norm_rope_write_fp8", "pa_decode_prologue")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -75,6 +75,9 @@ def load(path: str = LIB_PATH):
     lib.pa_qk_norm_rope_write_fp8.restype = ctypes.c_int
     lib.pa_qk_norm_rope_write_fp8.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, vp,
                                               vp, vp, vp, i32, pa_dims, vp, vp]
+    lib.pa_decode_prologue.restype = ctypes.c_int
+    lib.pa_decode_prologue.argtypes = [vp, vp, vp, f32, f32, f32, f32, vp, vp, vp, vp, f32, vp,
+                                       i32, vp, sz, i32, pa_dims, vp, vp]
     lib.pa_topk.restype = ctypes.c_int
     lib.pa_topk.argtypes = [vp, ctypes.c_int64, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.pa_topk_workspace_size.restype = sz
@@ -317,6 +320,50 @@ def pa_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, out=No
                           0 if workspace is None else workspace.numel() * workspace.element_size(),
                           int(num_splits), d, _ptr(status), _stream(stream))
     _check("pa_decode", rc)
+    return out
+
+
+def pa_decode_prologue(qkv, q_norm_w, k_norm_w, k_cache, v_cache, block_table, context_lens,
+                       eps=1e-6, rope_base=1e6, rope_scale=1.0, q_scale=1.0, scale=None,
+                       out=None, out_dtype=torch.bfloat16, workspace=None, num_splits=0,
+                       status=None, stream=None):
+    """The decode step with its prologue in the attention kernel: qkv is the fused
+    projection output [B, (Hq + 2 Hkv) * 128] bf16 (one new token per sequence);
+    writes the new tokens' K/V rows into the caches and returns out [B, Hq, 128].
+    Equal to pa_qk_norm_rope_write followed by pa_decode."""
+    dev = k_cache.device
+    _need(qkv, "qkv", torch.bfloat16, dev)
+    _need(q_norm_w, "q_norm_w", torch.float32, dev)
+    _need(k_norm_w, "k_norm_w", torch.float32, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    B = qkv.shape[0]
+    Hkv = k_cache.shape[2]
+    Hq = qkv.reshape(B, -1).shape[1] // HEAD_DIM - 2 * Hkv
+    d = _cache_dims(Hq, k_cache, block_table)
+    if B != d.num_seqs:
+        raise ValueError(f"qkv has {B} rows; expected one per sequence ({d.num_seqs})")
+    if out is None:
+        out = torch.empty(B, Hq, HEAD_DIM, dtype=out_dtype, device=dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or f32")
+    _need(out, "out", out.dtype, dev)
+    code = PA_F32 if out.dtype == torch.float32 else PA_BF16
+    need = pa_decode_workspace_size(d, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else float(scale)
+    rc = load().pa_decode_prologue(
+        _ptr(qkv), _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base),
+        float(rope_scale), float(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(context_lens), scale, _ptr(out), code, _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        int(num_splits), d, _ptr(status), _stream(stream))
+    _check("pa_decode_prologue", rc)
     return out
 
 

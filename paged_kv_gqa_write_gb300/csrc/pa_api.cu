@@ -313,11 +313,13 @@ size_t topk_ws_bytes(int rows, int vocab, int k, int num_sms) {
 // Shared tail of pa_decode, pa_decode_multi and pa_decode_noalloc: arguments
 // are checked and `ws` holds at least pl.ws_bytes (or is unused when that is
 // 0); q_len new tokens per sequence.
+// pro: the step's prologue runs in the decode kernel (q unused).
 int run_decode(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_table, const int32_t* context_lens, float scale, void* out,
                int32_t out_dtype, uint8_t* ws, const DecodePlan& pl, const pa_dims& d,
                int32_t q_len, int32_t* status, int sms, cudaStream_t st,
-               const float* k_scale = nullptr, const float* v_scale = nullptr) {
+               const float* k_scale = nullptr, const float* v_scale = nullptr,
+               const pa::DecodePrologue* pro = nullptr) {
   const bool fp8 = k_scale != nullptr;
   const int G = d.num_q_heads / d.num_kv_heads;
   int NT, Lg;
@@ -331,9 +333,10 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
                                  encode_cache_map(&tm_v, v_cache, d);
   // one token per sequence: q as [B * Hq rows, 128] with G-row boxes; more: a
   // 3-D map over [tokens][Hq][128] with (G heads x Lg tokens) boxes
-  const bool q_ok = q_len == 1 ? encode_2d(&tm_q, q, kHeadDim, (uint64_t)d.num_seqs * d.num_q_heads,
-                                           kHeadDim * 2, 64, (uint32_t)G, CU_TENSOR_MAP_SWIZZLE_128B)
-                               : encode_q_decode_map(&tm_q, q, d, q_len, G, Lg);
+  const bool q_ok = pro ? true
+                 : q_len == 1 ? encode_2d(&tm_q, q, kHeadDim, (uint64_t)d.num_seqs * d.num_q_heads,
+                                          kHeadDim * 2, 64, (uint32_t)G, CU_TENSOR_MAP_SWIZZLE_128B)
+                              : encode_q_decode_map(&tm_q, q, d, q_len, G, Lg);
   if (!maps_ok || !q_ok) return PA_ERR_TENSOR_MAP;
 
   pa::DecodeParams p = {};
@@ -370,7 +373,8 @@ int run_decode(const void* q, const void* k_cache, const void* v_cache,
                                 ws + align256((size_t)2 * pl.grid * kMaxColumns * kHeadDim *
                                               sizeof(float)))
                           : nullptr;
-  cudaError_t e = pa::launch_decode(tm_k, tm_v, tm_q, p, G * Lg, sms, st);
+  cudaError_t e = pro ? pa::launch_decode_prologue(tm_k, tm_v, p, *pro, G, sms, st)
+                      : pa::launch_decode(tm_k, tm_v, tm_q, p, G * Lg, sms, st);
   if (e != cudaSuccess) return launch_result(e);
   if (pl.balanced) {
     pa::BalCombineParams c;
@@ -495,6 +499,26 @@ int pa_kv_write_fp8(const void* k_new, const void* v_new, void* k_cache, void* v
 
 namespace {
 
+// The 64 NeoX pairs' frequencies base^(-2i/D) / scale in radians per position
+// (double) and in turns per position as an unevaluated float pair hi + lo.
+void rope_tables(float rope_base, float rope_scale, double* freq, float* turn_hi,
+                 float* turn_lo) {
+  const double log2_base = std::log2((double)rope_base);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < 64; ++i) {
+    const double f = std::exp2(-2.0 * i / kHeadDim * log2_base) / (double)rope_scale;
+    const double g = f / two_pi;
+    freq[i] = f;
+    turn_hi[i] = (float)g;
+    turn_lo[i] = (float)(g - (double)turn_hi[i]);
+  }
+}
+
+bool prologue_scalars_ok(float eps, float rope_base, float rope_scale, float q_scale) {
+  return eps >= 0.f && rope_base > 0.f && rope_scale > 0.f && std::isfinite(eps) &&
+         std::isfinite(rope_base) && std::isfinite(rope_scale) && std::isfinite(q_scale);
+}
+
 // The prologue into a bf16 cache (k_scale == v_scale == null) or an FP8 one.
 int prologue_impl(const void* qkv, const float* q_norm_w, const float* k_norm_w, float eps,
                   float rope_base, float rope_scale, float q_scale, void* q_out, void* k_cache,
@@ -508,9 +532,7 @@ int prologue_impl(const void* qkv, const float* q_norm_w, const float* k_norm_w,
   if (!chunk_lens && num_tokens != d.num_seqs) return PA_ERR_DIMS;
   if (chunk_lens && d.num_seqs > PA_MAX_CHUNKED_SEQS) return PA_ERR_TOO_MANY_SEQS;
   if (d.num_q_heads + 2 * d.num_kv_heads > PA_MAX_PROLOGUE_HEADS) return PA_ERR_HEADS;
-  if (!(eps >= 0.f) || !(rope_base > 0.f) || !(rope_scale > 0.f) || !std::isfinite(eps) ||
-      !std::isfinite(rope_base) || !std::isfinite(rope_scale) || !std::isfinite(q_scale))
-    return PA_ERR_DIMS;
+  if (!prologue_scalars_ok(eps, rope_base, rope_scale, q_scale)) return PA_ERR_DIMS;
   if (num_tokens == 0 || d.num_seqs == 0) return PA_OK;
   if (!qkv || !q_norm_w || !k_norm_w || !q_out || !k_cache || !v_cache || !block_table ||
       !context_lens)
@@ -535,17 +557,7 @@ int prologue_impl(const void* qkv, const float* q_norm_w, const float* k_norm_w,
   p.status = status;
   p.eps = eps;
   p.q_scale = q_scale;
-  {
-    const double log2_base = std::log2((double)rope_base);
-    const double two_pi = 6.283185307179586476925286766559;
-    for (int i = 0; i < 64; ++i) {
-      const double f = std::exp2(-2.0 * i / kHeadDim * log2_base) / (double)rope_scale;
-      const double g = f / two_pi;
-      p.freq[i] = f;
-      p.turn_hi[i] = (float)g;
-      p.turn_lo[i] = (float)(g - (double)p.turn_hi[i]);
-    }
-  }
+  rope_tables(rope_base, rope_scale, p.freq, p.turn_hi, p.turn_lo);
   p.B = d.num_seqs;
   p.T = num_tokens;
   p.Hq = d.num_q_heads;
@@ -667,6 +679,43 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               pa_dims d, int32_t* status, pa_stream_t stream) {
   return pa_decode_multi(q, k_cache, v_cache, block_table, context_lens, 1, scale, out,
                          out_dtype, workspace, ws_bytes, num_splits, d, status, stream);
+}
+
+int pa_decode_prologue(const void* qkv, const float* q_norm_w, const float* k_norm_w, float eps,
+                       float rope_base, float rope_scale, float q_scale, void* k_cache,
+                       void* v_cache, const int32_t* block_table, const int32_t* context_lens,
+                       float scale, void* out, int32_t out_dtype, void* workspace,
+                       size_t ws_bytes, int32_t num_splits, pa_dims d, int32_t* status,
+                       pa_stream_t stream) {
+  bool empty = false;
+  int rc = check_decode_args(d, 1, out_dtype, num_splits, qkv, k_cache, v_cache, block_table,
+                             context_lens, out, &empty);
+  if (rc) return rc;
+  if (d.num_q_heads / d.num_kv_heads > 16) return PA_ERR_HEADS;
+  if (!prologue_scalars_ok(eps, rope_base, rope_scale, q_scale)) return PA_ERR_DIMS;
+  if (empty) return PA_OK;
+  if (!q_norm_w || !k_norm_w) return PA_ERR_NULL_POINTER;
+  if (!aligned16(q_norm_w) || !aligned16(k_norm_w)) return PA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms <= 0) return PA_ERR_NO_DEVICE;
+  DecodePlan pl;
+  if (!make_plan(d, 1, num_splits, sms, &pl)) return PA_ERR_SPLITS;
+  if (pl.ws_bytes > 0) {
+    if (!workspace || ws_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+  }
+  pa::DecodePrologue pro = {};
+  pro.qkv = static_cast<const __nv_bfloat16*>(qkv);
+  pro.wq = q_norm_w;
+  pro.wk = k_norm_w;
+  pro.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  pro.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  pro.eps = eps;
+  pro.q_scale = q_scale;
+  rope_tables(rope_base, rope_scale, pro.freq, pro.turn_hi, pro.turn_lo);
+  return run_decode(nullptr, k_cache, v_cache, block_table, context_lens, scale, out, out_dtype,
+                    static_cast<uint8_t*>(workspace), pl, d, 1, status, sms,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, &pro);
 }
 
 int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,

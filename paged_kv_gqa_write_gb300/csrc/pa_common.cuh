@@ -35,6 +35,12 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// This thread's generic-proxy global writes, ordered before later async-proxy
+// (TMA) accesses that a barrier orders after them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -499,6 +505,10 @@ __device__ __forceinline__ bool named_bar_red_or(bool v, int id, int nthreads) {
   return r != 0;
 }
 
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
@@ -672,6 +682,80 @@ __device__ __forceinline__ int seq_ctx(const int32_t* context_lens, int s, int L
   const int c = __ldg(context_lens + s);
   return (L > 1 && c > 0 && c < L) ? -1 : c;
 }
+
+// ---------------------------------------------------------------- prologue arithmetic
+// Shared by the prologue kernel and the decode kernel's in-kernel prologue, so
+// that both produce the same bits.
+
+// cos and sin of a NeoX pair's angle at position pos: frequency f radians per
+// position, or (th + tl) turns per position as an unevaluated float pair.
+// `fast`: pos * th stays below 2^22 turns (and pos below 2^24), so the whole
+// turns drop out exactly and the float path keeps full accuracy; otherwise
+// the product and its reduction run in double precision.
+__device__ __forceinline__ void rope_sincos(int pos, bool fast, float th, float tl, double f,
+                                            float& sn, float& cs) {
+  if (fast) {
+    const float fpos = (float)pos;
+    const float hi = fpos * th;
+    const float lo = fmaf(fpos, tl, fmaf(fpos, th, -hi));
+    sincospif(2.f * ((hi - rintf(hi)) + lo), &sn, &cs);
+  } else {
+    constexpr double kTwoPiD = 6.283185307179586476925286766559;
+    const double a = (double)pos * f;
+    sincosf((float)fma(-rint(a * (1.0 / kTwoPiD)), kTwoPiD, a), &sn, &cs);
+  }
+}
+
+// Whether the float angle path holds at pos (gmax: the largest turn rate).
+__device__ __forceinline__ bool rope_fast(int pos, float gmax) {
+  return pos < (1 << 24) && (float)pos * gmax < 4194304.f;
+}
+
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
+  const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
+  return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// One head's per-head RMSNorm and NeoX rotation, a half-warp per head: lane
+// li of the half holds values 4 li .. 4 li + 3 (ra) and 64 + 4 li .. + 3 (rb),
+// both members of four pairs (i, i + 64); w*, c4 and s4 are the norm weights
+// and the pairs' cos / sin at those indices.  The results, times `post`,
+// rounded to bf16: oa (values 4 li ..) and ob (64 + 4 li ..).  Every lane of the
+// warp calls it (a 16-lane shuffle reduction).
+__device__ __forceinline__ void norm_rope_half(uint2 ra, uint2 rb, float4 wa, float4 wb,
+                                               float4 c4, float4 s4, float eps, float post,
+                                               float4& oa, float4& ob) {
+  const float4 xa = bf16x4_to_float4(ra), xb = bf16x4_to_float4(rb);
+  float ss = xa.x * xa.x + xa.y * xa.y + xa.z * xa.z + xa.w * xa.w +
+             xb.x * xb.x + xb.y * xb.y + xb.z * xb.z + xb.w * xb.w;
+#pragma unroll
+  for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float sc = rsqrtf(ss * (1.f / kHeadDim) + eps) * post;
+  const float4 ta = make_float4(xa.x * wa.x, xa.y * wa.y, xa.z * wa.z, xa.w * wa.w);
+  const float4 tb = make_float4(xb.x * wb.x, xb.y * wb.y, xb.z * wb.z, xb.w * wb.w);
+  // (x_i, x_{i+64}) -> (x_i cos - x_{i+64} sin, x_{i+64} cos + x_i sin), times the scale
+  oa = make_float4(fmaf(ta.x, c4.x, -tb.x * s4.x) * sc, fmaf(ta.y, c4.y, -tb.y * s4.y) * sc,
+                   fmaf(ta.z, c4.z, -tb.z * s4.z) * sc, fmaf(ta.w, c4.w, -tb.w * s4.w) * sc);
+  ob = make_float4(fmaf(tb.x, c4.x, ta.x * s4.x) * sc, fmaf(tb.y, c4.y, ta.y * s4.y) * sc,
+                   fmaf(tb.z, c4.z, ta.z * s4.z) * sc, fmaf(tb.w, c4.w, ta.w * s4.w) * sc);
+}
+
+// The decode step's prologue run inside the decode kernel (pa_decode_prologue):
+// the inputs of pa_qk_norm_rope_write for one new token per sequence.
+struct DecodePrologue {
+  const __nv_bfloat16* qkv;     // [B, (Hq + 2 Hkv) * D] bf16
+  const float* wq;              // [D] Q norm weight
+  const float* wk;              // [D] K norm weight
+  __nv_bfloat16* k_cache;       // the new token's K and V rows are written here
+  __nv_bfloat16* v_cache;
+  float eps, q_scale;
+  double freq[64];              // the 64 pairs' frequencies, as in PrologueParams
+  float turn_hi[64], turn_lo[64];
+};
 
 // Q/K RMSNorm -> NeoX RoPE -> KV cache write for the new tokens.
 struct PrologueParams {

@@ -51,6 +51,12 @@
 //    writes `out` (one split) or normalised partials (o, lse) for the combine.
 //  * FP8 cache: TMA lands e4m3 pages; converter warps rewrite K as F16 into
 //    tensor memory (QK^T takes A from TMEM) and V as F16 into shared memory.
+//  * In-kernel prologue (pa_decode_prologue; "Qwen3-14B", decode_fwd: the
+//    attention kernel there runs the RoPE/QKV step as its phase 0): warp 10
+//    walks the same items as the TMA warp, builds each item's query operand
+//    from the fused QKV row (per-head RMSNorm, NeoX RoPE, the Q scale) and
+//    stores the new token's K/V row into its slot ahead of the page load that
+//    reads it, so the TMA warp's page loads never wait for that arithmetic.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -64,6 +70,7 @@ constexpr int kMmaWarp = 1;
 constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
 constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
 constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert, one thread per key row
+constexpr int kProWarp = 10;   // in-kernel prologue (bf16 cache only): builds the query operands
 constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -107,7 +114,8 @@ struct Layout {
   static constexpr int kBars = kInfo + kSlots * 8 * 4;
   static constexpr int kNumBars =
       3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
-      (kN == 32 ? 2 : 0);  // 32 columns: a second pair of exchange slots
+      (kN == 32 ? 2 : 0) +  // 32 columns: a second pair of exchange slots
+      kSlots;               // the in-kernel prologue's K/V-row barriers
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
 };
 constexpr int kSmemLimit = 232448;
@@ -143,6 +151,7 @@ struct Bars {
   uint64_t* ml_full;   // [2] (m, l) of the item published
   uint64_t* x_full;    // [2] softmax-warp exchange slots (one arrival per warp)
   uint64_t* mma_done;  // drain at exit
+  uint64_t* kv_ready;  // [kSlots] in-kernel prologue: the item's new K/V row stored (or none)
 };
 
 // Item record in shared memory, written by the TMA warp, read by every role.
@@ -205,11 +214,17 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 // FP8: the cache holds e4m3 codes with per-KV-head scales.  MULTI: more than
 // one new token per sequence (per-column causal masks, (token, head) columns);
 // without it every column is a query head that sees the whole context.
-template <int NH, bool FP8, bool MULTI>
-__global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+// PRO: the decode step's prologue runs in this kernel (bf16 cache, one new
+// token per sequence): the TMA warp builds each item's query operand from the
+// fused QKV row (per-head RMSNorm, NeoX RoPE at the new token's position, the
+// Q scale) instead of loading q, and before it loads the page that holds the
+// new token it writes that token's K row (normed, rotated) and V row into the
+// cache slot -- the arithmetic of pa_qk_norm_rope_write, so the same bits.
+template <int NH, bool FP8, bool MULTI, bool PRO>
+__device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                            const CUtensorMap& tm_q, const DecodeParams& p,
+                                            const DecodePrologue* pro) {
+  static_assert(!PRO || (!FP8 && !MULTI), "the in-kernel prologue serves the bf16 single-token kernel");
   using Lay = Layout<FP8, NH>;
   constexpr int kConvWarps = Lay::kConvWarps;
   constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStageBytes;
@@ -240,6 +255,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   B.ml_full = B.o_free + 2;
   B.x_full = B.ml_full + 2;
   B.mma_done = B.x_full + (kN == 32 ? 4 : 2);
+  B.kv_ready = B.mma_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + kNumBars * 8);
   int* info = reinterpret_cast<int*>(smem + kInfo);
 
@@ -257,7 +273,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     if (FP8)
       for (int i = 0; i < kStages; ++i) mbar_init(&B.k_free[i], 1);
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_full[i], PRO ? 2 : 1);  // PRO: the record and the query operand
+      mbar_init(&B.kv_ready[i], 1);
       // MMA, 4 softmax warps, 4 epilogue warps (, the converter warps)
       mbar_init(&B.q_empty[i], 1 + 4 + 4 + kConvWarps);
     }
@@ -299,14 +316,30 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
   // it reads partials only after this grid has completed
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp == kTmaWarp) {
+  if (warp == kTmaWarp || (PRO && warp == kProWarp)) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // (PRO: and the prologue warp, which walks the same items: it builds each
+    // item's query operand and stores the new token's K/V row, so that the
+    // TMA warp's page loads never wait for that arithmetic)
+    const bool tma = warp == kTmaWarp;
+    if (tma && lane == 0) {
       prefetch_tensor_map(&tm_k);
       prefetch_tensor_map(&tm_v);
-      prefetch_tensor_map(&tm_q);
+      if (!PRO) prefetch_tensor_map(&tm_q);
     }
     const uint64_t pol = l2_policy_evict_first();
+    // PRO: lane li of each half-warp holds the norm weights of values
+    // 4 li .. 4 li + 3 and 64 + 4 li .. (the layout of the prologue's compute lanes)
+    const int pli = lane & 15;
+    float4 pwq_lo{}, pwq_hi{}, pwk_lo{}, pwk_hi{};
+    float pgmax = 0.f;
+    if (PRO && !tma) {
+      pwq_lo = __ldg(reinterpret_cast<const float4*>(pro->wq + 4 * pli));
+      pwq_hi = __ldg(reinterpret_cast<const float4*>(pro->wq + 4 * pli + 64));
+      pwk_lo = __ldg(reinterpret_cast<const float4*>(pro->wk + 4 * pli));
+      pwk_hi = __ldg(reinterpret_cast<const float4*>(pro->wk + 4 * pli + 64));
+      pgmax = fmaxf(pro->turn_hi[0], pro->turn_hi[63]);  // the frequencies are monotone
+    }
     // ---- work generator (warp-uniform state).  Fixed splits: items
     // i = blockIdx.x + k * gridDim.x of (split, sequence, unit).  Page-balanced:
     // the CTAs form groups of UPS (one CTA per unit = KV head x head group);
@@ -431,9 +464,25 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       const int pg = w.pg0 + lane;
       return pg < p.max_pages ? __ldg(p.block_table + (int64_t)w.s * p.max_pages + pg) : 0;
     };
+    // PRO: the fused QKV row parts an item reads (its G query heads, its K and
+    // V heads), prefetched into L1 when the item is generated
+    auto prefetch_row = [&](const Work& w) {
+      if (PRO && !tma) {
+        const uint8_t* xrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
+                              (int64_t)w.s * (p.Hq + 2 * p.Hkv) * (kHeadDim * 2);
+        for (int i = lane; i < 2 * p.G + 4; i += 32) {
+          const int64_t off = i < 2 * p.G ? (int64_t)w.unit * p.G * 256 + i * 128
+                            : i < 2 * p.G + 2 ? (int64_t)(p.Hq + w.unit) * 256 + (i - 2 * p.G) * 128
+                                              : (int64_t)(p.Hq + p.Hkv + w.unit) * 256 +
+                                                    (i - 2 * p.G - 2) * 128;
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(xrow + off));
+        }
+      }
+    };
     Work nx;
     bool have = gen_next(nx);
     int nx_pid = have ? first_pid(nx) : 0;
+    if (have) prefetch_row(nx);
     uint32_t gp = 0, n = 0;
     // per item slot: parity of its last use if that use loaded a query operand, else -1
     int q_pending[kSlots];
@@ -445,6 +494,7 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
       const int pid0 = nx_pid;
       const bool item = have;
       int flag = 0, npg = 0;
+      bool pkv = false;  // PRO: this item writes the new token's K/V row
       if (item) {
         // validate every page of the item; the next item's metadata loads
         // while this one's pages are issued
@@ -457,11 +507,120 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         bad = __any_sync(0xffffffffu, bad);
         flag = !ctx_ok(w.ctx, p) ? 2 : (bad ? 1 : 0);
         npg = flag ? 0 : w.pg1 - w.pg0;
+        if constexpr (PRO) {
+          // the new token's K/V row is written by the item that reads the page
+          // holding it, once every block-table entry of the sequence is valid
+          // (the prologue writes nothing for an invalid sequence); a sequence
+          // without that token (length 0) is flagged as the prologue flags it
+          pkv = npg > 0 && w.pg0 + npg == pages_of(w.ctx, p);
+          if (pkv) {
+            bool bad0 = false;
+            for (int e = lane; e < w.pg0; e += 32) {
+              const int pid = __ldg(bt + e);
+              bad0 |= pid < 0 || pid >= p.num_pages;
+            }
+            pkv = !__any_sync(0xffffffffu, bad0);
+          }
+          if (w.ctx == 0 && w.unit == 0 && lane == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_BAD_LENGTH);
+        }
         have = gen_next(nx);
-        if (have) nx_pid = first_pid(nx);
+        if (have) {
+          nx_pid = first_pid(nx);
+          prefetch_row(nx);
+        }
       }
       const int slot = n % kSlots;
       if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
+      if (PRO && !tma) {
+        // ---- prologue warp: the item's query operand, then its K/V row
+        // the cos / sin of this lane's four NeoX pairs at the new token's
+        // position (kept for the K row), then the G query heads, a half-warp
+        // per head, written into the operand in the 128-byte-swizzled layout
+        // the TMA load gives (rows past G stay zero)
+        float4 pc4{}, ps4{};
+        if constexpr (PRO) {
+          if (npg > 0) {
+            const int pos = w.ctx - 1;
+            float cs[4], sn[4];
+            auto angles = [&](bool fast) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int q = 4 * pli + j;
+                rope_sincos(pos, fast, pro->turn_hi[q], pro->turn_lo[q], pro->freq[q], sn[j], cs[j]);
+              }
+            };
+            if (rope_fast(pos, pgmax)) angles(true); else angles(false);
+            pc4 = make_float4(cs[0], cs[1], cs[2], cs[3]);
+            ps4 = make_float4(sn[0], sn[1], sn[2], sn[3]);
+            const uint8_t* qrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
+                                  ((int64_t)w.s * (p.Hq + 2 * p.Hkv) + w.unit * p.G) * (kHeadDim * 2);
+            const uint32_t qd = smem_u32(smem + kQ + slot * kOpBytes);
+            constexpr int kPasses = (NH + 1) / 2;
+            uint2 ra[kPasses], rb[kPasses];
+#pragma unroll
+            for (int m = 0; m < kPasses; ++m) {
+              const int r = min(2 * m + (lane >> 4), p.G - 1);
+              ra[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 8 * pli));
+              rb[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 128 + 8 * pli));
+            }
+#pragma unroll
+            for (int m = 0; m < kPasses; ++m) {
+              if (2 * m >= p.G) break;
+              const int r = 2 * m + (lane >> 4);
+              float4 oa, ob;
+              norm_rope_half(ra[m], rb[m], pwq_lo, pwq_hi, pc4, ps4, pro->eps, pro->q_scale, oa, ob);
+              if (r < p.G) {
+                const uint2 qa = float4_to_bf16x4(oa), qb = float4_to_bf16x4(ob);
+                const uint32_t off =
+                    r * 128 + ((((uint32_t)pli >> 1) ^ ((uint32_t)r & 7)) << 4) + (pli & 1) * 8;
+                sts64(qd + off, qa.x, qa.y);
+                sts64(qd + kAtom + off, qb.x, qb.y);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (pkv) {
+              // the new token's K row (normed, rotated; lanes 0-15 store it) and
+              // V row (copied; lanes 16-31) into its slot; the page holding it
+              // is loaded after a proxy fence (below), so the tensor load sees them
+              const int h = w.unit;
+              const uint8_t* xrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
+                                    (int64_t)w.s * (p.Hq + 2 * p.Hkv) * (kHeadDim * 2);
+              const uint8_t* krow = xrow + (int64_t)(p.Hq + h) * (kHeadDim * 2);
+              const uint8_t* vrow = xrow + (int64_t)(p.Hq + p.Hkv + h) * (kHeadDim * 2);
+              const uint2 ka = __ldg(reinterpret_cast<const uint2*>(krow + 8 * pli));
+              const uint2 kb = __ldg(reinterpret_cast<const uint2*>(krow + 128 + 8 * pli));
+              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vrow) + pli);
+              float4 oa, ob;
+              norm_rope_half(ka, kb, pwk_lo, pwk_hi, pc4, ps4, pro->eps, 1.f, oa, ob);
+              const int last = npg - 1;  // the item's page holding the token
+              const int pid_last = __shfl_sync(0xffffffffu, pid0, last & 31);
+              const int page = last < 32 ? pid_last
+                                         : __ldg(p.block_table + (int64_t)w.s * p.max_pages +
+                                                 w.pg0 + last);
+              const int64_t slot_row = ((int64_t)page * kPage + (w.ctx - 1) % kPage) * p.Hkv + h;
+              if (lane < 16) {
+                uint2* kd = reinterpret_cast<uint2*>(pro->k_cache + slot_row * kHeadDim);
+                kd[pli] = float4_to_bf16x4(oa);
+                kd[16 + pli] = float4_to_bf16x4(ob);
+              } else {
+                reinterpret_cast<uint4*>(pro->v_cache + slot_row * kHeadDim)[pli] = vv;
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.q_full[slot]);  // the query operand is in place
+        // the stored row reaches the async proxy before the page's tensor load
+        // (proxy fence in every writing lane, warp barrier, release by lane 0,
+        // acquire by the TMA warp)
+        if (pkv) fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.kv_ready[slot]);
+        if (!item) break;
+        continue;
+      }
       if constexpr (FP8) {
         if (npg > 0) {
           // the tensor core reads F16 here: the warp converts the item's query
@@ -507,8 +666,8 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         rec[kIUnit] = w.unit;
         rec[kIDest] = w.dest;
         rec[kIDone] = item ? 0 : 1;
-        if (FP8 || npg <= 0) {
-          mbar_arrive(&B.q_full[slot]);  // FP8: the rows above are in place
+        if (FP8 || PRO || npg <= 0) {
+          mbar_arrive(&B.q_full[slot]);  // FP8, PRO: the rows above are in place
           q_pending[slot] = -1;
         } else if (MULTI) {
           // q as [tokens][Hq][128]: Lg tokens x the G heads of this KV head
@@ -538,6 +697,10 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
         const int cnt = min(32, npg - c);
         for (int k = 0; k < cnt; ++k) {
           const int page = __shfl_sync(0xffffffffu, pid_l, k);
+          if (PRO && c + k == npg - 1) {
+            // the page holding the new token: its K/V row is stored first
+            if (!(ok = mbar_wait_warp(&B.kv_ready[slot], (n / kSlots) & 1, p.status))) break;
+          }
           int lok = 1;
           if (lane == 0 && FP8) {
             // e4m3 K and V tiles (128 one-byte dims x 128 tokens each)
@@ -572,7 +735,9 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
     }
     // drain: copies still in flight (only after a timeout elsewhere) must land
     // before the CTA exits
-    if (lane == 0 && FP8) {
+    if (!tma) {
+      // the prologue warp issues no copies
+    } else if (lane == 0 && FP8) {
       for (uint32_t g = gp > kStages8 ? gp - kStages8 : 0; g < gp; ++g)
         mbar_wait(&B.kv8_full[g % kStages8], (g / kStages8) & 1, nullptr);
     } else if (lane == 0) {
@@ -1251,6 +1416,24 @@ __global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
 }
 
 template <int NH, bool FP8, bool MULTI>
+__global__ void __launch_bounds__(Layout<FP8, NH>::kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ DecodeParams p) {
+  decode_body<NH, FP8, MULTI, false>(tm_k, tm_v, tm_q, p, nullptr);
+}
+
+// The decode step with its prologue (pa_decode_prologue): no q tensor map.
+template <int NH>
+__global__ void __launch_bounds__(Layout<false, NH>::kThreads + 32, 1)
+    decode_prologue_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ DecodeParams p,
+                           const __grid_constant__ DecodePrologue pro) {
+  decode_body<NH, false, false, true>(tm_k, tm_v, tm_k, p, &pro);
+}
+
+template <int NH, bool FP8, bool MULTI>
 cudaError_t launch_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                       const DecodeParams& p, int num_sms, cudaStream_t stream) {
   constexpr int smem = Layout<FP8, NH>::kSmem, threads = Layout<FP8, NH>::kThreads;
@@ -1286,7 +1469,40 @@ cudaError_t launch_multi(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   }
 }
 
+template <int NH>
+cudaError_t launch_pro_nh(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeParams& p,
+                          const DecodePrologue& pro, int num_sms, cudaStream_t stream) {
+  // one more warp than the plain kernel: the prologue warp
+  constexpr int smem = Layout<false, NH>::kSmem, threads = Layout<false, NH>::kThreads + 32;
+  cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.balanced ? p.grid : (p.num_items < num_sms ? p.num_items : num_sms);
+  if (grid < 1) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_prologue_kernel<NH>, tm_k, tm_v, p, pro);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_decode_prologue(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const DecodeParams& p, const DecodePrologue& pro, int g,
+                                   int num_sms, cudaStream_t stream) {
+  if (g < 1 || g > 16 || p.k_scale || p.L != 1) return cudaErrorInvalidValue;
+  return g <= 8 ? launch_pro_nh<8>(tm_k, tm_v, p, pro, num_sms, stream)
+                : launch_pro_nh<16>(tm_k, tm_v, p, pro, num_sms, stream);
+}
 
 cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,

@@ -39,6 +39,13 @@ cudaError_t launch_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const CUtensorMap& tm_q, const DecodeParams& p, int gc, int num_sms,
                           cudaStream_t stream);
 
+// Decode with its prologue in the kernel (bf16 cache, one token per sequence,
+// g = Hq / Hkv <= 16): q is built from pro.qkv, the new tokens' K/V rows are
+// written to pro.k_cache / pro.v_cache; no q tensor map.
+cudaError_t launch_decode_prologue(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const DecodeParams& p, const DecodePrologue& pro, int g,
+                                   int num_sms, cudaStream_t stream);
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Merge of the units a page-balanced decode launch of p.grid CTAs cut.

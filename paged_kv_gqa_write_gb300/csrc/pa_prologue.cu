@@ -51,7 +51,6 @@ constexpr int kComputeWarps = 8;
 constexpr int kThreads = (kComputeWarps + 1) * 32;  // warp 0: loader
 constexpr int kMaxStages = 4;
 constexpr int kStageBudget = 200 * 1024;            // shared memory for the row ring
-constexpr double kTwoPi = 6.283185307179586476925286766559;
 
 // per stage: the token's cache slot (-1: invalid sequence, nothing written)
 // and the cos / sin of its 64 rotary pairs
@@ -60,15 +59,6 @@ struct StageInfo {
   int32_t valid, pad;
   float cs[2][64];
 };
-
-__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
-  const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
-  return make_float4(a.x, a.y, b.x, b.y);
-}
-
-__device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
-  return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-}
 
 // 4 bf16 values over s -> 4 e4m3 codes (round to nearest even, saturating),
 // value i in byte i.
@@ -194,25 +184,16 @@ __global__ void __launch_bounds__(kThreads, 3)
         in.slot = valid ? (long long)page * kPage + pos % kPage : -1ll;
         in.valid = valid;
       }
-      // angles of pairs lane and lane + 32, reduced to [-1/2, 1/2] turns
+      // angles of pairs lane and lane + 32, reduced to [-1/2, 1/2] turns (pos
+      // exact in a float and pos * g < 2^22 turns: hi - rint(hi) is exact and
+      // the fraction keeps at least 2^-24 resolution; very long positions: the
+      // product and its reduction in double precision)
       float c_lo, s_lo, c_hi, s_hi;
-      const float fpos = (float)pos;
-      if (pos < (1 << 24) && fpos * gmax < 4194304.f) {
-        // pos is exact in a float and pos * g < 2^22 turns: hi - rint(hi) is
-        // exact and the fraction keeps at least 2^-24 resolution
-        auto frac = [&](int q) {
-          const float hi = fpos * turn_hi[q];
-          const float lo = fmaf(fpos, turn_lo[q], fmaf(fpos, turn_hi[q], -hi));
-          return (hi - rintf(hi)) + lo;
-        };
-        sincospif(2.f * frac(lane), &s_lo, &c_lo);
-        sincospif(2.f * frac(lane + 32), &s_hi, &c_hi);
-      } else {
-        // very long positions: the product and its reduction in double precision
-        const double a0 = (double)pos * freq[lane], a1 = (double)pos * freq[lane + 32];
-        sincosf((float)fma(-rint(a0 * (1.0 / kTwoPi)), kTwoPi, a0), &s_lo, &c_lo);
-        sincosf((float)fma(-rint(a1 * (1.0 / kTwoPi)), kTwoPi, a1), &s_hi, &c_hi);
-      }
+      auto angles = [&](bool fast) {
+        rope_sincos(pos, fast, turn_hi[lane], turn_lo[lane], freq[lane], s_lo, c_lo);
+        rope_sincos(pos, fast, turn_hi[lane + 32], turn_lo[lane + 32], freq[lane + 32], s_hi, c_hi);
+      };
+      if (rope_fast(pos, gmax)) angles(true); else angles(false);
       in.cs[0][lane] = c_lo;
       in.cs[0][lane + 32] = c_hi;
       in.cs[1][lane] = s_lo;
@@ -256,21 +237,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint8_t* hrow = row + (live ? hh : 0) * (kHeadDim * 2);
         const uint2 ra = *reinterpret_cast<const uint2*>(hrow + 8 * li);
         const uint2 rb = *reinterpret_cast<const uint2*>(hrow + 128 + 8 * li);
-        const float4 xa = bf16x4_to_float4(ra), xb = bf16x4_to_float4(rb);
-        float ss = xa.x * xa.x + xa.y * xa.y + xa.z * xa.z + xa.w * xa.w +
-                   xb.x * xb.x + xb.y * xb.y + xb.z * xb.z + xb.w * xb.w;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const bool is_q = hh < p.Hq;
-        const float sc = rsqrtf(ss * (1.f / kHeadDim) + p.eps) * (is_q ? p.q_scale : 1.f);
-        const float4 wa = is_q ? wq_lo : wk_lo, wb = is_q ? wq_hi : wk_hi;
-        const float4 ta = make_float4(xa.x * wa.x, xa.y * wa.y, xa.z * wa.z, xa.w * wa.w);
-        const float4 tb = make_float4(xb.x * wb.x, xb.y * wb.y, xb.z * wb.z, xb.w * wb.w);
-        // (x_i, x_{i+64}) -> (x_i cos - x_{i+64} sin, x_{i+64} cos + x_i sin), times the scale
-        const float4 oa = make_float4(fmaf(ta.x, c4.x, -tb.x * s4.x) * sc, fmaf(ta.y, c4.y, -tb.y * s4.y) * sc,
-                                      fmaf(ta.z, c4.z, -tb.z * s4.z) * sc, fmaf(ta.w, c4.w, -tb.w * s4.w) * sc);
-        const float4 ob = make_float4(fmaf(tb.x, c4.x, ta.x * s4.x) * sc, fmaf(tb.y, c4.y, ta.y * s4.y) * sc,
-                                      fmaf(tb.z, c4.z, ta.z * s4.z) * sc, fmaf(tb.w, c4.w, ta.w * s4.w) * sc);
+        float4 oa, ob;
+        norm_rope_half(ra, rb, is_q ? wq_lo : wk_lo, is_q ? wq_hi : wk_hi, c4, s4, p.eps,
+                       is_q ? p.q_scale : 1.f, oa, ob);
         if (!live) continue;
         uint2* dst;
         if (is_q) {

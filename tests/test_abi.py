@@ -137,6 +137,15 @@ def test_host_checks_kv_write_and_prefill(pa):
     assert pro8(ks=None) == h["PA_ERR_NULL_POINTER"] and pro8(vs=None) == h["PA_ERR_NULL_POINTER"]
     assert pro8(vs=ctypes.c_void_p(0x10002)) == h["PA_ERR_ALIGNMENT"]
     assert pro8(eps=-1.0) == h["PA_ERR_DIMS"] and pro8(n=3) == h["PA_ERR_DIMS"]
+    dp = lambda d=d, eps=1e-6, wq=FAKE, qkv=FAKE, od=0, ns=0, ws=None, nws=0: lib.pa_decode_prologue(
+        qkv, wq, FAKE, eps, 1e6, 1.0, 1.0, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, od, ws, nws, ns, d,
+        None, None)
+    assert dp(eps=-1.0) == h["PA_ERR_DIMS"]
+    assert dp(wq=None) == h["PA_ERR_NULL_POINTER"] and dp(qkv=None) == h["PA_ERR_NULL_POINTER"]
+    assert dp(qkv=MIS) == h["PA_ERR_ALIGNMENT"] and dp(wq=MIS) == h["PA_ERR_ALIGNMENT"]
+    assert dp(od=3) == h["PA_ERR_OUT_DTYPE"] and dp(ns=-2) == h["PA_ERR_SPLITS"]
+    assert dp(d=_dims(pa, num_q_heads=34, num_kv_heads=2)) == h["PA_ERR_HEADS"]   # G = 17
+    assert dp(d=_dims(pa, num_seqs=0)) == 0
     wide = _dims(pa, num_q_heads=352, num_kv_heads=32)  # G = 11, 416 heads in a row
     assert lib.pa_qk_norm_rope_write(FAKE, FAKE, FAKE, 1e-6, 1e6, 1.0, 1.0, FAKE, FAKE, FAKE, FAKE,
                                      FAKE, None, 2, wide, None, None) == h["PA_ERR_HEADS"]
