@@ -116,7 +116,11 @@ struct Layout {
       3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
       (kN == 32 ? 2 : 0) +  // 32 columns: a second pair of exchange slots
       kSlots;               // the in-kernel prologue's K/V-row barriers
-  static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;  // + room to align the base
+  // in-kernel prologue: the RoPE tables (64 double frequencies, 64 + 64 float
+  // turn rates), staged from the kernel parameters
+  static constexpr int kRope = kBars + kNumBars * 8 + 16;
+  static constexpr int kRopeBytes = (!FP8 && NH <= 16) ? 64 * 8 + 2 * 64 * 4 : 0;
+  static constexpr int kSmem = kRope + kRopeBytes + 1024;  // + room to align the base
 };
 constexpr int kSmemLimit = 232448;
 static_assert(Layout<false>::kSmem <= kSmemLimit, "decode shared memory exceeds the limit");
@@ -298,6 +302,16 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   // operands (columns past an item's GC are computed and never used)
   for (int o = threadIdx.x * 16; o < (kSlots + 2) * kOpBytes; o += kThreads * 16)
     sts128(smem_u32(smem + kQ + o), 0u, 0u, 0u, 0u);
+  if constexpr (PRO) {
+    // per-lane reads of the parameter block diverge; shared memory does not
+    double* rope_f = reinterpret_cast<double*>(smem + Lay::kRope);
+    float* rope_t = reinterpret_cast<float*>(smem + Lay::kRope + 64 * 8);
+    if (threadIdx.x < 64) {
+      rope_f[threadIdx.x] = pro->freq[threadIdx.x];
+      rope_t[threadIdx.x] = pro->turn_hi[threadIdx.x];
+      rope_t[64 + threadIdx.x] = pro->turn_lo[threadIdx.x];
+    }
+  }
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, Lay::kTmemCols);
@@ -333,12 +347,22 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     const int pli = lane & 15;
     float4 pwq_lo{}, pwq_hi{}, pwk_lo{}, pwk_hi{};
     float pgmax = 0.f;
+    float pth[4] = {}, ptl[4] = {};  // this lane's four pairs' turn rates (hi + lo)
+    double pfq[4] = {};               // ... and radians per position
     if (PRO && !tma) {
+      const double* rope_f = reinterpret_cast<const double*>(smem + Lay::kRope);
+      const float* rope_t = reinterpret_cast<const float*>(smem + Lay::kRope + 64 * 8);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pth[j] = rope_t[4 * pli + j];
+        ptl[j] = rope_t[64 + 4 * pli + j];
+        pfq[j] = rope_f[4 * pli + j];
+      }
       pwq_lo = __ldg(reinterpret_cast<const float4*>(pro->wq + 4 * pli));
       pwq_hi = __ldg(reinterpret_cast<const float4*>(pro->wq + 4 * pli + 64));
       pwk_lo = __ldg(reinterpret_cast<const float4*>(pro->wk + 4 * pli));
       pwk_hi = __ldg(reinterpret_cast<const float4*>(pro->wk + 4 * pli + 64));
-      pgmax = fmaxf(pro->turn_hi[0], pro->turn_hi[63]);  // the frequencies are monotone
+      pgmax = fmaxf(rope_t[0], rope_t[63]);  // the frequencies are monotone
     }
     // ---- work generator (warp-uniform state).  Fixed splits: items
     // i = blockIdx.x + k * gridDim.x of (split, sequence, unit).  Page-balanced:
@@ -495,6 +519,57 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       const bool item = have;
       int flag = 0, npg = 0;
       bool pkv = false;  // PRO: this item writes the new token's K/V row
+      const int slot = n % kSlots;
+      float4 pc4{}, ps4{};  // PRO: cos / sin of this lane's four NeoX pairs at the new token
+      if constexpr (PRO) {
+        if (!tma) {
+          // ---- prologue warp: the item's query operand first (it needs
+          // neither the block table nor the item's validation), then the
+          // validation below and the new token's K/V row
+          if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
+          if (item && w.pg1 > w.pg0 && w.ctx > 0 && ctx_ok(w.ctx, p)) {
+            const int pos = w.ctx - 1;
+            float cs[4], sn[4];
+            auto angles = [&](bool fast) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) rope_sincos(pos, fast, pth[j], ptl[j], pfq[j], sn[j], cs[j]);
+            };
+            if (rope_fast(pos, pgmax)) angles(true); else angles(false);
+            pc4 = make_float4(cs[0], cs[1], cs[2], cs[3]);
+            ps4 = make_float4(sn[0], sn[1], sn[2], sn[3]);
+            // the G query heads, a half-warp per head, into the operand in the
+            // 128-byte-swizzled layout the TMA load gives (rows past G stay zero)
+            const uint8_t* qrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
+                                  ((int64_t)w.s * (p.Hq + 2 * p.Hkv) + w.unit * p.G) * (kHeadDim * 2);
+            const uint32_t qd = smem_u32(smem + kQ + slot * kOpBytes);
+            constexpr int kPasses = (NH + 1) / 2;
+            uint2 ra[kPasses], rb[kPasses];
+#pragma unroll
+            for (int m = 0; m < kPasses; ++m) {
+              const int r = min(2 * m + (lane >> 4), p.G - 1);
+              ra[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 8 * pli));
+              rb[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 128 + 8 * pli));
+            }
+#pragma unroll
+            for (int m = 0; m < kPasses; ++m) {
+              if (2 * m >= p.G) break;
+              const int r = 2 * m + (lane >> 4);
+              float4 oa, ob;
+              norm_rope_half(ra[m], rb[m], pwq_lo, pwq_hi, pc4, ps4, pro->eps, pro->q_scale, oa, ob);
+              if (r < p.G) {
+                const uint2 qa = float4_to_bf16x4(oa), qb = float4_to_bf16x4(ob);
+                const uint32_t off =
+                    r * 128 + ((((uint32_t)pli >> 1) ^ ((uint32_t)r & 7)) << 4) + (pli & 1) * 8;
+                sts64(qd + off, qa.x, qa.y);
+                sts64(qd + kAtom + off, qb.x, qb.y);
+              }
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.q_full[slot]);  // the query operand is in place
+        }
+      }
       if (item) {
         // validate every page of the item; the next item's metadata loads
         // while this one's pages are issued
@@ -530,97 +605,46 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           prefetch_row(nx);
         }
       }
-      const int slot = n % kSlots;
-      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
-      if (PRO && !tma) {
-        // ---- prologue warp: the item's query operand, then its K/V row
-        // the cos / sin of this lane's four NeoX pairs at the new token's
-        // position (kept for the K row), then the G query heads, a half-warp
-        // per head, written into the operand in the 128-byte-swizzled layout
-        // the TMA load gives (rows past G stay zero)
-        float4 pc4{}, ps4{};
-        if constexpr (PRO) {
-          if (npg > 0) {
-            const int pos = w.ctx - 1;
-            float cs[4], sn[4];
-            auto angles = [&](bool fast) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int q = 4 * pli + j;
-                rope_sincos(pos, fast, pro->turn_hi[q], pro->turn_lo[q], pro->freq[q], sn[j], cs[j]);
-              }
-            };
-            if (rope_fast(pos, pgmax)) angles(true); else angles(false);
-            pc4 = make_float4(cs[0], cs[1], cs[2], cs[3]);
-            ps4 = make_float4(sn[0], sn[1], sn[2], sn[3]);
-            const uint8_t* qrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
-                                  ((int64_t)w.s * (p.Hq + 2 * p.Hkv) + w.unit * p.G) * (kHeadDim * 2);
-            const uint32_t qd = smem_u32(smem + kQ + slot * kOpBytes);
-            constexpr int kPasses = (NH + 1) / 2;
-            uint2 ra[kPasses], rb[kPasses];
-#pragma unroll
-            for (int m = 0; m < kPasses; ++m) {
-              const int r = min(2 * m + (lane >> 4), p.G - 1);
-              ra[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 8 * pli));
-              rb[m] = __ldg(reinterpret_cast<const uint2*>(qrow + r * (kHeadDim * 2) + 128 + 8 * pli));
+      if constexpr (PRO) {
+        if (!tma) {
+          if (pkv) {
+            // the new token's K row (normed, rotated; lanes 0-15 store it) and
+            // V row (copied; lanes 16-31) into its slot
+            const int h = w.unit;
+            const uint8_t* xrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
+                                  (int64_t)w.s * (p.Hq + 2 * p.Hkv) * (kHeadDim * 2);
+            const uint8_t* krow = xrow + (int64_t)(p.Hq + h) * (kHeadDim * 2);
+            const uint8_t* vrow = xrow + (int64_t)(p.Hq + p.Hkv + h) * (kHeadDim * 2);
+            const uint2 ka = __ldg(reinterpret_cast<const uint2*>(krow + 8 * pli));
+            const uint2 kb = __ldg(reinterpret_cast<const uint2*>(krow + 128 + 8 * pli));
+            const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vrow) + pli);
+            float4 oa, ob;
+            norm_rope_half(ka, kb, pwk_lo, pwk_hi, pc4, ps4, pro->eps, 1.f, oa, ob);
+            const int last = npg - 1;  // the item's page holding the token
+            const int pid_last = __shfl_sync(0xffffffffu, pid0, last & 31);
+            const int page = last < 32 ? pid_last
+                                       : __ldg(p.block_table + (int64_t)w.s * p.max_pages +
+                                               w.pg0 + last);
+            const int64_t slot_row = ((int64_t)page * kPage + (w.ctx - 1) % kPage) * p.Hkv + h;
+            if (lane < 16) {
+              uint2* kd = reinterpret_cast<uint2*>(pro->k_cache + slot_row * kHeadDim);
+              kd[pli] = float4_to_bf16x4(oa);
+              kd[16 + pli] = float4_to_bf16x4(ob);
+            } else {
+              reinterpret_cast<uint4*>(pro->v_cache + slot_row * kHeadDim)[pli] = vv;
             }
-#pragma unroll
-            for (int m = 0; m < kPasses; ++m) {
-              if (2 * m >= p.G) break;
-              const int r = 2 * m + (lane >> 4);
-              float4 oa, ob;
-              norm_rope_half(ra[m], rb[m], pwq_lo, pwq_hi, pc4, ps4, pro->eps, pro->q_scale, oa, ob);
-              if (r < p.G) {
-                const uint2 qa = float4_to_bf16x4(oa), qb = float4_to_bf16x4(ob);
-                const uint32_t off =
-                    r * 128 + ((((uint32_t)pli >> 1) ^ ((uint32_t)r & 7)) << 4) + (pli & 1) * 8;
-                sts64(qd + off, qa.x, qa.y);
-                sts64(qd + kAtom + off, qb.x, qb.y);
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (pkv) {
-              // the new token's K row (normed, rotated; lanes 0-15 store it) and
-              // V row (copied; lanes 16-31) into its slot; the page holding it
-              // is loaded after a proxy fence (below), so the tensor load sees them
-              const int h = w.unit;
-              const uint8_t* xrow = reinterpret_cast<const uint8_t*>(pro->qkv) +
-                                    (int64_t)w.s * (p.Hq + 2 * p.Hkv) * (kHeadDim * 2);
-              const uint8_t* krow = xrow + (int64_t)(p.Hq + h) * (kHeadDim * 2);
-              const uint8_t* vrow = xrow + (int64_t)(p.Hq + p.Hkv + h) * (kHeadDim * 2);
-              const uint2 ka = __ldg(reinterpret_cast<const uint2*>(krow + 8 * pli));
-              const uint2 kb = __ldg(reinterpret_cast<const uint2*>(krow + 128 + 8 * pli));
-              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vrow) + pli);
-              float4 oa, ob;
-              norm_rope_half(ka, kb, pwk_lo, pwk_hi, pc4, ps4, pro->eps, 1.f, oa, ob);
-              const int last = npg - 1;  // the item's page holding the token
-              const int pid_last = __shfl_sync(0xffffffffu, pid0, last & 31);
-              const int page = last < 32 ? pid_last
-                                         : __ldg(p.block_table + (int64_t)w.s * p.max_pages +
-                                                 w.pg0 + last);
-              const int64_t slot_row = ((int64_t)page * kPage + (w.ctx - 1) % kPage) * p.Hkv + h;
-              if (lane < 16) {
-                uint2* kd = reinterpret_cast<uint2*>(pro->k_cache + slot_row * kHeadDim);
-                kd[pli] = float4_to_bf16x4(oa);
-                kd[16 + pli] = float4_to_bf16x4(ob);
-              } else {
-                reinterpret_cast<uint4*>(pro->v_cache + slot_row * kHeadDim)[pli] = vv;
-              }
-            }
+            // the stored row reaches the async proxy before the page's tensor
+            // load (proxy fence in every writing lane, warp barrier, release
+            // by lane 0, acquire by the TMA warp)
+            fence_proxy_async_global();
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.kv_ready[slot]);
+          if (!item) break;
+          continue;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.q_full[slot]);  // the query operand is in place
-        // the stored row reaches the async proxy before the page's tensor load
-        // (proxy fence in every writing lane, warp barrier, release by lane 0,
-        // acquire by the TMA warp)
-        if (pkv) fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.kv_ready[slot]);
-        if (!item) break;
-        continue;
       }
+      if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
       if constexpr (FP8) {
         if (npg > 0) {
           // the tensor core reads F16 here: the warp converts the item's query
