@@ -49,8 +49,11 @@
 //  * warps 6-9, one thread per head dim: the epilogue of the previous item
 //    (O / l from TMEM, double-buffered) overlaps the next item's pages; it
 //    writes `out` (one split) or normalised partials (o, lse) for the combine.
-//  * FP8 cache: TMA lands e4m3 pages; converter warps rewrite K as F16 into
-//    tensor memory (QK^T takes A from TMEM) and V as F16 into shared memory.
+//  * FP8 cache: TMA lands e4m3 pages.  QK^T runs on the e4m3 K page itself
+//    (kind::f8f6f4, K-major): the TMA warp splits each query row into two
+//    e4m3 rows whose sum is the row (times a power of two), so S^T has a hi
+//    and a lo column per query column, which the softmax adds.  Converter
+//    warps rewrite V as F16 into shared memory for P.V (kind::f16).
 //  * In-kernel prologue (pa_decode_prologue; "Qwen3-14B", decode_fwd: the
 //    attention kernel there runs the RoPE/QKV step as its phase 0): warp 10
 //    walks the same items as the TMA warp, builds each item's query operand
@@ -69,51 +72,67 @@ constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kSoftWarp0 = 2;  // warps 2-5: softmax, one thread per key
 constexpr int kEpiWarp0 = 6;   // warps 6-9: epilogue, one thread per head dim
-constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert, one thread per key row
+constexpr int kConvWarp0 = 10; // FP8 cache: warps 10-13 convert V, one thread per key row
 constexpr int kProWarp = 10;   // in-kernel prologue (bf16 cache only): builds the query operands
 constexpr int kBalMaxSeqs = PA_BALANCED_MAX_SEQS;  // page-balanced schedule: sequences
 constexpr int kBox = 64 * 2 * kPage;       // 64 dims x 128 tokens of bf16 = 16 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// Item record in shared memory, written by the TMA warp, read by every role.
+enum : int {
+  kICtx = 0,   // context length of the sequence
+  kIPg0 = 1,   // first page of the item
+  kIPg1 = 2,   // end page (== kIPg0 when the item has no pages to read)
+  kIFlag = 3,  // 0 ok, 1 invalid block-table entry, 2 invalid context length
+  kISeq = 4,   // sequence
+  kIUnit = 5,  // KV head * NT + token group
+  kIDest = 6,  // -1: out; else the partial record (split index, or 2 * CTA + cut side)
+  kIDone = 7,  // no more items
+  kIQInv = 8,  // FP8: 1 / x (float bits), x the power of two the query rows were scaled by
+  kInfoInts = 10
+};
+
 // Shared memory (offsets from a 1024-aligned base).  BF16 cache: a 3-stage
 // ring of K/V operand pages loaded by TMA.  FP8 cache: a 4-stage ring of e4m3
-// pages (32 KB each) loaded by TMA; the converter warps rewrite each page's K
-// as F16 into one of two tensor-memory buffers (QK^T takes A from TMEM) and
-// its V as F16 into a 2-stage shared-memory ring (the tensor core reads F16;
-// every e4m3 value is exact in it).
+// pages (32 KB each) loaded by TMA; QK^T reads the K tile there, and the
+// converter warps rewrite each page's V as F16 into a 2-stage shared-memory
+// ring (the tensor core reads F16; every e4m3 value is exact in it).
 constexpr int kBox8 = 128 * kPage;         // 128 one-byte dims x 128 tokens = 16 KB
+constexpr uint32_t pow2_cols(uint32_t n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
 template <bool FP8, int NH = 16>
 struct Layout {
   // MMA N: the item's (token, query head) columns, padded to 16 or 32
   static constexpr int kN = NH > 16 ? 32 : 16;
+  // QK^T's N: FP8 doubles the query columns (hi rows 0 .. NH - 1, lo rows
+  // NH .. 2 NH - 1 of the e4m3 query operand)
+  static constexpr int kNS = FP8 ? (2 * NH > kN ? 2 * NH : kN) : kN;
   static constexpr int kAtom = kN * 128;     // kN rows x 128 bytes
   static constexpr int kOpBytes = 2 * kAtom; // Q or P operand: two 64-element atoms
+  static_assert(kNS * 128 <= kOpBytes, "the e4m3 query operand fits the query slot");
   // item slots: how far the TMA warp runs ahead (two with the wide operands,
   // which the shared-memory budget allows no more of)
   static constexpr int kSlots = kN == 32 ? 2 : 4;
-  // tensor-memory columns: S^T[2] and O^T[2], kN each; FP8: K[2] as F16
-  // pairs, 64 columns each (lane = key)
-  static constexpr uint32_t kColS = 0, kColO = 2 * kN, kColK = 4 * kN;
-  // operand stages: bf16 K lo, K hi, V lo, V hi; FP8 V lo, V hi (K is in TMEM)
+  // tensor-memory columns: S^T[2] (kNS each) and O^T[2] (kN each)
+  static constexpr uint32_t kColS = 0, kColO = 2 * kNS;
+  // operand stages: bf16 K lo, K hi, V lo, V hi; FP8 V lo, V hi as F16
   static constexpr int kStages = FP8 ? 2 : 3;
   static constexpr int kStageBytes = FP8 ? 2 * kBox : 4 * kBox;
   static constexpr int kStages8 = FP8 ? 4 : 0;  // e4m3 pages (K, V)
-  // converter warps: 8 (K and V converted side by side) where the registers
-  // allow it (the 8-column softmax), else 4 (K, then V)
-  static constexpr int kConvWarps = FP8 ? (NH == 8 ? 8 : 4) : 0;
+  // V converter warps, one thread per key row
+  static constexpr int kConvWarps = FP8 ? 4 : 0;
   static constexpr int kThreads = (10 + kConvWarps) * 32;
   static constexpr int kRing = 0;
   static constexpr int kRing8 = kRing + kStages * kStageBytes;
-  static constexpr uint32_t kTmemCols = FP8 ? 256 : 4 * kN;  // FP8: + two 64-column K buffers
+  static constexpr uint32_t kTmemCols = pow2_cols(2 * kNS + 2 * kN);
   static constexpr int kQ = kRing8 + kStages8 * 2 * kBox8;  // [kSlots] query operands
   static constexpr int kP = kQ + kSlots * kOpBytes;         // P operands [2]
   static constexpr int kX = kP + 2 * kOpBytes;              // float [2][4][kN]: softmax exchange
   static constexpr int kML = kX + 2 * 4 * kN * 4;           // float [2][kN][2]: (m, l) per O
-  static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][8]: item records
-  static constexpr int kBars = kInfo + kSlots * 8 * 4;
+  static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][kInfoInts]: item records
+  static constexpr int kBars = kInfo + kSlots * kInfoInts * 4;
   static constexpr int kNumBars =
-      3 * kStages + 2 * kStages8 + (FP8 ? kStages : 0) + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
+      3 * kStages + 3 * kStages8 + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
       (kN == 32 ? 2 : 0) +  // 32 columns: a second pair of exchange slots
       kSlots;               // the in-kernel prologue's K/V-row barriers
   // in-kernel prologue: the RoPE tables (64 double frequencies, 64 + 64 float
@@ -139,12 +158,12 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
 }
 
 struct Bars {
-  uint64_t* k_full;    // [kStages] operand page: K ready (TMA, or the FP8 converters)
-  uint64_t* v_full;    // [kStages] V ready
+  uint64_t* k_full;    // [kStages] operand page: K landed (bf16)
+  uint64_t* v_full;    // [kStages] V ready (TMA, or the FP8 converters)
   uint64_t* kv_empty;  // [kStages] P.V of the page done
-  uint64_t* kv8_full;  // [kStages8] FP8: e4m3 page landed
-  uint64_t* kv8_empty; // [kStages8] FP8: e4m3 page converted
-  uint64_t* k_free;    // [kStages] FP8: QK^T done with the TMEM K buffer
+  uint64_t* k8_full;   // [kStages8] FP8: e4m3 K tile landed
+  uint64_t* v8_full;   // [kStages8] FP8: e4m3 V tile landed
+  uint64_t* kv8_empty; // [kStages8] FP8: QK^T done with K and the converters with V
   uint64_t* q_full;    // [kSlots] item slot staged (info + query operand)
   uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
   uint64_t* s_full;    // [2] S^T of a page (by page parity)
@@ -156,19 +175,6 @@ struct Bars {
   uint64_t* x_full;    // [2] softmax-warp exchange slots (one arrival per warp)
   uint64_t* mma_done;  // drain at exit
   uint64_t* kv_ready;  // [kSlots] in-kernel prologue: the item's new K/V row stored (or none)
-};
-
-// Item record in shared memory, written by the TMA warp, read by every role.
-enum : int {
-  kICtx = 0,   // context length of the sequence
-  kIPg0 = 1,   // first page of the item
-  kIPg1 = 2,   // end page (== kIPg0 when the item has no pages to read)
-  kIFlag = 3,  // 0 ok, 1 invalid block-table entry, 2 invalid context length
-  kISeq = 4,   // sequence
-  kIUnit = 5,  // KV head * NT + token group
-  kIDest = 6,  // -1: out; else the partial record (split index, or 2 * CTA + cut side)
-  kIDone = 7,  // no more items
-  kInfoInts = 8
 };
 
 // A work item: pages [pg0, pg1) of unit (s, unit) whose result goes to `dest`.
@@ -203,14 +209,21 @@ __device__ __forceinline__ int unit_columns(const DecodeParams& p, int unit) {
   return min(p.Lg, p.L - t0) * p.G;
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 (lane = row, element pairs per
-// column), issued by one thread.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (format
+// code 0), both K-major, FP32 accumulate, an M x N tile.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int M, int N) {
+  return (1u << 4)                            // D format: F32
+         | ((uint32_t)(N >> 3) << 17)         // N / 8
+         | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem] over 32 e4m3 elements of K, issued by one thread.
+__device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -237,7 +250,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   constexpr int kX = Lay::kX, kML = Lay::kML, kInfo = Lay::kInfo, kBars = Lay::kBars;
   constexpr int kNumBars = Lay::kNumBars, kThreads = Lay::kThreads;
   constexpr int kN = Lay::kN, kAtom = Lay::kAtom, kOpBytes = Lay::kOpBytes, kSlots = Lay::kSlots;
-  constexpr uint32_t kColS = Lay::kColS, kColO = Lay::kColO, kColK = Lay::kColK;
+  constexpr int kNS = Lay::kNS;
+  constexpr uint32_t kColS = Lay::kColS, kColO = Lay::kColO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -246,10 +260,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   B.k_full = bar;
   B.v_full = B.k_full + kStages;
   B.kv_empty = B.v_full + kStages;
-  B.kv8_full = B.kv_empty + kStages;
-  B.kv8_empty = B.kv8_full + Lay::kStages8;  // (none in the bf16 kernel)
-  B.k_free = B.kv8_empty + Lay::kStages8;
-  B.q_full = B.k_free + (FP8 ? kStages : 0);
+  B.k8_full = B.kv_empty + kStages;
+  B.v8_full = B.k8_full + Lay::kStages8;  // (none in the bf16 kernel)
+  B.kv8_empty = B.v8_full + Lay::kStages8;
+  B.q_full = B.kv8_empty + Lay::kStages8;
   B.q_empty = B.q_full + kSlots;
   B.s_full = B.q_empty + kSlots;
   B.p_full = B.s_full + 2;
@@ -266,16 +280,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&B.k_full[i], FP8 ? 4 : 1);  // FP8: one arrival per converter warp
-      mbar_init(&B.v_full[i], FP8 ? 4 : 1);
+      mbar_init(&B.k_full[i], 1);
+      mbar_init(&B.v_full[i], FP8 ? kConvWarps : 1);  // FP8: one arrival per converter warp
       mbar_init(&B.kv_empty[i], 1);
     }
     for (int i = 0; i < Lay::kStages8; ++i) {
-      mbar_init(&B.kv8_full[i], 1);
-      mbar_init(&B.kv8_empty[i], kConvWarps);
+      mbar_init(&B.k8_full[i], 1);
+      mbar_init(&B.v8_full[i], 1);
+      mbar_init(&B.kv8_empty[i], kConvWarps + 1);  // + the QK^T commit
     }
-    if (FP8)
-      for (int i = 0; i < kStages; ++i) mbar_init(&B.k_free[i], 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&B.q_full[i], PRO ? 2 : 1);  // PRO: the record and the query operand
       mbar_init(&B.kv_ready[i], 1);
@@ -645,37 +658,81 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         }
       }
       if (!(ok = mbar_wait_warp(&B.q_empty[slot], ((n / kSlots) & 1) ^ 1, p.status))) break;
+      float q_inv = 1.f;  // FP8: 1 / x
       if constexpr (FP8) {
         if (npg > 0) {
-          // the tensor core reads F16 here: the warp converts the item's query
-          // rows (bf16 -> F16, exact below 65520 in magnitude) into the operand
+          // QK^T reads e4m3 on both sides.  Each query row r (token r / G,
+          // head r % G) times a power of two x is split into two e4m3 rows,
+          // hi = e4m3(x q) at operand row r and lo = e4m3(x q - hi) at row
+          // NH + r.  x brings the item's largest |q| into [128, 256), so hi
+          // and lo are e4m3 values (no saturation) and hi + lo = x q exactly
+          // for every element of magnitude at least 2^-2 after scaling, i.e.
+          // at least 2^-10 of the largest (a bf16 value has 8 significant
+          // bits, and the residual of its rounding to 4 is a multiple of its
+          // last bit with at most 4 significant bits); smaller ones are off
+          // by at most 2^-10 / x.
           const uint32_t qd = smem_u32(smem + kQ + slot * kOpBytes);
           const int qh = (w.unit / p.NT) * p.G;
           const int64_t qt = (int64_t)w.s * p.L + (w.unit % p.NT) * p.Lg;
           const int64_t T = (int64_t)p.B * p.L;
-          bool big = false;
-          for (int i = lane; i < p.Lg * p.G * 16; i += 32) {
-            const int r = i >> 4, k = i & 15;
+          const int rows = p.Lg * p.G;
+          auto q_chunk = [&](int r, int k) -> uint4 {  // bf16 dims 8k .. 8k + 7 of row r
             const int64_t tok = qt + r / p.G;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok < T)
-              v = __ldg(reinterpret_cast<const uint4*>(
-                            p.q + (tok * p.Hq + qh + r % p.G) * kHeadDim) + k);
+            return tok < T ? __ldg(reinterpret_cast<const uint4*>(
+                                       p.q + (tok * p.Hq + qh + r % p.G) * kHeadDim) + k)
+                           : make_uint4(0u, 0u, 0u, 0u);
+          };
+          // the largest magnitude (bf16 bits: the magnitude order is the
+          // integer order; above 0x7f80: inf or NaN)
+          uint32_t amax = 0;
+          for (int i = lane; i < rows * 16; i += 32) {
+            const uint4 v = q_chunk(i >> 4, i & 15);
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              amax = max(amax, max(wv[e] & 0x7fffu, (wv[e] >> 16) & 0x7fffu));
+          }
+          amax = __reduce_max_sync(0xffffffffu, amax);
+          float x;
+          if (amax >= 0x7f80u) {
+            // inf or NaN in q: flagged, and the item's scores become NaN
+            x = __uint_as_float(0x7fc00000u);
+            if (lane == 0 && p.status) atomicOr(p.status, PA_STATUS_Q_RANGE);
+          } else {
+            // largest = 1.f x 2^(be - 127); x = 2^(134 - be), kept a normal float
+            const int be = (int)(amax >> 7);
+            const int sx = min(134 - be, 126);
+            x = __uint_as_float((uint32_t)(127 + sx) << 23);
+            q_inv = __uint_as_float((uint32_t)(127 - sx) << 23);
+          }
+          for (int i = lane; i < rows * 8; i += 32) {
+            const int r = i >> 3, k = i & 7;  // dims 16k .. 16k + 15
+            const uint4 va = q_chunk(r, 2 * k), vb = q_chunk(r, 2 * k + 1);
+            const uint32_t wv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float a = __uint_as_float(wv[e] << 16);
-              const float b = __uint_as_float(wv[e] & 0xffff0000u);
-              big |= fabsf(a) >= 65520.f || fabsf(b) >= 65520.f;
-              const __half2 h2 = __floats2half2_rn(a, b);
-              o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              uint32_t h4 = 0, l4 = 0;
+#pragma unroll
+              for (int f = 0; f < 2; ++f) {
+                const uint32_t wd = wv[2 * e + f];
+                const float2 a = make_float2(__uint_as_float(wd << 16) * x,
+                                             __uint_as_float(wd & 0xffff0000u) * x);
+                const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+                const __half2 hh(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3));
+                const float2 hf = __half22float2(hh);
+                const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(
+                    make_float2(a.x - hf.x, a.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+                h4 |= (uint32_t)h << (16 * f);
+                l4 |= (uint32_t)l << (16 * f);
+              }
+              hi[e] = h4;
+              lo[e] = l4;
             }
-            sts128(qd + (k >> 3) * kAtom + r * 128 + (((k & 7) ^ (r & 7)) << 4), o[0], o[1],
-                   o[2], o[3]);
+            const uint32_t sw = (uint32_t)((k ^ (r & 7)) << 4);  // NH is a multiple of 8
+            sts128(qd + r * 128 + sw, hi[0], hi[1], hi[2], hi[3]);
+            sts128(qd + (NH + r) * 128 + sw, lo[0], lo[1], lo[2], lo[3]);
           }
-          if (__any_sync(0xffffffffu, big) && lane == 0 && p.status)
-            atomicOr(p.status, PA_STATUS_Q_RANGE);
           fence_proxy_async_smem();
           __syncwarp();
         }
@@ -690,6 +747,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         rec[kIUnit] = w.unit;
         rec[kIDest] = w.dest;
         rec[kIDone] = item ? 0 : 1;
+        rec[kIQInv] = __float_as_int(q_inv);
         if (FP8 || PRO || npg <= 0) {
           mbar_arrive(&B.q_full[slot]);  // FP8, PRO: the rows above are in place
           q_pending[slot] = -1;
@@ -727,15 +785,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           }
           int lok = 1;
           if (lane == 0 && FP8) {
-            // e4m3 K and V tiles (128 one-byte dims x 128 tokens each)
+            // e4m3 K and V tiles (128 one-byte dims x 128 tokens each, 128-byte
+            // swizzle: the K tile is QK^T's K-major A operand as it lands)
             const int st = gp % kStages8;
             lok = mbar_wait(&B.kv8_empty[st], ((gp / kStages8) & 1) ^ 1, p.status);
             if (lok) {
               uint8_t* dst = smem + kRing8 + st * 2 * kBox8;
               const int y = page * kPage;
-              mbar_arrive_expect_tx(&B.kv8_full[st], 2 * kBox8);
-              tma_load_2d(dst, &tm_k, x, y, &B.kv8_full[st], pol);
-              tma_load_2d(dst + kBox8, &tm_v, x, y, &B.kv8_full[st], pol);
+              mbar_arrive_expect_tx(&B.k8_full[st], kBox8);
+              tma_load_2d(dst, &tm_k, x, y, &B.k8_full[st], pol);
+              mbar_arrive_expect_tx(&B.v8_full[st], kBox8);
+              tma_load_2d(dst + kBox8, &tm_v, x, y, &B.v8_full[st], pol);
             }
           } else if (lane == 0) {
             const int st = gp % kStages;
@@ -762,8 +822,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     if (!tma) {
       // the prologue warp issues no copies
     } else if (lane == 0 && FP8) {
-      for (uint32_t g = gp > kStages8 ? gp - kStages8 : 0; g < gp; ++g)
-        mbar_wait(&B.kv8_full[g % kStages8], (g / kStages8) & 1, nullptr);
+      for (uint32_t g = gp > kStages8 ? gp - kStages8 : 0; g < gp; ++g) {
+        mbar_wait(&B.k8_full[g % kStages8], (g / kStages8) & 1, nullptr);
+        mbar_wait(&B.v8_full[g % kStages8], (g / kStages8) & 1, nullptr);
+      }
     } else if (lane == 0) {
       for (uint32_t g = gp > kStages ? gp - kStages : 0; g < gp; ++g) {
         mbar_wait(&B.k_full[g % kStages], (g / kStages) & 1, nullptr);
@@ -776,7 +838,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = FP8 ? umma_idesc_f16(128, kN, false, false)
+      // FP8: e4m3 x e4m3 (format code 0 in kind::f8f6f4), N = the hi and lo columns
+      const uint32_t idesc_qk = FP8 ? umma_idesc_e4m3(128, kNS)
                                     : umma_idesc_bf16(128, kN, false, false);
       const uint32_t idesc_pv = FP8 ? umma_idesc_f16(128, kN, true, false)
                                     : umma_idesc_bf16(128, kN, true, false);
@@ -797,19 +860,25 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         // QK^T of page g into S buffer g & 1 (free: the softmax read page
         // g - 2's scores before publishing its P, which the loop below waited for)
         auto qk = [&](uint32_t g) -> bool {
-          const int st = g % kStages;
-          if (!mbar_wait(&B.k_full[st], (g / kStages) & 1, p.status)) return false;
-          tc_fence_after();
-          const uint32_t s_cols = tmem + kColS + (g & 1) * kN;
+          const uint32_t s_cols = tmem + kColS + (g & 1) * kNS;
           if constexpr (FP8) {
-            // A = K from the TMEM buffer the converters filled
+            // A = the e4m3 K tile as TMA landed it (128 keys x 128 bytes,
+            // K-major, 128-byte swizzle); 32 dims per instruction
+            const int st8 = g % kStages8;
+            if (!mbar_wait(&B.k8_full[st8], (g / kStages8) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(smem + kRing8 + st8 * 2 * kBox8);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              umma_ts(s_cols, tmem + kColK + st * 64 + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = umma_sdesc_sw128(k_addr + kk * 32, 16, 1024);
+              const uint64_t bd = umma_sdesc_sw128(q_addr + kk * 32, 16, 1024);
+              umma_e4m3_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            umma_commit(&B.k_free[st]);
+            umma_commit(&B.kv8_empty[st8]);  // the K tile's share of the stage
           } else {
+            const int st = g % kStages;
+            if (!mbar_wait(&B.k_full[st], (g / kStages) & 1, p.status)) return false;
+            tc_fence_after();
             const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -853,21 +922,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     }
     __syncwarp();
   } else if (warp >= kConvWarp0) {
-    // ------------------------------------------------------------ FP8 converters, thread = key
-    // Each page: wait for its e4m3 tiles; K (once QK^T is done with the TMEM
-    // buffer two pages back) goes to tensor memory as F16 pairs, one lane per
-    // key, 64 columns; V (once P.V is done with the shared-memory stage two
-    // pages back) goes to shared memory as F16 in the swizzled layout the bf16
-    // path gets from TMA.  With eight converter warps, warps 10-13 take K and
-    // 14-17 V; with four, each warp takes both for its 32 keys.
+    // ------------------------------------------------------------ FP8 V converters, thread = key
+    // Each page: wait for its e4m3 V tile and for P.V to be done with the
+    // shared-memory stage two pages back, then write V as F16 in the swizzled
+    // layout the bf16 path gets from TMA.
     if constexpr (FP8) {
-      const int ct = threadIdx.x - kConvWarp0 * 32;
-      const int quarter = warp & 3;                   // TMEM lanes this warp may access
-      const int row = quarter * 32 + lane;            // key 0..127
-      const int sw = row & 7;                         // 128-byte swizzle of the row
-      const bool do_k = kConvWarps == 8 ? ct < 128 : true;
-      const bool do_v = kConvWarps == 8 ? ct >= 128 : true;
-      const uint32_t k_lanes = tmem + ((uint32_t)(quarter * 32) << 16) + kColK;
+      const int row = (warp & 3) * 32 + lane;  // key 0..127
+      const int sw = row & 7;                  // 128-byte swizzle of the row
       uint32_t gp = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
@@ -880,50 +941,25 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if (lane == 0) mbar_arrive(&B.q_empty[slot]);
         for (int j = 0; j < npg; ++j, ++gp) {
           const int st8 = gp % kStages8, st = gp % kStages;
-          const uint32_t ph = ((gp / kStages) & 1) ^ 1;  // the buffer's previous use
-          if (!(ok = mbar_wait_warp(&B.kv8_full[st8], (gp / kStages8) & 1, p.status))) break;
-          const uint32_t src = smem_u32(smem + kRing8 + st8 * 2 * kBox8) + row * 128;
-          if (do_k) {
-            if (!(ok = mbar_wait_warp(&B.k_free[st], ph, p.status))) break;
+          const uint32_t ph = ((gp / kStages) & 1) ^ 1;  // the stage's previous use
+          if (!(ok = mbar_wait_warp(&B.v8_full[st8], (gp / kStages8) & 1, p.status))) break;
+          if (!(ok = mbar_wait_warp(&B.kv_empty[st], ph, p.status))) break;
+          const uint32_t src = smem_u32(smem + kRing8 + st8 * 2 * kBox8 + kBox8) + row * 128;
+          const uint32_t dst = smem_u32(smem + kRing + st * kStageBytes) + row * 128;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // dims 64h .. 64h + 63: columns 32h .. 32h + 31
-              uint32_t w[32];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                uint4 lo, hi;
-                e4m3x16_to_f16(lds128(src + (((4 * h + c) ^ sw) << 4)), lo, hi);
-                w[8 * c] = lo.x;
-                w[8 * c + 1] = lo.y;
-                w[8 * c + 2] = lo.z;
-                w[8 * c + 3] = lo.w;
-                w[8 * c + 4] = hi.x;
-                w[8 * c + 5] = hi.y;
-                w[8 * c + 6] = hi.z;
-                w[8 * c + 7] = hi.w;
-              }
-              tmem_st32(k_lanes + st * 64 + 32 * h, w);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.k_full[st]);
+          for (int c = 0; c < 8; ++c) {  // dims 16c .. 16c + 15
+            uint4 lo, hi;
+            e4m3x16_to_f16(lds128(src + ((c ^ sw) << 4)), lo, hi);
+            const uint32_t d = dst + (c >> 2) * kBox;
+            sts128(d + (((2 * (c & 3)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
+            sts128(d + (((2 * (c & 3) + 1) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
           }
-          if (do_v) {
-            if (!(ok = mbar_wait_warp(&B.kv_empty[st], ph, p.status))) break;
-            const uint32_t dst = smem_u32(smem + kRing + st * kStageBytes) + row * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {  // dims 16c .. 16c + 15
-              uint4 lo, hi;
-              e4m3x16_to_f16(lds128(src + kBox8 + ((c ^ sw) << 4)), lo, hi);
-              const uint32_t d = dst + (c >> 2) * kBox;
-              sts128(d + (((2 * (c & 3)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
-              sts128(d + (((2 * (c & 3) + 1) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.v_full[st]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&B.v_full[st]);
+            mbar_arrive(&B.kv8_empty[st8]);
           }
-          if (lane == 0) mbar_arrive(&B.kv8_empty[st8]);
         }
       }
     }
@@ -966,12 +1002,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       if (rec[kIDone]) break;
       const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1], unit = rec[kIUnit];
       const int flag = rec[kIFlag], sq = rec[kISeq], dest = rec[kIDest];
+      const float q_inv = __int_as_float(rec[kIQInv]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
       const int GC = MULTI ? unit_columns(p, unit) : p.G;
       const int GL = min(max(GC - kH * sg, 0), kH);  // this group's columns
-      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
+      // FP8: times the item's K scale and 1 / x of its query split
+      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT) * q_inv;
       // column g = tl * G + head (token t0 + tl) sees key positions below lim[gl]
       int lim[kH];
       {
@@ -1015,8 +1053,20 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
           tc_fence_after();
           uint32_t sr[kH];
-          tmem_ld16(tmem + lane_base + kColS + (gp & 1) * kN + kH * sg, sr);
-          tmem_wait_ld();
+          const uint32_t s_base = tmem + lane_base + kColS + (gp & 1) * kNS + kH * sg;
+          if constexpr (FP8) {
+            // scores of the hi and lo query rows (columns NH apart), added
+            uint32_t lo[kH];
+            tmem_ld16(s_base, sr);
+            tmem_ld16(s_base + NH, lo);
+            tmem_wait_ld();
+#pragma unroll
+            for (int gl = 0; gl < kH; ++gl)
+              sr[gl] = __float_as_uint(__uint_as_float(sr[gl]) + __uint_as_float(lo[gl]));
+          } else {
+            tmem_ld16(s_base, sr);
+            tmem_wait_ld();
+          }
           float d[kH];
           bool need = j == 0;
           if (!need) {
@@ -1189,12 +1239,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       const int* rec = info + kInfoInts * slot;
       if (rec[kIDone]) break;
       const int ctx = rec[kICtx], pg0 = rec[kIPg0], pg1 = rec[kIPg1], unit = rec[kIUnit];
+      const float q_inv = __int_as_float(rec[kIQInv]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
       if (npg <= 0) continue;
       const int GC = MULTI ? unit_columns(p, unit) : p.G;
-      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT);
+      // FP8: times the item's K scale and 1 / x of its query split
+      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT) * q_inv;
       int lim[NH];
       if constexpr (MULTI) {
         int t = (unit % p.NT) * p.Lg, hg = 0;
@@ -1228,8 +1280,25 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
         tc_fence_after();
         uint32_t sr[kN];
-        tmem_ld_cols(tmem + lane_base + kColS + (gp & 1) * kN, sr);
-        tmem_wait_ld();
+        const uint32_t s_base = tmem + lane_base + kColS + (gp & 1) * kNS;
+        if constexpr (FP8 && NH == 16) {
+          // scores of the hi and lo query rows (columns 16 apart), added
+          uint32_t lo[16];
+          tmem_ld16(s_base, sr);
+          tmem_ld16(s_base + 16, lo);
+          tmem_wait_ld();
+#pragma unroll
+          for (int g = 0; g < 16; ++g)
+            sr[g] = __float_as_uint(__uint_as_float(sr[g]) + __uint_as_float(lo[g]));
+        } else {
+          tmem_ld_cols(s_base, sr);
+          tmem_wait_ld();
+          if constexpr (FP8) {  // NH == 8: the lo rows' scores are columns 8-15
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              sr[g] = __float_as_uint(__uint_as_float(sr[g]) + __uint_as_float(sr[g + 8]));
+          }
+        }
         float d[NH];
         bool need = j == 0;
         if (!need) {

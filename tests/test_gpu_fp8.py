@@ -113,12 +113,53 @@ def test_decode_fp8_bf16_output(cuda_lib):
     assert (np.abs(g - ref) <= 5e-3 + np.abs(ref) * 2.0 ** -8).all()
 
 
-def test_decode_fp8_q_out_of_f16_range_is_flagged(cuda_lib):
-    case = W.custom_case(840, [300, 200], Hq=8, Hkv=2, with_new=True)
+def test_decode_fp8_q_beyond_f16_range(cuda_lib):
+    """q . K runs on e4m3 codes with q split into hi + lo after scaling by a
+    power of two per work item, so no bf16 magnitude is out of range: q times
+    2^15 (elements past 65520) with the softmax scale times 2^-15 gives the
+    same codes, the same score factor and so the same bits as the unscaled
+    call, which matches the oracle."""
+    case = W.custom_case(840, [300, 200, 4096], Hq=8, Hkv=2, with_new=True)
     ks, vs, kc8, vc8 = _fp8_case(case, 5)
-    case.q[1, 3, 17] = 70000.0
-    _, _, _, st = _run(cuda_lib, case, ks, vs, kc8, vc8)
+    out, _, _, st = _run(cuda_lib, case, ks, vs, kc8, vc8)
+    assert st == 0
+    ref, _, _ = _oracle(case, ks, vs, kc8, vc8)
+    assert_close(out, ref, what="fp8 unscaled q")
+    big = W.custom_case(840, [300, 200, 4096], Hq=8, Hkv=2, with_new=True)
+    big.q = (big.q.float() * 2.0 ** 15).to(torch.bfloat16)
+    big.scale = case.scale * 2.0 ** -15
+    assert big.q.float().abs().max() > 65520
+    out_big, _, _, st = _run(cuda_lib, big, ks, vs, kc8, vc8)
+    assert st == 0
+    assert torch.equal(out_big.view(torch.int32), out.view(torch.int32))
+
+
+def test_decode_fp8_q_wide_dynamic_range(cuda_lib):
+    """Elements far below their row's largest (down to 2^-16 of it), where the
+    hi + lo split is no longer exact (error at most 2^-17 of the largest):
+    still within the tolerance of the oracle."""
+    case = W.custom_case(845, [777, 4096, 129], Hq=40, Hkv=8, with_new=True)
+    g = torch.Generator().manual_seed(845)
+    e = torch.randint(-16, 1, case.q.shape, generator=g).float()
+    case.q = (case.q.float() * torch.exp2(e) * 4.0).to(torch.bfloat16)
+    ks, vs, kc8, vc8 = _fp8_case(case, 7)
+    out, _, _, st = _run(cuda_lib, case, ks, vs, kc8, vc8)
+    assert st == 0
+    ref, _, _ = _oracle(case, ks, vs, kc8, vc8)
+    assert_close(out, ref, what="fp8 wide-range q")
+
+
+def test_decode_fp8_nonfinite_q_is_flagged(cuda_lib):
+    """An infinite q element sets PA_STATUS_Q_RANGE and its work item's rows
+    come out NaN; the other sequence is unaffected."""
+    case = W.custom_case(846, [300, 200], Hq=8, Hkv=2, with_new=True)
+    ks, vs, kc8, vc8 = _fp8_case(case, 5)
+    case.q[1, 3, 17] = float("inf")
+    out, _, _, st = _run(cuda_lib, case, ks, vs, kc8, vc8, splits=1)
     assert st & cuda_lib.PA_STATUS_Q_RANGE
+    assert torch.isnan(out[1, 0:4]).all()  # query heads 0-3 share KV head 0
+    ref, _, _ = _oracle(case, ks, vs, kc8, vc8)
+    assert_close(out[0:1], ref[0:1], what="fp8 other sequence")
 
 
 def test_decode_fp8_full_size_sampled(cuda_lib):
