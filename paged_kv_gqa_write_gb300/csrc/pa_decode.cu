@@ -34,7 +34,8 @@
 //  * warp 1: owns TMEM (S[2], O[2]) and issues the MMAs: QK^T(j + 1) before
 //    P.V(j), into the other of two S buffers, so the tensor core computes the
 //    next page's scores while the softmax works on this page's; P.V(j) once
-//    P(j) is in its shared-memory buffer (two, by page parity).
+//    P(j) is in its shared-memory buffer (two, by page parity).  FP8 cache:
+//    warp 1 issues QK^T only and warp 14 P.V, each on its own thread.
 //  * warps 2-5, one thread per key: tcgen05.ld of the key's scores, online
 //    softmax in the log2 domain with a per-head reference max shared by the
 //    CTA.  The reference only moves when some score exceeds it by more than
@@ -121,7 +122,10 @@ struct Layout {
   static constexpr int kStages8 = FP8 ? 4 : 0;  // e4m3 pages (K, V)
   // V converter warps, one thread per key row
   static constexpr int kConvWarps = FP8 ? 4 : 0;
-  static constexpr int kThreads = (10 + kConvWarps) * 32;
+  // FP8: P.V has an issuing thread of its own (warp 14), QK^T stays on warp 1
+  static constexpr bool kSplitIssue = FP8;
+  static constexpr int kPvWarp = 10 + kConvWarps;
+  static constexpr int kThreads = (10 + kConvWarps + (kSplitIssue ? 1 : 0)) * 32;
   static constexpr int kRing = 0;
   static constexpr int kRing8 = kRing + kStages * kStageBytes;
   static constexpr uint32_t kTmemCols = pow2_cols(2 * kNS + 2 * kN);
@@ -132,7 +136,7 @@ struct Layout {
   static constexpr int kInfo = kML + 2 * kN * 2 * 4;        // int [kSlots][kInfoInts]: item records
   static constexpr int kBars = kInfo + kSlots * kInfoInts * 4;
   static constexpr int kNumBars =
-      3 * kStages + 3 * kStages8 + 2 * kSlots + 2 * 2 + 1 + 4 * 2 + 1 +
+      3 * kStages + 3 * kStages8 + 2 * kSlots + 2 * 2 + 2 + 4 * 2 + 1 +
       (kN == 32 ? 2 : 0) +  // 32 columns: a second pair of exchange slots
       kSlots;               // the in-kernel prologue's K/V-row barriers
   // in-kernel prologue: the RoPE tables (64 double frequencies, 64 + 64 float
@@ -168,7 +172,8 @@ struct Bars {
   uint64_t* q_empty;   // [kSlots] item slot read by every role, query operand used
   uint64_t* s_full;    // [2] S^T of a page (by page parity)
   uint64_t* p_full;    // [2] P of a page
-  uint64_t* pv_done;   // every P.V, in page order (the softmax's O rescale waits on it)
+  uint64_t* pv_done;   // [2] P.V of a page done (by page parity): its P buffer is free,
+                       // and the softmax's O rescale of the next page may run
   uint64_t* o_full;    // [2] last P.V of the item done
   uint64_t* o_free;    // [2] epilogue read O and (m, l)
   uint64_t* ml_full;   // [2] (m, l) of the item published
@@ -268,7 +273,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   B.s_full = B.q_empty + kSlots;
   B.p_full = B.s_full + 2;
   B.pv_done = B.p_full + 2;
-  B.o_full = B.pv_done + 1;
+  B.o_full = B.pv_done + 2;
   B.o_free = B.o_full + 2;
   B.ml_full = B.o_free + 2;
   B.x_full = B.ml_full + 2;
@@ -292,8 +297,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&B.q_full[i], PRO ? 2 : 1);  // PRO: the record and the query operand
       mbar_init(&B.kv_ready[i], 1);
-      // MMA, 4 softmax warps, 4 epilogue warps (, the converter warps)
-      mbar_init(&B.q_empty[i], 1 + 4 + 4 + kConvWarps);
+      // the MMA issuer(s), 4 softmax warps, 4 epilogue warps (, the converter warps)
+      mbar_init(&B.q_empty[i], (Lay::kSplitIssue ? 2 : 1) + 4 + 4 + kConvWarps);
     }
     // 32 columns: two groups of 128 softmax threads, each also its columns' epilogue
     constexpr uint32_t kColThreads = kN == 32 ? 256 : 128;
@@ -307,8 +312,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       mbar_init(&B.s_full[i], 1);
       mbar_init(&B.p_full[i], kColThreads);
     }
-    mbar_init(B.pv_done, 1);
-    mbar_init(B.mma_done, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&B.pv_done[i], 1);
+    mbar_init(B.mma_done, Lay::kSplitIssue ? 2 : 1);  // every issuing thread
     fence_mbar_init();
   }
   // query rows past every item's box and unused P rows read as zero: clear the
@@ -835,14 +840,78 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if (q_pending[k] >= 0) mbar_wait(&B.q_full[k], (uint32_t)q_pending[k], nullptr);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || (Lay::kSplitIssue && warp == Lay::kPvWarp)) {
+    // ------------------------------------------------------------ MMA issuers
+    // QK^T of page g goes into S buffer g & 1 and P.V(j) runs once P(j) is
+    // in its shared-memory buffer (two, by page parity) and V(j) in the ring;
+    // P.V's completion frees the ring stage and the P buffer (K(j) is free
+    // too: QK^T(j) finished before the softmax could publish P(j)).
+    // One issuing thread (bf16): QK^T(j + 1) before P.V(j), so the tensor
+    // core computes the next page's scores while the softmax works on this
+    // page's; S buffer g & 1 is free because the thread waited for P(g - 2),
+    // and P buffer j & 1 because P.V(j - 2) was issued before QK^T(j).
+    // Two (FP8, where one thread's 12 issues per page bound the page period):
+    // warp 1 issues QK^T(g) once the softmax has published P(g - 2), warp 14
+    // P.V, and the softmax waits for P.V(j - 2) before it writes P(j).
+    const bool qk_role = warp == kMmaWarp;
     if (lane == 0) {
       // FP8: e4m3 x e4m3 (format code 0 in kind::f8f6f4), N = the hi and lo columns
       const uint32_t idesc_qk = FP8 ? umma_idesc_e4m3(128, kNS)
                                     : umma_idesc_bf16(128, kN, false, false);
       const uint32_t idesc_pv = FP8 ? umma_idesc_f16(128, kN, true, false)
                                     : umma_idesc_bf16(128, kN, true, false);
+      auto qk = [&](uint32_t g, uint32_t q_addr) -> bool {
+        if constexpr (Lay::kSplitIssue) {
+          if (!mbar_wait(&B.p_full[g & 1], ((g >> 1) & 1) ^ 1, p.status)) return false;
+        }
+        const uint32_t s_cols = tmem + kColS + (g & 1) * kNS;
+        if constexpr (FP8) {
+          // A = the e4m3 K tile as TMA landed it (128 keys x 128 bytes,
+          // K-major, 128-byte swizzle); 32 dims per instruction
+          const int st8 = g % kStages8;
+          if (!mbar_wait(&B.k8_full[st8], (g / kStages8) & 1, p.status)) return false;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + kRing8 + st8 * 2 * kBox8);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(k_addr + kk * 32, 16, 1024);
+            const uint64_t bd = umma_sdesc_sw128(q_addr + kk * 32, 16, 1024);
+            umma_e4m3_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&B.kv8_empty[st8]);  // the K tile's share of the stage
+        } else {
+          const int st = g % kStages;
+          if (!mbar_wait(&B.k_full[st], (g / kStages) & 1, p.status)) return false;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&B.s_full[g & 1]);
+        return true;
+      };
+      auto pv = [&](uint32_t g, bool first, int ob, uint32_t nb) -> bool {
+        const int st = g % kStages;
+        if (!mbar_wait(&B.p_full[g & 1], (g >> 1) & 1, p.status)) return false;
+        if (!mbar_wait(&B.v_full[st], (g / kStages) & 1, p.status)) return false;
+        if (first && !mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + kRing + st * kStageBytes) + (FP8 ? 0 : 2 * kBox);
+        const uint32_t p_addr = smem_u32(smem + kP + (g & 1) * kOpBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
+          const uint64_t bd = umma_sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&B.kv_empty[st]);
+        umma_commit(&B.pv_done[g & 1]);
+        return true;
+      };
       uint32_t gp = 0, nb = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
@@ -851,66 +920,29 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         const int* rec = info + kInfoInts * slot;
         if (rec[kIDone]) break;
         const int npg = rec[kIPg1] - rec[kIPg0];
+        const uint32_t q_addr = smem_u32(smem + kQ + slot * kOpBytes);
+        const int ob = nb & 1;
         if (npg <= 0) {
           mbar_arrive(&B.q_empty[slot]);
           continue;
         }
-        const int ob = nb & 1;
-        const uint32_t q_addr = smem_u32(smem + kQ + slot * kOpBytes);
-        // QK^T of page g into S buffer g & 1 (free: the softmax read page
-        // g - 2's scores before publishing its P, which the loop below waited for)
-        auto qk = [&](uint32_t g) -> bool {
-          const uint32_t s_cols = tmem + kColS + (g & 1) * kNS;
-          if constexpr (FP8) {
-            // A = the e4m3 K tile as TMA landed it (128 keys x 128 bytes,
-            // K-major, 128-byte swizzle); 32 dims per instruction
-            const int st8 = g % kStages8;
-            if (!mbar_wait(&B.k8_full[st8], (g / kStages8) & 1, p.status)) return false;
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(smem + kRing8 + st8 * 2 * kBox8);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = umma_sdesc_sw128(k_addr + kk * 32, 16, 1024);
-              const uint64_t bd = umma_sdesc_sw128(q_addr + kk * 32, 16, 1024);
-              umma_e4m3_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&B.kv8_empty[st8]);  // the K tile's share of the stage
-          } else {
-            const int st = g % kStages;
-            if (!mbar_wait(&B.k_full[st], (g / kStages) & 1, p.status)) return false;
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(smem + kRing + st * kStageBytes);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = umma_sdesc_sw128(k_addr + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = umma_sdesc_sw128(q_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              umma_bf16_ss(s_cols, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-            }
+        if (Lay::kSplitIssue && qk_role) {
+          for (int j = 0; ok && j < npg; ++j, ++gp) ok = qk(gp, q_addr);
+          if (!ok) break;
+          umma_commit(&B.q_empty[slot]);  // the query operand is read
+          continue;
+        }
+        if (Lay::kSplitIssue) {
+          mbar_arrive(&B.q_empty[slot]);  // the P.V thread reads only the record
+          for (int j = 0; ok && j < npg; ++j, ++gp) ok = pv(gp, j == 0, ob, nb);
+        } else {
+          if (!(ok = qk(gp, q_addr))) break;  // the item's first page
+          for (int j = 0; j < npg; ++j, ++gp) {
+            // the next page's QK^T runs on the tensor core during this page's softmax
+            if (j + 1 < npg && !(ok = qk(gp + 1, q_addr))) break;
+            if (j == npg - 1) umma_commit(&B.q_empty[slot]);
+            if (!(ok = pv(gp, j == 0, ob, nb))) break;
           }
-          umma_commit(&B.s_full[g & 1]);
-          return true;
-        };
-        if (!(ok = qk(gp))) break;  // the item's first page
-        for (int j = 0; j < npg; ++j, ++gp) {
-          // the next page's QK^T runs on the tensor core during this page's softmax
-          if (j + 1 < npg && !(ok = qk(gp + 1))) break;
-          if (j == npg - 1) umma_commit(&B.q_empty[slot]);
-          const int st = gp % kStages;
-          const uint32_t ph = (gp / kStages) & 1;
-          if (!(ok = mbar_wait(&B.p_full[gp & 1], (gp >> 1) & 1, p.status))) break;
-          if (!(ok = mbar_wait(&B.v_full[st], ph, p.status))) break;
-          if (j == 0 && !(ok = mbar_wait(&B.o_free[ob], ((nb >> 1) & 1) ^ 1, p.status))) break;
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(smem + kRing + st * kStageBytes) + (FP8 ? 0 : 2 * kBox);
-          const uint32_t p_addr = smem_u32(smem + kP + (gp & 1) * kOpBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_sdesc_sw128(v_addr + kk * 2048, kBox, 1024);
-            const uint64_t bd = umma_sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            umma_bf16_ss(tmem + kColO + ob * kN, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&B.kv_empty[st]);
-          umma_commit(B.pv_done);
         }
         if (!ok) break;
         umma_commit(&B.o_full[ob]);
@@ -1103,7 +1135,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
               d[gl] = fmaf(__uint_as_float(sr[gl]), c, -m[gl]);
             }
             if (j > 0) {
-              if (!(ok = mbar_wait_warp(B.pv_done, (gp - 1) & 1, p.status))) break;
+              if (!(ok = mbar_wait_warp(&B.pv_done[(gp - 1) & 1], ((gp - 1) >> 1) & 1, p.status)))
+                break;
               tc_fence_after();
               uint32_t orow[kH];
               const uint32_t o_cols = tmem + lane_base + kColO + ob * kN + kH * sg;
@@ -1114,6 +1147,11 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
                 orow[gl] = __float_as_uint(__uint_as_float(orow[gl]) * alpha[gl]);
               tmem_st16(o_cols, orow);
             }
+          }
+          // P(j) into operand buffer j & 1 once P.V(j - 2) has finished reading it
+          // (with one issuing thread it has, see the issuers)
+          if constexpr (Lay::kSplitIssue) {
+            if (!(ok = mbar_wait_warp(&B.pv_done[gp & 1], ((gp >> 1) & 1) ^ 1, p.status))) break;
           }
           const uint32_t pbase = smem_u32(smem + kP + (gp & 1) * kOpBytes) + p_key;
 #pragma unroll
@@ -1341,7 +1379,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
             // O^T holds P.V of the item's earlier pages once the previous
             // page's P.V is done (this page's QK^T was issued before it; the
             // one before it finished ahead of this page's scores)
-            if (!(ok = mbar_wait_warp(B.pv_done, (gp - 1) & 1, p.status))) break;
+            if (!(ok = mbar_wait_warp(&B.pv_done[(gp - 1) & 1], ((gp - 1) >> 1) & 1, p.status)))
+              break;
             tc_fence_after();
             uint32_t orow[kN];
             const uint32_t o_cols = tmem + lane_base + kColO + ob * kN;
@@ -1353,8 +1392,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
             tmem_st_cols(o_cols, orow);
           }
         }
-        // P(j) into operand buffer j & 1: P.V(j - 2) has finished reading it (it
-        // was issued before QK^T(j), whose commit published these scores)
+        // P(j) into operand buffer j & 1 once P.V(j - 2) has finished reading it
+        // (with one issuing thread it has: P.V(j - 2) was issued before QK^T(j),
+        // whose commit published these scores)
+        if constexpr (Lay::kSplitIssue) {
+          if (!(ok = mbar_wait_warp(&B.pv_done[gp & 1], ((gp >> 1) & 1) ^ 1, p.status))) break;
+        }
         const uint32_t pbase = smem_u32(smem + kP + (gp & 1) * kOpBytes) + p_key;
 #pragma unroll
         for (int g = 0; g < NH; ++g) {
