@@ -104,7 +104,7 @@ typedef struct pa_dims {
 #define PA_STATUS_BAD_LENGTH 2  /* inconsistent context/chunk lengths        */
 #define PA_STATUS_BAD_TOKENS 4  /* sum(chunk_lens) != num_tokens             */
 #define PA_STATUS_TIMEOUT 8     /* a bounded wait inside a kernel gave up    */
-#define PA_STATUS_Q_RANGE 16    /* FP8 cache: q not finite (decode) or |q| too large for F16 (prefill) */
+#define PA_STATUS_Q_RANGE 16    /* FP8 cache: a q element is not finite     */
 
 /* Largest batch accepted by the calls that take chunk_lens (the per-sequence
  * token offsets are built in shared memory). */
@@ -362,10 +362,13 @@ int pa_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
  * prefill step ("Qwen3-14B" pypto-lib doc, prefill_fwd: KV cache update, then
  * causal attention) with the "fp8_e4m3" KV cache dtype the SGLang launch in
  * the "Qwen4-Exp QSA..." blog selects.  The chunk's own K/V must already be
- * in the cache (pa_kv_write_fp8).  The e4m3 pages are converted on the chip
- * to F16, which holds every e4m3 value exactly, and q to F16 (|q| must stay
- * below 65520: larger elements set PA_STATUS_Q_RANGE and make the output
- * undefined); P is rounded to F16 for the P.V product.  The
+ * in the cache (pa_kv_write_fp8).  q . K runs on the e4m3 K codes as in
+ * pa_decode_fp8, with each query row split into e4m3 hi + lo after scaling by
+ * a power of two of its own (exact for every element of magnitude at least
+ * 2^-10 of the row's largest; any finite bf16 q; a non-finite element sets
+ * PA_STATUS_Q_RANGE and makes its row NaN); V is converted on the chip to
+ * F16, which holds every e4m3 value exactly, and P is rounded to F16 for the
+ * P.V product.  The
  * scores are q . K * k_scale[h] * scale and the output is multiplied by
  * v_scale[h].  Arguments, limits, status bits and errors as pa_prefill_chunk;
  * k_scale and v_scale (float32 [Hkv], device) must be non-null

@@ -57,6 +57,12 @@
 // after a cluster-scope release restricted to shared memory: a full
 // cluster-scope release waits for global memory and cost about 0.6 us per
 // arrival, the restricted one about as much as a local arrival.
+// FP8 cache (e4m3 codes, per-KV-head scales): the K halves land as e4m3 by
+// the same paired TMA and S = Q K^T runs on them (kind::f8f6f4); four
+// converter warps split each query row, times a power of two of its own, into
+// e4m3 hi and lo rows in the place of the BF16 tile's two boxes (S = hi K^T +
+// lo K^T, 8 products per step as with BF16), and rewrite the V halves as F16
+// for P.V (kind::f16, P in F16).
 // Epilogue: O / l per row.  A full 128-row tile with BF16 output is staged in
 // shared memory (128-byte swizzle) and written by one TMA tensor store that
 // runs on while the warps start the next item; partial tiles and FP32 output
@@ -66,6 +72,9 @@
 // masked.  Items are dealt to the pairs in decreasing order of key-tile
 // count, snaking across pairs (a greedy longest-first balance every CTA
 // computes from the lengths); very large launches fall back to round-robin.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <type_traits>
 
 #include "pa_launch.cuh"
@@ -95,32 +104,37 @@ constexpr int kSchedBytes = 3 * kMaxCost * 4; // the schedule's scratch ...
 constexpr int kSeqBytes = 48 * 1024;          // ... and its staged lengths
 constexpr int kMaxSchedSeqs = (kSeqBytes / 4 - 1) / 4;  // sequences the schedule stages
 // Shared memory layout (offsets from a 1024-aligned base; identical in both
-// CTAs: a pair MMA reads both at the same offsets).  BF16 cache: 3-stage K
-// and V operand rings, S(j) done frees K stage j % 3 and P.V(j) done V stage
-// j % 3.  FP8 cache: 2-stage F16 operand rings, filled by the converter warps
-// from 3-stage rings of e4m3 halves.
+// CTAs: a pair MMA reads both at the same offsets).  3-stage K ring (BF16, or
+// the e4m3 codes themselves with the FP8 cache), S(j) done frees K stage
+// j % 3.  BF16 cache: 3-stage V operand ring, P.V(j) done frees V stage j % 3.
+// FP8 cache: the V operand ring holds F16, filled by the converter warps
+// from a 3-stage ring of e4m3 V halves; the query tile holds the e4m3 hi and lo
+// halves of the split (below) in the place of the BF16 tile's two boxes.
 template <bool FP8>
 struct Lay {
   static constexpr int kThreads = (FP8 ? kConvWarp0 + 4 : kPvWarp + 1) * 32;
-  static constexpr int kRingK = FP8 ? 2 : 3, kRingV = FP8 ? 2 : 3;  // operand stages
-  static constexpr int kRing8 = FP8 ? 3 : 0;                        // e4m3 stages
+  static constexpr int kRingK = 3, kRingV = 3;  // operand stages
+  static constexpr int kKStage = FP8 ? kK8Bytes : kKBytes;
+  static constexpr int kRing8 = FP8 ? 3 : 0;               // e4m3 V stages
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kQBytes;
-  static constexpr int kV = kK + kRingK * kKBytes;
-  static constexpr int kK8 = kV + kRingV * kVBytes;
-  static constexpr int kV8 = kK8 + kRing8 * kK8Bytes;
+  static constexpr int kV = kK + kRingK * kKStage;
+  static constexpr int kV8 = kV + kRingV * kVBytes;
   static constexpr int kOut = kV8 + kRing8 * kV8Bytes;  // BF16 output tile staging: 2 boxes of 128 x 64
   static constexpr int kX = kOut + kOutBytes;           // row exchange between the two halves: [2][128] float
-  static constexpr int kList = kX + 2 * 128 * 4;        // schedule [kMaxList][kListInts] int
+  // FP8: 1 / x per query row, [4][128] float by item ordinal mod 4 (a slot
+  // is rewritten four items later, when the softmax is past the item after it)
+  static constexpr int kQInv = kX + 2 * 128 * 4;
+  static constexpr int kList = kQInv + (FP8 ? 4 * 128 * 4 : 0);  // schedule [kMaxList][kListInts] int
   static constexpr int kBars = kList + kMaxList * kListInts * 4;
   // q_full, q_empty, k_full, v_full, s_full, p_full, o_done, drain; FP8:
-  // q16_full, k16_full, v16_full, k8_full, k8_empty, v8_full, v8_empty
+  // q16_full, qs_full, v16_full, v8_full, v8_empty
   static constexpr int kNumBars = 2 + 2 + kRingK + kRingV + 3 * kNumS + 1 +
-                                  (FP8 ? 2 + kRingK + kRingV + 4 * kRing8 : 0);
+                                  (FP8 ? 2 + 4 + kRingV + 2 * kRing8 : 0);
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
-  // the rings are idle until the first load: scratch for the schedule
-  static constexpr int kSched = kK;
-  static constexpr int kSeqs = FP8 ? kK8 : kV;
+  // the buffers are idle until the first load: scratch for the schedule
+  static constexpr int kSched = FP8 ? kQ : kK;
+  static constexpr int kSeqs = FP8 ? kQ + kSchedBytes : kV;
   static_assert(kSched + kSchedBytes <= kSeqs, "schedule scratch must fit the operand rings");
   static_assert(kSeqs + kSeqBytes <= kOut, "schedule lengths must fit the rings");
   static_assert(kSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
@@ -138,6 +152,26 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint16_t kPairMask = 3;             // both CTAs of the cluster
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // copies land in microseconds
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (format
+// code 0), both K-major, FP32 accumulate, an M x N tile.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int M, int N) {
+  return (1u << 4)                            // D format: F32
+         | ((uint32_t)(N >> 3) << 17)         // N / 8
+         | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+
+// D (+)= A * B over 32 e4m3 elements of K across a CTA pair (cta_group::2,
+// M = 256), operands in both CTAs' shared memory as umma_bf16_ss_pair takes them.
+__device__ __forceinline__ void umma_e4m3_ss_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 struct Bars {
   uint64_t* q_full;   // [2] even CTA: both CTAs' query tiles landed
   uint64_t* q_empty;  // [2] the item's last S product read the tile
@@ -148,11 +182,9 @@ struct Bars {
   uint64_t* o_done;   // [3] P.V(g) done: O holds every step <= g, V stage g % 3 free
   uint64_t* drain;    // every MMA issued (by both issuers) has completed
   // FP8 cache (q_full then completes per CTA: each loads its own tile)
-  uint64_t* q16_full;  // [2] even CTA: both CTAs' query tiles converted to F16
-  uint64_t* k16_full;  // [2] even CTA: both CTAs' K halves converted to F16
+  uint64_t* q16_full;  // [2] even CTA: both CTAs' query tiles split into e4m3 hi / lo
+  uint64_t* qs_full;   // [4] this CTA's 1 / x per query row stored (item ordinal mod 4)
   uint64_t* v16_full;  // [2] this CTA's V half converted to F16
-  uint64_t* k8_full;   // [3] this CTA's e4m3 K half landed
-  uint64_t* k8_empty;  // [3] ... converted
   uint64_t* v8_full;   // [3] this CTA's e4m3 V half landed
   uint64_t* v8_empty;  // [3] ... converted
 };
@@ -421,17 +453,16 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
   B.drain = B.o_done + kNumS;
   if constexpr (FP8) {
     B.q16_full = B.drain + 1;
-    B.k16_full = B.q16_full + 2;
-    B.v16_full = B.k16_full + L::kRingK;
-    B.k8_full = B.v16_full + L::kRingV;
-    B.k8_empty = B.k8_full + L::kRing8;
-    B.v8_full = B.k8_empty + L::kRing8;
+    B.qs_full = B.q16_full + 2;
+    B.v16_full = B.qs_full + 4;
+    B.v8_full = B.v16_full + L::kRingV;
     B.v8_empty = B.v8_full + L::kRing8;
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + L::kNumBars * 8);
   int* list_count = reinterpret_cast<int*>(tmem_slot + 1);
   int* list = reinterpret_cast<int*>(smem + L::kList);
   float* xch = reinterpret_cast<float*>(smem + L::kX);
+  float* qinv = reinterpret_cast<float*>(smem + L::kQInv);  // FP8 only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // query tile of the pair this CTA owns
@@ -452,11 +483,9 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
     mbar_init(B.drain, 2);  // one commit from each issuer
     if constexpr (FP8) {
       for (int i = 0; i < 2; ++i) mbar_init(&B.q16_full[i], 8);  // 4 converter warps x 2 CTAs
-      for (int i = 0; i < L::kRingK; ++i) mbar_init(&B.k16_full[i], 8);
+      for (int i = 0; i < 4; ++i) mbar_init(&B.qs_full[i], 4);
       for (int i = 0; i < L::kRingV; ++i) mbar_init(&B.v16_full[i], 4);
       for (int i = 0; i < L::kRing8; ++i) {
-        mbar_init(&B.k8_full[i], 1);
-        mbar_init(&B.k8_empty[i], 4);
         mbar_init(&B.v8_full[i], 1);
         mbar_init(&B.v8_empty[i], 4);
       }
@@ -524,36 +553,31 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
           int page = __ldg(bt + kt);
           if (page < 0 || page >= p.num_pages) page = 0;  // sequence reported invalid
           const int y = page * kPage;
-          if constexpr (FP8) {
-            // e4m3 halves: K keys 64 rank .. + 63 (128 one-byte dims), V dims
-            // 64 rank .. + 63 of the 128 keys; stage tiles % 3 is free once the
-            // converter warps have read it
-            const int st = tiles % L::kRing8;
-            const uint32_t ph = ((tiles / L::kRing8) & 1) ^ 1;
-            uint64_t* empty = is_k ? &B.k8_empty[st] : &B.v8_empty[st];
-            uint64_t* full = is_k ? &B.k8_full[st] : &B.v8_full[st];
-            if (tiles >= (uint32_t)L::kRing8 && !(ok = mbar_wait(empty, ph, p.status))) break;
-            if (is_k) {
-              mbar_arrive_expect_tx(full, kK8Bytes);
-              tma_load_2d(smem + L::kK8 + st * kK8Bytes, &tm_k, it.h * kHeadDim,
-                          y + (int)rank * 64, full, pol_kv);
-            } else {
-              mbar_arrive_expect_tx(full, kV8Bytes);
-              tma_load_2d(smem + L::kV8 + st * kV8Bytes, &tm_v, it.h * kHeadDim + (int)rank * 64,
-                          y, full, pol_kv);
-            }
-          } else if (is_k) {
-            // stage tiles % 3 is free once S(tiles - 3) is done
+          if (is_k) {
+            // keys 64 rank .. + 63 of the page; stage tiles % 3 is free once
+            // S(tiles - 3) is done.  FP8: the e4m3 half (128 one-byte dims, one
+            // 128-byte-swizzled box) is QK^T's operand as it lands
             const int st = tiles % L::kRingK;
             if (tiles >= (uint32_t)L::kRingK &&
                 !(ok = mbar_wait(&B.s_full[st], ((tiles / L::kRingK) & 1) ^ 1, p.status)))
               break;
-            if (even) mbar_arrive_expect_tx(&B.k_full[st], 2 * kKBytes);
+            if (even) mbar_arrive_expect_tx(&B.k_full[st], 2 * L::kKStage);
             const uint32_t kbar = mapa_shared(smem_u32(&B.k_full[st]), 0);
-            uint8_t* dst = smem + L::kK + st * kKBytes;
+            uint8_t* dst = smem + L::kK + st * L::kKStage;
             tma_load_2d_pair(dst, &tm_k, it.h * kHeadDim, y + (int)rank * 64, kbar, pol_kv);
-            tma_load_2d_pair(dst + kKBox, &tm_k, it.h * kHeadDim + 64, y + (int)rank * 64, kbar,
-                             pol_kv);
+            if constexpr (!FP8)
+              tma_load_2d_pair(dst + kKBox, &tm_k, it.h * kHeadDim + 64, y + (int)rank * 64, kbar,
+                               pol_kv);
+          } else if constexpr (FP8) {
+            // e4m3 V half: dims 64 rank .. + 63 of the 128 keys; stage tiles % 3
+            // is free once the converter warps have read it
+            const int st = tiles % L::kRing8;
+            const uint32_t ph = ((tiles / L::kRing8) & 1) ^ 1;
+            if (tiles >= (uint32_t)L::kRing8 && !(ok = mbar_wait(&B.v8_empty[st], ph, p.status)))
+              break;
+            mbar_arrive_expect_tx(&B.v8_full[st], kV8Bytes);
+            tma_load_2d(smem + L::kV8 + st * kV8Bytes, &tm_v, it.h * kHeadDim + (int)rank * 64, y,
+                        &B.v8_full[st], pol_kv);
           } else {
             // stage tiles % 3 is free once P.V(tiles - 3) is done
             const int st = tiles % L::kRingV;
@@ -568,14 +592,13 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
       }
       // copies still in flight (only after a timeout) land before teardown;
       // the even CTA's barriers count both CTAs' Q and K halves
-      if constexpr (FP8) {
-        drain_loads(is_k ? B.k8_full : B.v8_full, L::kRing8, tiles, p.status, false);
-        if (is_k) drain_loads(B.q_full, 2, qitems, p.status, false);
-      } else if (!is_k) {
-        drain_loads(B.v_full, L::kRingV, tiles, p.status, false);
-      } else if (even) {
-        drain_loads(B.q_full, 2, qitems, p.status, true);
-        drain_loads(B.k_full, L::kRingK, tiles, p.status, true);
+      if (!is_k) {
+        if constexpr (FP8) drain_loads(B.v8_full, L::kRing8, tiles, p.status, false);
+        else drain_loads(B.v_full, L::kRingV, tiles, p.status, false);
+      } else {
+        if (FP8) drain_loads(B.q_full, 2, qitems, p.status, false);  // each CTA's own
+        else if (even) drain_loads(B.q_full, 2, qitems, p.status, true);
+        if (even) drain_loads(B.k_full, L::kRingK, tiles, p.status, true);
       }
     }
     __syncwarp();
@@ -590,8 +613,9 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
       // waits for P.V(g - 1) (the other thread's) to complete, which orders
       // the accumulation into O.  Thread 0 issues S(0..2) up front.
       const uint32_t par = warp == 1 ? 0u : 1u;
-      // Q, K: K-major; P (TMEM), V MN-major; F16 operands for the FP8 cache
-      const uint32_t idesc_qk = FP8 ? umma_idesc_f16(256, 128, false, false)
+      // Q, K: K-major (FP8: e4m3 x e4m3, kind::f8f6f4); P (TMEM), V MN-major
+      // (FP8: F16)
+      const uint32_t idesc_qk = FP8 ? umma_idesc_e4m3(256, 128)
                                     : umma_idesc_bf16(256, 128, false, false);
       const uint32_t idesc_pv = FP8 ? umma_idesc_f16(256, 128, false, true)
                                     : umma_idesc_bf16(256, 128, false, true);
@@ -606,7 +630,7 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
         const int qb = qi & 1;
         if (issue) {
           if (q_waited != qi) {
-            // FP8: both CTAs' tiles rewritten as F16 by their converter warps
+            // FP8: both CTAs' tiles split into e4m3 hi and lo by their converter warps
             if (!(ok = FP8 ? mbar_wait_cl(&B.q16_full[qb], (qi >> 1) & 1, p.status)
                            : mbar_wait(&B.q_full[qb], (qi >> 1) & 1, p.status)))
               return;
@@ -614,18 +638,27 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
           }
           const int sb = gq % kNumS, kb = gq % L::kRingK;
           const uint32_t kph = (gq / L::kRingK) & 1;
-          if (!(ok = FP8 ? mbar_wait_cl(&B.k16_full[kb], kph, p.status)
-                         : mbar_wait(&B.k_full[kb], kph, p.status)))
-            return;
+          if (!(ok = mbar_wait(&B.k_full[kb], kph, p.status))) return;
           tc_fence_after();
           const uint32_t qa = smem_u32(smem + L::kQ + qb * kQBytes);
-          const uint32_t ka = smem_u32(smem + L::kK + kb * kKBytes);
+          const uint32_t ka = smem_u32(smem + L::kK + kb * L::kKStage);
           const uint32_t d = tmem + kColS + sb * 128;
+          if constexpr (FP8) {
+            // S = (hi + lo) K^T: the hi rows (box 0) then the lo rows (box 1)
+            // against the same e4m3 K half, 32 dims per instruction
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = umma_sdesc_sw128(qa + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_sdesc_sw128(ka + (k >> 2) * kKBox + (k & 3) * 32, 16, 1024);
-            umma_bf16_ss_pair(d, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = umma_sdesc_sw128(qa + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024);
+              const uint64_t bd = umma_sdesc_sw128(ka + (k & 3) * 32, 16, 1024);
+              umma_e4m3_ss_pair(d, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = umma_sdesc_sw128(qa + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024);
+              const uint64_t bd = umma_sdesc_sw128(ka + (k >> 2) * kKBox + (k & 3) * 32, 16, 1024);
+              umma_bf16_ss_pair(d, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair(&B.s_full[sb], kPairMask);
         }
@@ -679,88 +712,103 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
     __syncwarp();
   } else if (warp >= kConvWarp0) {
     // ------------------------------------------------------------ FP8 converters
-    // Four warps (128 threads) per CTA, per item: this CTA's query tile from
-    // BF16 to F16 in place (thread = row), then per step this CTA's e4m3 K
-    // half (thread = key, 64 dims) and V half (thread = key) to F16, in the
-    // swizzled layouts the BF16 path gets from TMA (e4m3 values are exact in
-    // F16).  K and V stages are reused two steps later, once S(j - 2) and
-    // P.V(j - 2) are done.  The even CTA's issuer waits for both CTAs' Q and
-    // K (remote arrivals from the odd CTA); V is this CTA's, behind the
-    // softmax's P barrier.
+    // Four warps (128 threads) per CTA.  Per item: this CTA's query tile, row
+    // ct, times a power of two x_ct that brings the row's largest |q| into
+    // [128, 256), split into two e4m3 rows hi = e4m3(x q) (box 0 of the tile)
+    // and lo = e4m3(x q - hi) (box 1), in place; hi + lo = x q exactly for
+    // every element of magnitude at least 2^-10 of the row's largest (a bf16
+    // value has 8 significant bits, and the residual of its rounding to 4 is a
+    // multiple of its last bit with at most 4 significant bits), smaller ones
+    // are off by at most 2^-10 / x.  1 / x goes to the softmax.  QK^T then
+    // runs on the e4m3 K halves as TMA lands them.  Per step: this CTA's e4m3
+    // V half (thread = key) to F16 in the swizzled layout the BF16 path gets
+    // from TMA (e4m3 values are exact in F16); a V stage is reused three
+    // steps later, once P.V(j - 3) is done.  The even CTA's issuer waits for both
+    // CTAs' query splits (remote arrivals from the odd CTA); V is this CTA's,
+    // behind the softmax's P barrier.
     if constexpr (FP8) {
       const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-      uint32_t q16_even[2], k16_even[L::kRingK];
+      uint32_t q16_even[2];
       for (int i = 0; i < 2; ++i) q16_even[i] = mapa_shared(smem_u32(&B.q16_full[i]), 0);
-      for (int i = 0; i < L::kRingK; ++i) k16_even[i] = mapa_shared(smem_u32(&B.k16_full[i]), 0);
-      auto arrive_even = [&](uint64_t* local, uint32_t remote) {
-        __syncwarp();
-        if (lane == 0) {
-          if (even) mbar_arrive(local);
-          else mbar_arrive_cluster_smem(remote);
-        }
-      };
       uint32_t tiles = 0, qitems = 0;
       bool ok = true;
       Item it;
       int r = 0;
       while (src.next_with_tiles(p, r, it)) {
-        // ---- Q: row ct of this CTA's tile, 16 chunks of 8 values, in place
+        // ---- Q: row ct of this CTA's tile (16 chunks of 8 BF16 values, two
+        // boxes) into e4m3 hi (box 0) and lo (box 1), in place
         const int qb = qitems & 1;
         if (ok) ok = mbar_wait_warp(&B.q_full[qb], (qitems >> 1) & 1, p.status);
         ++qitems;
         {
           const uint32_t qrow = smem_u32(smem + L::kQ + qb * kQBytes) + ct * 128;
-          bool big = false;
-#pragma unroll 4
+          uint32_t w[64];  // the row's 128 BF16 values
+#pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const uint32_t a = qrow + (c >> 3) * kQBox + ((((uint32_t)c & 7) ^ (ct & 7)) << 4);
-            const uint4 v = lds128(a);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
+            const uint4 v = lds128(qrow + (c >> 3) * kQBox + ((((uint32_t)c & 7) ^ (ct & 7)) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          // the largest magnitude (BF16 bits: the magnitude order is the
+          // integer order; from 0x7f80 up: inf or NaN)
+          uint32_t amax = 0;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) amax = max(amax, max(w[e] & 0x7fffu, (w[e] >> 16) & 0x7fffu));
+          float x, xinv = 1.f;
+          if (amax >= 0x7f80u) {
+            // inf or NaN in q: flagged, and the row's scores become NaN
+            x = __uint_as_float(0x7fc00000u);
+            if (p.status) atomicOr(p.status, PA_STATUS_Q_RANGE);
+          } else {
+            // largest = 1.f x 2^(be - 127); x = 2^(134 - be), kept a normal float
+            const int sx = min(134 - (int)(amax >> 7), 126);
+            x = __uint_as_float((uint32_t)(127 + sx) << 23);
+            xinv = __uint_as_float((uint32_t)(127 - sx) << 23);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // dims 16 c .. 16 c + 15
+            uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f = bf16x2_to_float2(wv[e]);
-              big |= fabsf(f.x) >= 65520.f || fabsf(f.y) >= 65520.f;
-              o[e] = pack_f16x2(f.x, f.y);
+              uint32_t h4 = 0, l4 = 0;
+#pragma unroll
+              for (int f = 0; f < 2; ++f) {
+                const float2 a = bf16x2_to_float2(w[8 * c + 2 * e + f]);
+                const float2 ax = make_float2(a.x * x, a.y * x);
+                const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(ax, __NV_SATFINITE, __NV_E4M3);
+                const __half2 hh(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3));
+                const float2 hf = __half22float2(hh);
+                const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(
+                    make_float2(ax.x - hf.x, ax.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+                h4 |= (uint32_t)h << (16 * f);
+                l4 |= (uint32_t)l << (16 * f);
+              }
+              hi[e] = h4;
+              lo[e] = l4;
             }
-            sts128(a, o[0], o[1], o[2], o[3]);
+            const uint32_t a = qrow + ((((uint32_t)c) ^ (ct & 7)) << 4);
+            sts128(a, hi[0], hi[1], hi[2], hi[3]);
+            sts128(a + kQBox, lo[0], lo[1], lo[2], lo[3]);
           }
-          if (__any_sync(0xffffffffu, big) && lane == 0 && p.status)
-            atomicOr(p.status, PA_STATUS_Q_RANGE);
+          qinv[((qitems - 1) & 3) * 128 + ct] = xinv;
         }
         fence_proxy_async_smem();
-        arrive_even(&B.q16_full[qb], q16_even[qb]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&B.qs_full[(qitems - 1) & 3]);
+          if (even) mbar_arrive(&B.q16_full[qb]);
+          else mbar_arrive_cluster_smem(q16_even[qb]);
+        }
         for (int kt = 0; kt < it.nmax; ++kt, ++tiles) {
           const int st8 = tiles % L::kRing8;
           const uint32_t ph8 = (tiles / L::kRing8) & 1;
-          // ---- K: key ct % 64, dims 64 (ct / 64) .. + 63 -> box ct / 64 of the stage
-          const int kb = tiles % L::kRingK;
-          if (ok) ok = mbar_wait_warp(&B.k8_full[st8], ph8, p.status);
-          if (tiles >= (uint32_t)L::kRingK) {
-            const uint32_t s2 = tiles - L::kRingK;  // S(tiles - 2) done: the stage is free
-            if (ok) ok = mbar_wait_warp(&B.s_full[s2 % kNumS], (s2 / kNumS) & 1, p.status);
-          }
-          {
-            const int key = ct & 63, hb = ct >> 6, sw = key & 7;
-            const uint32_t src8 = smem_u32(smem + L::kK8 + st8 * kK8Bytes) + key * 128;
-            const uint32_t dst = smem_u32(smem + L::kK + kb * kKBytes) + hb * kKBox + key * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {  // dims 64 hb + 16 c .. + 15
-              uint4 lo, hi;
-              e4m3x16_to_f16(lds128(src8 + ((((uint32_t)(4 * hb + c)) ^ sw) << 4)), lo, hi);
-              sts128(dst + ((((uint32_t)(2 * c)) ^ sw) << 4), lo.x, lo.y, lo.z, lo.w);
-              sts128(dst + ((((uint32_t)(2 * c + 1)) ^ sw) << 4), hi.x, hi.y, hi.z, hi.w);
-            }
-          }
-          fence_proxy_async_smem();
-          arrive_even(&B.k16_full[kb], k16_even[kb]);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&B.k8_empty[st8]);
           // ---- V: key ct, this CTA's 64 dims
           const int vb = tiles % L::kRingV;
           if (ok) ok = mbar_wait_warp(&B.v8_full[st8], ph8, p.status);
           if (tiles >= (uint32_t)L::kRingV) {
-            const uint32_t g2 = tiles - L::kRingV;  // P.V(tiles - 2) done: the stage is free
+            const uint32_t g2 = tiles - L::kRingV;  // P.V(tiles - 3) done: the stage is free
             if (ok) ok = mbar_wait_warp(&B.o_done[g2 % kNumS], (g2 / kNumS) & 1, p.status);
           }
           {
@@ -811,7 +859,8 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
     // After a wait gives up (PA_STATUS_TIMEOUT) the warps skip every later
     // wait but still walk all items and steps, so the two warps of a row
     // quarter keep meeting at the same named barriers and reach the end.
-    uint32_t g = 0;  // steps so far (all items)
+    uint32_t g = 0;       // steps so far (all items)
+    uint32_t qitems = 0;  // items with key tiles so far
     bool ok = true;
     Item it;
     for (int r = 0; src.get(p, r, it); ++r) {
@@ -830,7 +879,13 @@ __global__ void __launch_bounds__(Lay<FP8>::kThreads, 1)
             reinterpret_cast<uint4*>(dst)[cc] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + it.h);
+      if constexpr (FP8) {
+        // the item's K scale and this row's 1 / x of the query split
+        const uint32_t qs = qitems & 3;
+        if (ok) ok = mbar_wait_warp(&B.qs_full[qs], (qitems >> 2) & 1, p.status);
+        c = p.scale_log2 * __ldg(p.k_scale + it.h) * qinv[qs * 128 + row];
+      }
+      ++qitems;
       const int pos = it.prior + it.pair * 256 + (int)rank * 128 + row;  // this row's position
       const int last_page = (it.ctx - 1) / kPage;
       const int vtail = it.ctx % kPage;  // rows >= vtail of the last page are past the context

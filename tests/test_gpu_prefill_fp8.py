@@ -153,14 +153,51 @@ def test_invalid_page_zeroes_sequence(cuda_lib):
     assert_close(out[100:], ref[100:], what="prefill fp8 valid neighbour")
 
 
-def test_q_out_of_f16_range_sets_status(cuda_lib):
-    """A q element beyond F16's range sets PA_STATUS_Q_RANGE (that item's
-    output is undefined; the other items are still right)."""
-    case = W.custom_case(944, [300, 300], Hq=8, Hkv=2, chunk_lens=[100, 100], with_new=True)
+def test_q_beyond_f16_range(cuda_lib):
+    """QK^T runs on the e4m3 K codes with each query row split into e4m3 hi +
+    lo after scaling by a power of two of its own, so no bf16 magnitude is out
+    of range: q times 2^15 (elements past 65520) with the softmax scale times
+    2^-15 gives the same codes, the same score factor and so the same bits as
+    the unscaled call, which matches the oracle."""
+    case = W.custom_case(944, [300, 1000], Hq=8, Hkv=2, chunk_lens=[100, 260], with_new=True)
+    ks, vs, kc8, vc8 = _fp8_case(case, 17)
+    out, _, st = _write_and_prefill(cuda_lib, case, ks, vs, kc8, vc8)
+    assert st == 0
+    ref, _ = _oracle(case, ks, vs, kc8, vc8)
+    assert_close(out, ref, what="prefill fp8 unscaled q")
+    big = W.custom_case(944, [300, 1000], Hq=8, Hkv=2, chunk_lens=[100, 260], with_new=True)
+    big.q = (big.q.float() * 2.0 ** 15).to(torch.bfloat16)
+    big.scale = case.scale * 2.0 ** -15
+    assert big.q.float().abs().max() > 65520
+    out_big, _, st = _write_and_prefill(cuda_lib, big, ks, vs, kc8, vc8)
+    assert st == 0
+    assert torch.equal(out_big.view(torch.int32), out.view(torch.int32))
+
+
+def test_q_wide_dynamic_range(cuda_lib):
+    """Elements far below their row's largest (down to 2^-16 of it), where the
+    hi + lo split is no longer exact (error at most 2^-17 of the largest):
+    still within the tolerance of the oracle."""
+    case = W.custom_case(945, [700, 129], Hq=40, Hkv=8, chunk_lens=[300, 129], with_new=True)
+    g = torch.Generator().manual_seed(945)
+    e = torch.randint(-16, 1, case.q.shape, generator=g).float()
+    case.q = (case.q.float() * torch.exp2(e) * 4.0).to(torch.bfloat16)
+    ks, vs, kc8, vc8 = _fp8_case(case, 18)
+    out, _, st = _write_and_prefill(cuda_lib, case, ks, vs, kc8, vc8)
+    assert st == 0
+    ref, _ = _oracle(case, ks, vs, kc8, vc8)
+    assert_close(out, ref, what="prefill fp8 wide-range q")
+
+
+def test_nonfinite_q_sets_status(cuda_lib):
+    """An infinite q element sets PA_STATUS_Q_RANGE (that row's output is NaN;
+    the other sequence is still right)."""
+    case = W.custom_case(946, [300, 300], Hq=8, Hkv=2, chunk_lens=[100, 100], with_new=True)
     ks, vs, kc8, vc8 = _fp8_case(case, 17)
     ref, _ = _oracle(case, ks, vs, kc8, vc8)
     q = case.q.clone().cuda()
-    q[150, 3, 7] = 1.0e5
+    q[150, 3, 7] = float("inf")
     out, _, st = _write_and_prefill(cuda_lib, case, ks, vs, kc8, vc8, q=q)
     assert st & cuda_lib.PA_STATUS_Q_RANGE
-    assert_close(out[:100], ref[:100], what="prefill fp8 beside a q out of range")
+    assert torch.isnan(out[150, 3]).all()
+    assert_close(out[:100], ref[:100], what="prefill fp8 beside a non-finite q")
