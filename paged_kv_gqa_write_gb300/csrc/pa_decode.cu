@@ -232,6 +232,27 @@ __device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// 16 columns of one lane as two 8-column accesses (any 8-column boundary)
+__device__ __forceinline__ void tmem_ld8x2(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "r"(taddr + 8));
+}
+__device__ __forceinline__ void tmem_st8x2(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%2, %3, %4, %5, %6, %7, %8, %9};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%10, %11, %12, %13, %14, %15, %16, %17};"
+      ::"r"(taddr), "r"(taddr + 8),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // NH: columns the softmax and epilogue handle (8, 16 or 32, >= any item's GC).
 // FP8: the cache holds e4m3 codes with per-KV-head scales.  MULTI: more than
 // one new token per sequence (per-column causal masks, (token, head) columns);
@@ -997,10 +1018,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     }
   } else if (kN == 32) {
     // ------------------------------------------------------------ 32 columns: softmax + epilogue
-    // Warps 2-5 take columns 0-15, warps 6-9 columns 16-31, each group as the
-    // 16-column softmax does (thread = key, its own exchange slots), and at
-    // the item's end the same threads (thread = head dim) write their
-    // columns' outputs.
+    // Warps 2-5 take the item's first 8 or 16 columns, warps 6-9 the rest
+    // (at most 16), each group as the 16-column softmax does (thread = key,
+    // its own exchange slots), and at the item's end the same threads
+    // (thread = head dim) write their columns' outputs.
     const int sg = (warp - kSoftWarp0) >> 2;  // column group
     const int wi = (warp - kSoftWarp0) & 3;
     const int quarter = warp & 3;             // TMEM lanes this warp may access
@@ -1039,13 +1060,20 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       if (lane == 0) mbar_arrive(&B.q_empty[slot]);
       const int npg = pg1 - pg0;
       const int GC = MULTI ? unit_columns(p, unit) : p.G;
-      const int GL = min(max(GC - kH * sg, 0), kH);  // this group's columns
+      // the groups split the item's columns at cb1, a multiple of 8 (so each
+      // group's first column is on an 8-column boundary of tensor memory): 8
+      // below 24 columns, else 16.  Neither group holds more than 16, and the
+      // busier one at most 15 from 17 to 23 columns (a split at 16 would give
+      // 20 columns, 4 new tokens of 5 heads, as 16 + 4).
+      const int cb1 = GC >= 24 ? 16 : 8;
+      const int cb = sg == 0 ? 0 : cb1;  // this group's first column
+      const int GL = sg == 0 ? min(GC, cb1) : max(GC - cb1, 0);  // this group's columns
       // FP8: times the item's K scale and 1 / x of its query split
       if constexpr (FP8) c = p.scale_log2 * __ldg(p.k_scale + unit / p.NT) * q_inv;
       // column g = tl * G + head (token t0 + tl) sees key positions below lim[gl]
       int lim[kH];
       {
-        int t = (unit % p.NT) * p.Lg + (kH * sg) / p.G, hg = (kH * sg) % p.G;
+        int t = (unit % p.NT) * p.Lg + cb / p.G, hg = cb % p.G;
 #pragma unroll
         for (int gl = 0; gl < kH; ++gl) {
           lim[gl] = gl < GL ? ctx - (p.L - 1 - t) : 0;
@@ -1085,18 +1113,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           if (!(ok = mbar_wait_warp(&B.s_full[gp & 1], (gp >> 1) & 1, p.status))) break;
           tc_fence_after();
           uint32_t sr[kH];
-          const uint32_t s_base = tmem + lane_base + kColS + (gp & 1) * kNS + kH * sg;
+          const uint32_t s_base = tmem + lane_base + kColS + (gp & 1) * kNS + cb;
           if constexpr (FP8) {
             // scores of the hi and lo query rows (columns NH apart), added
             uint32_t lo[kH];
-            tmem_ld16(s_base, sr);
-            tmem_ld16(s_base + NH, lo);
+            tmem_ld8x2(s_base, sr);
+            tmem_ld8x2(s_base + NH, lo);
             tmem_wait_ld();
 #pragma unroll
             for (int gl = 0; gl < kH; ++gl)
               sr[gl] = __float_as_uint(__uint_as_float(sr[gl]) + __uint_as_float(lo[gl]));
           } else {
-            tmem_ld16(s_base, sr);
+            tmem_ld8x2(s_base, sr);
             tmem_wait_ld();
           }
           float d[kH];
@@ -1139,13 +1167,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
                 break;
               tc_fence_after();
               uint32_t orow[kH];
-              const uint32_t o_cols = tmem + lane_base + kColO + ob * kN + kH * sg;
-              tmem_ld16(o_cols, orow);
+              const uint32_t o_cols = tmem + lane_base + kColO + ob * kN + cb;
+              tmem_ld8x2(o_cols, orow);
               tmem_wait_ld();
 #pragma unroll
               for (int gl = 0; gl < kH; ++gl)
                 orow[gl] = __float_as_uint(__uint_as_float(orow[gl]) * alpha[gl]);
-              tmem_st16(o_cols, orow);
+              tmem_st8x2(o_cols, orow);
             }
           }
           // P(j) into operand buffer j & 1 once P.V(j - 2) has finished reading it
@@ -1157,7 +1185,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
 #pragma unroll
           for (int gl = 0; gl < kH; ++gl) {
             if (gl < GL) {
-              const int g = kH * sg + gl;
+              const int g = cb + gl;
               const float pv = visible(gl) ? fast_exp2(d[gl]) : 0.f;
               uint16_t pbf;
               if constexpr (FP8) {
@@ -1202,7 +1230,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if (!(ok = mbar_wait_warp(&B.o_full[ob], (nb >> 1) & 1, p.status))) break;
         tc_fence_after();
         uint32_t orow[kH];
-        tmem_ld16(tmem + lane_base + kColO + ob * kN + kH * sg, orow);
+        tmem_ld8x2(tmem + lane_base + kColO + ob * kN + cb, orow);
         tmem_wait_ld();
 #pragma unroll
         for (int gl = 0; gl < kH; ++gl) {
@@ -1222,7 +1250,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
 #pragma unroll
       for (int gl = 0; gl < kH; ++gl) {
         if (gl < GL) {
-          const int g = kH * sg + gl;
+          const int g = cb + gl;
           const int64_t row = (tok0 + g / p.G) * p.Hq + head0 + g % p.G;
           if (dest < 0) {
             if (p.out_f32)
